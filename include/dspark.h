@@ -1,0 +1,228 @@
+/*
+ * dspark.h -- C ABI of libdspark: the batched hot path of one DSpark
+ * speculative-decoding round over R concurrent requests on one GB300 GPU.
+ *
+ * Method: "DSpark: Confidence-Scheduled Speculative Decoding with
+ * Semi-Autoregressive Generation" (arXiv:2607.05147), as described on the
+ * caijizhuo.github.io page (sections 2-4: serial sampling loop, survival /
+ * expected-length / throughput table, "dspark_cycle" and "admit" sketches) and
+ * the zhongzhuzhou.org reading notes (eq. 4-5 Markov head, eq. 7 confidence
+ * head, Algorithm 1, Appendix A, section 5.2 asynchronous capacity).
+ *
+ * Conventions shared by every call
+ *  - Every tensor pointer is a caller-owned DEVICE pointer (for example the
+ *    storage of a torch tensor) in row-major layout with the shape stated. The
+ *    library allocates nothing, keeps nothing between calls and never writes
+ *    an input.
+ *  - Scratch memory is a caller-owned device buffer of at least the size the
+ *    matching *_workspace_size call reports; distinct concurrent calls need
+ *    distinct workspaces. The workspace's first 256 bytes hold a device status
+ *    word.
+ *  - Calls are asynchronous on the caller's cudaStream_t (passed as void*,
+ *    NULL = legacy default stream). Argument errors found on the host are
+ *    returned before any launch. Errors found on the device (an out-of-range
+ *    token id or length, a bounded wait that ran out) are recorded in the
+ *    workspace status word, the kernels keep every access in bounds, and
+ *    dspark_check() reports the word after synchronising the stream.
+ *  - Argument structs start with struct_size = sizeof(struct); a mismatch
+ *    returns DSPARK_ERR_INVALID_ARGUMENT.
+ *  - Random numbers: Philox4x32-10 (Salmon et al., SC'11) with key
+ *    (seed low word, seed high word) and counter (e>>2, position, request,
+ *    (round<<3)|purpose); output word e&3; uniform u = (2*(x>>9)+1)*2^-24;
+ *    Gumbel noise -log(-log u). round must be below 2^29.
+ *  - Draws are two-level Gumbel-max samples from the normalised weights: a
+ *    Gumbel-max over the log-masses of vocabulary blocks of DSPARK_NOISE_BLOCK
+ *    ids picks a block, then a Gumbel-max over the log-weights inside it picks
+ *    the token (exact sampling; for V <= DSPARK_NOISE_BLOCK the flat Gumbel-max).
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSPARK_ABI_VERSION 1
+#define DSPARK_NOISE_BLOCK 128   /* vocabulary block width of the two-level Gumbel-max */
+#define DSPARK_MAX_GAMMA 32      /* largest draft block length gamma_max */
+#define DSPARK_MAX_SLOTS 8192    /* largest R * gamma_max the scheduler accepts */
+
+typedef int32_t dspark_status;
+enum {
+    DSPARK_OK = 0,
+    DSPARK_ERR_INVALID_ARGUMENT = 1,  /* null pointer, bad size, bad enum, struct_size mismatch */
+    DSPARK_ERR_UNSUPPORTED_SHAPE = 2, /* shape outside what the kernels handle (stated per call) */
+    DSPARK_ERR_WORKSPACE = 3,         /* workspace missing or smaller than *_workspace_size */
+    DSPARK_ERR_CUDA = 4,              /* a CUDA runtime / driver call failed */
+    DSPARK_ERR_TIMEOUT = 5,           /* a bounded device-side wait ran out (device status word) */
+    DSPARK_ERR_DEVICE_INPUT = 6       /* an out-of-range device value was clamped (device status word) */
+};
+
+enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 };
+
+enum {
+    DSPARK_SCHED_SYNC = 0,           /* Algorithm 1: stop at the first Theta <= Theta_best */
+    DSPARK_SCHED_ASYNC_CAPACITY = 1, /* section 5.2: capacity K from old survivals, current ranking */
+    DSPARK_SCHED_FULL_SCAN = 2       /* arg-max of Theta over every prefix of the sorted pool */
+};
+
+enum {
+    DSPARK_PATH_AUTO = 0,            /* tensor cores when the shape allows, else CUDA cores */
+    DSPARK_PATH_CUDA_CORE = 1,       /* fp32 FMA bias contraction */
+    DSPARK_PATH_TENSOR_CORE = 2      /* tcgen05 bias contraction (bf16, r % 64 == 0, V % 8 == 0) */
+};
+
+/*
+ * dspark_sample_block -- Markov-head serial sampling, confidence head and
+ * survival products (eq. 4, 5, 7; "dspark_cycle" step 3).
+ *
+ * For each request r and draft position k = 0 .. gamma_r-1, with x_0 = anchor[r]:
+ *   B_k  = W_1[x_{k-1}] W_2        (E row times W; zero for k = 0 when bias_first = 0)
+ *   l_k  = (U[r][k] + B_k) / temperature[r]
+ *   x_k  ~ softmax(l_k)            (two-level Gumbel-max, purposes 0 and 3)
+ *   c_k  = sigmoid(w_h . h[r][k] + w_e . W_1[x] + b), x = x_{k-1} (conf_token 0, eq. 7)
+ *          or x_k (conf_token 1)
+ *   a_k  = a_{k-1} c_k             (a_0 = 1)
+ * Outputs for k >= gamma_r are token -1 and zeros.
+ */
+typedef struct {
+    uint32_t struct_size;
+    int32_t R;            /* requests, >= 1 */
+    int32_t gamma_max;    /* 1 .. DSPARK_MAX_GAMMA */
+    int32_t V;            /* vocabulary, 1 .. 2^24 */
+    int32_t r;            /* Markov rank, 1 .. 1024 */
+    int32_t d;            /* hidden width, >= 1 */
+    int32_t dtype;        /* element type of U, E, W, h: DSPARK_F32 or DSPARK_BF16 */
+    int32_t conf_token;   /* 0 or 1, see above */
+    int32_t bias_first;   /* 1: B_1 = W_1[x_0] W_2 (eq. 4-5); 0: B_1 = 0 */
+    int32_t path;         /* DSPARK_PATH_* for the bias contraction */
+    const int32_t* gamma; /* [R] per-request gamma_r in 0..gamma_max, or NULL = gamma_max */
+    const void* U;        /* [R][gamma_max][V] parallel-backbone logits */
+    const void* E;        /* [V][r] W_1 */
+    const void* W;        /* [r][V] W_2 */
+    const void* h;        /* [R][gamma_max][d] backbone hidden states */
+    const float* w_h;     /* [d] */
+    const float* w_e;     /* [r] */
+    float b;
+    const float* temperature; /* [R], > 0 */
+    const int32_t* anchor;    /* [R] x_0 in 0..V-1 */
+    uint64_t seed;
+    uint64_t round;
+    int32_t* tokens;          /* out [R][gamma_max] */
+    float* conf;              /* out [R][gamma_max] c_k */
+    float* surv;              /* out [R][gamma_max] a_k */
+    float* draft_lse;         /* out [R][gamma_max] log sum_v exp(l_k(v)) */
+    float* draft_logit;       /* out [R][gamma_max] l_k(x_k) */
+} dspark_sample_args;
+
+dspark_status dspark_sample_workspace_size(const dspark_sample_args* args, size_t* bytes);
+dspark_status dspark_sample_block(const dspark_sample_args* args, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/*
+ * dspark_schedule -- hardware-aware prefix scheduler (Algorithm 1; "admit").
+ *
+ * Pool = {(r, j) : j <= gamma_r, a_{r,j} = surv[r][j-1] > 0}, sorted by a
+ * descending, then r ascending, then j ascending. With tau_m = R + sum of the
+ * first m a's and Theta_m = tau_m * SPS(R + m):
+ *   SYNC:  m* = (first m >= 1 with Theta_m <= Theta_{m-1}) - 1, else |pool|
+ *   FULL_SCAN: m* = smallest arg-max of Theta_m over m = 0..|pool|
+ *   ASYNC_CAPACITY: K = FULL_SCAN count over the pool of surv_capacity
+ *          (survivals two rounds old); m* = min(K, |pool|)
+ * keep[r] = number of admitted slots of request r (a prefix length, 0..gamma_r).
+ * The prefix sums are exact fixed-point sums of the fp32 a's (2^-48 units) and
+ * Theta is formed in double from them.
+ * Unsupported: R * gamma_max > DSPARK_MAX_SLOTS.
+ */
+typedef struct {
+    double theta_best;    /* Theta_{m*} with the current survivals */
+    int32_t admitted;     /* m* */
+    int32_t capacity;     /* K (async) or -1 */
+    int32_t batch;        /* B = R + m* */
+    int32_t pool;         /* |pool| */
+} dspark_schedule_stats;
+
+typedef struct {
+    uint32_t struct_size;
+    int32_t R;
+    int32_t gamma_max;
+    int32_t mode;                 /* DSPARK_SCHED_* */
+    int32_t n_sps;                /* >= R * (1 + gamma_max) */
+    const int32_t* gamma;         /* [R] or NULL */
+    const float* surv;            /* [R][gamma_max] current survivals */
+    const float* surv_capacity;   /* [R][gamma_max] survivals two rounds old (ASYNC_CAPACITY only) */
+    const float* sps;             /* [n_sps] SPS(B) at index B-1 */
+    int32_t* keep;                /* out [R] */
+    dspark_schedule_stats* stats; /* out, one device struct */
+} dspark_schedule_args;
+
+dspark_status dspark_schedule_workspace_size(const dspark_schedule_args* args, size_t* bytes);
+dspark_status dspark_schedule(const dspark_schedule_args* args, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
+ * dspark_verify -- lossless rejection-sampling verification of the admitted
+ * prefixes ("dspark_cycle" steps 5-6; accept rule min(1, p_t/p_d) and the
+ * residual norm(max(0, p_t - p_d)) of Leviathan et al.).
+ *
+ * Target row i of request r (target[r][i]) is the target's distribution for
+ * draft position i; row keep[r] supplies the bonus token. With
+ * p_t = softmax(target[r][i] / T_r) and p_d(x) = exp(draft_logit - draft_lse):
+ *   for j = 0 .. keep[r]-1: accept tokens[r][j] iff log u_j < log p_t(x) - log p_d(x)
+ *     (u_j: purpose 1, position j); stop at the first rejection.
+ *   accepted[r] = n, the accepted prefix length.
+ *   n < keep[r]: next_token ~ norm(max(0, p_t - p_d)) at position n, with p_d
+ *     recomputed from U, E, W (purposes 2 and 4); resampled[r] = 1.
+ *     If that residual is zero everywhere (possible only through rounding)
+ *     next_token ~ p_t of row n.
+ *   n = keep[r]: next_token ~ p_t of row keep[r]; resampled[r] = 0.
+ * Committed tokens: tokens[r][0:n] followed by next_token[r] (the next anchor).
+ */
+typedef struct {
+    uint32_t struct_size;
+    int32_t R;
+    int32_t gamma_max;
+    int32_t V;
+    int32_t r;
+    int32_t dtype;               /* element type of target, U, E, W */
+    int32_t bias_first;          /* as passed to dspark_sample_block */
+    int32_t path;                /* DSPARK_PATH_* for the residual's bias recompute */
+    const int32_t* gamma;        /* [R] or NULL */
+    const void* target;          /* [R][gamma_max+1][V] */
+    const void* U;               /* [R][gamma_max][V] */
+    const void* E;               /* [V][r] */
+    const void* W;               /* [r][V] */
+    const int32_t* anchor;       /* [R] */
+    const int32_t* tokens;       /* [R][gamma_max] */
+    const float* draft_lse;      /* [R][gamma_max] */
+    const float* draft_logit;    /* [R][gamma_max] */
+    const int32_t* keep;         /* [R] */
+    const float* temperature;    /* [R] */
+    uint64_t seed;
+    uint64_t round;
+    int32_t* accepted;           /* out [R] */
+    int32_t* next_token;         /* out [R] */
+    uint8_t* resampled;          /* out [R] */
+} dspark_verify_args;
+
+dspark_status dspark_verify_workspace_size(const dspark_verify_args* args, size_t* bytes);
+dspark_status dspark_verify(const dspark_verify_args* args, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* Synchronise `stream`, then return the device status word of `workspace`
+ * (DSPARK_OK, DSPARK_ERR_TIMEOUT or DSPARK_ERR_DEVICE_INPUT) and clear it. */
+dspark_status dspark_check(void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* dspark_status_string(dspark_status status);
+
+/* DSPARK_ABI_VERSION of the loaded library. */
+int32_t dspark_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
