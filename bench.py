@@ -1,0 +1,420 @@
+#!/usr/bin/env python
+"""Benchmark one DSpark draft round (sample + schedule + verify) on GB300.
+
+Workload (default): config 3 -- R=128 requests, gamma=16, V=151936, r=256,
+d=4096, bf16 inputs, synthetic structured logits (top-1 boosted +6 on 70% of
+positions), T in {0.6, 1.0}, staircase SPS, synchronous scheduler. A step is
+one whole round over one batch; inputs stay resident in HBM, `round` advances
+so every step draws fresh noise, and L2 is flushed (256 MiB write) between
+steps outside the timed events.
+
+Prints one JSON line. Metric: draft tokens per second (sum of gamma_r over the
+batch / round time). Multi-GPU (torchrun): every rank runs an independent
+replica on its own batch (weak scaling, no collective on the data path); the
+value is all ranks' draft tokens over the slowest rank's time.
+
+--impl reference times the CPU oracle (test infrastructure, the only
+reference this method has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSpark round: draft tokens/s (sample+schedule+verify) & % of HBM roofline"
+UNIT = "draft tokens/s"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join("/tmp", "dspark_clocks_%d.csv" % os.getpid())
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ------------------------------------------------------------------ accounting
+
+def round_bytes(rnd, keep_sum: int, n_rejected: int) -> dict:
+    """Compulsory HBM bytes of one round, each tensor read once (algorithmic)."""
+    es = 2 if rnd.dtype == "bf16" else 4
+    g = rnd.gamma.cpu().numpy() if rnd.gamma is not None else np.full(rnd.R, rnd.gamma_max)
+    drafted = int(g.sum())
+    b = {
+        "U": drafted * rnd.V * es,
+        "W": rnd.r * rnd.V * es,
+        "h": drafted * rnd.d * es,
+        "E_rows": 2 * drafted * rnd.r * es,                       # bias rows + confidence rows
+        "target_rows": (keep_sum + rnd.R) * rnd.V * es,
+        "residual_recompute": n_rejected * rnd.V * es + (rnd.r * rnd.V * es if n_rejected else 0),
+    }
+    b["total"] = sum(b.values())
+    return b
+
+
+def draft_stats_launch_bytes(rnd) -> float:
+    """Algorithmic bytes of one draft_stats launch: that step's U slice, the W
+    share amortised over the round (W is read once per round and kept in L2),
+    the gathered E rows and the block statistics written."""
+    es = 2 if rnd.dtype == "bf16" else 4
+    g = rnd.gamma.cpu().numpy() if rnd.gamma is not None else np.full(rnd.R, rnd.gamma_max)
+    drafted = int(g.sum())
+    nblk = -(-rnd.V // 128)
+    per_round = drafted * rnd.V * es + rnd.r * rnd.V * es + drafted * rnd.r * es + drafted * nblk * 8
+    return per_round / rnd.gamma_max
+
+
+def kernel_hash(files) -> str:
+    h = hashlib.sha1()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(kernel: str, workload: str, src_hash: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload and parts[2] == src_hash:
+                return float(parts[3])
+    return None
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def run_oracle_round(rnd, ids, threads, rnd_index):
+    import oracle
+
+    def to_np(t):
+        t = t.detach().contiguous().cpu()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
+
+    idx = torch.as_tensor(ids, dtype=torch.long, device=rnd.U.device)
+    U = to_np(rnd.U.index_select(0, idx))
+    h = to_np(rnd.h.index_select(0, idx))
+    target = to_np(rnd.target.index_select(0, idx))
+    E, W = to_np(rnd.E), to_np(rnd.W)
+    T = to_np(rnd.temperature)[ids]
+    anchor = to_np(rnd.anchor)[ids]
+    gamma = None if rnd.gamma is None else to_np(rnd.gamma)[ids]
+    sps = to_np(rnd.sps).astype(np.float64)
+    t0 = time.perf_counter()
+    s = oracle.sample_block(U, E, W, h, to_np(rnd.w_h), to_np(rnd.w_e), rnd.b, T, anchor, rnd.seed, rnd_index,
+                            gamma=gamma, req_ids=np.asarray(ids), conf_token=rnd.conf_token,
+                            bias_first=rnd.bias_first, threads=threads)
+    mode = rnd.mode
+    cap = s["surv"] if mode == 1 else None   # the sample has no older round; reuse current survivals
+    c = oracle.schedule(s["surv"], sps, mode, gamma=gamma, surv_capacity=cap)
+    oracle.verify(target, U, E, W, anchor, np.where(s["tokens"] < 0, 0, s["tokens"]), s["lse"], s["logit"],
+                  c["keep"], T, rnd.seed, rnd_index, gamma=gamma, req_ids=np.asarray(ids),
+                  bias_first=rnd.bias_first, threads=threads)
+    dt = time.perf_counter() - t0
+    drafted = int(gamma.sum()) if gamma is not None else len(ids) * rnd.gamma_max
+    return drafted, dt
+
+
+def cpu_threads():
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+# ------------------------------------------------------------------ arms
+
+def bench_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_draft_round_gb300 import workloads as wl
+    dev = "cuda:%d" % local if torch.cuda.is_available() else "cpu"
+    rnd = wl.CONFIGS[args.workload](device=dev)
+    threads = cpu_threads()
+    n_req = threads
+    ids = list(range(0, rnd.R, max(1, rnd.R // n_req)))[:n_req]
+    for i in range(args.warmup):
+        run_oracle_round(rnd, ids, threads, i)
+    tok = 0
+    tot = 0.0
+    for i in range(args.steps):
+        d, dt = run_oracle_round(rnd, ids, threads, args.warmup + i)
+        tok += d
+        tot += dt
+    value = tok / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": rnd.name, "R": rnd.R, "gamma": rnd.gamma_max, "V": rnd.V,
+                                           "r": rnd.r, "d": rnd.d, "sample_requests": len(ids)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "%d of %d requests per step, whole round (sample+schedule+verify)"
+                                       % (len(ids), rnd.R)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def bench_ours(args):
+    import speculative_decoding_draft_round_gb300 as ds
+    from speculative_decoding_draft_round_gb300 import build as dsbuild
+    from speculative_decoding_draft_round_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    dsbuild.build()
+    path = {"auto": ds.PATH_AUTO, "cuda_core": ds.PATH_CUDA_CORE, "tensor_core": ds.PATH_TENSOR_CORE}[args.path]
+    rnd = wl.CONFIGS[args.workload](device=dev)
+    if world > 1:   # independent replica per rank
+        rnd.seed = rnd.seed + 1000 * rank
+    cap = None
+    if rnd.mode == wl.SCHED_ASYNC_CAPACITY:
+        old = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                              rnd.seed, 0, gamma=rnd.gamma, path=path)
+        cap = old["surv"].clone()
+    runner = ds.RoundRunner(rnd, surv_capacity=cap, path=path)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    uses_tc = path != ds.PATH_CUDA_CORE and rnd.dtype == "bf16"
+
+    clocks = ClockSampler(gpu_id_for(local))
+    clocks.start()
+    # warm-up: at least W rounds and at least one second of work, so the clock sampler sees load
+    t_start = time.time()
+    i = 0
+    while i < args.warmup or time.time() - t_start < 1.0:
+        runner.set_round(2 + i)
+        runner.run()
+        torch.cuda.synchronize()
+        i += 1
+    status = runner.check()
+    if status:
+        raise RuntimeError("device status %d after warm-up" % status)
+
+    n_timed = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
+    timer = ds.KernelTimer("draft_stats", n_timed * rnd.gamma_max)
+    launches0 = ds.launch_count()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with timer:
+        for s in range(n_timed):
+            flush.zero_()
+            runner.set_round(1000 + s)
+            starts[s].record(stream)
+            runner.run()
+            stops[s].record(stream)
+    torch.cuda.synchronize()
+    launches = ds.launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, stops)]
+    total_ms = sum(step_ms)
+    stats_ms = timer.durations_ms()
+    status = runner.check()
+    if status:
+        raise RuntimeError("device status %d after timing" % status)
+    res = runner.results()
+    keep_sum = int(res["keep"].sum())
+    n_rej = int(res["resampled"].to(torch.int32).sum())
+
+    # end to end through the public API: per-round inputs copied from pinned host memory,
+    # results read back, every step
+    host_in = {k: getattr(rnd, k).cpu().pin_memory() for k in ("U", "h", "target", "temperature", "anchor", "sps")}
+    if rnd.gamma is not None:
+        host_in["gamma"] = rnd.gamma.cpu().pin_memory()
+    dev_in = {k: getattr(rnd, k) for k in host_in}
+    outs = [res["tokens"], res["keep"], res["accepted"], res["next_token"], res["stats"]]
+    host_out = [o.cpu().pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    n_e2e = max(3, min(args.steps, 10))
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    e_stops = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
+    torch.cuda.synchronize()
+    for s in range(n_e2e):
+        e_starts[s].record(stream)
+        for k, t in host_in.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        runner.set_round(5000 + s)
+        runner.run()
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+        e_stops[s].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_starts, e_stops))
+    clock = clocks.stop()
+
+    drafted = rnd.draft_tokens()
+    total_s = total_ms / 1e3
+    if world > 1:
+        t = torch.tensor([total_s, e2e_ms / 1e3], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s, e2e_s = float(t[0]), float(t[1])
+    else:
+        e2e_s = e2e_ms / 1e3
+    value = drafted * n_timed * world / total_s
+    e2e_value = drafted * n_e2e * world / e2e_s
+
+    peaks = measured_peaks()
+    launch_bytes = draft_stats_launch_bytes(rnd)
+    stats_mean_s = (sum(stats_ms) / len(stats_ms)) / 1e3 if stats_ms else float("nan")
+    achieved = launch_bytes / stats_mean_s / 1e9
+    src = ["speculative_decoding_draft_round_gb300/csrc/%s" % f for f in
+           (("sample_tc.cu",) if uses_tc else ("sample.cu",)) + ("common.cuh",)]
+    kname = "draft_stats_tc" if uses_tc else "draft_stats_simt"
+    traffic = profiled_traffic(kname, rnd.name, kernel_hash(src))
+    rb = round_bytes(rnd, keep_sum, n_rej)
+    round_s = total_s / n_timed
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": n_timed, "warmup": args.warmup,
+        "ms_per_step": 1e3 * round_s, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if uses_tc else "f32", "data": "synthetic",
+        "config": {"workload": rnd.name, "R": rnd.R, "gamma": rnd.gamma_max, "V": rnd.V, "r": rnd.r, "d": rnd.d,
+                   "sched_mode": {0: "sync", 1: "async_capacity", 2: "full_scan"}[rnd.mode],
+                   "path": "tensor_core" if uses_tc else "cuda_core", "parallelism": "replica x%d" % world,
+                   "l2": "flushed between steps (256 MiB write, outside the timed events)",
+                   "inputs": "resident in HBM"},
+        "rounds_per_s": world * n_timed / total_s,
+        "admitted_per_round": keep_sum,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "bytes_per_launch": launch_bytes, "launch_us": stats_mean_s * 1e6,
+                     "launches_timed": len(stats_ms), "peak_source": peaks["source"]},
+        "round_roofline": {"bytes_per_round": rb["total"], "achieved_gbs": rb["total"] / round_s / 1e9,
+                           "frac": rb["total"] / round_s / 1e9 / peaks["hbm_gbs"],
+                           "floor_us": rb["total"] / (peaks["hbm_gbs"] * 1e9) * 1e6,
+                           "bias_gemm_tflops": 2.0 * rnd.r * rnd.V * drafted / round_s / 1e12,
+                           "breakdown": rb},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": n_e2e, "note": "per-round inputs (U, h, target, T, anchor, SPS) copied in, results "
+                                        "copied out; E, W, w_h, w_e stay resident"},
+        "gpu_launches": launches,
+        "clocks": clock,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = cpu_threads()
+        ids = list(range(0, rnd.R, max(1, rnd.R // threads)))[:threads]
+        d, dt = run_oracle_round(rnd, ids, threads, 7)
+        line["cpu_baseline"] = {"value": d / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": "%d of %d requests, one whole round (sample+schedule+verify), %.1f s"
+                                          % (len(ids), rnd.R, dt)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--path", choices=["auto", "cuda_core", "tensor_core"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

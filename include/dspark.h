@@ -212,6 +212,39 @@ dspark_status dspark_verify_workspace_size(const dspark_verify_args* args, size_
 dspark_status dspark_verify(const dspark_verify_args* args, void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/*
+ * Launch accounting and timing (measurement support, not part of the method).
+ *
+ * dspark_launch_count: number of kernels this library has launched in this
+ * process (all calls, all streams).
+ *
+ * dspark_time_kernel: while enabled, every launch of kernel family `kernel`
+ * (DSPARK_KERNEL_*) records events[i].start on the call's stream just before
+ * the launch and events[i].stop just after it, for i = *count, *count+1, ...
+ * up to `capacity`; *count (a host int) is incremented per recorded pair. The
+ * events are cudaEvent_t handles created by the caller and passed as void*.
+ * kernel = -1 disables timing. The setting is process-wide and not
+ * thread-safe; it adds one event record before and after each timed launch.
+ */
+enum {
+    DSPARK_KERNEL_CONF_HIDDEN = 0,    /* w_h . h for every (request, position) */
+    DSPARK_KERNEL_DRAFT_STATS = 1,    /* bias contraction + block softmax statistics, one per draft step */
+    DSPARK_KERNEL_DRAFT_COMMIT = 2,   /* two-level draw, confidence, survival, one per draft step */
+    DSPARK_KERNEL_SCHEDULE = 3,
+    DSPARK_KERNEL_VERIFY_ROWS = 4,
+    DSPARK_KERNEL_VERIFY_DECIDE = 5,
+    DSPARK_KERNEL_RESIDUAL_STATS = 6,
+    DSPARK_KERNEL_RESIDUAL_PICK = 7
+};
+
+typedef struct {
+    void* start;   /* cudaEvent_t */
+    void* stop;    /* cudaEvent_t */
+} dspark_event_pair;
+
+uint64_t dspark_launch_count(void);
+dspark_status dspark_time_kernel(int32_t kernel, dspark_event_pair* events, int32_t capacity, int32_t* count);
+
 /* Synchronise `stream`, then return the device status word of `workspace`
  * (DSPARK_OK, DSPARK_ERR_TIMEOUT or DSPARK_ERR_DEVICE_INPUT) and clear it. */
 dspark_status dspark_check(void* workspace, void* stream);

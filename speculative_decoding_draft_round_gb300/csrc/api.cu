@@ -1,0 +1,356 @@
+// api.cu -- the C ABI of libdspark (include/dspark.h): argument validation,
+// workspace layout and the launch sequence of each call. Every step of the
+// round runs in this library's kernels; nothing here computes on the host.
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace dspark;
+
+namespace {
+
+// ------------------------------------------------------------ launch accounting
+
+std::atomic<unsigned long long> g_launches{0};
+
+struct KernelTimer {
+    int kernel = -1;
+    dspark_event_pair* events = nullptr;
+    int capacity = 0;
+    int32_t* count = nullptr;
+} g_timer;
+
+bool timing(int kernel) { return g_timer.kernel == kernel && g_timer.count && *g_timer.count < g_timer.capacity; }
+
+// Launch one kernel family through `fn`, counting it and recording the timing events if enabled.
+template <typename F>
+cudaError_t launch(int kernel, cudaStream_t s, F&& fn)
+{
+    const bool t = timing(kernel);
+    if (t) cudaEventRecord(static_cast<cudaEvent_t>(g_timer.events[*g_timer.count].start), s);
+    const cudaError_t e = fn();
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (t) {
+        cudaEventRecord(static_cast<cudaEvent_t>(g_timer.events[*g_timer.count].stop), s);
+        ++*g_timer.count;
+    }
+    return e;
+}
+
+constexpr size_t kAlign = 256;
+constexpr size_t kStatusBytes = 256;
+
+
+dspark_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA; }
+
+// ------------------------------------------------------------ sample_block
+
+struct SampleLayout {
+    size_t x_cur, hw, stats, total;
+};
+
+dspark_status check_sample(const dspark_sample_args* a)
+{
+    if (!a || a->struct_size != sizeof(dspark_sample_args)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->R < 1 || a->gamma_max < 1 || a->gamma_max > DSPARK_MAX_GAMMA) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->V < 1 || a->V > (1 << 24) || a->r < 1 || a->r > 1024 || a->d < 1) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->dtype != DSPARK_F32 && a->dtype != DSPARK_BF16) return DSPARK_ERR_INVALID_ARGUMENT;
+    if ((a->conf_token | 1) != 1 || (a->bias_first | 1) != 1) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->path < DSPARK_PATH_AUTO || a->path > DSPARK_PATH_TENSOR_CORE) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->round >= (1ull << 29)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if ((long long)a->R * a->gamma_max * a->V >= (1ll << 40)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+    if (!a->U || !a->E || !a->W || !a->h || !a->w_h || !a->w_e || !a->temperature || !a->anchor)
+        return DSPARK_ERR_INVALID_ARGUMENT;
+    if (!a->tokens || !a->conf || !a->surv || !a->draft_lse || !a->draft_logit) return DSPARK_ERR_INVALID_ARGUMENT;
+    return DSPARK_OK;
+}
+
+bool sample_uses_tc(const dspark_sample_args* a)
+{
+    if (a->path == DSPARK_PATH_CUDA_CORE) return false;
+    return tc_supported(a->dtype, a->R, a->V, a->r, a->U, a->E, a->W);
+}
+
+SampleLayout sample_layout(const dspark_sample_args* a)
+{
+    const int nblk = cdiv(a->V, kNoiseBlock);
+    const size_t rows = sample_uses_tc(a) ? tc_stats_rows(a->R) : (size_t)a->R;
+    SampleLayout L;
+    size_t o = kStatusBytes;
+    L.x_cur = o;
+    o = align_up(o + sizeof(int32_t) * a->R, kAlign);
+    L.hw = o;
+    o = align_up(o + sizeof(float) * (size_t)a->R * a->gamma_max, kAlign);
+    L.stats = o;
+    o = align_up(o + sizeof(float2) * rows * nblk, kAlign);
+    L.total = o;
+    return L;
+}
+
+// ------------------------------------------------------------ verify
+
+struct VerifyLayout {
+    size_t row_stats, lse_t, rej, res_stats, total;
+};
+
+dspark_status check_verify(const dspark_verify_args* a)
+{
+    if (!a || a->struct_size != sizeof(dspark_verify_args)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->R < 1 || a->gamma_max < 1 || a->gamma_max > DSPARK_MAX_GAMMA) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->V < 1 || a->V > (1 << 24) || a->r < 1 || a->r > 1024) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->dtype != DSPARK_F32 && a->dtype != DSPARK_BF16) return DSPARK_ERR_INVALID_ARGUMENT;
+    if ((a->bias_first | 1) != 1) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->path < DSPARK_PATH_AUTO || a->path > DSPARK_PATH_TENSOR_CORE) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->round >= (1ull << 29)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if ((long long)a->R * (a->gamma_max + 1) * a->V >= (1ll << 40)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+    if (!a->target || !a->U || !a->E || !a->W || !a->anchor || !a->tokens || !a->draft_lse || !a->draft_logit ||
+        !a->keep || !a->temperature)
+        return DSPARK_ERR_INVALID_ARGUMENT;
+    if (!a->accepted || !a->next_token || !a->resampled) return DSPARK_ERR_INVALID_ARGUMENT;
+    return DSPARK_OK;
+}
+
+bool verify_uses_tc(const dspark_verify_args* a)
+{
+    if (a->path == DSPARK_PATH_CUDA_CORE) return false;
+    return tc_supported(a->dtype, a->R, a->V, a->r, a->U, a->E, a->W);
+}
+
+VerifyLayout verify_layout(const dspark_verify_args* a)
+{
+    const int nblk = cdiv(a->V, kNoiseBlock);
+    const size_t rows = verify_uses_tc(a) ? tc_stats_rows(a->R) : (size_t)a->R;
+    VerifyLayout L;
+    size_t o = kStatusBytes;
+    L.row_stats = o;
+    o = align_up(o + sizeof(float2) * (size_t)a->R * (a->gamma_max + 1) * nblk, kAlign);
+    L.lse_t = o;
+    o = align_up(o + sizeof(float) * (size_t)a->R * (a->gamma_max + 1), kAlign);
+    L.rej = o;
+    o = align_up(o + sizeof(int32_t) * a->R, kAlign);
+    L.res_stats = o;
+    o = align_up(o + sizeof(float) * rows * nblk, kAlign);
+    L.total = o;
+    return L;
+}
+
+// ------------------------------------------------------------ schedule
+
+dspark_status check_schedule(const dspark_schedule_args* a)
+{
+    if (!a || a->struct_size != sizeof(dspark_schedule_args)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->R < 1 || a->gamma_max < 1 || a->gamma_max > DSPARK_MAX_GAMMA) return DSPARK_ERR_INVALID_ARGUMENT;
+    if ((long long)a->R * a->gamma_max > DSPARK_MAX_SLOTS) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+    if (a->mode < DSPARK_SCHED_SYNC || a->mode > DSPARK_SCHED_FULL_SCAN) return DSPARK_ERR_INVALID_ARGUMENT;
+    if ((long long)a->n_sps < (long long)a->R * (1 + a->gamma_max)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (!a->surv || !a->sps || !a->keep || !a->stats) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->mode == DSPARK_SCHED_ASYNC_CAPACITY && !a->surv_capacity) return DSPARK_ERR_INVALID_ARGUMENT;
+    return DSPARK_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off)
+{
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dspark_abi_version(void) { return DSPARK_ABI_VERSION; }
+
+const char* dspark_status_string(dspark_status s)
+{
+    switch (s) {
+    case DSPARK_OK: return "ok";
+    case DSPARK_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case DSPARK_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case DSPARK_ERR_WORKSPACE: return "workspace missing or too small";
+    case DSPARK_ERR_CUDA: return "CUDA error";
+    case DSPARK_ERR_TIMEOUT: return "bounded device wait ran out";
+    case DSPARK_ERR_DEVICE_INPUT: return "out-of-range device input (clamped)";
+    default: return "unknown status";
+    }
+}
+
+dspark_status dspark_sample_workspace_size(const dspark_sample_args* a, size_t* bytes)
+{
+    const dspark_status st = check_sample(a);
+    if (st != DSPARK_OK) return st;
+    if (!bytes) return DSPARK_ERR_INVALID_ARGUMENT;
+    *bytes = sample_layout(a).total;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t ws_bytes, void* stream)
+{
+    dspark_status st = check_sample(a);
+    if (st != DSPARK_OK) return st;
+    if (a->path == DSPARK_PATH_TENSOR_CORE && !sample_uses_tc(a)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+    const SampleLayout L = sample_layout(a);
+    if (!ws || ws_bytes < L.total) return DSPARK_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DraftStep p;
+    memset(&p, 0, sizeof p);
+    p.R = a->R;
+    p.G = a->gamma_max;
+    p.V = a->V;
+    p.r = a->r;
+    p.d = a->d;
+    p.nblk = cdiv(a->V, kNoiseBlock);
+    p.dtype = a->dtype;
+    p.conf_token = a->conf_token;
+    p.bias_first = a->bias_first;
+    p.gamma = a->gamma;
+    p.U = a->U;
+    p.E = a->E;
+    p.W = a->W;
+    p.h = a->h;
+    p.w_h = a->w_h;
+    p.w_e = a->w_e;
+    p.b = a->b;
+    p.temperature = a->temperature;
+    p.anchor = a->anchor;
+    p.seed = a->seed;
+    p.round = a->round;
+    p.tokens = a->tokens;
+    p.conf = a->conf;
+    p.surv = a->surv;
+    p.draft_lse = a->draft_lse;
+    p.draft_logit = a->draft_logit;
+    p.status = at<int>(ws, 0);
+    p.x_cur = at<int32_t>(ws, L.x_cur);
+    p.hw = at<float>(ws, L.hw);
+    p.stats = at<float2>(ws, L.stats);
+    const bool tc = sample_uses_tc(a);
+    cudaError_t e = launch(DSPARK_KERNEL_CONF_HIDDEN, s, [&] { return launch_conf_hidden(p, s); });
+    for (int k = 0; k < a->gamma_max && e == cudaSuccess; ++k) {
+        p.k = k;
+        e = launch(DSPARK_KERNEL_DRAFT_STATS, s,
+                   [&] { return tc ? launch_draft_stats_tc(p, s) : launch_draft_stats_simt(p, s); });
+        if (e == cudaSuccess) e = launch(DSPARK_KERNEL_DRAFT_COMMIT, s, [&] { return launch_draft_commit(p, s); });
+    }
+    return cuda_status(e);
+}
+
+dspark_status dspark_schedule_workspace_size(const dspark_schedule_args* a, size_t* bytes)
+{
+    const dspark_status st = check_schedule(a);
+    if (st != DSPARK_OK) return st;
+    if (!bytes) return DSPARK_ERR_INVALID_ARGUMENT;
+    *bytes = kStatusBytes;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_schedule(const dspark_schedule_args* a, void* ws, size_t ws_bytes, void* stream)
+{
+    const dspark_status st = check_schedule(a);
+    if (st != DSPARK_OK) return st;
+    if (!ws || ws_bytes < kStatusBytes) return DSPARK_ERR_WORKSPACE;
+    ScheduleParams p;
+    p.R = a->R;
+    p.G = a->gamma_max;
+    p.mode = a->mode;
+    p.n_sps = a->n_sps;
+    p.gamma = a->gamma;
+    p.surv = a->surv;
+    p.surv_capacity = a->surv_capacity;
+    p.sps = a->sps;
+    p.keep = a->keep;
+    p.stats = a->stats;
+    p.status = at<int>(ws, 0);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(launch(DSPARK_KERNEL_SCHEDULE, s, [&] { return launch_schedule(p, s); }));
+}
+
+dspark_status dspark_verify_workspace_size(const dspark_verify_args* a, size_t* bytes)
+{
+    const dspark_status st = check_verify(a);
+    if (st != DSPARK_OK) return st;
+    if (!bytes) return DSPARK_ERR_INVALID_ARGUMENT;
+    *bytes = verify_layout(a).total;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_verify(const dspark_verify_args* a, void* ws, size_t ws_bytes, void* stream)
+{
+    const dspark_status st = check_verify(a);
+    if (st != DSPARK_OK) return st;
+    if (a->path == DSPARK_PATH_TENSOR_CORE && !verify_uses_tc(a)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+    const VerifyLayout L = verify_layout(a);
+    if (!ws || ws_bytes < L.total) return DSPARK_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    VerifyParams p;
+    memset(&p, 0, sizeof p);
+    p.R = a->R;
+    p.G = a->gamma_max;
+    p.V = a->V;
+    p.r = a->r;
+    p.nblk = cdiv(a->V, kNoiseBlock);
+    p.dtype = a->dtype;
+    p.bias_first = a->bias_first;
+    p.gamma = a->gamma;
+    p.target = a->target;
+    p.U = a->U;
+    p.E = a->E;
+    p.W = a->W;
+    p.anchor = a->anchor;
+    p.tokens = a->tokens;
+    p.draft_lse = a->draft_lse;
+    p.draft_logit = a->draft_logit;
+    p.keep = a->keep;
+    p.temperature = a->temperature;
+    p.seed = a->seed;
+    p.round = a->round;
+    p.accepted = a->accepted;
+    p.next_token = a->next_token;
+    p.resampled = a->resampled;
+    p.status = at<int>(ws, 0);
+    p.row_stats = at<float2>(ws, L.row_stats);
+    p.lse_t = at<float>(ws, L.lse_t);
+    p.rej = at<int32_t>(ws, L.rej);
+    p.res_stats = at<float>(ws, L.res_stats);
+    const bool tc = verify_uses_tc(a);
+    cudaError_t e = launch(DSPARK_KERNEL_VERIFY_ROWS, s, [&] { return launch_verify_rows(p, s); });
+    if (e == cudaSuccess) e = launch(DSPARK_KERNEL_VERIFY_DECIDE, s, [&] { return launch_verify_decide(p, s); });
+    if (e == cudaSuccess)
+        e = launch(DSPARK_KERNEL_RESIDUAL_STATS, s,
+                   [&] { return tc ? launch_residual_stats_tc(p, s) : launch_residual_stats_simt(p, s); });
+    if (e == cudaSuccess) e = launch(DSPARK_KERNEL_RESIDUAL_PICK, s, [&] { return launch_residual_pick(p, s); });
+    return cuda_status(e);
+}
+
+uint64_t dspark_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+dspark_status dspark_time_kernel(int32_t kernel, dspark_event_pair* events, int32_t capacity, int32_t* count)
+{
+    if (kernel < 0) {
+        g_timer = KernelTimer();
+        return DSPARK_OK;
+    }
+    if (kernel > DSPARK_KERNEL_RESIDUAL_PICK || !events || capacity < 0 || !count) return DSPARK_ERR_INVALID_ARGUMENT;
+    g_timer.kernel = kernel;
+    g_timer.events = events;
+    g_timer.capacity = capacity;
+    g_timer.count = count;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_check(void* ws, void* stream)
+{
+    if (!ws) return DSPARK_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, ws, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    return h;
+}
+
+}  // extern "C"

@@ -1,0 +1,217 @@
+// common.cuh -- device helpers shared by the libdspark kernels.
+//
+// Random numbers follow the counter-based generator stated in dspark.h:
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy
+// as 1, 2, 3", SC'11), key = (seed lo, seed hi), counter =
+// (e>>2, position, request, (round<<3)|purpose), word e&3,
+// u = (2*(x>>9)+1) * 2^-24, Gumbel noise -log(-log u).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+constexpr int kNoiseBlock = DSPARK_NOISE_BLOCK;   // vocabulary block of the two-level Gumbel-max
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// random purposes (low 3 bits of counter word 3)
+enum Purpose : uint32_t {
+    kDraftElem = 0,    // element-level Gumbel of a draft draw
+    kAccept = 1,       // acceptance uniform
+    kFinalElem = 2,    // element-level Gumbel of the residual / bonus draw
+    kDraftBlock = 3,   // block-level Gumbel of a draft draw
+    kFinalBlock = 4    // block-level Gumbel of the residual / bonus draw
+};
+
+struct PhiloxKey {
+    uint32_t k0, k1;
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key)
+{
+    uint32_t k0 = key.k0, k1 = key.k1;
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+__device__ __forceinline__ float bits_to_uniform(uint32_t x)
+{
+    // (x>>9) + 1/2 in units of 2^-23: exact in binary32 (24 significant bits)
+    return __fmaf_rn((float)(x >> 9), 0x1.0p-23f, 0x1.0p-24f);
+}
+
+__device__ __forceinline__ uint32_t counter_word3(uint64_t round, uint32_t purpose)
+{
+    return (uint32_t)(round << 3) | purpose;
+}
+
+// one uniform for element e of (purpose, request, position)
+__device__ __forceinline__ float uniform_at(PhiloxKey key, uint64_t round, uint32_t purpose, uint32_t req,
+                                            uint32_t pos, uint32_t e)
+{
+    const uint4 w = philox4x32_10(make_uint4(e >> 2, pos, req, counter_word3(round, purpose)), key);
+    const uint32_t sel = e & 3u;
+    const uint32_t x = sel == 0 ? w.x : sel == 1 ? w.y : sel == 2 ? w.z : w.w;
+    return bits_to_uniform(x);
+}
+
+__device__ __forceinline__ float gumbel_at(PhiloxKey key, uint64_t round, uint32_t purpose, uint32_t req,
+                                           uint32_t pos, uint32_t e)
+{
+    return -logf(-logf(uniform_at(key, round, purpose, req, pos, e)));
+}
+
+__host__ __device__ inline PhiloxKey make_key(uint64_t seed)
+{
+    return PhiloxKey{(uint32_t)seed, (uint32_t)(seed >> 32)};
+}
+
+// ------------------------------------------------------------------ element loads
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ float ld(const T* p, size_t i) { return to_f32<T>(p[i]); }
+
+// ------------------------------------------------------------------ status word
+
+__device__ __forceinline__ void raise_status(int* status, int code)
+{
+    if (status) atomicCAS(status, 0, code);
+}
+
+// clamp a device-supplied index into [0, n) and flag an out-of-range value
+__device__ __forceinline__ int checked_index(int x, int n, int* status)
+{
+    if (x < 0 || x >= n) {
+        raise_status(status, DSPARK_ERR_DEVICE_INPUT);
+        return x < 0 ? 0 : n - 1;
+    }
+    return x;
+}
+
+// ------------------------------------------------------------------ reductions
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ int warp_min_int(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// (value, index) arg-max: larger value wins, lower index on ties; NaN never wins
+struct ArgMax {
+    float v;
+    int i;
+};
+
+__device__ __forceinline__ ArgMax argmax_better(ArgMax a, ArgMax b)
+{
+    if (b.i < 0) return a;
+    if (a.i < 0) return b;
+    if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+    return a;
+}
+
+__device__ __forceinline__ ArgMax warp_argmax(ArgMax a)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ArgMax b{__shfl_xor_sync(0xffffffffu, a.v, o), __shfl_xor_sync(0xffffffffu, a.i, o)};
+        a = argmax_better(a, b);
+    }
+    return a;
+}
+
+// block-wide reductions for a block of NT threads (NT multiple of 32, <= 1024)
+template <int NT>
+__device__ __forceinline__ float block_max(float v, float* scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_max(v);
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    float r = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) r = fmaxf(r, scratch[w]);
+    return r;
+}
+
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float* scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    float r = 0.f;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) r += scratch[w];
+    return r;
+}
+
+template <int NT>
+__device__ __forceinline__ ArgMax block_argmax(ArgMax a, float* sv, int* si)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    a = warp_argmax(a);
+    __syncthreads();
+    if (lane == 0) {
+        sv[warp] = a.v;
+        si[warp] = a.i;
+    }
+    __syncthreads();
+    ArgMax r{-INFINITY, -1};
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) r = argmax_better(r, ArgMax{sv[w], si[w]});
+    return r;
+}
+
+template <int NT>
+__device__ __forceinline__ int block_min_int(int v, int* scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_min_int(v);
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    int r = INT32_MAX;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) r = min(r, scratch[w]);
+    return r;
+}
+
+}  // namespace dspark

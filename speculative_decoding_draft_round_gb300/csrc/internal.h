@@ -1,0 +1,102 @@
+// internal.h -- parameter blocks and launchers shared between the libdspark
+// translation units (host side). Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+// One serial step of the draft sampler (dspark_sample_block).
+struct DraftStep {
+    int R, G, V, r, d, k, nblk;
+    int dtype, conf_token, bias_first;
+    const int32_t* gamma;
+    const void* U;
+    const void* E;
+    const void* W;
+    const void* h;
+    const float* w_h;
+    const float* w_e;
+    float b;
+    const float* temperature;
+    const int32_t* anchor;
+    uint64_t seed, round;
+    int32_t* tokens;
+    float* conf;
+    float* surv;
+    float* draft_lse;
+    float* draft_logit;
+    // workspace
+    int* status;
+    int32_t* x_cur;      // [R] token committed at the previous step
+    float* hw;           // [R][G] w_h . h[r][k]
+    float2* stats;       // [R_pad][nblk] (max, sum) of exp2 over each vocabulary block, log2 units
+};
+
+// Verification (dspark_verify).
+struct VerifyParams {
+    int R, G, V, r, nblk;
+    int dtype, bias_first;
+    const int32_t* gamma;
+    const void* target;
+    const void* U;
+    const void* E;
+    const void* W;
+    const int32_t* anchor;
+    const int32_t* tokens;
+    const float* draft_lse;
+    const float* draft_logit;
+    const int32_t* keep;
+    const float* temperature;
+    uint64_t seed, round;
+    int32_t* accepted;
+    int32_t* next_token;
+    uint8_t* resampled;
+    // workspace
+    int* status;
+    float2* row_stats;   // [R][G+1][nblk] block (max, sum) of the target rows, log2 units
+    float* lse_t;        // [R][G+1]
+    int32_t* rej;        // [R] rejected position, -1 if every admitted token was accepted
+    float* res_stats;    // [R_pad][nblk] block sums of max(0, p_t - p_d)
+};
+
+struct ScheduleParams {
+    int R, G, mode, n_sps;
+    const int32_t* gamma;
+    const float* surv;
+    const float* surv_capacity;
+    const float* sps;
+    int32_t* keep;
+    dspark_schedule_stats* stats;
+    int* status;
+};
+
+// sample.cu
+cudaError_t launch_conf_hidden(const DraftStep& p, cudaStream_t s);
+cudaError_t launch_draft_stats_simt(const DraftStep& p, cudaStream_t s);
+cudaError_t launch_draft_commit(const DraftStep& p, cudaStream_t s);
+
+// sample_tc.cu
+bool tc_supported(int dtype, int R, int V, int r, const void* U, const void* E, const void* W);
+size_t tc_stats_rows(int R);  // rows of the block-statistics workspace the tensor-core path writes
+cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s);
+cudaError_t launch_residual_stats_tc(const VerifyParams& p, cudaStream_t s);
+
+// verify.cu
+cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_verify_decide(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_residual_stats_simt(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_residual_pick(const VerifyParams& p, cudaStream_t s);
+
+// schedule.cu
+size_t schedule_smem_bytes();
+cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
+
+inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace dspark

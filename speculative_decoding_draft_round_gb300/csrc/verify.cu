@@ -1,0 +1,349 @@
+// verify.cu -- lossless rejection-sampling verification of the admitted prefixes.
+//
+// "DSpark" dspark_cycle steps 5-6 (caijizhuo.github.io, section 4) with the
+// standard accept rule min(1, p_t/p_d) and residual norm(max(0, p_t - p_d))
+// (Leviathan et al. 2023; zhongzhuzhou.org notes, eq. 8a). Target row i is the
+// target's distribution for draft position i; row keep[r] supplies the bonus.
+// Launches:
+//   verify_rows      -- per (request, row i <= keep, vocabulary chunk): block
+//                       (max, sum exp2) of target/T, one warp per 128-block.
+//   verify_decide    -- per request: target log-normalisers, accept tests,
+//                       first rejection; bonus draw when nothing was rejected.
+//   residual_stats   -- per (rejecting request, vocabulary block): p_d
+//                       recomputed with the Markov bias of the rejected
+//                       position, block sums of max(0, p_t - p_d).
+//   residual_pick    -- per rejecting request: two-level Gumbel-max over the
+//                       residual (p_t of the same row if the residual is zero).
+#include "common.cuh"
+#include "internal.h"
+
+namespace dspark {
+
+__device__ __forceinline__ int request_gamma(const VerifyParams& p, int q)
+{
+    int g = p.gamma ? p.gamma[q] : p.G;
+    if (g < 0 || g > p.G) {
+        raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+        g = g < 0 ? 0 : p.G;
+    }
+    return g;
+}
+
+__device__ __forceinline__ int request_keep(const VerifyParams& p, int q)
+{
+    const int g = request_gamma(p, q);
+    int ell = p.keep[q];
+    if (ell < 0 || ell > g) {
+        raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+        ell = ell < 0 ? 0 : g;
+    }
+    return ell;
+}
+
+// ----------------------------------------------------------------- target row statistics
+
+constexpr int kRowWarps = 8;
+constexpr int kRowBlocksPerWarp = 4;
+
+template <typename T>
+__global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParams p)
+{
+    const int q = blockIdx.z, i = blockIdx.y;
+    const int ell = request_keep(p, q);
+    if (i > ell) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float scale = kLog2e / p.temperature[q];
+    const T* row = static_cast<const T*>(p.target) + ((size_t)q * (p.G + 1) + i) * p.V;
+    float2* out = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
+    const int b0 = (blockIdx.x * kRowWarps + warp) * kRowBlocksPerWarp;
+    for (int bb = 0; bb < kRowBlocksPerWarp; ++bb) {
+        const int b = b0 + bb;
+        if (b >= p.nblk) break;
+        float x[kNoiseBlock / 32];
+        float m = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < kNoiseBlock / 32; ++e) {
+            const int v = b * kNoiseBlock + e * 32 + lane;
+            x[e] = v < p.V ? ld(row, v) * scale : -INFINITY;
+            m = fmaxf(m, x[e]);
+        }
+        m = warp_max(m);
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < kNoiseBlock / 32; ++e) s += exp2f(x[e] - m);
+        s = warp_sum(s);
+        if (lane == 0) out[b] = make_float2(m, s);
+    }
+}
+
+// ----------------------------------------------------------------- accept tests and bonus
+
+constexpr int kDecideThreads = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyParams p)
+{
+    __shared__ float red[8];
+    __shared__ float sv[8];
+    __shared__ int si[8];
+    __shared__ float lse_s[DSPARK_MAX_GAMMA + 1];
+    const int q = blockIdx.x, t = threadIdx.x;
+    const int ell = request_keep(p, q);
+    const float invT = 1.f / p.temperature[q];
+    const T* target = static_cast<const T*>(p.target);
+
+    // log-normalisers of target rows 0..ell (natural log)
+    for (int i = 0; i <= ell; ++i) {
+        const float2* st = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
+        float lm = -INFINITY;
+        for (int b = t; b < p.nblk; b += kDecideThreads) lm = fmaxf(lm, st[b].x + log2f(st[b].y));
+        lm = block_max<kDecideThreads>(lm, red);
+        float acc = 0.f;
+        for (int b = t; b < p.nblk; b += kDecideThreads) acc += exp2f(st[b].x - lm) * st[b].y;
+        acc = block_sum<kDecideThreads>(acc, red);
+        if (t == 0) {
+            lse_s[i] = (lm + log2f(acc)) * kLn2;
+            p.lse_t[(size_t)q * (p.G + 1) + i] = lse_s[i];
+        }
+    }
+    __syncthreads();
+
+    // accept x_j with probability min(1, p_t / p_d): log u < log p_t(x) - log p_d(x)
+    const PhiloxKey key = make_key(p.seed);
+    int first_reject = ell;
+    for (int j = t; j < ell; j += kDecideThreads) {
+        const size_t o = (size_t)q * p.G + j;
+        const int x = checked_index(p.tokens[o], p.V, p.status);
+        const float zt = ld(target, ((size_t)q * (p.G + 1) + j) * p.V + x) * invT;
+        const float log_pt = zt - lse_s[j];
+        const float log_pd = p.draft_logit[o] - p.draft_lse[o];
+        const float u = uniform_at(key, p.round, kAccept, (uint32_t)q, (uint32_t)j, 0u);
+        if (!(logf(u) < log_pt - log_pd)) first_reject = min(first_reject, j);
+    }
+    const int n = block_min_int<kDecideThreads>(first_reject, si);
+    if (t == 0) {
+        p.accepted[q] = n;
+        p.rej[q] = n < ell ? n : -1;
+    }
+    if (n < ell) return;   // residual draw happens in residual_pick
+
+    // bonus token from target row ell: two-level Gumbel-max over z_t / T
+    const float2* st = p.row_stats + ((size_t)q * (p.G + 1) + ell) * p.nblk;
+    ArgMax best{-INFINITY, -1};
+    for (int b = t; b < p.nblk; b += kDecideThreads) {
+        const float z = (st[b].x + log2f(st[b].y)) * kLn2 + gumbel_at(key, p.round, kFinalBlock, (uint32_t)q, 0u, (uint32_t)b);
+        best = argmax_better(best, ArgMax{z, b});
+    }
+    best = block_argmax<kDecideThreads>(best, sv, si);
+    const int bstar = best.i < 0 ? 0 : best.i;
+    const int v = bstar * kNoiseBlock + t;
+    ArgMax cand{-INFINITY, -1};
+    if (v < p.V) {
+        const float zt = ld(target, ((size_t)q * (p.G + 1) + ell) * p.V + v) * invT;
+        cand = ArgMax{zt + gumbel_at(key, p.round, kFinalElem, (uint32_t)q, 0u, (uint32_t)v), v};
+    }
+    const ArgMax win = block_argmax<kDecideThreads>(cand, sv, si);
+    if (t == 0) {
+        int tok = win.i;
+        if (tok < 0) {
+            raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+            tok = min(bstar * kNoiseBlock, p.V - 1);
+        }
+        p.next_token[q] = tok;
+        p.resampled[q] = 0;
+    }
+}
+
+// ----------------------------------------------------------------- residual block sums (CUDA cores)
+
+constexpr int kResReq = 8;
+
+struct ResRequest {
+    int active, n, prev, use_bias;
+    float invT, lse_d, lse_t;
+};
+
+__device__ __forceinline__ ResRequest residual_request(const VerifyParams& p, int q)
+{
+    ResRequest s{0, 0, 0, 0, 0.f, 0.f, 0.f};
+    if (q >= p.R) return s;
+    const int n = p.rej[q];
+    if (n < 0) return s;
+    s.active = 1;
+    s.n = n;
+    s.prev = checked_index(n == 0 ? p.anchor[q] : p.tokens[(size_t)q * p.G + n - 1], p.V, p.status);
+    s.use_bias = (n > 0) || p.bias_first;
+    s.invT = 1.f / p.temperature[q];
+    s.lse_d = p.draft_lse[(size_t)q * p.G + n];
+    s.lse_t = p.lse_t[(size_t)q * (p.G + 1) + n];
+    return s;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kNoiseBlock) residual_stats_simt_kernel(VerifyParams p)
+{
+    extern __shared__ float es[];   // [kResReq][r]
+    __shared__ ResRequest req[kResReq];
+    __shared__ float red[8];
+    const int b = blockIdx.x, q0 = blockIdx.y * kResReq, t = threadIdx.x;
+    if (t < kResReq) req[t] = residual_request(p, q0 + t);
+    __syncthreads();
+    bool any = false;
+#pragma unroll
+    for (int j = 0; j < kResReq; ++j) any |= req[j].active != 0;
+    if (!any) return;
+    const T* E = static_cast<const T*>(p.E);
+    const T* W = static_cast<const T*>(p.W);
+    for (int i = t; i < kResReq * p.r; i += blockDim.x) {
+        const int j = i / p.r, c = i % p.r;
+        es[i] = (req[j].active && req[j].use_bias) ? ld(E, (size_t)req[j].prev * p.r + c) : 0.f;
+    }
+    __syncthreads();
+    const int v = b * kNoiseBlock + t;
+    float acc[kResReq];
+#pragma unroll
+    for (int j = 0; j < kResReq; ++j) acc[j] = 0.f;
+    if (v < p.V) {
+        for (int i = 0; i < p.r; ++i) {
+            const float w = ld(W, (size_t)i * p.V + v);
+#pragma unroll
+            for (int j = 0; j < kResReq; ++j) acc[j] = fmaf(es[j * p.r + i], w, acc[j]);
+        }
+    }
+    const T* U = static_cast<const T*>(p.U);
+    const T* target = static_cast<const T*>(p.target);
+#pragma unroll 1
+    for (int j = 0; j < kResReq; ++j) {
+        if (!req[j].active) continue;
+        const int q = q0 + j;
+        float res = 0.f;
+        if (v < p.V) {
+            const float ldv = (ld(U, ((size_t)q * p.G + req[j].n) * p.V + v) + acc[j]) * req[j].invT;
+            const float pd = expf(ldv - req[j].lse_d);
+            const float zt = ld(target, ((size_t)q * (p.G + 1) + req[j].n) * p.V + v) * req[j].invT;
+            const float pt = expf(zt - req[j].lse_t);
+            res = fmaxf(pt - pd, 0.f);
+        }
+        const float s = block_sum<kNoiseBlock>(res, red);
+        if (t == 0) p.res_stats[(size_t)q * p.nblk + b] = s;
+    }
+}
+
+// ----------------------------------------------------------------- residual draw
+
+template <typename T>
+__global__ void __launch_bounds__(kNoiseBlock) residual_pick_kernel(VerifyParams p)
+{
+    extern __shared__ float erow[];   // [r]
+    __shared__ float sv[8];
+    __shared__ int si[8];
+    __shared__ float red[8];
+    const int q = blockIdx.x, t = threadIdx.x;
+    const ResRequest rq = residual_request(p, q);
+    if (!rq.active) return;
+    const PhiloxKey key = make_key(p.seed);
+    const float* rs = p.res_stats + (size_t)q * p.nblk;
+    const float2* st = p.row_stats + ((size_t)q * (p.G + 1) + rq.n) * p.nblk;
+    // residual mass anywhere?
+    float tot = 0.f;
+    for (int b = t; b < p.nblk; b += kNoiseBlock) tot += rs[b];
+    tot = block_sum<kNoiseBlock>(tot, red);
+    const bool fallback = !(tot > 0.f);   // residual zero through rounding: draw from p_t of the row
+    ArgMax best{-INFINITY, -1};
+    for (int b = t; b < p.nblk; b += kNoiseBlock) {
+        float L;
+        if (fallback) {
+            L = (st[b].x + log2f(st[b].y)) * kLn2;
+        } else {
+            if (!(rs[b] > 0.f)) continue;
+            L = logf(rs[b]);
+        }
+        const float z = L + gumbel_at(key, p.round, kFinalBlock, (uint32_t)q, 0u, (uint32_t)b);
+        best = argmax_better(best, ArgMax{z, b});
+    }
+    best = block_argmax<kNoiseBlock>(best, sv, si);
+    const int bstar = best.i < 0 ? 0 : best.i;
+    const T* E = static_cast<const T*>(p.E);
+    const T* W = static_cast<const T*>(p.W);
+    for (int i = t; i < p.r; i += kNoiseBlock) erow[i] = rq.use_bias ? ld(E, (size_t)rq.prev * p.r + i) : 0.f;
+    __syncthreads();
+    const int v = bstar * kNoiseBlock + t;
+    ArgMax cand{-INFINITY, -1};
+    if (v < p.V) {
+        const T* target = static_cast<const T*>(p.target);
+        const float zt = ld(target, ((size_t)q * (p.G + 1) + rq.n) * p.V + v) * rq.invT;
+        float L = -INFINITY;
+        if (fallback) {
+            L = zt;
+        } else {
+            float bias = 0.f;
+            if (rq.use_bias)
+                for (int i = 0; i < p.r; ++i) bias = fmaf(erow[i], ld(W, (size_t)i * p.V + v), bias);
+            const T* U = static_cast<const T*>(p.U);
+            const float ldv = (ld(U, ((size_t)q * p.G + rq.n) * p.V + v) + bias) * rq.invT;
+            const float res = expf(zt - rq.lse_t) - expf(ldv - rq.lse_d);
+            if (res > 0.f) L = logf(res);
+        }
+        if (L > -INFINITY) cand = ArgMax{L + gumbel_at(key, p.round, kFinalElem, (uint32_t)q, 0u, (uint32_t)v), v};
+    }
+    const ArgMax win = block_argmax<kNoiseBlock>(cand, sv, si);
+    if (t == 0) {
+        int tok = win.i;
+        if (tok < 0) {
+            raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+            tok = min(bstar * kNoiseBlock, p.V - 1);
+        }
+        p.next_token[q] = tok;
+        p.resampled[q] = 1;
+    }
+}
+
+// ----------------------------------------------------------------- launchers
+
+cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s)
+{
+    const int per_cta = kRowWarps * kRowBlocksPerWarp;
+    const dim3 grid(cdiv(p.nblk, per_cta), p.G + 1, p.R);
+    if (p.dtype == DSPARK_BF16)
+        verify_rows_kernel<__nv_bfloat16><<<grid, kRowWarps * 32, 0, s>>>(p);
+    else
+        verify_rows_kernel<float><<<grid, kRowWarps * 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify_decide(const VerifyParams& p, cudaStream_t s)
+{
+    if (p.dtype == DSPARK_BF16)
+        verify_decide_kernel<__nv_bfloat16><<<p.R, kDecideThreads, 0, s>>>(p);
+    else
+        verify_decide_kernel<float><<<p.R, kDecideThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_residual_stats_simt(const VerifyParams& p, cudaStream_t s)
+{
+    const dim3 grid(p.nblk, cdiv(p.R, kResReq));
+    const size_t smem = (size_t)kResReq * p.r * sizeof(float);
+    if (p.dtype == DSPARK_BF16) {
+        cudaFuncSetAttribute(residual_stats_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        residual_stats_simt_kernel<__nv_bfloat16><<<grid, kNoiseBlock, smem, s>>>(p);
+    } else {
+        cudaFuncSetAttribute(residual_stats_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        residual_stats_simt_kernel<float><<<grid, kNoiseBlock, smem, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_residual_pick(const VerifyParams& p, cudaStream_t s)
+{
+    const size_t smem = (size_t)p.r * sizeof(float);
+    if (p.dtype == DSPARK_BF16)
+        residual_pick_kernel<__nv_bfloat16><<<p.R, kNoiseBlock, smem, s>>>(p);
+    else
+        residual_pick_kernel<float><<<p.R, kNoiseBlock, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

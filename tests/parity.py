@@ -1,0 +1,121 @@
+"""Helpers shared by the GPU parity tests: move workload tensors to numpy for
+the oracle and compare the CUDA results with the oracle stage by stage.
+
+Stage-wise parity feeds each oracle stage the GPU's own upstream outputs
+(draft tokens for the sampler's later positions, GPU survivals for the
+scheduler, GPU tokens / log-normalisers / keep lengths for the verifier).
+Integer decisions must then agree exactly, except where the oracle's own
+floating-point margin is below the stated tolerance:
+  - a draw whose top-two perturbed values (block level or element level)
+    differ by < 1e-4 (plus, for a residual draw, the fp32 error bound of the
+    residual mass);
+  - an accept test with |log u - log(p_t/p_d)| < 1e-4;
+  - a scheduler decision whose relative Theta margin is <= 1e-12.
+Excusals are counted and returned."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+TOK_TOL = 1e-4      # top-two gap below which a draw is excused
+ACC_TOL = 1e-4      # accept-test margin below which a decision is excused
+THETA_TOL = 1e-12   # relative Theta margin below which a scheduler decision is excused
+CONF_TOL = 1e-5     # c_k and a_k, absolute
+LSE_TOL = 1e-5      # log-normalisers and logits, relative to max(1, |value|)
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def rows(t: torch.Tensor, ids) -> np.ndarray:
+    idx = torch.as_tensor(np.asarray(ids), dtype=torch.long, device=t.device)
+    return to_np(t.index_select(0, idx))
+
+
+def check_sample(rnd, out, ids, threads=8):
+    """Compare dspark_sample_block outputs with the oracle on requests `ids`."""
+    ids = np.asarray(ids)
+    tok = to_np(out["tokens"])[ids]
+    gamma = None if rnd.gamma is None else to_np(rnd.gamma)[ids]
+    o = oracle.sample_block(rows(rnd.U, ids), to_np(rnd.E), to_np(rnd.W), rows(rnd.h, ids), to_np(rnd.w_h),
+                            to_np(rnd.w_e), rnd.b, to_np(rnd.temperature)[ids], to_np(rnd.anchor)[ids],
+                            rnd.seed, rnd.round, gamma=gamma, req_ids=ids, conf_token=rnd.conf_token,
+                            bias_first=rnd.bias_first, forced_tokens=np.where(tok < 0, 0, tok),
+                            threads=threads)
+    G = rnd.gamma_max
+    g = np.full(len(ids), G) if gamma is None else gamma
+    active = np.arange(G)[None, :] < g[:, None]
+    assert np.all(tok[~active] == -1)
+    mism = (tok != o["tokens"]) & active
+    excused = mism & ((o["gap1"] < TOK_TOL) | (o["gap2"] < TOK_TOL))
+    bad = mism & ~excused
+    assert not bad.any(), "token mismatch at %s (gpu %s oracle %s gaps %s %s)" % (
+        np.argwhere(bad)[:5].tolist(), tok[bad][:5], o["tokens"][bad][:5], o["gap1"][bad][:5], o["gap2"][bad][:5])
+    for key, okey, tol, rel in (("conf", "conf", CONF_TOL, False), ("surv", "surv", CONF_TOL, False),
+                                ("draft_lse", "lse", LSE_TOL, True), ("draft_logit", "logit", LSE_TOL, True)):
+        g_ = to_np(out[key])[ids].astype(np.float64)
+        err = np.abs(g_ - o[okey])
+        lim = tol * (np.maximum(1.0, np.abs(o[okey])) if rel else 1.0)
+        worst = np.max(np.where(active, err - lim, -1.0))
+        assert worst <= 0, "%s differs by %.3g (limit %.3g)" % (key, np.max(np.where(active, err, 0)), tol)
+    return int(excused.sum())
+
+
+def check_schedule(surv, sps, mode, out, *, gamma=None, surv_capacity=None):
+    """Compare dspark_schedule on GPU survivals with the oracle."""
+    import speculative_decoding_draft_round_gb300 as ds
+    s = to_np(surv).astype(np.float64)
+    gam = None if gamma is None else to_np(gamma)
+    cap = None if surv_capacity is None else to_np(surv_capacity).astype(np.float64)
+    o = oracle.schedule(s, to_np(sps).astype(np.float64), mode, gamma=gam, surv_capacity=cap)
+    keep = to_np(out["keep"])
+    st = ds.decode_stats(out["stats"])
+    if o["min_margin"] <= THETA_TOL:
+        return 1
+    assert keep.tolist() == o["keep"].tolist(), "keep differs: gpu %s oracle %s" % (
+        keep[keep != o["keep"]][:8], o["keep"][keep != o["keep"]][:8])
+    assert st["admitted"] == int(o["admitted"])
+    assert st["pool"] == int(o["pool"])
+    assert st["batch"] == s.shape[0] + int(o["admitted"])
+    assert st["capacity"] == int(o["capacity"])
+    assert abs(st["theta_best"] - o["theta_best"]) <= 1e-9 * abs(o["theta_best"])
+    return 0
+
+
+def check_verify(rnd, sout, keep, vout, ids, threads=8):
+    """Compare dspark_verify with the oracle on requests `ids`, fed the GPU's draft outputs."""
+    ids = np.asarray(ids)
+    gamma = None if rnd.gamma is None else to_np(rnd.gamma)[ids]
+    tok = to_np(sout["tokens"])[ids]
+    kp = to_np(keep)[ids]
+    o = oracle.verify(rows(rnd.target, ids), rows(rnd.U, ids), to_np(rnd.E), to_np(rnd.W),
+                      to_np(rnd.anchor)[ids], np.where(tok < 0, 0, tok),
+                      to_np(sout["draft_lse"])[ids].astype(np.float64),
+                      to_np(sout["draft_logit"])[ids].astype(np.float64), kp, to_np(rnd.temperature)[ids],
+                      rnd.seed, rnd.round, gamma=gamma, req_ids=ids, bias_first=rnd.bias_first, threads=threads)
+    acc = to_np(vout["accepted"])[ids]
+    nxt = to_np(vout["next_token"])[ids]
+    res = to_np(vout["resampled"])[ids]
+    n_exc = 0
+    for i in range(len(ids)):
+        a_o = int(o["accepted"][i])
+        if acc[i] != a_o:
+            j = min(acc[i], a_o)
+            assert o["accept_margin"][i, j] < ACC_TOL, "accepted differs for request %d: gpu %d oracle %d" % (
+                ids[i], acc[i], a_o)
+            n_exc += 1
+            continue
+        assert res[i] == o["resampled"][i]
+        if nxt[i] != o["next_token"][i]:
+            ok = o["gap1"][i] < TOK_TOL + o["slack1"][i] or o["gap2"][i] < TOK_TOL + o["slack2"][i]
+            assert ok, "next token differs for request %d: gpu %d oracle %d (gaps %g %g)" % (
+                ids[i], nxt[i], o["next_token"][i], o["gap1"][i], o["gap2"][i])
+            n_exc += 1
+    assert np.all((acc >= 0) & (acc <= kp))
+    return n_exc

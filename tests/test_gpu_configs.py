@@ -1,0 +1,70 @@
+"""GPU parity at the full workload sizes, in the launch configuration the bench
+times: the whole round runs on the GPU, then sampled requests are checked
+stage-wise against the oracle, the scheduler is checked on every survival,
+and size-independent invariants are checked on every request."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_draft_round_gb300 as ds
+from speculative_decoding_draft_round_gb300 import workloads as wl
+from parity import check_sample, check_schedule, check_verify, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    ds.lib()
+    oracle.build()
+
+
+def _capacity_survivals(rnd, rnd_idx):
+    old = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                          rnd.seed, rnd_idx, gamma=rnd.gamma)
+    return old["surv"].clone()
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_full_size_round(cfg):
+    torch.cuda.empty_cache()
+    rnd = wl.CONFIGS[cfg](device=DEV)
+    t = 2
+    rnd.round = t
+    cap = _capacity_survivals(rnd, t - 2) if rnd.mode == wl.SCHED_ASYNC_CAPACITY else None
+    runner = ds.RoundRunner(rnd, surv_capacity=cap)
+    runner.set_round(t)
+    runner.run()
+    assert runner.check() == 0
+    res = runner.results()
+    R, G = rnd.R, rnd.gamma_max
+    rng = np.random.default_rng(cfg)
+    ids = np.unique(np.concatenate([[0, 1, R // 2, R - 1], rng.integers(0, R, 2)]))
+    check_sample(rnd, res, ids)
+    assert check_schedule(res["surv"], rnd.sps, rnd.mode, res, gamma=rnd.gamma, surv_capacity=cap) <= 1
+    check_verify(rnd, res, res["keep"], res, ids)
+
+    # invariants on every request
+    tok = to_np(res["tokens"])
+    g = np.full(R, G) if rnd.gamma is None else to_np(rnd.gamma)
+    active = np.arange(G)[None, :] < g[:, None]
+    assert np.all((tok[active] >= 0) & (tok[active] < rnd.V)) and np.all(tok[~active] == -1)
+    surv = to_np(res["surv"])
+    conf = to_np(res["conf"])
+    assert np.all((conf[active] > 0) & (conf[active] < 1))
+    assert np.all(np.diff(np.where(active, surv, 0), axis=1) <= 1e-7)
+    keep = to_np(res["keep"])
+    acc = to_np(res["accepted"])
+    nxt = to_np(res["next_token"])
+    assert np.all((keep >= 0) & (keep <= g))
+    assert np.all((acc >= 0) & (acc <= keep))
+    assert np.all((nxt >= 0) & (nxt < rnd.V))
+    st = ds.decode_stats(res["stats"])
+    assert st["admitted"] == keep.sum()
+    lse = to_np(res["draft_lse"])
+    logit = to_np(res["draft_logit"])
+    assert np.all(logit[active] <= lse[active] + 1e-4)

@@ -1,0 +1,260 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same
+seeded inputs, at sizes that span several vocabulary blocks, several request
+tiles and ragged tails, and the degenerate cases of the method."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_draft_round_gb300 as ds
+from speculative_decoding_draft_round_gb300 import workloads as wl
+from parity import check_sample, check_schedule, check_verify, to_np
+from conftest import load_golden
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    ds.lib()
+    oracle.build()
+
+
+def _paths(rnd):
+    paths = [ds.PATH_CUDA_CORE]
+    a, _ = ds.sample_args(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                          rnd.seed, rnd.round, gamma=rnd.gamma, path=ds.PATH_TENSOR_CORE)
+    try:
+        ds.workspace_bytes("sample", a)
+        import ctypes as C
+        if ds.lib().dspark_sample_block(C.byref(a), None, 0, None) != 2:   # 2 = unsupported shape
+            paths.append(ds.PATH_TENSOR_CORE)
+    except ds.DsparkError:
+        pass
+    return paths
+
+
+SMALL = [
+    dict(name="c1", R=4, G=4, V=64, r=8, d=32, dtype="f32", u_std=2.0, t_std=2.0, ew_std=0.1, wh_std=0.3),
+    dict(name="ragged_f32", R=11, G=5, V=300, r=24, d=20, dtype="f32", ew_std=0.2,
+         gamma=[5, 0, 3, 5, 1, 2, 5, 4, 5, 0, 5]),
+    dict(name="tiles_bf16", R=160, G=3, V=1000, r=64, d=96, dtype="bf16", ew_std=0.15,
+         temperature=lambda R, g, dev: 0.4 + torch.rand((R,), generator=g, device=dev)),
+    dict(name="wide_bf16", R=37, G=4, V=2056, r=256, d=64, dtype="bf16", ew_std=0.05,
+         gamma=[4, 2] * 18 + [3]),
+]
+
+
+def _make(spec, seed=123, **over):
+    spec = dict(spec)
+    spec.update(over)
+    name = spec.pop("name")
+    R, G, V, r, d, dtype = (spec.pop(k) for k in ("R", "G", "V", "r", "d", "dtype"))
+    sps = spec.pop("sps", None)
+    if sps is None:
+        sps = wl.sps_hyperbolic(R * (1 + G), a=1e-3, b=4e-5)
+    return wl.make_round(name, R, G, V, r, d, dtype, seed=seed, device=DEV, sps=sps, **spec)
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=[s["name"] for s in SMALL])
+@pytest.mark.parametrize("conf_token", [0, 1])
+def test_sample_block_matches_oracle(spec, conf_token):
+    rnd = _make(spec, conf_token=conf_token)
+    ids = np.arange(rnd.R)
+    for path in _paths(rnd):
+        for rnd_idx in (0, 7):
+            out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature,
+                                  rnd.anchor, rnd.seed, rnd_idx, gamma=rnd.gamma, conf_token=conf_token,
+                                  path=path)
+            assert ds.check(out["workspace"]) == 0
+            rnd.round = rnd_idx
+            n_exc = check_sample(rnd, out, ids)
+            assert n_exc <= max(2, rnd.R * rnd.gamma_max // 1000)
+
+
+def test_bias_first_off_and_tiny_vocab():
+    rnd = _make(dict(name="v5", R=6, G=3, V=5, r=4, d=8, dtype="f32", ew_std=0.5), bias_first=0)
+    out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                          rnd.seed, 0, bias_first=0)
+    check_sample(rnd, out, np.arange(rnd.R))
+
+
+def _rand_surv(R, G, gen, zero_frac=0.1, ties=False):
+    c = torch.rand((R, G), generator=gen) * 0.95 + 0.05
+    if ties:
+        c = torch.round(c * 10) / 10
+    a = torch.cumprod(c, dim=1)
+    a[torch.rand((R, G), generator=gen) < zero_frac] = 0.0
+    return a.to(torch.float32)
+
+
+@pytest.mark.parametrize("mode", [ds.SCHED_SYNC, ds.SCHED_FULL_SCAN, ds.SCHED_ASYNC_CAPACITY])
+def test_schedule_matches_oracle(mode):
+    gen = torch.Generator().manual_seed(77)
+    cases = [(1, 1), (3, 2), (4, 4), (32, 16), (128, 16), (100, 7), (512, 16), (8192, 1), (256, 32)]
+    n_exc = 0
+    for R, G in cases:
+        for sps_kind in ("hyper", "stair", "steep"):
+            n = R * (1 + G)
+            if sps_kind == "hyper":
+                sps = wl.sps_hyperbolic(n, a=1e-3, b=2e-6 * 32 / R)
+            elif sps_kind == "stair":
+                sps = wl.sps_staircase(n)
+            else:
+                sps = wl.sps_hyperbolic(n, a=1e-3, b=1e-4)
+            for ties in (False, True):
+                surv = _rand_surv(R, G, gen, ties=ties).to(DEV)
+                old = _rand_surv(R, G, gen).to(DEV) if mode == ds.SCHED_ASYNC_CAPACITY else None
+                gamma = torch.randint(0, G + 1, (R,), generator=gen, dtype=torch.int32).to(DEV) if ties else None
+                out = ds.schedule(surv, sps.to(DEV), mode, gamma=gamma, surv_capacity=old)
+                assert ds.check(out["workspace"]) == 0
+                n_exc += check_schedule(surv, sps, mode, out, gamma=gamma, surv_capacity=old)
+    assert n_exc <= 2
+
+
+def test_schedule_worked_examples_on_gpu():
+    ex = load_golden("worked_examples.json")
+    s = ex["single_request"]
+    surv = torch.tensor([np.cumprod(s["c"])], dtype=torch.float32, device=DEV)
+    out = ds.schedule(surv, torch.tensor(s["sps"], dtype=torch.float32, device=DEV), ds.SCHED_SYNC)
+    assert out["keep"].tolist() == [3]
+    assert ds.decode_stats(out["stats"])["theta_best"] == pytest.approx(1212.746, abs=1e-3)
+    t = ex["two_requests"]
+    surv = torch.tensor(np.cumprod(t["c"], axis=1), dtype=torch.float32, device=DEV)
+    sps = torch.tensor([9.0] + t["sps_from_B2"], dtype=torch.float32, device=DEV)
+    for mode in (ds.SCHED_SYNC, ds.SCHED_FULL_SCAN):
+        out = ds.schedule(surv, sps, mode)
+        assert out["keep"].tolist() == t["keep"]
+    h = ex["three_requests"]
+    surv = torch.tensor(np.cumprod(h["c"], axis=1), dtype=torch.float32, device=DEV)
+    sps = torch.tensor([9.0, 9.0] + h["sps_from_B3"], dtype=torch.float32, device=DEV)
+    out = ds.schedule(surv, sps, ds.SCHED_SYNC)
+    assert out["keep"].tolist() == h["keep"]
+    a = ex["appendix_a"]
+    sps = torch.tensor(a["sps"], dtype=torch.float32, device=DEV)
+    assert ds.schedule(torch.tensor([[0.8, 0.72]], device=DEV), sps, ds.SCHED_SYNC)["keep"].tolist() == [0]
+    assert ds.schedule(torch.tensor([[0.8, 0.72]], device=DEV), sps, ds.SCHED_FULL_SCAN)["keep"].tolist() == [2]
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=[s["name"] for s in SMALL])
+def test_verify_matches_oracle(spec):
+    rnd = _make(spec, seed=321)
+    ids = np.arange(rnd.R)
+    gen = torch.Generator().manual_seed(5)
+    for path in _paths(rnd):
+        sout = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature,
+                               rnd.anchor, rnd.seed, rnd.round, gamma=rnd.gamma, path=path)
+        g = torch.full((rnd.R,), rnd.gamma_max) if rnd.gamma is None else rnd.gamma.cpu()
+        for trial in range(3):
+            if trial == 0:
+                keep = g.clone()                                  # verify everything drafted
+            elif trial == 1:
+                keep = torch.zeros_like(g)                        # bonus only
+            else:
+                keep = (torch.rand(rnd.R, generator=gen) * (g + 1)).floor().to(torch.int32)
+            keep = keep.to(torch.int32).to(DEV)
+            vout = ds.verify(rnd.target, rnd.U, rnd.E, rnd.W, rnd.anchor, sout["tokens"], sout["draft_lse"],
+                             sout["draft_logit"], keep, rnd.temperature, rnd.seed, rnd.round, gamma=rnd.gamma,
+                             path=path)
+            assert ds.check(vout["workspace"]) == 0
+            n_exc = check_verify(rnd, sout, keep, vout, ids)
+            assert n_exc <= max(2, rnd.R // 100)
+
+
+def test_config1_round_end_to_end():
+    """Config 1 exactly: the oracle runs alone from the inputs (its own draws feed its
+    scheduler and verifier) and every output must equal the GPU's."""
+    rnd = wl.config1(device=DEV)
+    runner = ds.RoundRunner(rnd)
+    for rnd_idx in range(20):
+        runner.set_round(rnd_idx)
+        runner.run()
+        assert runner.check() == 0
+        res = runner.results()
+        o_s = oracle.sample_block(to_np(rnd.U), to_np(rnd.E), to_np(rnd.W), to_np(rnd.h), to_np(rnd.w_h),
+                                  to_np(rnd.w_e), rnd.b, to_np(rnd.temperature), to_np(rnd.anchor), rnd.seed,
+                                  rnd_idx)
+        gap = np.minimum(o_s["gap1"], o_s["gap2"])
+        if np.any(gap < 1e-4):
+            continue   # a near-tie draw: covered by the stage-wise tests
+        assert np.array_equal(to_np(res["tokens"]), o_s["tokens"])
+        assert np.allclose(to_np(res["surv"]), o_s["surv"], atol=1e-5)
+        o_c = oracle.schedule(o_s["surv"], to_np(rnd.sps).astype(np.float64), rnd.mode)
+        if o_c["min_margin"] <= 1e-12:
+            continue
+        assert to_np(res["keep"]).tolist() == o_c["keep"].tolist()
+        o_v = oracle.verify(to_np(rnd.target), to_np(rnd.U), to_np(rnd.E), to_np(rnd.W), to_np(rnd.anchor),
+                            o_s["tokens"], o_s["lse"], o_s["logit"], o_c["keep"], to_np(rnd.temperature),
+                            rnd.seed, rnd_idx)
+        if np.nanmin(o_v["accept_margin"], initial=1.0) < 1e-4 or np.min(o_v["gap1"]) < 1e-4 or \
+                np.min(o_v["gap2"]) < 1e-4:
+            continue
+        assert to_np(res["accepted"]).tolist() == o_v["accepted"].tolist()
+        assert to_np(res["next_token"]).tolist() == o_v["next_token"].tolist()
+        assert to_np(res["resampled"]).tolist() == o_v["resampled"].tolist()
+
+
+def test_out_of_range_device_inputs_are_clamped_and_reported():
+    rnd = _make(SMALL[0])
+    bad = rnd.anchor.clone()
+    bad[1] = rnd.V + 5
+    out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, bad, rnd.seed, 0)
+    assert ds.check(out["workspace"]) == 6
+    assert ds.check(out["workspace"]) == 0     # the word is cleared by the check
+    toks = to_np(out["tokens"])
+    assert np.all((toks >= 0) & (toks < rnd.V))
+    keep = torch.tensor([9, 0, 1, 2], dtype=torch.int32, device=DEV)   # 9 > gamma
+    v = ds.verify(rnd.target, rnd.U, rnd.E, rnd.W, rnd.anchor, out["tokens"], out["draft_lse"],
+                  out["draft_logit"], keep, rnd.temperature, rnd.seed, 0)
+    assert ds.check(v["workspace"]) == 6
+    assert int(v["accepted"][0]) <= rnd.gamma_max
+
+
+@pytest.mark.parametrize("n", [1_000_000])
+def test_gpu_acceptance_rate_and_losslessness(n):
+    """TV identity (0.8 at p_t = (0.7, 0.3), p_d = (0.5, 0.5)) and the law of the first
+    emitted token over 10^6 rounds run on the GPU."""
+    from scipy import special, stats
+    ex = load_golden("worked_examples.json")["tv_identity"]
+    R = 8192
+    rounds = n // R + 1
+    V, G = 16, 2
+    rng = np.random.default_rng(3)
+    ld = rng.normal(0, 1.5, (G, V))
+    lt = rng.normal(0, 1.5, (G + 1, V))
+    U = torch.tensor(ld, dtype=torch.float32, device=DEV).expand(R, G, V).contiguous()
+    E = torch.zeros((V, 8), device=DEV)
+    W = torch.zeros((8, V), device=DEV)
+    h = torch.zeros((R, G, 8), device=DEV)
+    z8 = torch.zeros(8, device=DEV)
+    T = torch.ones(R, device=DEV)
+    anchor = torch.zeros(R, dtype=torch.int32, device=DEV)
+    target = torch.tensor(lt, dtype=torch.float32, device=DEV).expand(R, G + 1, V).contiguous()
+    keep = torch.full((R,), 2, dtype=torch.int32, device=DEV)
+    y1 = []
+    for t in range(rounds):
+        s = ds.sample_block(U, E, W, h, z8, z8, 0.0, T, anchor, 11, t)
+        v = ds.verify(target, U, E, W, anchor, s["tokens"], s["draft_lse"], s["draft_logit"], keep, T, 11, t)
+        y1.append(torch.where(v["accepted"] >= 1, s["tokens"][:, 0], v["next_token"]).cpu().numpy())
+    y1 = np.concatenate(y1)
+    pt = special.softmax(lt[0])
+    counts = np.bincount(y1, minlength=V)
+    assert stats.chisquare(counts, pt * counts.sum()).pvalue > 1e-3
+    # two-point TV identity
+    U2 = torch.tensor(np.log(ex["p_d"]), dtype=torch.float32, device=DEV).view(1, 1, 2).expand(R, 1, 2).contiguous()
+    t2 = torch.tensor(np.log([ex["p_t"], [0.5, 0.5]]), dtype=torch.float32, device=DEV).view(1, 2, 2)
+    t2 = t2.expand(R, 2, 2).contiguous()
+    E2, W2 = torch.zeros((2, 8), device=DEV), torch.zeros((8, 2), device=DEV)
+    h2 = torch.zeros((R, 1, 8), device=DEV)
+    k1 = torch.ones(R, dtype=torch.int32, device=DEV)
+    acc = 0
+    for t in range(rounds):
+        s = ds.sample_block(U2, E2, W2, h2, z8, z8, 0.0, T, anchor, 12, t)
+        v = ds.verify(t2, U2, E2, W2, anchor, s["tokens"], s["draft_lse"], s["draft_logit"], k1, T, 12, t)
+        acc += int(v["accepted"].sum())
+    rate = acc / (rounds * R)
+    assert abs(rate - ex["accept"]) < 5 * np.sqrt(0.16 / (rounds * R))
