@@ -266,7 +266,7 @@ def bench_ours(args):
     runner = ds.RoundRunner(rnd, surv_capacity=cap, path=path)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    uses_tc = path != ds.PATH_CUDA_CORE and rnd.dtype == "bf16"
+    uses_tc = ds.sample_path(runner.sa) == ds.PATH_TENSOR_CORE
 
     clocks = ClockSampler(gpu_id_for(local))
     clocks.start()

@@ -119,6 +119,9 @@ typedef struct {
 } dspark_sample_args;
 
 dspark_status dspark_sample_workspace_size(const dspark_sample_args* args, size_t* bytes);
+/* The bias-contraction path these arguments select (DSPARK_PATH_CUDA_CORE or
+ * DSPARK_PATH_TENSOR_CORE), or -status for invalid arguments. */
+int32_t dspark_sample_path(const dspark_sample_args* args);
 dspark_status dspark_sample_block(const dspark_sample_args* args, void* workspace, size_t workspace_bytes,
                                   void* stream);
 
@@ -132,7 +135,9 @@ dspark_status dspark_sample_block(const dspark_sample_args* args, void* workspac
  *   FULL_SCAN: m* = smallest arg-max of Theta_m over m = 0..|pool|
  *   ASYNC_CAPACITY: K = FULL_SCAN count over the pool of surv_capacity
  *          (survivals two rounds old); m* = min(K, |pool|)
- * keep[r] = number of admitted slots of request r (a prefix length, 0..gamma_r).
+ * keep[r] = l_r, the largest admitted position j of request r (Algorithm 1 sets
+ * l_r = j on each admission); with survivals non-increasing in j (true for
+ * products of confidences in (0,1)) it is the number of admitted slots.
  * The prefix sums are exact fixed-point sums of the fp32 a's (2^-48 units) and
  * Theta is formed in double from them.
  * Unsupported: R * gamma_max > DSPARK_MAX_SLOTS.
@@ -248,6 +253,10 @@ dspark_status dspark_time_kernel(int32_t kernel, dspark_event_pair* events, int3
 /* Synchronise `stream`, then return the device status word of `workspace`
  * (DSPARK_OK, DSPARK_ERR_TIMEOUT or DSPARK_ERR_DEVICE_INPUT) and clear it. */
 dspark_status dspark_check(void* workspace, void* stream);
+
+/* Description of the last CUDA failure seen by a call on this thread (the kernel
+ * family and the CUDA error name and string), or "no error". */
+const char* dspark_last_error(void);
 
 /* Static description of a status code. */
 const char* dspark_status_string(dspark_status status);

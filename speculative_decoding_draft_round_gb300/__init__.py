@@ -72,7 +72,8 @@ class VerifyArgs(C.Structure):
 
 EXPORTS = ("dspark_sample_workspace_size", "dspark_sample_block", "dspark_schedule_workspace_size",
            "dspark_schedule", "dspark_verify_workspace_size", "dspark_verify", "dspark_check",
-           "dspark_status_string", "dspark_abi_version", "dspark_launch_count", "dspark_time_kernel")
+           "dspark_status_string", "dspark_abi_version", "dspark_launch_count", "dspark_time_kernel",
+           "dspark_last_error", "dspark_sample_path")
 
 KERNELS = {"conf_hidden": 0, "draft_stats": 1, "draft_commit": 2, "schedule": 3, "verify_rows": 4,
            "verify_decide": 5, "residual_stats": 6, "residual_pick": 7}
@@ -85,8 +86,11 @@ _lib = None
 
 
 class DsparkError(RuntimeError):
-    def __init__(self, fn, code):
-        super().__init__("%s failed: %s (%d)" % (fn, STATUS.get(code, "unknown"), code))
+    def __init__(self, fn, code, detail=""):
+        msg = "%s failed: %s (%d)" % (fn, STATUS.get(code, "unknown"), code)
+        if detail:
+            msg += ": " + detail
+        super().__init__(msg)
         self.code = code
 
 
@@ -112,6 +116,10 @@ def lib():
         L.dspark_status_string.restype = C.c_char_p
         L.dspark_abi_version.argtypes = []
         L.dspark_abi_version.restype = C.c_int32
+        L.dspark_sample_path.argtypes = [C.POINTER(SampleArgs)]
+        L.dspark_sample_path.restype = C.c_int32
+        L.dspark_last_error.argtypes = []
+        L.dspark_last_error.restype = C.c_char_p
         L.dspark_launch_count.argtypes = []
         L.dspark_launch_count.restype = C.c_uint64
         L.dspark_time_kernel.argtypes = [C.c_int32, C.c_void_p, C.c_int32, C.POINTER(C.c_int32)]
@@ -157,7 +165,8 @@ def _stream(stream):
 def _call(fn, *args):
     rc = getattr(lib(), fn)(*args)
     if rc != 0:
-        raise DsparkError(fn, rc)
+        detail = lib().dspark_last_error().decode() if rc == 4 else ""
+        raise DsparkError(fn, rc, detail)
 
 
 def _workspace(fn_size, args, workspace, device):
@@ -176,6 +185,14 @@ def workspace_bytes(kind: str, args) -> int:
     return n.value
 
 
+def sample_path(args) -> int:
+    """PATH_CUDA_CORE or PATH_TENSOR_CORE: the contraction path dspark_sample_block takes for `args`."""
+    p = int(lib().dspark_sample_path(C.byref(args)))
+    if p < 0:
+        raise DsparkError("dspark_sample_path", -p)
+    return p
+
+
 def launch_count() -> int:
     """Kernels launched by libdspark in this process."""
     return int(lib().dspark_launch_count())
@@ -188,6 +205,11 @@ class KernelTimer:
         self.kernel = KERNELS[kernel]
         self.events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(capacity)]
+        # torch creates the underlying cudaEvent_t on first record: record once so the handles exist
+        for a, b in self.events:
+            a.record()
+            b.record()
+        torch.cuda.synchronize()
         self.pairs = (EventPair * capacity)()
         for i, (a, b) in enumerate(self.events):
             self.pairs[i].start = a.cuda_event

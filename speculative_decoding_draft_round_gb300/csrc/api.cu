@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libdspark (include/dspark.h): argument validation,
 // workspace layout and the launch sequence of each call. Every step of the
 // round runs in this library's kernels; nothing here computes on the host.
+#include <stdio.h>
 #include <string.h>
 
 #include <atomic>
@@ -25,20 +26,37 @@ struct KernelTimer {
 
 bool timing(int kernel) { return g_timer.kernel == kernel && g_timer.count && *g_timer.count < g_timer.capacity; }
 
+const char* kernel_name(int kernel)
+{
+    static const char* names[] = {"conf_hidden", "draft_stats", "draft_commit", "schedule",
+                                  "verify_rows", "verify_decide", "residual_stats", "residual_pick"};
+    return kernel >= 0 && kernel <= DSPARK_KERNEL_RESIDUAL_PICK ? names[kernel] : "?";
+}
+
+thread_local char g_last_error[256] = "no error";
+
 // Launch one kernel family through `fn`, counting it and recording the timing events if enabled.
 template <typename F>
 cudaError_t launch(int kernel, cudaStream_t s, F&& fn)
 {
     const bool t = timing(kernel);
-    if (t) cudaEventRecord(static_cast<cudaEvent_t>(g_timer.events[*g_timer.count].start), s);
-    const cudaError_t e = fn();
+    cudaError_t e = cudaSuccess;
+    if (t) e = cudaEventRecord(static_cast<cudaEvent_t>(g_timer.events[*g_timer.count].start), s);
+    if (e == cudaSuccess) e = fn();
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    if (t) {
-        cudaEventRecord(static_cast<cudaEvent_t>(g_timer.events[*g_timer.count].stop), s);
+    if (t && e == cudaSuccess) {
+        e = cudaEventRecord(static_cast<cudaEvent_t>(g_timer.events[*g_timer.count].stop), s);
         ++*g_timer.count;
     }
+    if (e != cudaSuccess)
+        snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", kernel_name(kernel), cudaGetErrorName(e),
+                 cudaGetErrorString(e));
     return e;
 }
+
+// Clear a non-sticky error another library left in this thread's runtime state, so that
+// the checks after our own launches report only our launches.
+void clear_stale_error() { (void)cudaGetLastError(); }
 
 constexpr size_t kAlign = 256;
 constexpr size_t kStatusBytes = 256;
@@ -186,8 +204,17 @@ dspark_status dspark_sample_workspace_size(const dspark_sample_args* a, size_t* 
     return DSPARK_OK;
 }
 
+int32_t dspark_sample_path(const dspark_sample_args* a)
+{
+    const dspark_status st = check_sample(a);
+    if (st != DSPARK_OK) return -st;
+    if (a->path == DSPARK_PATH_TENSOR_CORE && !sample_uses_tc(a)) return -DSPARK_ERR_UNSUPPORTED_SHAPE;
+    return sample_uses_tc(a) ? DSPARK_PATH_TENSOR_CORE : DSPARK_PATH_CUDA_CORE;
+}
+
 dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t ws_bytes, void* stream)
 {
+    clear_stale_error();
     dspark_status st = check_sample(a);
     if (st != DSPARK_OK) return st;
     if (a->path == DSPARK_PATH_TENSOR_CORE && !sample_uses_tc(a)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
@@ -248,6 +275,7 @@ dspark_status dspark_schedule_workspace_size(const dspark_schedule_args* a, size
 
 dspark_status dspark_schedule(const dspark_schedule_args* a, void* ws, size_t ws_bytes, void* stream)
 {
+    clear_stale_error();
     const dspark_status st = check_schedule(a);
     if (st != DSPARK_OK) return st;
     if (!ws || ws_bytes < kStatusBytes) return DSPARK_ERR_WORKSPACE;
@@ -278,6 +306,7 @@ dspark_status dspark_verify_workspace_size(const dspark_verify_args* a, size_t* 
 
 dspark_status dspark_verify(const dspark_verify_args* a, void* ws, size_t ws_bytes, void* stream)
 {
+    clear_stale_error();
     const dspark_status st = check_verify(a);
     if (st != DSPARK_OK) return st;
     if (a->path == DSPARK_PATH_TENSOR_CORE && !verify_uses_tc(a)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
@@ -323,6 +352,8 @@ dspark_status dspark_verify(const dspark_verify_args* a, void* ws, size_t ws_byt
     if (e == cudaSuccess) e = launch(DSPARK_KERNEL_RESIDUAL_PICK, s, [&] { return launch_residual_pick(p, s); });
     return cuda_status(e);
 }
+
+const char* dspark_last_error(void) { return g_last_error; }
 
 uint64_t dspark_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -294,11 +294,15 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedulePara
     else
         m_star = min(capacity, n);
 
-    // keep[r] = admitted slots of request r
+    // keep[r] = l_r, the largest admitted position of request r (Algorithm 1 sets l_r = j on
+    // each admission); with survivals non-increasing in j it is also the admitted count
     uint32_t* cnt = sm.hist;
     for (int q = threadIdx.x; q < p.R; q += kSchedThreads) cnt[q] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < m_star; i += kSchedThreads) atomicAdd(&cnt[sm.val[0][i] / p.G], 1u);
+    for (int i = threadIdx.x; i < m_star; i += kSchedThreads) {
+        const int slot = sm.val[0][i];
+        atomicMax(&cnt[slot / p.G], (uint32_t)(slot % p.G + 1));
+    }
     __syncthreads();
     for (int q = threadIdx.x; q < p.R; q += kSchedThreads) p.keep[q] = (int32_t)cnt[q];
 

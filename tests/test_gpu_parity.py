@@ -25,16 +25,12 @@ def _lib():
 
 
 def _paths(rnd):
+    """The contraction paths these inputs support: CUDA cores always, tensor cores when the shape allows."""
     paths = [ds.PATH_CUDA_CORE]
     a, _ = ds.sample_args(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
-                          rnd.seed, rnd.round, gamma=rnd.gamma, path=ds.PATH_TENSOR_CORE)
-    try:
-        ds.workspace_bytes("sample", a)
-        import ctypes as C
-        if ds.lib().dspark_sample_block(C.byref(a), None, 0, None) != 2:   # 2 = unsupported shape
-            paths.append(ds.PATH_TENSOR_CORE)
-    except ds.DsparkError:
-        pass
+                          rnd.seed, rnd.round, gamma=rnd.gamma)
+    if ds.sample_path(a) == ds.PATH_TENSOR_CORE:
+        paths.append(ds.PATH_TENSOR_CORE)
     return paths
 
 
