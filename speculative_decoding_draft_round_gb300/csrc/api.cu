@@ -134,7 +134,7 @@ dspark_status check_verify(const dspark_verify_args* a)
 bool verify_uses_tc(const dspark_verify_args* a)
 {
     if (a->path == DSPARK_PATH_CUDA_CORE) return false;
-    return tc_supported(a->dtype, a->R, a->V, a->r, a->U, a->E, a->W);
+    return tc_residual_supported(a->dtype, a->R, a->V, a->r, a->U, a->E, a->W);
 }
 
 VerifyLayout verify_layout(const dspark_verify_args* a)
@@ -309,7 +309,8 @@ dspark_status dspark_verify(const dspark_verify_args* a, void* ws, size_t ws_byt
     clear_stale_error();
     const dspark_status st = check_verify(a);
     if (st != DSPARK_OK) return st;
-    if (a->path == DSPARK_PATH_TENSOR_CORE && !verify_uses_tc(a)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+    if (a->path == DSPARK_PATH_TENSOR_CORE && !tc_supported(a->dtype, a->R, a->V, a->r, a->U, a->E, a->W))
+        return DSPARK_ERR_UNSUPPORTED_SHAPE;
     const VerifyLayout L = verify_layout(a);
     if (!ws || ws_bytes < L.total) return DSPARK_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

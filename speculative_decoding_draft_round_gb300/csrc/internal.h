@@ -82,6 +82,7 @@ cudaError_t launch_draft_commit(const DraftStep& p, cudaStream_t s);
 
 // sample_tc.cu
 bool tc_supported(int dtype, int R, int V, int r, const void* U, const void* E, const void* W);
+bool tc_residual_supported(int dtype, int R, int V, int r, const void* U, const void* E, const void* W);
 size_t tc_stats_rows(int R);  // rows of the block-statistics workspace the tensor-core path writes
 cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s);
 cudaError_t launch_residual_stats_tc(const VerifyParams& p, cudaStream_t s);

@@ -1,12 +1,674 @@
-// sample_tc.cu -- tensor-core (tcgen05) bias contraction for the draft sampler.
+// sample_tc.cu -- the per-step bias contraction of the draft sampler on the
+// 5th-generation tensor cores (tcgen05 + TMEM + TMA), with the softmax
+// statistics fused into the epilogue.
+//
+// For draft step k of "DSpark" (Markov head, zhongzhuzhou.org notes eq. 4-5;
+// caijizhuo.github.io section 4 step 3), every request tile of 128 rows and
+// every 128-wide vocabulary block b:
+//   D[m][n]  = sum_i W_1[x_{k-1}(m)][i] * W_2[i][b*128 + n]        (bf16 x bf16 -> fp32 in TMEM)
+//   x[m][n]  = (U[m][k][b*128 + n] + D[m][n]) * log2(e) / T_m
+//   stats[m][b] = (max_n x, sum_n 2^(x - max))                       (log2 units)
+// The V-wide bias lives only in TMEM; it never reaches global memory.
+//
+// Layout and roles (one persistent CTA per SM, 640 threads):
+//   warp 0      TMA producer of W tiles: per item 4 K-chunks of [64 K x 128 N]
+//               bf16, two 64-column boxes each, 128-byte swizzle (MN-major B).
+//   warp 1      TMEM allocator (512 columns = 4 accumulators of 128 x 128 fp32)
+//               and the single MMA-issuing thread (tcgen05.mma kind::f16,
+//               M=128, N=128, K=16 per instruction, cta_group::1).
+//   warp 3      TMA producer of U tiles: [128 requests x 128 columns] per item
+//               via a 3-D map (V, gamma, R), evict-first L2 policy.
+//   warps 4-19  epilogue: four warpgroups, each owns 32 of the 128 accumulator
+//               columns; a thread owns one request row (TMEM lane). They also
+//               gather the A operand (rows W_1[x_{k-1}] of the tile's requests)
+//               into shared memory in the 128-byte-swizzled K-major layout.
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+// DSPARK_ERR_TIMEOUT, stops issuing work, waits (bounded) for its own TMA copies
+// and frees its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace dspark {
+namespace {
 
-bool tc_supported(int, int, int, int, const void*, const void*, const void*) { return false; }
+constexpr int BM = 128;             // requests per tile = TMEM lanes
+constexpr int BN = 128;             // vocabulary columns per item = one noise block
+constexpr int BK = 64;              // K per shared-memory chunk (128 bytes of bf16)
+constexpr int KMAX = 256;           // largest Markov rank held in the A tile
+constexpr int W_STAGES = 4;
+constexpr int U_STAGES = 2;
+constexpr int TMEM_BUFS = 4;
+constexpr int EPI_WARPS = 16;
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int THREADS = 128 + EPI_THREADS;
+constexpr uint32_t TMEM_COLS = TMEM_BUFS * BN;   // 512
+
+constexpr uint32_t A_CHUNK_BYTES = BM * BK * 2;      // 16 KB: [128 rows x 64 K]
+constexpr uint32_t W_BOX_BYTES = BK * 64 * 2;        // 8 KB: [64 K x 64 N]
+constexpr uint32_t W_STAGE_BYTES = 2 * W_BOX_BYTES;  // 16 KB
+constexpr uint32_t U_BOX_BYTES = BM * 64 * 2;        // 16 KB: [128 rows x 64 N]
+constexpr uint32_t U_STAGE_BYTES = 2 * U_BOX_BYTES;  // 32 KB
+
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_W = OFF_A + (KMAX / BK) * A_CHUNK_BYTES;
+constexpr uint32_t OFF_U = OFF_W + W_STAGES * W_STAGE_BYTES;
+constexpr uint32_t OFF_PART = OFF_U + U_STAGES * U_STAGE_BYTES;           // [2][4][128] float2
+constexpr uint32_t OFF_META = OFF_PART + 2 * 4 * BM * 8;                   // prev, scale, active
+constexpr uint32_t OFF_BAR = OFF_META + 3 * BM * 4;
+constexpr int N_BARS = 2 * W_STAGES + 2 * U_STAGES + 2 * TMEM_BUFS + 2;
+constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
+constexpr int MAX_TILES = 64;                                              // R <= 8192
+constexpr uint32_t SMEM_USED = OFF_MISC + 16 + MAX_TILES * 4;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;                          // alignment slack
+
+constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;   // 4 s
+
+// instruction descriptor, kind::f16: D fp32, A = B = bf16, A K-major, B MN-major, M = 128, N = 128
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
+                           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+struct Ctl {
+    volatile int* abort;
+    int* status;
+};
+
+// Wait for the phase of `bar` with the given parity; false if the CTA aborted or the wait ran out.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Ctl c)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*c.abort) return false;
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+            *c.abort = 1;
+            raise_status(c.status, DSPARK_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Every lane waits; the result is uniform across the warp (false if any lane gave up), so that
+// warp-collective instructions after it are never reached by part of a warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c)
+{
+    const bool ok = mbar_wait(bar, parity, c);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait that ignores the abort flag (used to drain our own copies before exit).
+__device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity)
+{
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+    }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
+                                            uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory"); }
+
+// shared-memory matrix descriptor, 128-byte swizzle (layout type 2), descriptor version 1
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_global_nc_v4(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ------------------------------------------------------------------ kernel
+
+struct Ring {
+    int idx = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int n)
+    {
+        if (++idx == n) {
+            idx = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+__global__ void __launch_bounds__(THREADS, 1)
+    draft_stats_tc_kernel(const DraftStep p, const __grid_constant__ CUtensorMap tmW,
+                          const __grid_constant__ CUtensorMap tmU)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_addr(smem);
+    float2* part = reinterpret_cast<float2*>(smem + OFF_PART);
+    int* s_prev = reinterpret_cast<int*>(smem + OFF_META);
+    float* s_scale = reinterpret_cast<float*>(smem + OFF_META + BM * 4);
+    int* s_active = reinterpret_cast<int*>(smem + OFF_META + 2 * BM * 4);
+    const uint32_t bar0 = sbase + OFF_BAR;
+    auto w_full = [&](int i) { return bar0 + 8u * i; };
+    auto w_empty = [&](int i) { return bar0 + 8u * (W_STAGES + i); };
+    auto u_full = [&](int i) { return bar0 + 8u * (2 * W_STAGES + i); };
+    auto u_empty = [&](int i) { return bar0 + 8u * (2 * W_STAGES + U_STAGES + i); };
+    auto t_full = [&](int i) { return bar0 + 8u * (2 * W_STAGES + 2 * U_STAGES + i); };
+    auto t_empty = [&](int i) { return bar0 + 8u * (2 * W_STAGES + 2 * U_STAGES + TMEM_BUFS + i); };
+    const uint32_t a_full = bar0 + 8u * (2 * W_STAGES + 2 * U_STAGES + 2 * TMEM_BUFS);
+    const uint32_t a_empty = a_full + 8u;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    int* s_ntiles = reinterpret_cast<int*>(smem + OFF_MISC + 8);
+    int* s_tiles = reinterpret_cast<int*>(smem + OFF_MISC + 16);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Ctl ctl{s_abort, p.status};
+    const int n_mt = (p.R + BM - 1) / BM;
+
+    // tiles with at least one request still drafting at step k
+    if (tid == 0) {
+        *s_ntiles = 0;
+        *s_abort = 0;
+    }
+    __syncthreads();
+    for (int mt = 0; mt < n_mt; ++mt) {
+        bool act = false;
+        if (tid < BM) {
+            const int q = mt * BM + tid;
+            if (q < p.R) {
+                const int g = p.gamma ? p.gamma[q] : p.G;
+                act = p.k < g;
+            }
+        }
+        if (__syncthreads_or(act) && tid == 0) s_tiles[(*s_ntiles)++] = mt;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < W_STAGES; ++i) {
+            mbar_init(w_full(i), 1);
+            mbar_init(w_empty(i), 1);
+        }
+        for (int i = 0; i < U_STAGES; ++i) {
+            mbar_init(u_full(i), 1);
+            mbar_init(u_empty(i), EPI_WARPS);
+        }
+        for (int i = 0; i < TMEM_BUFS; ++i) {
+            mbar_init(t_full(i), 1);
+            mbar_init(t_empty(i), EPI_WARPS);
+        }
+        mbar_init(a_full, 1);
+        mbar_init(a_empty, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(s_tmem)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+
+    const int n_items = *s_ntiles * p.nblk;
+    const int i0 = (int)((long long)n_items * blockIdx.x / gridDim.x);
+    const int i1 = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
+    const int KC = p.r / BK;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- W producer
+        const uint64_t pol = l2_policy_evict_last();
+        Ring ws;
+        uint32_t last_par[W_STAGES];
+        bool filled[W_STAGES] = {false, false, false, false};
+        for (int it = i0; it < i1 && !*s_abort; ++it) {
+            const int b = it % p.nblk;
+            for (int kc = 0; kc < KC; ++kc) {
+                if (!mbar_wait(w_empty(ws.idx), ws.phase ^ 1u, ctl)) break;
+                const uint32_t dst = sbase + OFF_W + ws.idx * W_STAGE_BYTES;
+                mbar_expect_tx(w_full(ws.idx), W_STAGE_BYTES);
+                tma_load_2d(dst, &tmW, b * BN, kc * BK, w_full(ws.idx), pol);
+                tma_load_2d(dst + W_BOX_BYTES, &tmW, b * BN + 64, kc * BK, w_full(ws.idx), pol);
+                filled[ws.idx] = true;
+                last_par[ws.idx] = ws.phase;
+                ws.next(W_STAGES);
+            }
+        }
+        if (*s_abort)
+            for (int i = 0; i < W_STAGES; ++i)
+                if (filled[i]) mbar_drain(w_full(i), last_par[i]);
+    } else if (warp == 3 && lane == 0) {
+        // ---------------- U producer
+        const uint64_t pol = l2_policy_evict_first();
+        Ring us;
+        uint32_t last_par[U_STAGES];
+        bool filled[U_STAGES] = {false, false};
+        for (int it = i0; it < i1 && !*s_abort; ++it) {
+            const int mt = s_tiles[it / p.nblk], b = it % p.nblk;
+            if (!mbar_wait(u_empty(us.idx), us.phase ^ 1u, ctl)) break;
+            const uint32_t dst = sbase + OFF_U + us.idx * U_STAGE_BYTES;
+            mbar_expect_tx(u_full(us.idx), U_STAGE_BYTES);
+            tma_load_3d(dst, &tmU, b * BN, p.k, mt * BM, u_full(us.idx), pol);
+            tma_load_3d(dst + U_BOX_BYTES, &tmU, b * BN + 64, p.k, mt * BM, u_full(us.idx), pol);
+            filled[us.idx] = true;
+            last_par[us.idx] = us.phase;
+            us.next(U_STAGES);
+        }
+        if (*s_abort)
+            for (int i = 0; i < U_STAGES; ++i)
+                if (filled[i]) mbar_drain(u_full(i), last_par[i]);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        Ring ws, tb;
+        uint32_t a_par = 0;
+        int cur_tile = -1;
+        for (int it = i0; it < i1; ++it) {
+            const int tile = it / p.nblk;
+            if (tile != cur_tile) {
+                if (cur_tile >= 0) mma_commit(a_empty);   // old A is free once its MMAs retire
+                if (!mbar_wait(a_full, a_par, ctl)) break;
+                a_par ^= 1u;
+                cur_tile = tile;
+                tc_fence_after();
+            }
+            if (!mbar_wait(t_empty(tb.idx), tb.phase ^ 1u, ctl)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(tb.idx * BN);
+            bool ok = true;
+            for (int kc = 0; kc < KC; ++kc) {
+                if (!mbar_wait(w_full(ws.idx), ws.phase, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = sbase + OFF_A + kc * A_CHUNK_BYTES;
+                const uint32_t b_addr = sbase + OFF_W + ws.idx * W_STAGE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t ad = sw128_desc(a_addr + kk * 32, 16, 1024);
+                    const uint64_t bd = sw128_desc(b_addr + kk * 16 * 128, W_BOX_BYTES, 1024);
+                    mma_bf16(d_tmem, ad, bd, (kc | kk) != 0);
+                }
+                mma_commit(w_empty(ws.idx));
+                ws.next(W_STAGES);
+            }
+            if (!ok) break;
+            mma_commit(t_full(tb.idx));
+            tb.next(TMEM_BUFS);
+        }
+    } else if (warp >= 4) {
+        // ---------------- epilogue (and A gather)
+        // Every epilogue warp runs the same sequence of named barriers whatever happens: after
+        // an abort (a wait that gave up) a warp keeps iterating but skips its memory work, so no
+        // warp is ever left alone in a barrier.
+        const int e = tid - 128;
+        const int q4 = warp & 3, g = (warp - 4) >> 2;
+        const int m = q4 * 32 + lane;
+        const bool use_bias = (p.k > 0) || p.bias_first;
+        const __nv_bfloat16* E = static_cast<const __nv_bfloat16*>(p.E);
+        Ring us, tb;
+        uint32_t a_par = 0;
+        int cur_tile = -1;
+        float scale = 0.f;
+        bool row_active = false;
+        bool live = true;
+        for (int it = i0; it < i1; ++it) {
+            const int tile = it / p.nblk, b = it % p.nblk;
+            const int mt = s_tiles[tile];
+            if (tile != cur_tile) {
+                if (cur_tile >= 0) {
+                    live = live && warp_wait(a_empty, a_par, ctl);
+                    a_par ^= 1u;
+                }
+                // request metadata of the tile
+                if (e < BM) {
+                    const int q = mt * BM + e;
+                    int act = 0, prev = 0;
+                    float sc = 0.f;
+                    if (q < p.R) {
+                        int gq = p.gamma ? p.gamma[q] : p.G;
+                        if (gq < 0 || gq > p.G) {
+                            raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+                            gq = gq < 0 ? 0 : p.G;
+                        }
+                        if (p.k < gq) {
+                            act = 1;
+                            prev = checked_index(p.k == 0 ? p.anchor[q] : p.x_cur[q], p.V, p.status);
+                            sc = kLog2e / p.temperature[q];
+                        }
+                    }
+                    s_prev[e] = prev;
+                    s_scale[e] = sc;
+                    s_active[e] = act;
+                }
+                epi_barrier();
+                // gather A = W_1[x_{k-1}] rows into the swizzled K-major tile
+                if (live) {
+                    const int cpr = p.r / 8;   // 16-byte chunks per row
+                    for (int idx = e; idx < BM * cpr; idx += EPI_THREADS) {
+                        const int row = idx / cpr, c = idx % cpr;
+                        uint4 v = make_uint4(0, 0, 0, 0);
+                        if (use_bias && s_active[row]) v = ld_global_nc_v4(E + (size_t)s_prev[row] * p.r + c * 8);
+                        const uint32_t dst = sbase + OFF_A + (c >> 3) * A_CHUNK_BYTES + row * 128 +
+                                             ((uint32_t)((c & 7) ^ (row & 7)) << 4);
+                        st_shared_v4(dst, v);
+                    }
+                    fence_proxy_async();
+                }
+                epi_barrier();
+                if (e == 0 && live) mbar_arrive(a_full);
+                scale = s_scale[m];
+                row_active = s_active[m] != 0;
+                cur_tile = tile;
+            }
+            // U values of this thread's row and 32 columns (swizzled 128-byte rows)
+            uint4 uv[4] = {};
+            const bool u_ok = live && warp_wait(u_full(us.idx), us.phase, ctl);
+            if (u_ok) {
+                const uint32_t ubox = sbase + OFF_U + us.idx * U_STAGE_BYTES + (g >> 1) * U_BOX_BYTES + m * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    uv[c] = ld_shared_v4(ubox + ((uint32_t)((((g & 1) << 2) + c) ^ (m & 7)) << 4));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(u_empty(us.idx));
+            }
+            us.next(U_STAGES);
+            // accumulator columns 32g .. 32g+31 of this row
+            uint32_t acc[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = 0u;
+            const bool t_ok = u_ok && warp_wait(t_full(tb.idx), tb.phase, ctl);
+            if (t_ok) {
+                tc_fence_after();
+                tmem_ld32(tmem_base + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(tb.idx * BN + g * 32), acc);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(t_empty(tb.idx));
+            }
+            tb.next(TMEM_BUFS);
+            live = t_ok;
+            // x = U + B (unscaled); max, then sum of 2^((x - max) * scale)
+            float x[32];
+            const int v0 = b * BN + g * 32;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t w4[4] = {uv[c].x, uv[c].y, uv[c].z, uv[c].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int j = c * 8 + h * 2;
+                    x[j] = __uint_as_float(w4[h] << 16) + __uint_as_float(acc[j]);
+                    x[j + 1] = __uint_as_float(w4[h] & 0xFFFF0000u) + __uint_as_float(acc[j + 1]);
+                }
+            }
+            if (v0 + 32 > p.V) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (v0 + j >= p.V) x[j] = -INFINITY;
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) mx = fmaxf(mx, x[j]);
+            float pm = -INFINITY, ps = 0.f;
+            if (mx > -INFINITY) {
+                const float nb = -mx * scale;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) {
+                    s0 += ex2(fmaf(x[j], scale, nb));
+                    s1 += ex2(fmaf(x[j + 1], scale, nb));
+                }
+                pm = mx * scale;
+                ps = s0 + s1;
+            }
+            float2* pp = part + ((it - i0) & 1) * 4 * BM;
+            pp[g * BM + m] = make_float2(pm, ps);
+            epi_barrier();
+            if (g == 0 && row_active && live) {
+                float M = pp[m].x;
+#pragma unroll
+                for (int gg = 1; gg < 4; ++gg) M = fmaxf(M, pp[gg * BM + m].x);
+                float S = 0.f;
+#pragma unroll
+                for (int gg = 0; gg < 4; ++gg) {
+                    const float2 t = pp[gg * BM + m];
+                    if (t.y > 0.f) S += t.y * ex2(t.x - M);
+                }
+                p.stats[(size_t)(mt * BM + m) * p.nblk + b] = make_float2(M, S);
+            }
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        else
+            (void)cudaGetLastError();
+    }
+    return fn;
+}
+
+int num_sms()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    }
+    return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+bool tc_supported(int dtype, int R, int V, int r, const void* U, const void* E, const void* W)
+{
+    if (dtype != DSPARK_BF16) return false;
+    if (r % BK != 0 || r > KMAX || V % 8 != 0 || V < BN || R > MAX_TILES * BM) return false;
+    if (!aligned16(U) || !aligned16(E) || !aligned16(W)) return false;
+    return encode_fn() != nullptr;
+}
+
+// The residual's bias recompute still runs on CUDA cores.
+bool tc_residual_supported(int, int, int, int, const void*, const void*, const void*) { return false; }
+
 size_t tc_stats_rows(int R) { return (size_t)R; }
-cudaError_t launch_draft_stats_tc(const DraftStep&, cudaStream_t) { return cudaErrorNotSupported; }
+
+cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s)
+{
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap tmW, tmU;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)p.V, (cuuint64_t)p.r};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.V * 2};
+        const cuuint32_t box[2] = {64, BK};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.W), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)p.V, (cuuint64_t)p.G, (cuuint64_t)p.R};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.V * 2, (cuuint64_t)p.G * p.V * 2};
+        const cuuint32_t box[3] = {64, 1, BM};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.U), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(draft_stats_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int items = ((p.R + BM - 1) / BM) * p.nblk;
+    const int grid = items < num_sms() ? items : num_sms();
+    draft_stats_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(p, tmW, tmU);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_residual_stats_tc(const VerifyParams&, cudaStream_t) { return cudaErrorNotSupported; }
 
 }  // namespace dspark
