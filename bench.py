@@ -398,6 +398,31 @@ def bench_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def bench_profile(args):
+    """Plain rounds for an external profiler: warm-up W rounds, then K rounds, no clocks,
+    no end-to-end leg and no CPU baseline."""
+    import speculative_decoding_draft_round_gb300 as ds
+    from speculative_decoding_draft_round_gb300 import build as dsbuild
+    from speculative_decoding_draft_round_gb300 import workloads as wl
+    dsbuild.build()
+    path = {"auto": ds.PATH_AUTO, "cuda_core": ds.PATH_CUDA_CORE, "tensor_core": ds.PATH_TENSOR_CORE}[args.path]
+    rnd = wl.CONFIGS[args.workload](device="cuda")
+    cap = None
+    if rnd.mode == wl.SCHED_ASYNC_CAPACITY:
+        cap = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                              rnd.seed, 0, gamma=rnd.gamma, path=path)["surv"].clone()
+    runner = ds.RoundRunner(rnd, surv_capacity=cap, path=path)
+    for i in range(args.warmup + args.steps):
+        runner.set_round(2 + i)
+        runner.run()
+    torch.cuda.synchronize()
+    status = runner.check()
+    print(json.dumps({"profile_rounds": args.warmup + args.steps, "workload": rnd.name, "status": status,
+                      "launches": ds.launch_count()}))
+    if status:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,10 +432,13 @@ def main():
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--path", choices=["auto", "cuda_core", "tensor_core"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true", help="plain rounds for ncu (no timing, no baselines)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile:
+        bench_profile(args)
+    elif args.impl == "reference":
         bench_reference(args)
     else:
         bench_ours(args)

@@ -215,3 +215,78 @@ __device__ __forceinline__ int block_min_int(int v, int* scratch)
 }
 
 }  // namespace dspark
+
+namespace dspark {
+
+// ------------------------------------------------------------------ one block of the Markov bias
+//
+// bias[n] = sum_i e[i] * W[i][v0 + n] for the kNoiseBlock columns n of one vocabulary block,
+// computed by a CTA of kBlockGemvThreads threads: thread t owns 8 consecutive columns
+// (t % 16) and a K-slice (t / 16) of the rows, reads W with 16-byte vector loads that are all
+// independent, and the 16 K-slice partials are added in a fixed order. `e` (length r) and
+// `part` ([16][kNoiseBlock] floats) live in shared memory. Columns at or beyond V give 0.
+constexpr int kBlockGemvThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&w)[8]);
+
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&w)[8])
+{
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        w[2 * h] = __uint_as_float(u[h] << 16);
+        w[2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
+    }
+}
+
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&w)[8])
+{
+    const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
+// Returns, in thread t < kNoiseBlock, the bias of column v0 + t. Contains __syncthreads().
+template <typename T>
+__device__ float block_bias(const float* e, const T* W, int V, int r, int v0, float* part)
+{
+    const int t = threadIdx.x;
+    const bool vec = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(W) & 15u) == 0);
+    if (vec) {
+        const int cg = t & 15, ks = t >> 4;
+        const int c0 = v0 + cg * 8;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (c0 < V) {   // V % 8 == 0: the 8 columns are all in range or all out
+            for (int i = ks; i < r; i += 16) {
+                float w[8];
+                load8<T>(W + (size_t)i * V + c0, w);
+                const float ei = e[i];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[j] = fmaf(ei, w[j], acc[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[ks * kNoiseBlock + cg * 8 + j] = acc[j];
+    } else {
+        // scalar fallback: thread t < kNoiseBlock handles column v0 + t alone
+        float acc = 0.f;
+        if (t < kNoiseBlock && v0 + t < V)
+            for (int i = 0; i < r; ++i) acc = fmaf(e[i], ld(W, (size_t)i * V + v0 + t), acc);
+        if (t < kNoiseBlock) {
+            part[t] = acc;
+            for (int s = 1; s < 16; ++s) part[s * kNoiseBlock + t] = 0.f;
+        }
+    }
+    __syncthreads();
+    float bias = 0.f;
+    if (t < kNoiseBlock)
+        for (int s = 0; s < 16; ++s) bias += part[s * kNoiseBlock + t];
+    return bias;
+}
+
+}  // namespace dspark

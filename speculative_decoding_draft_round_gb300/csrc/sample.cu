@@ -35,7 +35,20 @@ __global__ void __launch_bounds__(256) conf_hidden_kernel(DraftStep p)
     if (k >= g) return;
     const T* h = static_cast<const T*>(p.h) + (size_t)warp * p.d;
     float acc = 0.f;
-    for (int j = lane; j < p.d; j += 32) acc += p.w_h[j] * ld(h, j);
+    const bool vec = (p.d % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.h) & 15u) == 0) &&
+                     ((reinterpret_cast<uintptr_t>(p.w_h) & 15u) == 0);
+    if (vec) {
+        // 8 elements (16 bytes of bf16, 32 of fp32) per lane per step, all loads independent
+        for (int j = lane * 8; j < p.d; j += 256) {
+            float w[8], x[8];
+            load8<T>(h + j, x);
+            load8<float>(p.w_h + j, w);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc = fmaf(w[e], x[e], acc);
+        }
+    } else {
+        for (int j = lane; j < p.d; j += 32) acc += p.w_h[j] * ld(h, j);
+    }
     acc = warp_sum(acc);
     if (lane == 0) p.hw[warp] = acc;
 }
@@ -111,18 +124,39 @@ __global__ void __launch_bounds__(kNoiseBlock) draft_stats_simt_kernel(DraftStep
 
 // ----------------------------------------------------------------- commit
 
-constexpr int kCommitThreads = kNoiseBlock;
+constexpr int kCommitThreads = kBlockGemvThreads;
+
+// Online (max, sum) pair in log2 units: represents sum_i 2^{x_i} as s * 2^m.
+struct LseAcc {
+    float m, s;
+};
+
+__device__ __forceinline__ LseAcc lse_add(LseAcc a, float L2)
+{
+    if (L2 <= a.m) return LseAcc{a.m, a.s + exp2f(L2 - a.m)};
+    return LseAcc{L2, a.s * exp2f(a.m - L2) + 1.f};
+}
+
+__device__ __forceinline__ LseAcc lse_merge(LseAcc a, LseAcc b)
+{
+    if (b.m == -INFINITY) return a;
+    if (a.m == -INFINITY) return b;
+    return a.m >= b.m ? LseAcc{a.m, a.s + b.s * exp2f(b.m - a.m)} : LseAcc{b.m, b.s + a.s * exp2f(a.m - b.m)};
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep p)
 {
-    extern __shared__ float erow[];   // [r] W_1[prev] (and then W_1[x] for the confidence head)
-    __shared__ float sv[8];
-    __shared__ int si[8];
-    __shared__ float red[8];
+    extern __shared__ float sm_dyn[];   // [r] W_1[prev], then [16][128] K-slice partials
+    float* erow = sm_dyn;
+    float* part = sm_dyn + ((p.r + 3) & ~3);
+    __shared__ float sv[kCommitThreads / 32];
+    __shared__ int si[kCommitThreads / 32];
+    __shared__ float lm_s[kCommitThreads / 32], ls_s[kCommitThreads / 32];
+    __shared__ float red[kCommitThreads / 32];
     __shared__ int s_tok;
     __shared__ float s_logit;
-    const int q = blockIdx.x, t = threadIdx.x;
+    const int q = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const StepRequest rq = draft_request(p, q);
     const size_t o = (size_t)q * p.G + p.k;
     if (!rq.active) {
@@ -137,42 +171,55 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     const PhiloxKey key = make_key(p.seed);
     const float2* st = p.stats + (size_t)q * p.nblk;
 
-    // log-normaliser over all blocks (log2 units): M = max(m_b + log2 s_b)
-    float lmax = -INFINITY;
+    // W_1[prev] for the element-level recompute (independent of the block draw)
+    for (int i = t; i < p.r; i += kCommitThreads) erow[i] = rq.use_bias ? ld(E, (size_t)rq.prev * p.r + i) : 0.f;
+
+    // block level: Gumbel-max over ln(block mass), one Philox call per 4 consecutive blocks,
+    // and the log-normaliser accumulated in the same pass
     ArgMax best{-INFINITY, -1};
-    for (int b = t; b < p.nblk; b += kCommitThreads) {
-        const float2 ms = st[b];
-        const float L2 = ms.x + log2f(ms.y);
-        lmax = fmaxf(lmax, L2);
-        // block-level Gumbel-max over the natural-log block masses
-        const float z = L2 * kLn2 + gumbel_at(key, p.round, kDraftBlock, (uint32_t)q, (uint32_t)p.k, (uint32_t)b);
-        best = argmax_better(best, ArgMax{z, b});
+    LseAcc acc{-INFINITY, 0.f};
+    for (int g4 = t; g4 * 4 < p.nblk; g4 += kCommitThreads) {
+        const uint4 w = philox4x32_10(
+            make_uint4((uint32_t)g4, (uint32_t)p.k, (uint32_t)q, counter_word3(p.round, kDraftBlock)), key);
+        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = g4 * 4 + j;
+            if (b < p.nblk) {
+                const float2 ms = st[b];
+                const float L2 = ms.x + log2f(ms.y);
+                acc = lse_add(acc, L2);
+                const float z = L2 * kLn2 - logf(-logf(bits_to_uniform(words[j])));
+                best = argmax_better(best, ArgMax{z, b});
+            }
+        }
     }
-    lmax = block_max<kCommitThreads>(lmax, red);
-    float acc = 0.f;
-    for (int b = t; b < p.nblk; b += kCommitThreads) {
-        const float2 ms = st[b];
-        acc += exp2f(ms.x - lmax) * ms.y;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const LseAcc other{__shfl_xor_sync(0xffffffffu, acc.m, off), __shfl_xor_sync(0xffffffffu, acc.s, off)};
+        acc = lse_merge(acc, other);
     }
-    const float tot = block_sum<kCommitThreads>(acc, red);
-    best = block_argmax<kCommitThreads>(best, sv, si);
+    if (lane == 0) {
+        lm_s[warp] = acc.m;
+        ls_s[warp] = acc.s;
+    }
+    best = block_argmax<kCommitThreads>(best, sv, si);   // contains __syncthreads
+    LseAcc tot{-INFINITY, 0.f};
+#pragma unroll
+    for (int w = 0; w < kCommitThreads / 32; ++w) tot = lse_merge(tot, LseAcc{lm_s[w], ls_s[w]});
     int bstar = best.i;
     if (bstar < 0) {
         raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
         bstar = 0;
     }
 
-    // element-level Gumbel-max inside the chosen block; recompute its logits
-    for (int i = t; i < p.r; i += kCommitThreads)
-        erow[i] = rq.use_bias ? ld(E, (size_t)rq.prev * p.r + i) : 0.f;
-    __syncthreads();
+    // element level inside the chosen block: recompute its 128 logits
+    float bias = 0.f;
+    if (rq.use_bias) bias = block_bias<T>(erow, W, p.V, p.r, bstar * kNoiseBlock, part);
     const int v = bstar * kNoiseBlock + t;
     ArgMax cand{-INFINITY, -1};
     float lv = 0.f;
-    if (v < p.V) {
-        float bias = 0.f;
-        if (rq.use_bias)
-            for (int i = 0; i < p.r; ++i) bias = fmaf(erow[i], ld(W, (size_t)i * p.V + v), bias);
+    if (t < kNoiseBlock && v < p.V) {
         const T* U = static_cast<const T*>(p.U);
         lv = (ld(U, o * p.V + v) + bias) / p.temperature[q];
         cand = ArgMax{lv + gumbel_at(key, p.round, kDraftElem, (uint32_t)q, (uint32_t)p.k, (uint32_t)v), v};
@@ -183,11 +230,10 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
         raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
         tok = min(bstar * kNoiseBlock, p.V - 1);
     }
-    if (v == tok) {
+    if (t < kNoiseBlock && v == tok) {
         s_tok = tok;
         s_logit = lv;
     }
-    __syncthreads();
 
     // confidence head (eq. 7) on W_1[x_{k-1}] or W_1[x_k]
     const int xc = p.conf_token ? tok : rq.prev;
@@ -201,7 +247,7 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
         p.tokens[o] = s_tok;
         p.conf[o] = c;
         p.surv[o] = prev_s * c;
-        p.draft_lse[o] = (lmax + log2f(tot)) * kLn2;
+        p.draft_lse[o] = (tot.m + log2f(tot.s)) * kLn2;
         p.draft_logit[o] = s_logit;
         p.x_cur[q] = s_tok;
     }
@@ -237,7 +283,7 @@ cudaError_t launch_draft_stats_simt(const DraftStep& p, cudaStream_t s)
 
 cudaError_t launch_draft_commit(const DraftStep& p, cudaStream_t s)
 {
-    const size_t smem = (size_t)p.r * sizeof(float);
+    const size_t smem = (size_t)(((p.r + 3) & ~3) + 16 * kNoiseBlock) * sizeof(float);
     if (p.dtype == DSPARK_BF16)
         draft_commit_kernel<__nv_bfloat16><<<p.R, kCommitThreads, smem, s>>>(p);
     else

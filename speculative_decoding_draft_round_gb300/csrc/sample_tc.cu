@@ -27,6 +27,7 @@
 // and frees its TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -56,8 +57,9 @@ constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_W = OFF_A + (KMAX / BK) * A_CHUNK_BYTES;
 constexpr uint32_t OFF_U = OFF_W + W_STAGES * W_STAGE_BYTES;
 constexpr uint32_t OFF_PART = OFF_U + U_STAGES * U_STAGE_BYTES;           // [2][4][128] float2
-constexpr uint32_t OFF_META = OFF_PART + 2 * 4 * BM * 8;                   // prev, scale, active
-constexpr uint32_t OFF_BAR = OFF_META + 3 * BM * 4;
+constexpr uint32_t OFF_META = OFF_PART + 2 * 4 * BM * 8;                   // per-row metadata, see RowMeta
+constexpr uint32_t META_BYTES = BM * 32;
+constexpr uint32_t OFF_BAR = OFF_META + META_BYTES;
 constexpr int N_BARS = 2 * W_STAGES + 2 * U_STAGES + 2 * TMEM_BUFS + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
 constexpr int MAX_TILES = 64;                                              // R <= 8192
@@ -248,16 +250,90 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)
                  : "memory");
 }
 
-__device__ __forceinline__ uint4 ld_global_nc_v4(const void* p)
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p)
 {
     uint4 v;
-    asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
 }
 
 // ------------------------------------------------------------------ kernel
+
+enum Mode { kDraftMode = 0, kResidualMode = 1 };
+
+// Per-row metadata of the current request tile (shared memory, 32 bytes per row).
+struct RowMeta {
+    int prev;         // token whose W_1 row forms this A row
+    int active;       // row takes part (draft: k < gamma_q; residual: request rejected)
+    int use_bias;     // A row is W_1[prev] (else zero)
+    float scale;      // log2(e) / T
+    float lse_d2;     // residual: draft log-normaliser of the rejected position, log2 units
+    float lse_t2;     // residual: target log-normaliser of the same row, log2 units
+    uint32_t u_row;   // residual: row index q*G + n of U (row of V elements)
+    uint32_t t_row;   // residual: row index q*(G+1) + n of the target
+};
+static_assert(sizeof(RowMeta) == 32, "RowMeta is 32 bytes");
+
+struct TcParams {
+    DraftStep d;      // draft mode
+    VerifyParams v;   // residual mode
+    int R, G, V, r, nblk, k;
+    int* status;
+};
+
+// Does request q take part at this launch?
+template <int MODE>
+__device__ __forceinline__ bool row_takes_part(const TcParams& P, int q)
+{
+    if (q >= P.R) return false;
+    if (MODE == kDraftMode) {
+        const int g = P.d.gamma ? P.d.gamma[q] : P.G;
+        return P.k < g;
+    }
+    return P.v.rej[q] >= 0;
+}
+
+template <int MODE>
+__device__ __forceinline__ RowMeta row_meta(const TcParams& P, int q)
+{
+    RowMeta m{0, 0, 0, 0.f, 0.f, 0.f, 0u, 0u};
+    if (q >= P.R) return m;
+    if (MODE == kDraftMode) {
+        const DraftStep& p = P.d;
+        int g = p.gamma ? p.gamma[q] : p.G;
+        if (g < 0 || g > p.G) {
+            raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+            g = g < 0 ? 0 : p.G;
+        }
+        if (p.k >= g) return m;
+        m.active = 1;
+        m.prev = checked_index(p.k == 0 ? p.anchor[q] : p.x_cur[q], p.V, p.status);
+        m.use_bias = (p.k > 0) || p.bias_first;
+        m.scale = kLog2e / p.temperature[q];
+    } else {
+        const VerifyParams& p = P.v;
+        const int n = p.rej[q];
+        if (n < 0) return m;
+        m.active = 1;
+        m.prev = checked_index(n == 0 ? p.anchor[q] : p.tokens[(size_t)q * p.G + n - 1], p.V, p.status);
+        m.use_bias = (n > 0) || p.bias_first;
+        m.scale = kLog2e / p.temperature[q];
+        m.lse_d2 = p.draft_lse[(size_t)q * p.G + n] * kLog2e;
+        m.lse_t2 = p.lse_t[(size_t)q * (p.G + 1) + n] * kLog2e;
+        m.u_row = (uint32_t)(q * p.G + n);
+        m.t_row = (uint32_t)(q * (p.G + 1) + n);
+    }
+    return m;
+}
 
 struct Ring {
     int idx = 0;
@@ -271,17 +347,15 @@ struct Ring {
     }
 };
 
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    draft_stats_tc_kernel(const DraftStep p, const __grid_constant__ CUtensorMap tmW,
-                          const __grid_constant__ CUtensorMap tmU)
+    stats_tc_kernel(const TcParams P, const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
     float2* part = reinterpret_cast<float2*>(smem + OFF_PART);
-    int* s_prev = reinterpret_cast<int*>(smem + OFF_META);
-    float* s_scale = reinterpret_cast<float*>(smem + OFF_META + BM * 4);
-    int* s_active = reinterpret_cast<int*>(smem + OFF_META + 2 * BM * 4);
+    RowMeta* s_meta = reinterpret_cast<RowMeta*>(smem + OFF_META);
     const uint32_t bar0 = sbase + OFF_BAR;
     auto w_full = [&](int i) { return bar0 + 8u * i; };
     auto w_empty = [&](int i) { return bar0 + 8u * (W_STAGES + i); };
@@ -297,8 +371,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     int* s_tiles = reinterpret_cast<int*>(smem + OFF_MISC + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const Ctl ctl{s_abort, p.status};
-    const int n_mt = (p.R + BM - 1) / BM;
+    const Ctl ctl{s_abort, P.status};
+    const int n_mt = (P.R + BM - 1) / BM;
 
     // tiles with at least one request still drafting at step k
     if (tid == 0) {
@@ -307,14 +381,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncthreads();
     for (int mt = 0; mt < n_mt; ++mt) {
-        bool act = false;
-        if (tid < BM) {
-            const int q = mt * BM + tid;
-            if (q < p.R) {
-                const int g = p.gamma ? p.gamma[q] : p.G;
-                act = p.k < g;
-            }
-        }
+        const bool act = tid < BM && row_takes_part<MODE>(P, mt * BM + tid);
         if (__syncthreads_or(act) && tid == 0) s_tiles[(*s_ntiles)++] = mt;
     }
     if (tid == 0) {
@@ -346,10 +413,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
 
-    const int n_items = *s_ntiles * p.nblk;
+    const int nblk = P.nblk;
+    const int n_items = *s_ntiles * nblk;
     const int i0 = (int)((long long)n_items * blockIdx.x / gridDim.x);
     const int i1 = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
-    const int KC = p.r / BK;
+    const int KC = P.r / BK;
 
     if (warp == 0 && lane == 0) {
         // ---------------- W producer
@@ -358,7 +426,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t last_par[W_STAGES];
         bool filled[W_STAGES] = {false, false, false, false};
         for (int it = i0; it < i1 && !*s_abort; ++it) {
-            const int b = it % p.nblk;
+            const int b = it % nblk;
             for (int kc = 0; kc < KC; ++kc) {
                 if (!mbar_wait(w_empty(ws.idx), ws.phase ^ 1u, ctl)) break;
                 const uint32_t dst = sbase + OFF_W + ws.idx * W_STAGE_BYTES;
@@ -373,19 +441,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (*s_abort)
             for (int i = 0; i < W_STAGES; ++i)
                 if (filled[i]) mbar_drain(w_full(i), last_par[i]);
-    } else if (warp == 3 && lane == 0) {
+    } else if (MODE == kDraftMode && warp == 3 && lane == 0) {
         // ---------------- U producer
         const uint64_t pol = l2_policy_evict_first();
         Ring us;
         uint32_t last_par[U_STAGES];
         bool filled[U_STAGES] = {false, false};
         for (int it = i0; it < i1 && !*s_abort; ++it) {
-            const int mt = s_tiles[it / p.nblk], b = it % p.nblk;
+            const int mt = s_tiles[it / nblk], b = it % nblk;
             if (!mbar_wait(u_empty(us.idx), us.phase ^ 1u, ctl)) break;
             const uint32_t dst = sbase + OFF_U + us.idx * U_STAGE_BYTES;
             mbar_expect_tx(u_full(us.idx), U_STAGE_BYTES);
-            tma_load_3d(dst, &tmU, b * BN, p.k, mt * BM, u_full(us.idx), pol);
-            tma_load_3d(dst + U_BOX_BYTES, &tmU, b * BN + 64, p.k, mt * BM, u_full(us.idx), pol);
+            tma_load_3d(dst, &tmU, b * BN, P.k, mt * BM, u_full(us.idx), pol);
+            tma_load_3d(dst + U_BOX_BYTES, &tmU, b * BN + 64, P.k, mt * BM, u_full(us.idx), pol);
             filled[us.idx] = true;
             last_par[us.idx] = us.phase;
             us.next(U_STAGES);
@@ -399,7 +467,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t a_par = 0;
         int cur_tile = -1;
         for (int it = i0; it < i1; ++it) {
-            const int tile = it / p.nblk;
+            const int tile = it / nblk;
             if (tile != cur_tile) {
                 if (cur_tile >= 0) mma_commit(a_empty);   // old A is free once its MMAs retire
                 if (!mbar_wait(a_full, a_par, ctl)) break;
@@ -440,75 +508,69 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int e = tid - 128;
         const int q4 = warp & 3, g = (warp - 4) >> 2;
         const int m = q4 * 32 + lane;
-        const bool use_bias = (p.k > 0) || p.bias_first;
-        const __nv_bfloat16* E = static_cast<const __nv_bfloat16*>(p.E);
+        const __nv_bfloat16* E = static_cast<const __nv_bfloat16*>(MODE == kDraftMode ? P.d.E : P.v.E);
         Ring us, tb;
         uint32_t a_par = 0;
         int cur_tile = -1;
-        float scale = 0.f;
-        bool row_active = false;
+        RowMeta rm{};
         bool live = true;
         for (int it = i0; it < i1; ++it) {
-            const int tile = it / p.nblk, b = it % p.nblk;
+            const int tile = it / nblk, b = it % nblk;
             const int mt = s_tiles[tile];
             if (tile != cur_tile) {
                 if (cur_tile >= 0) {
                     live = live && warp_wait(a_empty, a_par, ctl);
                     a_par ^= 1u;
                 }
-                // request metadata of the tile
-                if (e < BM) {
-                    const int q = mt * BM + e;
-                    int act = 0, prev = 0;
-                    float sc = 0.f;
-                    if (q < p.R) {
-                        int gq = p.gamma ? p.gamma[q] : p.G;
-                        if (gq < 0 || gq > p.G) {
-                            raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
-                            gq = gq < 0 ? 0 : p.G;
-                        }
-                        if (p.k < gq) {
-                            act = 1;
-                            prev = checked_index(p.k == 0 ? p.anchor[q] : p.x_cur[q], p.V, p.status);
-                            sc = kLog2e / p.temperature[q];
-                        }
-                    }
-                    s_prev[e] = prev;
-                    s_scale[e] = sc;
-                    s_active[e] = act;
-                }
+                if (e < BM) s_meta[e] = row_meta<MODE>(P, mt * BM + e);
                 epi_barrier();
-                // gather A = W_1[x_{k-1}] rows into the swizzled K-major tile
+                // gather A = W_1[prev] rows into the swizzled K-major tile; all copies in flight at once
                 if (live) {
-                    const int cpr = p.r / 8;   // 16-byte chunks per row
+                    const int cpr = P.r / 8;   // 16-byte chunks per row
                     for (int idx = e; idx < BM * cpr; idx += EPI_THREADS) {
                         const int row = idx / cpr, c = idx % cpr;
-                        uint4 v = make_uint4(0, 0, 0, 0);
-                        if (use_bias && s_active[row]) v = ld_global_nc_v4(E + (size_t)s_prev[row] * p.r + c * 8);
                         const uint32_t dst = sbase + OFF_A + (c >> 3) * A_CHUNK_BYTES + row * 128 +
                                              ((uint32_t)((c & 7) ^ (row & 7)) << 4);
-                        st_shared_v4(dst, v);
+                        const RowMeta& mr = s_meta[row];
+                        if (mr.active && mr.use_bias)
+                            cp_async_16(dst, E + (size_t)mr.prev * P.r + c * 8);
+                        else
+                            st_shared_v4(dst, make_uint4(0, 0, 0, 0));
                     }
+                    cp_async_wait_all();
                     fence_proxy_async();
                 }
                 epi_barrier();
                 if (e == 0 && live) mbar_arrive(a_full);
-                scale = s_scale[m];
-                row_active = s_active[m] != 0;
+                rm = s_meta[m];
                 cur_tile = tile;
             }
-            // U values of this thread's row and 32 columns (swizzled 128-byte rows)
-            uint4 uv[4] = {};
-            const bool u_ok = live && warp_wait(u_full(us.idx), us.phase, ctl);
-            if (u_ok) {
-                const uint32_t ubox = sbase + OFF_U + us.idx * U_STAGE_BYTES + (g >> 1) * U_BOX_BYTES + m * 128;
+            const int v0 = b * BN + g * 32;
+            // this thread's 32 columns of the row's input logits: U (draft) or U and target (residual)
+            uint4 uv[4] = {}, tv[4] = {};
+            bool u_ok = live;
+            if (MODE == kDraftMode) {
+                u_ok = live && warp_wait(u_full(us.idx), us.phase, ctl);
+                if (u_ok) {
+                    const uint32_t ubox = sbase + OFF_U + us.idx * U_STAGE_BYTES + (g >> 1) * U_BOX_BYTES + m * 128;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    uv[c] = ld_shared_v4(ubox + ((uint32_t)((((g & 1) << 2) + c) ^ (m & 7)) << 4));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(u_empty(us.idx));
+                    for (int c = 0; c < 4; ++c)
+                        uv[c] = ld_shared_v4(ubox + ((uint32_t)((((g & 1) << 2) + c) ^ (m & 7)) << 4));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(u_empty(us.idx));
+                }
+                us.next(U_STAGES);
+            } else if (live && rm.active) {
+                const __nv_bfloat16* U = static_cast<const __nv_bfloat16*>(P.v.U) + (size_t)rm.u_row * P.V;
+                const __nv_bfloat16* Tg = static_cast<const __nv_bfloat16*>(P.v.target) + (size_t)rm.t_row * P.V;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (v0 + 8 * c < P.V) {   // V % 8 == 0: each 8-column chunk is all in or all out
+                        uv[c] = ld_stream_v4(U + v0 + 8 * c);
+                        tv[c] = ld_stream_v4(Tg + v0 + 8 * c);
+                    }
+                }
             }
-            us.next(U_STAGES);
             // accumulator columns 32g .. 32g+31 of this row
             uint32_t acc[32];
 #pragma unroll
@@ -523,9 +585,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tb.next(TMEM_BUFS);
             live = t_ok;
-            // x = U + B (unscaled); max, then sum of 2^((x - max) * scale)
+            // x = U + B (unscaled logits of the draft)
             float x[32];
-            const int v0 = b * BN + g * 32;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint32_t w4[4] = {uv[c].x, uv[c].y, uv[c].z, uv[c].w};
@@ -536,40 +597,71 @@ __global__ void __launch_bounds__(THREADS, 1)
                     x[j + 1] = __uint_as_float(w4[h] & 0xFFFF0000u) + __uint_as_float(acc[j + 1]);
                 }
             }
-            if (v0 + 32 > p.V) {
+            const bool tail = v0 + 32 > P.V;
+            float2 partial;
+            if (MODE == kDraftMode) {
+                // block softmax statistics: max, then sum of 2^((x - max) * scale)
+                if (tail) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (v0 + j >= p.V) x[j] = -INFINITY;
-            }
-            float mx = x[0];
-#pragma unroll
-            for (int j = 1; j < 32; ++j) mx = fmaxf(mx, x[j]);
-            float pm = -INFINITY, ps = 0.f;
-            if (mx > -INFINITY) {
-                const float nb = -mx * scale;
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                    s0 += ex2(fmaf(x[j], scale, nb));
-                    s1 += ex2(fmaf(x[j + 1], scale, nb));
+                    for (int j = 0; j < 32; ++j)
+                        if (v0 + j >= P.V) x[j] = -INFINITY;
                 }
-                pm = mx * scale;
-                ps = s0 + s1;
+                float mx = x[0];
+#pragma unroll
+                for (int j = 1; j < 32; ++j) mx = fmaxf(mx, x[j]);
+                float pm = -INFINITY, ps = 0.f;
+                if (mx > -INFINITY) {
+                    const float nb = -mx * rm.scale;
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        s0 += ex2(fmaf(x[j], rm.scale, nb));
+                        s1 += ex2(fmaf(x[j + 1], rm.scale, nb));
+                    }
+                    pm = mx * rm.scale;
+                    ps = s0 + s1;
+                }
+                partial = make_float2(pm, ps);
+            } else {
+                // residual mass: sum of max(0, p_t - p_d), both from log2-unit logits
+                float rs = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t w4[4] = {tv[c].x, tv[c].y, tv[c].z, tv[c].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+#pragma unroll
+                        for (int s2 = 0; s2 < 2; ++s2) {
+                            const int j = c * 8 + h * 2 + s2;
+                            const float zt = __uint_as_float(s2 ? (w4[h] & 0xFFFF0000u) : (w4[h] << 16));
+                            const float pt = ex2(fmaf(zt, rm.scale, -rm.lse_t2));
+                            const float pd = ex2(fmaf(x[j], rm.scale, -rm.lse_d2));
+                            const float d = pt - pd;
+                            if (!(tail && v0 + j >= P.V) && d > 0.f) rs += d;
+                        }
+                    }
+                }
+                partial = make_float2(rs, 0.f);
             }
             float2* pp = part + ((it - i0) & 1) * 4 * BM;
-            pp[g * BM + m] = make_float2(pm, ps);
+            pp[g * BM + m] = partial;
             epi_barrier();
-            if (g == 0 && row_active && live) {
-                float M = pp[m].x;
+            if (g == 0 && rm.active && live) {
+                const size_t o = (size_t)(mt * BM + m) * nblk + b;
+                if (MODE == kDraftMode) {
+                    float M = pp[m].x;
 #pragma unroll
-                for (int gg = 1; gg < 4; ++gg) M = fmaxf(M, pp[gg * BM + m].x);
-                float S = 0.f;
+                    for (int gg = 1; gg < 4; ++gg) M = fmaxf(M, pp[gg * BM + m].x);
+                    float S = 0.f;
 #pragma unroll
-                for (int gg = 0; gg < 4; ++gg) {
-                    const float2 t = pp[gg * BM + m];
-                    if (t.y > 0.f) S += t.y * ex2(t.x - M);
+                    for (int gg = 0; gg < 4; ++gg) {
+                        const float2 t = pp[gg * BM + m];
+                        if (t.y > 0.f) S += t.y * ex2(t.x - M);
+                    }
+                    P.d.stats[o] = make_float2(M, S);
+                } else {
+                    P.v.res_stats[o] = pp[m].x + pp[BM + m].x + pp[2 * BM + m].x + pp[3 * BM + m].x;
                 }
-                p.stats[(size_t)(mt * BM + m) * p.nblk + b] = make_float2(M, S);
             }
         }
     }
@@ -626,49 +718,96 @@ bool tc_supported(int dtype, int R, int V, int r, const void* U, const void* E, 
     return encode_fn() != nullptr;
 }
 
-// The residual's bias recompute still runs on CUDA cores.
-bool tc_residual_supported(int, int, int, int, const void*, const void*, const void*) { return false; }
+bool tc_residual_supported(int dtype, int R, int V, int r, const void* U, const void* E, const void* W)
+{
+    return tc_supported(dtype, R, V, r, U, E, W);
+}
 
 size_t tc_stats_rows(int R) { return (size_t)R; }
 
-cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s)
+namespace {
+
+cudaError_t encode_w(CUtensorMap* m, const void* W, int V, int r)
 {
-    auto enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    CUtensorMap tmW, tmU;
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)p.V, (cuuint64_t)p.r};
-        const cuuint64_t strides[1] = {(cuuint64_t)p.V * 2};
-        const cuuint32_t box[2] = {64, BK};
-        const cuuint32_t es[2] = {1, 1};
-        if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.W), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    {
-        const cuuint64_t dims[3] = {(cuuint64_t)p.V, (cuuint64_t)p.G, (cuuint64_t)p.R};
-        const cuuint64_t strides[2] = {(cuuint64_t)p.V * 2, (cuuint64_t)p.G * p.V * 2};
-        const cuuint32_t box[3] = {64, 1, BM};
-        const cuuint32_t es[3] = {1, 1, 1};
-        if (enc(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.U), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    const cuuint64_t dims[2] = {(cuuint64_t)V, (cuuint64_t)r};
+    const cuuint64_t strides[1] = {(cuuint64_t)V * 2};
+    const cuuint32_t box[2] = {64, BK};
+    const cuuint32_t es[2] = {1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? cudaSuccess
+               : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_u(CUtensorMap* m, const void* U, int V, int G, int R)
+{
+    const cuuint64_t dims[3] = {(cuuint64_t)V, (cuuint64_t)G, (cuuint64_t)R};
+    const cuuint64_t strides[2] = {(cuuint64_t)V * 2, (cuuint64_t)G * V * 2};
+    const cuuint32_t box[3] = {64, 1, BM};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(U), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? cudaSuccess
+               : cudaErrorInvalidValue;
+}
+
+template <int MODE>
+cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorMap& tmU, cudaStream_t s)
+{
     static bool attr = false;
     if (!attr) {
         const cudaError_t e =
-            cudaFuncSetAttribute(draft_stats_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+            cudaFuncSetAttribute(stats_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const int items = ((p.R + BM - 1) / BM) * p.nblk;
+    const int items = ((P.R + BM - 1) / BM) * P.nblk;
     const int grid = items < num_sms() ? items : num_sms();
-    draft_stats_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(p, tmW, tmU);
+    stats_tc_kernel<MODE><<<grid, THREADS, SMEM_BYTES, s>>>(P, tmW, tmU);
     return cudaGetLastError();
 }
 
-cudaError_t launch_residual_stats_tc(const VerifyParams&, cudaStream_t) { return cudaErrorNotSupported; }
+}  // namespace
+
+cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s)
+{
+    if (!encode_fn()) return cudaErrorNotSupported;
+    CUtensorMap tmW, tmU;
+    cudaError_t e = encode_w(&tmW, p.W, p.V, p.r);
+    if (e == cudaSuccess) e = encode_u(&tmU, p.U, p.V, p.G, p.R);
+    if (e != cudaSuccess) return e;
+    TcParams P;
+    memset(&P, 0, sizeof P);
+    P.d = p;
+    P.R = p.R;
+    P.G = p.G;
+    P.V = p.V;
+    P.r = p.r;
+    P.nblk = p.nblk;
+    P.k = p.k;
+    P.status = p.status;
+    return launch_tc<kDraftMode>(P, tmW, tmU, s);
+}
+
+cudaError_t launch_residual_stats_tc(const VerifyParams& p, cudaStream_t s)
+{
+    if (!encode_fn()) return cudaErrorNotSupported;
+    CUtensorMap tmW;
+    const cudaError_t e = encode_w(&tmW, p.W, p.V, p.r);
+    if (e != cudaSuccess) return e;
+    TcParams P;
+    memset(&P, 0, sizeof P);
+    P.v = p;
+    P.R = p.R;
+    P.G = p.G;
+    P.V = p.V;
+    P.r = p.r;
+    P.nblk = p.nblk;
+    P.k = 0;
+    P.status = p.status;
+    return launch_tc<kResidualMode>(P, tmW, tmW, s);
+}
 
 }  // namespace dspark

@@ -45,34 +45,69 @@ __device__ __forceinline__ int request_keep(const VerifyParams& p, int q)
 constexpr int kRowWarps = 8;
 constexpr int kRowBlocksPerWarp = 4;
 
+// Block (max, sum exp2) of one 128-wide block of z/T, log2 units, computed by one warp.
+template <typename T>
+__device__ __forceinline__ float2 row_block_stats(const T* row, int V, int b, float scale, int lane, bool vec)
+{
+    float x[4];
+    if (vec) {
+        // lane owns 4 consecutive columns; V % 4 == 0 so they are all in or all out
+        const int v = b * kNoiseBlock + lane * 4;
+        if (v < V) {
+            if (sizeof(T) == 2) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(row + v));
+                x[0] = __uint_as_float(u.x << 16);
+                x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+                x[2] = __uint_as_float(u.y << 16);
+                x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+            } else {
+                const float4 f = __ldg(reinterpret_cast<const float4*>(row + v));
+                x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] *= scale;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = -INFINITY;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int v = b * kNoiseBlock + e * 32 + lane;
+            x[e] = v < V ? ld(row, v) * scale : -INFINITY;
+        }
+    }
+    float m = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    m = warp_max(m);
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s += exp2f(x[e] - m);
+    s = warp_sum(s);
+    return make_float2(m, s);
+}
+
+// grid (vocabulary chunks, R): the CTA walks target rows 0..keep[r] of its request
 template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParams p)
 {
-    const int q = blockIdx.z, i = blockIdx.y;
+    const int q = blockIdx.y;
     const int ell = request_keep(p, q);
-    if (i > ell) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float scale = kLog2e / p.temperature[q];
-    const T* row = static_cast<const T*>(p.target) + ((size_t)q * (p.G + 1) + i) * p.V;
-    float2* out = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
+    const bool vec = (p.V % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.target) & 15u) == 0);
     const int b0 = (blockIdx.x * kRowWarps + warp) * kRowBlocksPerWarp;
-    for (int bb = 0; bb < kRowBlocksPerWarp; ++bb) {
-        const int b = b0 + bb;
-        if (b >= p.nblk) break;
-        float x[kNoiseBlock / 32];
-        float m = -INFINITY;
+    for (int i = 0; i <= ell; ++i) {
+        const T* row = static_cast<const T*>(p.target) + ((size_t)q * (p.G + 1) + i) * p.V;
+        float2* out = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
+        float2 st[kRowBlocksPerWarp];
 #pragma unroll
-        for (int e = 0; e < kNoiseBlock / 32; ++e) {
-            const int v = b * kNoiseBlock + e * 32 + lane;
-            x[e] = v < p.V ? ld(row, v) * scale : -INFINITY;
-            m = fmaxf(m, x[e]);
+        for (int bb = 0; bb < kRowBlocksPerWarp; ++bb)
+            if (b0 + bb < p.nblk) st[bb] = row_block_stats<T>(row, p.V, b0 + bb, scale, lane, vec);
+        if (lane == 0) {
+#pragma unroll
+            for (int bb = 0; bb < kRowBlocksPerWarp; ++bb)
+                if (b0 + bb < p.nblk) out[b0 + bb] = st[bb];
         }
-        m = warp_max(m);
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < kNoiseBlock / 32; ++e) s += exp2f(x[e] - m);
-        s = warp_sum(s);
-        if (lane == 0) out[b] = make_float2(m, s);
     }
 }
 
@@ -130,9 +165,17 @@ __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyPar
     // bonus token from target row ell: two-level Gumbel-max over z_t / T
     const float2* st = p.row_stats + ((size_t)q * (p.G + 1) + ell) * p.nblk;
     ArgMax best{-INFINITY, -1};
-    for (int b = t; b < p.nblk; b += kDecideThreads) {
-        const float z = (st[b].x + log2f(st[b].y)) * kLn2 + gumbel_at(key, p.round, kFinalBlock, (uint32_t)q, 0u, (uint32_t)b);
-        best = argmax_better(best, ArgMax{z, b});
+    for (int g4 = t; g4 * 4 < p.nblk; g4 += kDecideThreads) {
+        const uint4 w = philox4x32_10(make_uint4((uint32_t)g4, 0u, (uint32_t)q, counter_word3(p.round, kFinalBlock)), key);
+        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = g4 * 4 + j;
+            if (b < p.nblk) {
+                const float z = (st[b].x + log2f(st[b].y)) * kLn2 - logf(-logf(bits_to_uniform(words[j])));
+                best = argmax_better(best, ArgMax{z, b});
+            }
+        }
     }
     best = block_argmax<kDecideThreads>(best, sv, si);
     const int bstar = best.i < 0 ? 0 : best.i;
@@ -231,54 +274,64 @@ __global__ void __launch_bounds__(kNoiseBlock) residual_stats_simt_kernel(Verify
 
 // ----------------------------------------------------------------- residual draw
 
+constexpr int kPickThreads = kBlockGemvThreads;
+
 template <typename T>
-__global__ void __launch_bounds__(kNoiseBlock) residual_pick_kernel(VerifyParams p)
+__global__ void __launch_bounds__(kPickThreads) residual_pick_kernel(VerifyParams p)
 {
-    extern __shared__ float erow[];   // [r]
-    __shared__ float sv[8];
-    __shared__ int si[8];
-    __shared__ float red[8];
+    extern __shared__ float sm_dyn[];   // [r] W_1[prev], then [16][128] K-slice partials
+    float* erow = sm_dyn;
+    float* part = sm_dyn + ((p.r + 3) & ~3);
+    __shared__ float sv[kPickThreads / 32];
+    __shared__ int si[kPickThreads / 32];
+    __shared__ float red[kPickThreads / 32];
     const int q = blockIdx.x, t = threadIdx.x;
     const ResRequest rq = residual_request(p, q);
     if (!rq.active) return;
     const PhiloxKey key = make_key(p.seed);
     const float* rs = p.res_stats + (size_t)q * p.nblk;
     const float2* st = p.row_stats + ((size_t)q * (p.G + 1) + rq.n) * p.nblk;
-    // residual mass anywhere?
-    float tot = 0.f;
-    for (int b = t; b < p.nblk; b += kNoiseBlock) tot += rs[b];
-    tot = block_sum<kNoiseBlock>(tot, red);
-    const bool fallback = !(tot > 0.f);   // residual zero through rounding: draw from p_t of the row
-    ArgMax best{-INFINITY, -1};
-    for (int b = t; b < p.nblk; b += kNoiseBlock) {
-        float L;
-        if (fallback) {
-            L = (st[b].x + log2f(st[b].y)) * kLn2;
-        } else {
-            if (!(rs[b] > 0.f)) continue;
-            L = logf(rs[b]);
-        }
-        const float z = L + gumbel_at(key, p.round, kFinalBlock, (uint32_t)q, 0u, (uint32_t)b);
-        best = argmax_better(best, ArgMax{z, b});
-    }
-    best = block_argmax<kNoiseBlock>(best, sv, si);
-    const int bstar = best.i < 0 ? 0 : best.i;
     const T* E = static_cast<const T*>(p.E);
     const T* W = static_cast<const T*>(p.W);
-    for (int i = t; i < p.r; i += kNoiseBlock) erow[i] = rq.use_bias ? ld(E, (size_t)rq.prev * p.r + i) : 0.f;
-    __syncthreads();
+    for (int i = t; i < p.r; i += kPickThreads) erow[i] = rq.use_bias ? ld(E, (size_t)rq.prev * p.r + i) : 0.f;
+    // residual mass anywhere?
+    float tot = 0.f;
+    for (int b = t; b < p.nblk; b += kPickThreads) tot += rs[b];
+    tot = block_sum<kPickThreads>(tot, red);
+    const bool fallback = !(tot > 0.f);   // zero only through rounding: draw from p_t of the row
+    // block level, one Philox call per 4 consecutive blocks
+    ArgMax best{-INFINITY, -1};
+    for (int g4 = t; g4 * 4 < p.nblk; g4 += kPickThreads) {
+        const uint4 w = philox4x32_10(make_uint4((uint32_t)g4, 0u, (uint32_t)q, counter_word3(p.round, kFinalBlock)), key);
+        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = g4 * 4 + j;
+            if (b >= p.nblk) break;
+            float L;
+            if (fallback) {
+                L = (st[b].x + log2f(st[b].y)) * kLn2;
+            } else {
+                if (!(rs[b] > 0.f)) continue;
+                L = logf(rs[b]);
+            }
+            best = argmax_better(best, ArgMax{L - logf(-logf(bits_to_uniform(words[j]))), b});
+        }
+    }
+    best = block_argmax<kPickThreads>(best, sv, si);
+    const int bstar = best.i < 0 ? 0 : best.i;
+    // element level inside the chosen block
+    float bias = 0.f;
+    if (!fallback && rq.use_bias) bias = block_bias<T>(erow, W, p.V, p.r, bstar * kNoiseBlock, part);
     const int v = bstar * kNoiseBlock + t;
     ArgMax cand{-INFINITY, -1};
-    if (v < p.V) {
+    if (t < kNoiseBlock && v < p.V) {
         const T* target = static_cast<const T*>(p.target);
         const float zt = ld(target, ((size_t)q * (p.G + 1) + rq.n) * p.V + v) * rq.invT;
         float L = -INFINITY;
         if (fallback) {
             L = zt;
         } else {
-            float bias = 0.f;
-            if (rq.use_bias)
-                for (int i = 0; i < p.r; ++i) bias = fmaf(erow[i], ld(W, (size_t)i * p.V + v), bias);
             const T* U = static_cast<const T*>(p.U);
             const float ldv = (ld(U, ((size_t)q * p.G + rq.n) * p.V + v) + bias) * rq.invT;
             const float res = expf(zt - rq.lse_t) - expf(ldv - rq.lse_d);
@@ -286,7 +339,7 @@ __global__ void __launch_bounds__(kNoiseBlock) residual_pick_kernel(VerifyParams
         }
         if (L > -INFINITY) cand = ArgMax{L + gumbel_at(key, p.round, kFinalElem, (uint32_t)q, 0u, (uint32_t)v), v};
     }
-    const ArgMax win = block_argmax<kNoiseBlock>(cand, sv, si);
+    const ArgMax win = block_argmax<kPickThreads>(cand, sv, si);
     if (t == 0) {
         int tok = win.i;
         if (tok < 0) {
@@ -303,7 +356,7 @@ __global__ void __launch_bounds__(kNoiseBlock) residual_pick_kernel(VerifyParams
 cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s)
 {
     const int per_cta = kRowWarps * kRowBlocksPerWarp;
-    const dim3 grid(cdiv(p.nblk, per_cta), p.G + 1, p.R);
+    const dim3 grid(cdiv(p.nblk, per_cta), p.R);
     if (p.dtype == DSPARK_BF16)
         verify_rows_kernel<__nv_bfloat16><<<grid, kRowWarps * 32, 0, s>>>(p);
     else
@@ -338,11 +391,11 @@ cudaError_t launch_residual_stats_simt(const VerifyParams& p, cudaStream_t s)
 
 cudaError_t launch_residual_pick(const VerifyParams& p, cudaStream_t s)
 {
-    const size_t smem = (size_t)p.r * sizeof(float);
+    const size_t smem = (size_t)(((p.r + 3) & ~3) + 16 * kNoiseBlock) * sizeof(float);
     if (p.dtype == DSPARK_BF16)
-        residual_pick_kernel<__nv_bfloat16><<<p.R, kNoiseBlock, smem, s>>>(p);
+        residual_pick_kernel<__nv_bfloat16><<<p.R, kPickThreads, smem, s>>>(p);
     else
-        residual_pick_kernel<float><<<p.R, kNoiseBlock, smem, s>>>(p);
+        residual_pick_kernel<float><<<p.R, kPickThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
