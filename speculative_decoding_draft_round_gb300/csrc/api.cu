@@ -67,7 +67,7 @@ dspark_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK :
 // ------------------------------------------------------------ sample_block
 
 struct SampleLayout {
-    size_t x_cur, hw, stats, total;
+    size_t x_cur, hw, stats, pick, a_next, total;
 };
 
 dspark_status check_sample(const dspark_sample_args* a)
@@ -104,6 +104,10 @@ SampleLayout sample_layout(const dspark_sample_args* a)
     o = align_up(o + sizeof(float) * (size_t)a->R * a->gamma_max, kAlign);
     L.stats = o;
     o = align_up(o + sizeof(float2) * rows * nblk, kAlign);
+    L.pick = o;
+    o = align_up(o + sizeof(unsigned long long) * (size_t)a->R * a->gamma_max, kAlign);
+    L.a_next = o;
+    o = align_up(o + (a->dtype == DSPARK_BF16 ? 2 : 4) * (size_t)a->R * a->r, kAlign);
     L.total = o;
     return L;
 }
@@ -253,6 +257,8 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.x_cur = at<int32_t>(ws, L.x_cur);
     p.hw = at<float>(ws, L.hw);
     p.stats = at<float2>(ws, L.stats);
+    p.pick = at<unsigned long long>(ws, L.pick);
+    p.a_next = at<unsigned char>(ws, L.a_next);
     const bool tc = sample_uses_tc(a);
     cudaError_t e = launch(DSPARK_KERNEL_CONF_HIDDEN, s, [&] { return launch_conf_hidden(p, s); });
     for (int k = 0; k < a->gamma_max && e == cudaSuccess; ++k) {

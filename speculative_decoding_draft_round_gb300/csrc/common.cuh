@@ -78,6 +78,14 @@ __host__ __device__ inline PhiloxKey make_key(uint64_t seed)
     return PhiloxKey{(uint32_t)seed, (uint32_t)(seed >> 32)};
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+//
+// A kernel launched with the programmatic-serialization attribute may start while the previous
+// kernel on the stream is still running; it must call pdl_wait() before it reads anything that
+// kernel writes or writes anything that kernel reads. pdl_trigger() lets the next such kernel start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ------------------------------------------------------------------ element loads
 
 template <typename T>
@@ -89,6 +97,21 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return
 
 template <typename T>
 __device__ __forceinline__ float ld(const T* p, size_t i) { return to_f32<T>(p[i]); }
+
+// ------------------------------------------------------------------ packed arg-max key
+//
+// (value, index) packed into 64 bits so that unsigned atomicMax keeps the larger value and, on
+// equal values, the lower index: high word = value bits made order-preserving, low = ~index.
+// NaN values are packed as -infinity; 0 means "no candidate".
+__device__ __forceinline__ unsigned long long pack_pick(float z, int idx)
+{
+    if (z != z) z = -INFINITY;
+    const uint32_t b = __float_as_uint(z);
+    const uint32_t key = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)idx;
+}
+
+__device__ __forceinline__ int unpack_pick_index(unsigned long long k) { return (int)~(uint32_t)k; }
 
 // ------------------------------------------------------------------ status word
 
@@ -262,7 +285,20 @@ __device__ float block_bias(const float* e, const T* W, int V, int r, int v0, fl
         const int c0 = v0 + cg * 8;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (c0 < V) {   // V % 8 == 0: the 8 columns are all in range or all out
-            for (int i = ks; i < r; i += 16) {
+            // rows in batches of 8 so that eight independent 16-byte loads are in flight
+            int i = ks;
+            for (; i + 7 * 16 < r; i += 8 * 16) {
+                float w[8][8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) load8<T>(W + (size_t)(i + u * 16) * V + c0, w[u]);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float ei = e[i + u * 16];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] = fmaf(ei, w[u][j], acc[j]);
+                }
+            }
+            for (; i < r; i += 16) {
                 float w[8];
                 load8<T>(W + (size_t)i * V + c0, w);
                 const float ei = e[i];

@@ -35,6 +35,8 @@ struct DraftStep {
     int32_t* x_cur;      // [R] token committed at the previous step
     float* hw;           // [R][G] w_h . h[r][k]
     float2* stats;       // [R_pad][nblk] (max, sum) of exp2 over each vocabulary block, log2 units
+    unsigned long long* pick;   // [G][R] packed block-level arg-max of each step (cleared per call)
+    void* a_next;        // [R][r] (element type of E): W_1 row of the token each request conditions on next
 };
 
 // Verification (dspark_verify).

@@ -27,6 +27,19 @@ namespace dspark {
 template <typename T>
 __global__ void __launch_bounds__(256) conf_hidden_kernel(DraftStep p)
 {
+    // clear the per-step block-draw slots of this call, and set the first step's conditioning rows
+    // (W_1[x_0], x_0 = anchor) for the tensor-core statistics kernel
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.R * p.G; i += gridDim.x * blockDim.x) p.pick[i] = 0ull;
+    {
+        const T* E = static_cast<const T*>(p.E);
+        T* an = static_cast<T*>(p.a_next);
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)p.R * p.r;
+             i += (long long)gridDim.x * blockDim.x) {
+            const int q = (int)(i / p.r), c = (int)(i % p.r);
+            const int x0 = checked_index(p.anchor[q], p.V, p.status);
+            an[i] = E[(size_t)x0 * p.r + c];
+        }
+    }
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= p.R * p.G) return;
@@ -79,6 +92,23 @@ __device__ __forceinline__ StepRequest draft_request(const DraftStep& p, int q)
     return s;
 }
 
+// the part of draft_request that reads only inputs (no earlier kernel's output)
+__device__ __forceinline__ StepRequest draft_request_inputs(const DraftStep& p, int q)
+{
+    StepRequest s{0, 0, 0, 0.f};
+    if (q >= p.R) return s;
+    int g = p.gamma ? p.gamma[q] : p.G;
+    if (g < 0 || g > p.G) {
+        raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+        g = g < 0 ? 0 : p.G;
+    }
+    if (p.k >= g) return s;
+    s.active = 1;
+    s.use_bias = (p.k > 0) || p.bias_first;
+    s.scale = kLog2e / p.temperature[q];
+    return s;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kNoiseBlock) draft_stats_simt_kernel(DraftStep p)
 {
@@ -118,7 +148,13 @@ __global__ void __launch_bounds__(kNoiseBlock) draft_stats_simt_kernel(DraftStep
         const float m = block_max<kNoiseBlock>(x, red);
         const float e = v < p.V ? exp2f(x - m) : 0.f;
         const float s = block_sum<kNoiseBlock>(e, red);
-        if (t == 0) p.stats[(size_t)q * p.nblk + b] = make_float2(m, s);
+        if (t == 0) {
+            p.stats[(size_t)q * p.nblk + b] = make_float2(m, s);
+            const float z = (m + log2f(s)) * kLn2 -
+                            logf(-logf(uniform_at(make_key(p.seed), p.round, kDraftBlock, (uint32_t)q, (uint32_t)p.k,
+                                                  (uint32_t)b)));
+            atomicMax(p.pick + (size_t)p.k * p.R + q, pack_pick(z, b));
+        }
     }
 }
 
@@ -144,6 +180,14 @@ __device__ __forceinline__ LseAcc lse_merge(LseAcc a, LseAcc b)
     return a.m >= b.m ? LseAcc{a.m, a.s + b.s * exp2f(b.m - a.m)} : LseAcc{b.m, b.s + a.s * exp2f(a.m - b.m)};
 }
 
+// Phase structure (each phase issues all of its global reads before using any):
+//   A  pick slot of this step, every block statistic, W_1[prev], per-request scalars
+//   B  (needs b*) the block's W columns (one 16-byte vector per K-slice row) and U values,
+//      while the log-normaliser of phase A is reduced
+//   C  (needs x_k) W_1[x_k]: the next step's conditioning row and, for conf_token = 1, eq. (7)
+constexpr int kStatsPerThread = 8;       // block statistics held in registers per thread (nblk <= 2048)
+constexpr int kBiasRows = 16;            // W rows per thread in the fast path (r <= 256)
+
 template <typename T>
 __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep p)
 {
@@ -157,8 +201,13 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     __shared__ int s_tok;
     __shared__ float s_logit;
     const int q = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const StepRequest rq = draft_request(p, q);
+    // inputs that no earlier kernel writes can be read before the dependency wait
+    const StepRequest rq = draft_request_inputs(p, q);
     const size_t o = (size_t)q * p.G + p.k;
+    const float invT = 1.f / p.temperature[q];
+    const float hw = p.hw[o];
+    pdl_wait();      // block statistics, pick slots and x_cur come from the kernels before this one
+    pdl_trigger();   // the next step's statistics kernel may start its prefetch
     if (!rq.active) {
         if (t == 0) {
             p.tokens[o] = -1;
@@ -166,33 +215,62 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
         }
         return;
     }
+    const int prev = checked_index(p.k == 0 ? p.anchor[q] : p.x_cur[q], p.V, p.status);
     const T* E = static_cast<const T*>(p.E);
     const T* W = static_cast<const T*>(p.W);
+    const T* U = static_cast<const T*>(p.U);
     const PhiloxKey key = make_key(p.seed);
     const float2* st = p.stats + (size_t)q * p.nblk;
 
-    // W_1[prev] for the element-level recompute (independent of the block draw)
-    for (int i = t; i < p.r; i += kCommitThreads) erow[i] = rq.use_bias ? ld(E, (size_t)rq.prev * p.r + i) : 0.f;
-
-    // block level: Gumbel-max over ln(block mass), one Philox call per 4 consecutive blocks,
-    // and the log-normaliser accumulated in the same pass
-    ArgMax best{-INFINITY, -1};
-    LseAcc acc{-INFINITY, 0.f};
-    for (int g4 = t; g4 * 4 < p.nblk; g4 += kCommitThreads) {
-        const uint4 w = philox4x32_10(
-            make_uint4((uint32_t)g4, (uint32_t)p.k, (uint32_t)q, counter_word3(p.round, kDraftBlock)), key);
-        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+    // ---- phase A
+    const unsigned long long pk = p.pick[(size_t)p.k * p.R + q];
+    const float surv_prev = p.k == 0 ? 1.f : p.surv[o - 1];
+    const bool fast_stats = p.nblk <= kStatsPerThread * kCommitThreads;
+    float2 ms[kStatsPerThread];
+    if (fast_stats) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int b = g4 * 4 + j;
-            if (b < p.nblk) {
-                const float2 ms = st[b];
-                const float L2 = ms.x + log2f(ms.y);
-                acc = lse_add(acc, L2);
-                const float z = L2 * kLn2 - logf(-logf(bits_to_uniform(words[j])));
-                best = argmax_better(best, ArgMax{z, b});
-            }
+        for (int u = 0; u < kStatsPerThread; ++u) {
+            const int b = t + u * kCommitThreads;
+            ms[u] = b < p.nblk ? st[b] : make_float2(-INFINITY, 1.f);
         }
+    }
+    float e_prev = 0.f;
+    const bool need_prev_row = rq.use_bias || !p.conf_token;
+    for (int i = t; i < p.r; i += kCommitThreads) {
+        const float ev = need_prev_row ? ld(E, (size_t)prev * p.r + i) : 0.f;
+        if (i == t) e_prev = ev;
+        erow[i] = ev;
+    }
+    int bstar = pk == 0ull ? -1 : unpack_pick_index(pk);
+    if (bstar < 0 || bstar >= p.nblk) {
+        raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+        bstar = 0;
+    }
+
+    // ---- phase B: the chosen block's W columns and U values
+    const int v = bstar * kNoiseBlock + t;
+    const float u_v = (t < kNoiseBlock && v < p.V) ? ld(U, o * p.V + v) : 0.f;
+    const bool fast_bias = rq.use_bias && sizeof(T) == 2 && p.V % 8 == 0 && p.r % 16 == 0 &&
+                           p.r <= 16 * kBiasRows && ((reinterpret_cast<uintptr_t>(W) & 15u) == 0);
+    const int cg = t & 15, ks = t >> 4;
+    const int c0 = bstar * kNoiseBlock + cg * 8;
+    uint4 wv[kBiasRows];
+    if (fast_bias) {
+#pragma unroll
+        for (int j = 0; j < kBiasRows; ++j) {
+            const int i = ks + 16 * j;
+            wv[j] = (i < p.r && c0 < p.V) ? __ldg(reinterpret_cast<const uint4*>(W + (size_t)i * p.V + c0))
+                                          : make_uint4(0, 0, 0, 0);
+        }
+    }
+    // log-normaliser from phase A while the phase-B loads fly
+    LseAcc acc{-INFINITY, 0.f};
+    if (fast_stats) {
+#pragma unroll
+        for (int u = 0; u < kStatsPerThread; ++u)
+            if (t + u * kCommitThreads < p.nblk) acc = lse_add(acc, ms[u].x + log2f(ms[u].y));
+    } else {
+        for (int b = t; b < p.nblk; b += kCommitThreads) acc = lse_add(acc, st[b].x + log2f(st[b].y));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -203,25 +281,38 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
         lm_s[warp] = acc.m;
         ls_s[warp] = acc.s;
     }
-    best = block_argmax<kCommitThreads>(best, sv, si);   // contains __syncthreads
+    __syncthreads();   // also publishes erow
     LseAcc tot{-INFINITY, 0.f};
 #pragma unroll
     for (int w = 0; w < kCommitThreads / 32; ++w) tot = lse_merge(tot, LseAcc{lm_s[w], ls_s[w]});
-    int bstar = best.i;
-    if (bstar < 0) {
-        raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
-        bstar = 0;
-    }
-
-    // element level inside the chosen block: recompute its 128 logits
     float bias = 0.f;
-    if (rq.use_bias) bias = block_bias<T>(erow, W, p.V, p.r, bstar * kNoiseBlock, part);
-    const int v = bstar * kNoiseBlock + t;
+    if (fast_bias) {
+        float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < kBiasRows; ++j) {
+            const int i = ks + 16 * j;
+            if (i < p.r) {
+                const float ei = erow[i];
+                const uint32_t u4[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    a8[2 * h] = fmaf(ei, __uint_as_float(u4[h] << 16), a8[2 * h]);
+                    a8[2 * h + 1] = fmaf(ei, __uint_as_float(u4[h] & 0xFFFF0000u), a8[2 * h + 1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) part[ks * kNoiseBlock + cg * 8 + j] = a8[j];
+        __syncthreads();
+        if (t < kNoiseBlock)
+            for (int s2 = 0; s2 < 16; ++s2) bias += part[s2 * kNoiseBlock + t];
+    } else if (rq.use_bias) {
+        bias = block_bias<T>(erow, W, p.V, p.r, bstar * kNoiseBlock, part);
+    }
     ArgMax cand{-INFINITY, -1};
     float lv = 0.f;
     if (t < kNoiseBlock && v < p.V) {
-        const T* U = static_cast<const T*>(p.U);
-        lv = (ld(U, o * p.V + v) + bias) / p.temperature[q];
+        lv = (u_v + bias) * invT;
         cand = ArgMax{lv + gumbel_at(key, p.round, kDraftElem, (uint32_t)q, (uint32_t)p.k, (uint32_t)v), v};
     }
     const ArgMax win = block_argmax<kCommitThreads>(cand, sv, si);
@@ -235,18 +326,22 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
         s_logit = lv;
     }
 
-    // confidence head (eq. 7) on W_1[x_{k-1}] or W_1[x_k]
-    const int xc = p.conf_token ? tok : rq.prev;
+    // ---- phase C: W_1[x_k] for the next step's conditioning rows and the confidence head (eq. 7)
     float dot = 0.f;
-    for (int i = t; i < p.r; i += kCommitThreads) dot = fmaf(p.w_e[i], ld(E, (size_t)xc * p.r + i), dot);
+    T* an = static_cast<T*>(p.a_next) + (size_t)q * p.r;
+    for (int i = t; i < p.r; i += kCommitThreads) {
+        const T et = E[(size_t)tok * p.r + i];
+        an[i] = et;
+        dot = fmaf(p.w_e[i], p.conf_token ? to_f32<T>(et) : erow[i], dot);   // eq. (7) reads W_1[x_{k-1}]
+    }
+    (void)e_prev;
     dot = block_sum<kCommitThreads>(dot, red);
     if (t == 0) {
-        const float logit = p.hw[o] + dot + p.b;
+        const float logit = hw + dot + p.b;
         const float c = 1.f / (1.f + expf(-logit));
-        const float prev_s = p.k == 0 ? 1.f : p.surv[o - 1];
         p.tokens[o] = s_tok;
         p.conf[o] = c;
-        p.surv[o] = prev_s * c;
+        p.surv[o] = surv_prev * c;
         p.draft_lse[o] = (tot.m + log2f(tot.s)) * kLn2;
         p.draft_logit[o] = s_logit;
         p.x_cur[q] = s_tok;
@@ -284,11 +379,18 @@ cudaError_t launch_draft_stats_simt(const DraftStep& p, cudaStream_t s)
 cudaError_t launch_draft_commit(const DraftStep& p, cudaStream_t s)
 {
     const size_t smem = (size_t)(((p.r + 3) & ~3) + 16 * kNoiseBlock) * sizeof(float);
-    if (p.dtype == DSPARK_BF16)
-        draft_commit_kernel<__nv_bfloat16><<<p.R, kCommitThreads, smem, s>>>(p);
-    else
-        draft_commit_kernel<float><<<p.R, kCommitThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.R);
+    cfg.blockDim = dim3(kCommitThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.dtype == DSPARK_BF16) return cudaLaunchKernelEx(&cfg, draft_commit_kernel<__nv_bfloat16>, p);
+    return cudaLaunchKernelEx(&cfg, draft_commit_kernel<float>, p);
 }
 
 }  // namespace dspark

@@ -39,22 +39,22 @@ constexpr int BM = 128;             // requests per tile = TMEM lanes
 constexpr int BN = 128;             // vocabulary columns per item = one noise block
 constexpr int BK = 64;              // K per shared-memory chunk (128 bytes of bf16)
 constexpr int KMAX = 256;           // largest Markov rank held in the A tile
-constexpr int W_STAGES = 4;
+constexpr int W_STAGES = 8;
 constexpr int U_STAGES = 2;
-constexpr int TMEM_BUFS = 4;
+constexpr int TMEM_BUFS = 3;
 constexpr int EPI_WARPS = 16;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int THREADS = 128 + EPI_THREADS;
-constexpr uint32_t TMEM_COLS = TMEM_BUFS * BN;   // 512
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t A_TMEM_COL = TMEM_BUFS * BN;      // A operand: 128 columns of packed bf16 pairs (K <= 256)
+static_assert(A_TMEM_COL + KMAX / 2 <= TMEM_COLS, "accumulators and A must fit in TMEM");
 
-constexpr uint32_t A_CHUNK_BYTES = BM * BK * 2;      // 16 KB: [128 rows x 64 K]
 constexpr uint32_t W_BOX_BYTES = BK * 64 * 2;        // 8 KB: [64 K x 64 N]
 constexpr uint32_t W_STAGE_BYTES = 2 * W_BOX_BYTES;  // 16 KB
 constexpr uint32_t U_BOX_BYTES = BM * 64 * 2;        // 16 KB: [128 rows x 64 N]
 constexpr uint32_t U_STAGE_BYTES = 2 * U_BOX_BYTES;  // 32 KB
 
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_W = OFF_A + (KMAX / BK) * A_CHUNK_BYTES;
+constexpr uint32_t OFF_W = 0;
 constexpr uint32_t OFF_U = OFF_W + W_STAGES * W_STAGE_BYTES;
 constexpr uint32_t OFF_PART = OFF_U + U_STAGES * U_STAGE_BYTES;           // [2][4][128] float2
 constexpr uint32_t OFF_META = OFF_PART + 2 * 4 * BM * 8;                   // per-row metadata, see RowMeta
@@ -68,7 +68,8 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;                          // al
 
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;   // 4 s
 
-// instruction descriptor, kind::f16: D fp32, A = B = bf16, A K-major, B MN-major, M = 128, N = 128
+// instruction descriptor, kind::f16: D fp32, A = B = bf16, A K-major (A read from TMEM), B MN-major,
+// M = 128, N = 128
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
@@ -200,15 +201,32 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint
     return d;
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+// D (TMEM) += A (TMEM: lane m = row m, column c = bf16 pair (2c, 2c+1)) x B (shared memory descriptor)
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(IDESC), "r"(accumulate)
         : "memory");
 }
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+
 
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
@@ -243,19 +261,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
 }
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v)
-{
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p)
 {
@@ -308,6 +313,7 @@ __device__ __forceinline__ RowMeta row_meta(const TcParams& P, int q)
     RowMeta m{0, 0, 0, 0.f, 0.f, 0.f, 0u, 0u};
     if (q >= P.R) return m;
     if (MODE == kDraftMode) {
+        // inputs only (no output of the previous kernel): the A row itself comes from a_next
         const DraftStep& p = P.d;
         int g = p.gamma ? p.gamma[q] : p.G;
         if (g < 0 || g > p.G) {
@@ -316,7 +322,7 @@ __device__ __forceinline__ RowMeta row_meta(const TcParams& P, int q)
         }
         if (p.k >= g) return m;
         m.active = 1;
-        m.prev = checked_index(p.k == 0 ? p.anchor[q] : p.x_cur[q], p.V, p.status);
+        m.prev = q;   // row of a_next
         m.use_bias = (p.k > 0) || p.bias_first;
         m.scale = kLog2e / p.temperature[q];
     } else {
@@ -413,10 +419,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
 
+    pdl_trigger();
     const int nblk = P.nblk;
     const int n_items = *s_ntiles * nblk;
-    const int i0 = (int)((long long)n_items * blockIdx.x / gridDim.x);
-    const int i1 = (int)((long long)n_items * (blockIdx.x + 1) / gridDim.x);
+    // items are dealt round-robin: at any moment the CTAs work on adjacent vocabulary blocks, so
+    // their U and W reads fall in the same DRAM pages
+    const int i0 = blockIdx.x, istep = gridDim.x;
     const int KC = P.r / BK;
 
     if (warp == 0 && lane == 0) {
@@ -425,7 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         Ring ws;
         uint32_t last_par[W_STAGES];
         bool filled[W_STAGES] = {false, false, false, false};
-        for (int it = i0; it < i1 && !*s_abort; ++it) {
+        for (int it = i0; it < n_items && !*s_abort; it += istep) {
             const int b = it % nblk;
             for (int kc = 0; kc < KC; ++kc) {
                 if (!mbar_wait(w_empty(ws.idx), ws.phase ^ 1u, ctl)) break;
@@ -447,7 +455,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         Ring us;
         uint32_t last_par[U_STAGES];
         bool filled[U_STAGES] = {false, false};
-        for (int it = i0; it < i1 && !*s_abort; ++it) {
+        for (int it = i0; it < n_items && !*s_abort; it += istep) {
             const int mt = s_tiles[it / nblk], b = it % nblk;
             if (!mbar_wait(u_empty(us.idx), us.phase ^ 1u, ctl)) break;
             const uint32_t dst = sbase + OFF_U + us.idx * U_STAGE_BYTES;
@@ -466,7 +474,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         Ring ws, tb;
         uint32_t a_par = 0;
         int cur_tile = -1;
-        for (int it = i0; it < i1; ++it) {
+        for (int it = i0; it < n_items; it += istep) {
             const int tile = it / nblk;
             if (tile != cur_tile) {
                 if (cur_tile >= 0) mma_commit(a_empty);   // old A is free once its MMAs retire
@@ -485,13 +493,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a_addr = sbase + OFF_A + kc * A_CHUNK_BYTES;
                 const uint32_t b_addr = sbase + OFF_W + ws.idx * W_STAGE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint64_t ad = sw128_desc(a_addr + kk * 32, 16, 1024);
+                    const uint32_t a_tmem = tmem_base + A_TMEM_COL + (uint32_t)(kc * (BK / 2) + kk * 8);
                     const uint64_t bd = sw128_desc(b_addr + kk * 16 * 128, W_BOX_BYTES, 1024);
-                    mma_bf16(d_tmem, ad, bd, (kc | kk) != 0);
+                    mma_bf16_ts(d_tmem, a_tmem, bd, (kc | kk) != 0);
                 }
                 mma_commit(w_empty(ws.idx));
                 ws.next(W_STAGES);
@@ -502,6 +509,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp >= 4) {
         // ---------------- epilogue (and A gather)
+        // The A rows read the previous kernel's output and the block statistics overwrite what it
+        // read: everything after the first tile's metadata waits for it (programmatic dependent
+        // launch); residual-mode metadata itself reads the previous kernel's output.
+        if (MODE == kResidualMode) pdl_wait();
+        bool waited = MODE == kResidualMode;
         // Every epilogue warp runs the same sequence of named barriers whatever happens: after
         // an abort (a wait that gave up) a warp keeps iterating but skips its memory work, so no
         // warp is ever left alone in a barrier.
@@ -514,7 +526,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int cur_tile = -1;
         RowMeta rm{};
         bool live = true;
-        for (int it = i0; it < i1; ++it) {
+        for (int it = i0; it < n_items; it += istep) {
             const int tile = it / nblk, b = it % nblk;
             const int mt = s_tiles[tile];
             if (tile != cur_tile) {
@@ -523,22 +535,36 @@ __global__ void __launch_bounds__(THREADS, 1)
                     a_par ^= 1u;
                 }
                 if (e < BM) s_meta[e] = row_meta<MODE>(P, mt * BM + e);
+                if (!waited) {
+                    pdl_wait();
+                    waited = true;
+                }
                 epi_barrier();
-                // gather A = W_1[prev] rows into the swizzled K-major tile; all copies in flight at once
-                if (live) {
-                    const int cpr = P.r / 8;   // 16-byte chunks per row
-                    for (int idx = e; idx < BM * cpr; idx += EPI_THREADS) {
-                        const int row = idx / cpr, c = idx % cpr;
-                        const uint32_t dst = sbase + OFF_A + (c >> 3) * A_CHUNK_BYTES + row * 128 +
-                                             ((uint32_t)((c & 7) ^ (row & 7)) << 4);
-                        const RowMeta& mr = s_meta[row];
-                        if (mr.active && mr.use_bias)
-                            cp_async_16(dst, E + (size_t)mr.prev * P.r + c * 8);
-                        else
-                            st_shared_v4(dst, make_uint4(0, 0, 0, 0));
+                // A = W_1[prev] rows into TMEM: warpgroup g writes K elements [64g, 64g + 64) of
+                // its four warps' lanes (32 columns of bf16 pairs), loaded with 8 independent
+                // 16-byte reads per thread
+                if (live && g * BK < P.r) {
+                    const RowMeta& mr = s_meta[m];
+                    uint32_t a[32];
+                    if (mr.active && mr.use_bias) {
+                        const __nv_bfloat16* rows = MODE == kDraftMode ? static_cast<const __nv_bfloat16*>(P.d.a_next) : E;
+                        const uint4* src = reinterpret_cast<const uint4*>(rows + (size_t)mr.prev * P.r + g * BK);
+                        uint4 c8[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) c8[c] = __ldg(src + c);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            a[4 * c] = c8[c].x;
+                            a[4 * c + 1] = c8[c].y;
+                            a[4 * c + 2] = c8[c].z;
+                            a[4 * c + 3] = c8[c].w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) a[c] = 0u;
                     }
-                    cp_async_wait_all();
-                    fence_proxy_async();
+                    tmem_st32(tmem_base + ((uint32_t)(q4 * 32) << 16) + A_TMEM_COL + (uint32_t)(g * 32), a);
+                    tc_fence_before();
                 }
                 epi_barrier();
                 if (e == 0 && live) mbar_arrive(a_full);
@@ -643,7 +669,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 partial = make_float2(rs, 0.f);
             }
-            float2* pp = part + ((it - i0) & 1) * 4 * BM;
+            float2* pp = part + (((it - i0) / istep) & 1) * 4 * BM;
             pp[g * BM + m] = partial;
             epi_barrier();
             if (g == 0 && rm.active && live) {
@@ -659,6 +685,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (t.y > 0.f) S += t.y * ex2(t.x - M);
                     }
                     P.d.stats[o] = make_float2(M, S);
+                    // block-level Gumbel-max of the two-level draw, folded into a packed key
+                    const int q = mt * BM + m;
+                    const float z = (M + log2f(S)) * kLn2 -
+                                    logf(-logf(uniform_at(make_key(P.d.seed), P.d.round, kDraftBlock, (uint32_t)q,
+                                                          (uint32_t)P.k, (uint32_t)b)));
+                    atomicMax(P.d.pick + (size_t)P.k * P.R + q, pack_pick(z, b));
                 } else {
                     P.v.res_stats[o] = pp[m].x + pp[BM + m].x + pp[2 * BM + m].x + pp[3 * BM + m].x;
                 }
@@ -756,16 +788,27 @@ cudaError_t encode_u(CUtensorMap* m, const void* U, int V, int G, int R)
 template <int MODE>
 cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorMap& tmU, cudaStream_t s)
 {
-    static bool attr = false;
-    if (!attr) {
+    static bool smem_set = false;
+    if (!smem_set) {
         const cudaError_t e =
             cudaFuncSetAttribute(stats_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr = true;
+        smem_set = true;
     }
     const int items = ((P.R + BM - 1) / BM) * P.nblk;
     const int grid = items < num_sms() ? items : num_sms();
-    stats_tc_kernel<MODE><<<grid, THREADS, SMEM_BYTES, s>>>(P, tmW, tmU);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, stats_tc_kernel<MODE>, P, tmW, tmU);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
