@@ -49,6 +49,7 @@ extern "C" {
 #define DSPARK_NOISE_BLOCK 128   /* vocabulary block width of the two-level Gumbel-max */
 #define DSPARK_MAX_GAMMA 32      /* largest draft block length gamma_max */
 #define DSPARK_MAX_SLOTS 8192    /* largest R * gamma_max the scheduler accepts */
+#define DSPARK_STATIC_WORKSPACE_BYTES (8u << 20)  /* scratch of dspark_sample_block_static */
 
 typedef int32_t dspark_status;
 enum {
@@ -124,6 +125,28 @@ dspark_status dspark_sample_workspace_size(const dspark_sample_args* args, size_
 int32_t dspark_sample_path(const dspark_sample_args* args);
 dspark_status dspark_sample_block(const dspark_sample_args* args, void* workspace, size_t workspace_bytes,
                                   void* stream);
+
+/*
+ * dspark_sample_block_static -- dspark_sample_block for callers that cannot allocate device
+ * memory (no counterpart in the paper: it is a deployment convenience). Some callers cannot
+ * call cudaMalloc where they run a round -- code living inside another framework's memory pool
+ * without access to its allocator, code that must not grow the device footprint after start-up,
+ * or runtimes that only hand the library its input and output buffers. This entry point takes
+ * no workspace: its scratch lives in one file-scope device array of
+ * DSPARK_STATIC_WORKSPACE_BYTES (8 MiB) that every GPU loading the library holds until the
+ * process exits. It calls no cudaMalloc, cudaFree or allocating library routine.
+ *  - Arguments and results are those of dspark_sample_block.
+ *  - Shapes whose dspark_sample_workspace_size exceeds DSPARK_STATIC_WORKSPACE_BYTES return
+ *    DSPARK_ERR_UNSUPPORTED_SHAPE before any launch.
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *    that device current; make that first call before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the previous call's contents (the
+ *    call clears what must start at zero). Calls whose work overlaps on the GPU (other streams,
+ *    other host threads) race on it: serialise them.
+ *  - Device-side status (clamped out-of-range device inputs) is kept in the array and not
+ *    reported; use dspark_sample_block with a workspace and dspark_check to observe it.
+ */
+dspark_status dspark_sample_block_static(const dspark_sample_args* args, void* stream);
 
 /*
  * dspark_schedule -- hardware-aware prefix scheduler (Algorithm 1; "admit").

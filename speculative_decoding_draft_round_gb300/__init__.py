@@ -73,7 +73,7 @@ class VerifyArgs(C.Structure):
 EXPORTS = ("dspark_sample_workspace_size", "dspark_sample_block", "dspark_schedule_workspace_size",
            "dspark_schedule", "dspark_verify_workspace_size", "dspark_verify", "dspark_check",
            "dspark_status_string", "dspark_abi_version", "dspark_launch_count", "dspark_time_kernel",
-           "dspark_last_error", "dspark_sample_path")
+           "dspark_last_error", "dspark_sample_path", "dspark_sample_block_static")
 
 KERNELS = {"conf_hidden": 0, "draft_stats": 1, "draft_commit": 2, "schedule": 3, "verify_rows": 4,
            "verify_decide": 5, "residual_stats": 6, "residual_pick": 7}
@@ -116,6 +116,8 @@ def lib():
         L.dspark_status_string.restype = C.c_char_p
         L.dspark_abi_version.argtypes = []
         L.dspark_abi_version.restype = C.c_int32
+        L.dspark_sample_block_static.argtypes = [C.POINTER(SampleArgs), _vp]
+        L.dspark_sample_block_static.restype = C.c_int32
         L.dspark_sample_path.argtypes = [C.POINTER(SampleArgs)]
         L.dspark_sample_path.restype = C.c_int32
         L.dspark_last_error.argtypes = []
@@ -279,6 +281,20 @@ def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gam
     ws = _workspace("dspark_sample_workspace_size", a, workspace, U.device)
     _call("dspark_sample_block", C.byref(a), _ptr(ws), ws.numel(), _stream(stream))
     out["workspace"] = ws
+    return out
+
+
+STATIC_WORKSPACE_BYTES = 8 << 20
+
+
+def sample_block_static(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamma=None, conf_token=0,
+                        bias_first=1, path=PATH_AUTO, out=None, stream=None):
+    """dspark_sample_block_static: the sampler with its scratch in the library's static device
+    array (for callers that cannot allocate device memory). Only the output tensors are
+    allocated here, by torch, when `out` is not given."""
+    a, out = sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, gamma=gamma,
+                         conf_token=conf_token, bias_first=bias_first, path=path, out=out)
+    _call("dspark_sample_block_static", C.byref(a), _stream(stream))
     return out
 
 
