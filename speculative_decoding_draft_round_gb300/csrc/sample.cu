@@ -51,8 +51,21 @@ __global__ void __launch_bounds__(256) conf_hidden_kernel(DraftStep p)
     const bool vec = (p.d % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.h) & 15u) == 0) &&
                      ((reinterpret_cast<uintptr_t>(p.w_h) & 15u) == 0);
     if (vec) {
-        // 8 elements (16 bytes of bf16, 32 of fp32) per lane per step, all loads independent
-        for (int j = lane * 8; j < p.d; j += 256) {
+        // 8 elements (16 bytes of bf16, 32 of fp32) per lane per step, four steps' loads in flight
+        int j = lane * 8;
+        for (; j + 3 * 256 < p.d; j += 4 * 256) {
+            float w[4][8], x[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                load8<T>(h + j + u * 256, x[u]);
+                load8<float>(p.w_h + j + u * 256, w[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc = fmaf(w[u][e], x[u][e], acc);
+        }
+        for (; j < p.d; j += 256) {
             float w[8], x[8];
             load8<T>(h + j, x);
             load8<float>(p.w_h + j, w);
@@ -215,7 +228,8 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
         }
         return;
     }
-    const int prev = checked_index(p.k == 0 ? p.anchor[q] : p.x_cur[q], p.V, p.status);
+    // W_1[x_{k-1}] is the conditioning row the previous commit (or conf_hidden for k = 0) wrote
+    const T* prev_row = static_cast<const T*>(p.a_next) + (size_t)q * p.r;
     const T* E = static_cast<const T*>(p.E);
     const T* W = static_cast<const T*>(p.W);
     const T* U = static_cast<const T*>(p.U);
@@ -237,7 +251,7 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     float e_prev = 0.f;
     const bool need_prev_row = rq.use_bias || !p.conf_token;
     for (int i = t; i < p.r; i += kCommitThreads) {
-        const float ev = need_prev_row ? ld(E, (size_t)prev * p.r + i) : 0.f;
+        const float ev = need_prev_row ? ld(prev_row, i) : 0.f;
         if (i == t) e_prev = ev;
         erow[i] = ev;
     }

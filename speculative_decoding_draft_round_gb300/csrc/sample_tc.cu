@@ -39,8 +39,6 @@ constexpr int BM = 128;             // requests per tile = TMEM lanes
 constexpr int BN = 128;             // vocabulary columns per item = one noise block
 constexpr int BK = 64;              // K per shared-memory chunk (128 bytes of bf16)
 constexpr int KMAX = 256;           // largest Markov rank held in the A tile
-constexpr int W_STAGES = 8;
-constexpr int U_STAGES = 2;
 constexpr int TMEM_BUFS = 3;
 constexpr int EPI_WARPS = 16;
 constexpr int EPI_THREADS = EPI_WARPS * 32;
@@ -52,19 +50,31 @@ static_assert(A_TMEM_COL + KMAX / 2 <= TMEM_COLS, "accumulators and A must fit i
 constexpr uint32_t W_BOX_BYTES = BK * 64 * 2;        // 8 KB: [64 K x 64 N]
 constexpr uint32_t W_STAGE_BYTES = 2 * W_BOX_BYTES;  // 16 KB
 constexpr uint32_t U_BOX_BYTES = BM * 64 * 2;        // 16 KB: [128 rows x 64 N]
-constexpr uint32_t U_STAGE_BYTES = 2 * U_BOX_BYTES;  // 32 KB
 
-constexpr uint32_t OFF_W = 0;
-constexpr uint32_t OFF_U = OFF_W + W_STAGES * W_STAGE_BYTES;
-constexpr uint32_t OFF_PART = OFF_U + U_STAGES * U_STAGE_BYTES;           // [2][4][128] float2
-constexpr uint32_t OFF_META = OFF_PART + 2 * 4 * BM * 8;                   // per-row metadata, see RowMeta
-constexpr uint32_t META_BYTES = BM * 32;
-constexpr uint32_t OFF_BAR = OFF_META + META_BYTES;
-constexpr int N_BARS = 2 * W_STAGES + 2 * U_STAGES + 2 * TMEM_BUFS + 2;
-constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
+enum Mode { kDraftMode = 0, kResidualMode = 1 };
+
 constexpr int MAX_TILES = 64;                                              // R <= 8192
-constexpr uint32_t SMEM_USED = OFF_MISC + 16 + MAX_TILES * 4;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;                          // alignment slack
+constexpr uint32_t META_BYTES = BM * 32;
+constexpr uint32_t RES_ROW_BYTES = 272;   // residual stage row: 256 bytes of 128 bf16 + 16 bytes padding
+
+// Shared-memory layout of one mode. Draft mode: 8 W stages, U stages of two 128-byte-swizzled
+// [128 x 64] boxes. Residual mode: 4 W stages; a U stage holds 128 U rows then 128 target rows of
+// one item, RES_ROW_BYTES apart (the padding keeps the thread-per-row reads conflict-free).
+template <int MODE>
+struct Lay {
+    static constexpr int W_ST = MODE == kDraftMode ? 8 : 4;
+    static constexpr int U_ST = 2;
+    static constexpr uint32_t U_ST_BYTES = MODE == kDraftMode ? 2 * U_BOX_BYTES : 2 * BM * RES_ROW_BYTES;
+    static constexpr uint32_t OFF_W = 0;
+    static constexpr uint32_t OFF_U = OFF_W + W_ST * W_STAGE_BYTES;
+    static constexpr uint32_t OFF_PART = OFF_U + U_ST * U_ST_BYTES;        // [2][4][128] float2
+    static constexpr uint32_t OFF_META = OFF_PART + 2 * 4 * BM * 8;        // per-row metadata, see RowMeta
+    static constexpr uint32_t OFF_BAR = OFF_META + META_BYTES;
+    static constexpr int N_BARS = 2 * W_ST + 2 * U_ST + 2 * TMEM_BUFS + 2;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
+    static constexpr uint32_t SMEM_USED = OFF_MISC + 16 + MAX_TILES * 4;
+    static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;               // alignment slack
+};
 
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;   // 4 s
 
@@ -262,18 +272,15 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t policy)
 {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
 }
 
 // ------------------------------------------------------------------ kernel
-
-enum Mode { kDraftMode = 0, kResidualMode = 1 };
 
 // Per-row metadata of the current request tile (shared memory, 32 bytes per row).
 struct RowMeta {
@@ -360,9 +367,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
-    float2* part = reinterpret_cast<float2*>(smem + OFF_PART);
-    RowMeta* s_meta = reinterpret_cast<RowMeta*>(smem + OFF_META);
-    const uint32_t bar0 = sbase + OFF_BAR;
+    using L = Lay<MODE>;
+    constexpr int W_STAGES = L::W_ST, U_STAGES = L::U_ST;
+    constexpr uint32_t OFF_W = L::OFF_W, OFF_U = L::OFF_U, OFF_MISC = L::OFF_MISC;
+    constexpr uint32_t U_STAGE_BYTES = L::U_ST_BYTES;
+    float2* part = reinterpret_cast<float2*>(smem + L::OFF_PART);
+    RowMeta* s_meta = reinterpret_cast<RowMeta*>(smem + L::OFF_META);
+    const uint32_t bar0 = sbase + L::OFF_BAR;
     auto w_full = [&](int i) { return bar0 + 8u * i; };
     auto w_empty = [&](int i) { return bar0 + 8u * (W_STAGES + i); };
     auto u_full = [&](int i) { return bar0 + 8u * (2 * W_STAGES + i); };
@@ -432,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint64_t pol = l2_policy_evict_last();
         Ring ws;
         uint32_t last_par[W_STAGES];
-        bool filled[W_STAGES] = {false, false, false, false};
+        bool filled[W_STAGES] = {};
         for (int it = i0; it < n_items && !*s_abort; it += istep) {
             const int b = it % nblk;
             for (int kc = 0; kc < KC; ++kc) {
@@ -467,6 +478,60 @@ __global__ void __launch_bounds__(THREADS, 1)
             us.next(U_STAGES);
         }
         if (*s_abort)
+            for (int i = 0; i < U_STAGES; ++i)
+                if (filled[i]) mbar_drain(u_full(i), last_par[i]);
+    } else if (MODE == kResidualMode && warp == 3) {
+        // ---------------- residual U / target producer: lane l copies rows l, l+32, l+64, l+96 of
+        // the tile (256 bytes of U and of the target per active row) with 1-D bulk copies
+        pdl_wait();   // rej (rejected positions) comes from the previous kernel
+        const uint64_t pol = l2_policy_evict_first();
+        const char* Ub = static_cast<const char*>(P.v.U);
+        const char* Tb = static_cast<const char*>(P.v.target);
+        Ring us;
+        uint32_t last_par[U_STAGES];
+        bool filled[U_STAGES] = {};
+        int cur_tile = -1, cur_mt = 0, n_act = 0;
+        bool act[4] = {false, false, false, false};
+        uint32_t urow[4] = {0, 0, 0, 0};   // U row index q * G + n; the target row is urow + q
+        for (int it = i0; it < n_items && !*s_abort; it += istep) {
+            const int tile = it / nblk, b = it % nblk;
+            if (tile != cur_tile) {
+                const int mt = s_tiles[tile];
+                int cnt = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int q = mt * BM + lane + 32 * j;
+                    const int n = q < P.R ? P.v.rej[q] : -1;
+                    act[j] = n >= 0 && n < P.G;
+                    urow[j] = act[j] ? (uint32_t)(q * P.G + n) : 0u;
+                    cnt += act[j] ? 1 : 0;
+                }
+                n_act = __reduce_add_sync(0xffffffffu, cnt);
+                cur_tile = tile;
+                cur_mt = mt;
+            }
+            const int cols = min(BN, P.V - b * BN);   // V % 8 == 0: a multiple of 16 bytes
+            const uint32_t row_bytes = (uint32_t)cols * 2;
+            if (!warp_wait(u_empty(us.idx), us.phase ^ 1u, ctl)) break;
+            const uint32_t dst = sbase + OFF_U + us.idx * U_STAGE_BYTES;
+            if (lane == 0) mbar_expect_tx(u_full(us.idx), (uint32_t)n_act * 2u * row_bytes);
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (!act[j]) continue;
+                const uint32_t m = lane + 32 * j;
+                const uint32_t trow = urow[j] + (uint32_t)(cur_mt * BM) + m;   // q * (G + 1) + n
+                const size_t col_off = (size_t)b * BN * 2;
+                bulk_load(dst + m * RES_ROW_BYTES, Ub + (size_t)urow[j] * P.V * 2 + col_off, row_bytes,
+                          u_full(us.idx), pol);
+                bulk_load(dst + BM * RES_ROW_BYTES + m * RES_ROW_BYTES, Tb + (size_t)trow * P.V * 2 + col_off,
+                          row_bytes, u_full(us.idx), pol);
+            }
+            filled[us.idx] = true;
+            last_par[us.idx] = us.phase;
+            us.next(U_STAGES);
+        }
+        if (*s_abort && lane == 0)
             for (int i = 0; i < U_STAGES; ++i)
                 if (filled[i]) mbar_drain(u_full(i), last_par[i]);
     } else if (warp == 1 && lane == 0) {
@@ -586,16 +651,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lane == 0) mbar_arrive(u_empty(us.idx));
                 }
                 us.next(U_STAGES);
-            } else if (live && rm.active) {
-                const __nv_bfloat16* U = static_cast<const __nv_bfloat16*>(P.v.U) + (size_t)rm.u_row * P.V;
-                const __nv_bfloat16* Tg = static_cast<const __nv_bfloat16*>(P.v.target) + (size_t)rm.t_row * P.V;
+            } else {
+                u_ok = live && warp_wait(u_full(us.idx), us.phase, ctl);
+                if (u_ok) {
+                    const uint32_t ubase = sbase + OFF_U + us.idx * U_STAGE_BYTES + m * RES_ROW_BYTES + g * 64;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (v0 + 8 * c < P.V) {   // V % 8 == 0: each 8-column chunk is all in or all out
-                        uv[c] = ld_stream_v4(U + v0 + 8 * c);
-                        tv[c] = ld_stream_v4(Tg + v0 + 8 * c);
+                    for (int c = 0; c < 4; ++c) {
+                        uv[c] = ld_shared_v4(ubase + c * 16);
+                        tv[c] = ld_shared_v4(ubase + BM * RES_ROW_BYTES + c * 16);
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(u_empty(us.idx));
                 }
+                us.next(U_STAGES);
             }
             // accumulator columns 32g .. 32g+31 of this row
             uint32_t acc[32];
@@ -788,6 +856,7 @@ cudaError_t encode_u(CUtensorMap* m, const void* U, int V, int G, int R)
 template <int MODE>
 cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorMap& tmU, cudaStream_t s)
 {
+    constexpr uint32_t SMEM_BYTES = Lay<MODE>::SMEM_BYTES;
     static bool smem_set = false;
     if (!smem_set) {
         const cudaError_t e =

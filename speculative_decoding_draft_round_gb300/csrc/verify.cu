@@ -43,47 +43,75 @@ __device__ __forceinline__ int request_keep(const VerifyParams& p, int q)
 // ----------------------------------------------------------------- target row statistics
 
 constexpr int kRowWarps = 8;
-constexpr int kRowBlocksPerWarp = 4;
+constexpr int kRowBlocksPerWarp = 8;   // 1024 columns per warp: four 16-byte loads per lane
 
-// Block (max, sum exp2) of one 128-wide block of z/T, log2 units, computed by one warp.
+// Block (max, sum exp2) of z/T (log2 units) for the 8 consecutive 128-wide blocks starting at
+// block b0, one warp: in the vector path lane l owns columns 256j + 8l .. +7 (j = 0..3), so
+// half-warp h of load j covers block b0 + 2j + h; all four loads are issued before any use.
 template <typename T>
-__device__ __forceinline__ float2 row_block_stats(const T* row, int V, int b, float scale, int lane, bool vec)
+__device__ __forceinline__ void row_block_stats8(const T* row, int V, int b0, float scale, int lane, bool vec,
+                                                 float2 (&out)[kRowBlocksPerWarp])
 {
-    float x[4];
-    if (vec) {
-        // lane owns 4 consecutive columns; V % 4 == 0 so they are all in or all out
-        const int v = b * kNoiseBlock + lane * 4;
-        if (v < V) {
-            if (sizeof(T) == 2) {
-                const uint2 u = __ldg(reinterpret_cast<const uint2*>(row + v));
-                x[0] = __uint_as_float(u.x << 16);
-                x[1] = __uint_as_float(u.x & 0xFFFF0000u);
-                x[2] = __uint_as_float(u.y << 16);
-                x[3] = __uint_as_float(u.y & 0xFFFF0000u);
-            } else {
-                const float4 f = __ldg(reinterpret_cast<const float4*>(row + v));
-                x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+    const int half = lane >> 4;
+    if (vec && sizeof(T) == 2) {
+        uint4 raw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int v = b0 * kNoiseBlock + j * 256 + lane * 8;
+            raw[j] = v < V ? __ldg(reinterpret_cast<const uint4*>(row + v)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int v = b0 * kNoiseBlock + j * 256 + lane * 8;
+            const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+            float x[8];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                x[2 * h] = __uint_as_float(w4[h] << 16) * scale;
+                x[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u) * scale;
+            }
+            const bool in = v < V;   // V % 8 == 0: 8 columns all in or all out
+            float m = -INFINITY;
+            if (in) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m = fmaxf(m, x[e]);
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] *= scale;
-        } else {
+            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            float sacc = 0.f;
+            if (in && m > -INFINITY) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[e] = -INFINITY;
+                for (int e = 0; e < 8; ++e) sacc += exp2f(x[e] - m);
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
+            const float m0 = __shfl_sync(0xffffffffu, m, 0), s0 = __shfl_sync(0xffffffffu, sacc, 0);
+            const float m1 = __shfl_sync(0xffffffffu, m, 16), s1 = __shfl_sync(0xffffffffu, sacc, 16);
+            out[2 * j] = make_float2(m0, s0);
+            out[2 * j + 1] = make_float2(m1, s1);
+            (void)half;
         }
     } else {
+#pragma unroll 1
+        for (int bb = 0; bb < kRowBlocksPerWarp; ++bb) {
+            const int b = b0 + bb;
+            float x[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int v = b * kNoiseBlock + e * 32 + lane;
-            x[e] = v < V ? ld(row, v) * scale : -INFINITY;
+            for (int e = 0; e < 4; ++e) {
+                const int v = b * kNoiseBlock + e * 32 + lane;
+                x[e] = v < V ? ld(row, v) * scale : -INFINITY;
+            }
+            float m = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            m = warp_max(m);
+            float sacc = 0.f;
+            if (m > -INFINITY) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc += exp2f(x[e] - m);
+            }
+            sacc = warp_sum(sacc);
+            out[bb] = make_float2(m, sacc);
         }
     }
-    float m = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    m = warp_max(m);
-    float s = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) s += exp2f(x[e] - m);
-    s = warp_sum(s);
-    return make_float2(m, s);
 }
 
 // grid (vocabulary chunks, R): the CTA walks target rows 0..keep[r] of its request
@@ -94,19 +122,20 @@ __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParam
     const int ell = request_keep(p, q);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float scale = kLog2e / p.temperature[q];
-    const bool vec = (p.V % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.target) & 15u) == 0);
+    const bool vec = (p.V % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.target) & 15u) == 0);
     const int b0 = (blockIdx.x * kRowWarps + warp) * kRowBlocksPerWarp;
+    if (b0 >= p.nblk) return;
     for (int i = 0; i <= ell; ++i) {
         const T* row = static_cast<const T*>(p.target) + ((size_t)q * (p.G + 1) + i) * p.V;
         float2* out = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
         float2 st[kRowBlocksPerWarp];
+        row_block_stats8<T>(row, p.V, b0, scale, lane, vec, st);
+        if (lane < kRowBlocksPerWarp && b0 + lane < p.nblk) {
+            float2 v = st[0];
 #pragma unroll
-        for (int bb = 0; bb < kRowBlocksPerWarp; ++bb)
-            if (b0 + bb < p.nblk) st[bb] = row_block_stats<T>(row, p.V, b0 + bb, scale, lane, vec);
-        if (lane == 0) {
-#pragma unroll
-            for (int bb = 0; bb < kRowBlocksPerWarp; ++bb)
-                if (b0 + bb < p.nblk) out[b0 + bb] = st[bb];
+            for (int bb = 1; bb < kRowBlocksPerWarp; ++bb)
+                if (lane == bb) v = st[bb];
+            out[b0 + lane] = v;
         }
     }
 }
