@@ -106,8 +106,9 @@ SampleLayout sample_layout(const dspark_sample_args* a)
     o = align_up(o + sizeof(float2) * rows * nblk, kAlign);
     L.pick = o;
     o = align_up(o + sizeof(unsigned long long) * (size_t)a->R * a->gamma_max, kAlign);
-    L.a_next = o;
-    o = align_up(o + (a->dtype == DSPARK_BF16 ? 2 : 4) * (size_t)a->R * a->r, kAlign);
+    L.a_next = o;   // the tensor-core path keeps kAReplicas copies of the next step's A rows
+    o = align_up(o + (sample_uses_tc(a) ? kAReplicas : 1) * (a->dtype == DSPARK_BF16 ? 2 : 4) * (size_t)a->R * a->r,
+                 kAlign);
     L.total = o;
     return L;
 }
@@ -260,6 +261,7 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.pick = at<unsigned long long>(ws, L.pick);
     p.a_next = at<unsigned char>(ws, L.a_next);
     const bool tc = sample_uses_tc(a);
+    p.a_replicas = tc ? kAReplicas : 1;
     cudaError_t e = launch(DSPARK_KERNEL_CONF_HIDDEN, s, [&] { return launch_conf_hidden(p, s); });
     for (int k = 0; k < a->gamma_max && e == cudaSuccess; ++k) {
         p.k = k;

@@ -10,6 +10,10 @@
 
 namespace dspark {
 
+// Copies of the next step's A rows the tensor-core draft path keeps, so that the 152 CTAs reading
+// the same 64 KB tile spread over 8 copies instead of one.
+constexpr int kAReplicas = 8;
+
 // One serial step of the draft sampler (dspark_sample_block).
 struct DraftStep {
     int R, G, V, r, d, k, nblk;
@@ -36,7 +40,9 @@ struct DraftStep {
     float* hw;           // [R][G] w_h . h[r][k]
     float2* stats;       // [R_pad][nblk] (max, sum) of exp2 over each vocabulary block, log2 units
     unsigned long long* pick;   // [G][R] packed block-level arg-max of each step (cleared per call)
-    void* a_next;        // [R][r] (element type of E): W_1 row of the token each request conditions on next
+    void* a_next;        // [a_replicas][R][r] (element type of E): W_1 row of the token each request
+                         // conditions on next, in a_replicas identical copies
+    int a_replicas;      // 1 (CUDA-core path) or kAReplicas (tensor-core path: each CTA reads one copy)
 };
 
 // Verification (dspark_verify).

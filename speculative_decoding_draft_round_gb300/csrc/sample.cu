@@ -33,11 +33,13 @@ __global__ void __launch_bounds__(256) conf_hidden_kernel(DraftStep p)
     {
         const T* E = static_cast<const T*>(p.E);
         T* an = static_cast<T*>(p.a_next);
-        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)p.R * p.r;
+        const size_t n = (size_t)p.R * p.r;
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)n;
              i += (long long)gridDim.x * blockDim.x) {
             const int q = (int)(i / p.r), c = (int)(i % p.r);
             const int x0 = checked_index(p.anchor[q], p.V, p.status);
-            an[i] = E[(size_t)x0 * p.r + c];
+            const T v = E[(size_t)x0 * p.r + c];
+            for (int rp = 0; rp < p.a_replicas; ++rp) an[rp * n + i] = v;
         }
     }
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -343,9 +345,10 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     // ---- phase C: W_1[x_k] for the next step's conditioning rows and the confidence head (eq. 7)
     float dot = 0.f;
     T* an = static_cast<T*>(p.a_next) + (size_t)q * p.r;
+    const size_t rep_stride = (size_t)p.R * p.r;
     for (int i = t; i < p.r; i += kCommitThreads) {
         const T et = E[(size_t)tok * p.r + i];
-        an[i] = et;
+        for (int rp = 0; rp < p.a_replicas; ++rp) an[rp * rep_stride + i] = et;
         dot = fmaf(p.w_e[i], p.conf_token ? to_f32<T>(et) : erow[i], dot);   // eq. (7) reads W_1[x_{k-1}]
     }
     (void)e_prev;

@@ -53,33 +53,41 @@ constexpr uint32_t U_BOX_BYTES = BM * 64 * 2;        // 16 KB: [128 rows x 64 N]
 
 enum Mode { kDraftMode = 0, kResidualMode = 1 };
 
+constexpr int A_REPLICAS = kAReplicas;   // copies of the draft A rows, so that ~19 CTAs share one
+
 constexpr int MAX_TILES = 64;                                              // R <= 8192
 constexpr uint32_t META_BYTES = BM * 32;
 constexpr uint32_t RES_ROW_BYTES = 272;   // residual stage row: 256 bytes of 128 bf16 + 16 bytes padding
 
-// Shared-memory layout of one mode. Draft mode: 8 W stages, U stages of two 128-byte-swizzled
-// [128 x 64] boxes. Residual mode: 4 W stages; a U stage holds 128 U rows then 128 target rows of
-// one item, RES_ROW_BYTES apart (the padding keeps the thread-per-row reads conflict-free).
+// Shared-memory layout of one mode. Draft mode: 5 W stages, U stages of two 128-byte-swizzled
+// [128 x 64] boxes, and the A tile (the W_1 rows of the tile's previous tokens, K-major,
+// 128-byte swizzle, r/64 boxes of [128 x 64]) loaded by TMA. Residual mode: 4 W stages; a U
+// stage holds 128 U rows then 128 target rows of one item, RES_ROW_BYTES apart (the padding
+// keeps the thread-per-row reads conflict-free); A lives in TMEM.
 template <int MODE>
 struct Lay {
-    static constexpr int W_ST = MODE == kDraftMode ? 8 : 4;
+    static constexpr int W_ST = MODE == kDraftMode ? 5 : 4;
     static constexpr int U_ST = 2;
     static constexpr uint32_t U_ST_BYTES = MODE == kDraftMode ? 2 * U_BOX_BYTES : 2 * BM * RES_ROW_BYTES;
+    static constexpr uint32_t A_BYTES = MODE == kDraftMode ? BM * KMAX * 2 : 0;   // draft: A tile in shared memory
     static constexpr uint32_t OFF_W = 0;
     static constexpr uint32_t OFF_U = OFF_W + W_ST * W_STAGE_BYTES;
-    static constexpr uint32_t OFF_PART = OFF_U + U_ST * U_ST_BYTES;        // [2][4][128] float2
+    static constexpr uint32_t OFF_A = OFF_U + U_ST * U_ST_BYTES;           // 1024-byte aligned
+    static constexpr uint32_t OFF_PART = OFF_A + A_BYTES;                   // [2][4][128] float2
     static constexpr uint32_t OFF_META = OFF_PART + 2 * 4 * BM * 8;        // per-row metadata, see RowMeta
     static constexpr uint32_t OFF_BAR = OFF_META + META_BYTES;
     static constexpr int N_BARS = 2 * W_ST + 2 * U_ST + 2 * TMEM_BUFS + 2;
     static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16 + MAX_TILES * 4;
     static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;               // alignment slack
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+    static_assert(OFF_A % 1024 == 0, "A tile on a 1024-byte boundary (128-byte swizzle atoms)");
 };
 
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;   // 4 s
 
-// instruction descriptor, kind::f16: D fp32, A = B = bf16, A K-major (A read from TMEM), B MN-major,
-// M = 128, N = 128
+// instruction descriptor, kind::f16: D fp32, A = B = bf16, A K-major (shared memory in draft mode,
+// TMEM in residual mode), B MN-major, M = 128, N = 128
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u << 16) |
                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
@@ -219,6 +227,17 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+
+// D (TMEM) += A (shared memory descriptor) x B (shared memory descriptor)
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
         : "memory");
 }
 
@@ -362,7 +381,8 @@ struct Ring {
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    stats_tc_kernel(const TcParams P, const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU)
+    stats_tc_kernel(const TcParams P, const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU,
+                    const __grid_constant__ CUtensorMap tmA)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -391,7 +411,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const Ctl ctl{s_abort, P.status};
     const int n_mt = (P.R + BM - 1) / BM;
 
-    // tiles with at least one request still drafting at step k
+    // tiles with at least one request taking part (residual mode: which requests were rejected
+    // comes from the previous kernel)
+    if (MODE == kResidualMode) pdl_wait();
     if (tid == 0) {
         *s_ntiles = 0;
         *s_abort = 0;
@@ -561,9 +583,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t b_addr = sbase + OFF_W + ws.idx * W_STAGE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint32_t a_tmem = tmem_base + A_TMEM_COL + (uint32_t)(kc * (BK / 2) + kk * 8);
                     const uint64_t bd = sw128_desc(b_addr + kk * 16 * 128, W_BOX_BYTES, 1024);
-                    mma_bf16_ts(d_tmem, a_tmem, bd, (kc | kk) != 0);
+                    if (MODE == kDraftMode) {
+                        // A: box kc of the tile in shared memory, K-major; 16 K elements = 32 bytes per step
+                        const uint64_t ad = sw128_desc(sbase + L::OFF_A + kc * (BM * 128) + kk * 32, 16, 1024);
+                        mma_bf16_ss(d_tmem, ad, bd, (kc | kk) != 0);
+                    } else {
+                        const uint32_t a_tmem = tmem_base + A_TMEM_COL + (uint32_t)(kc * (BK / 2) + kk * 8);
+                        mma_bf16_ts(d_tmem, a_tmem, bd, (kc | kk) != 0);
+                    }
                 }
                 mma_commit(w_empty(ws.idx));
                 ws.next(W_STAGES);
@@ -605,34 +633,47 @@ __global__ void __launch_bounds__(THREADS, 1)
                     waited = true;
                 }
                 epi_barrier();
-                // A = W_1[prev] rows into TMEM: warpgroup g writes K elements [64g, 64g + 64) of
-                // its four warps' lanes (32 columns of bf16 pairs), loaded with 8 independent
-                // 16-byte reads per thread
-                if (live && g * BK < P.r) {
-                    const RowMeta& mr = s_meta[m];
-                    uint32_t a[32];
-                    if (mr.active && mr.use_bias) {
-                        const __nv_bfloat16* rows = MODE == kDraftMode ? static_cast<const __nv_bfloat16*>(P.d.a_next) : E;
-                        const uint4* src = reinterpret_cast<const uint4*>(rows + (size_t)mr.prev * P.r + g * BK);
-                        uint4 c8[8];
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) c8[c] = __ldg(src + c);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            a[4 * c] = c8[c].x;
-                            a[4 * c + 1] = c8[c].y;
-                            a[4 * c + 2] = c8[c].z;
-                            a[4 * c + 3] = c8[c].w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) a[c] = 0u;
+                if (MODE == kDraftMode) {
+                    // A = the tile's rows of a_next (W_1 of the previous tokens, written by the
+                    // previous kernel) from this CTA's replica, one TMA tile per 64 columns
+                    if (e == 0 && live) {
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        mbar_expect_tx(a_full, (uint32_t)(P.r / BK) * BM * 128u);
+                        const uint64_t pol = l2_policy_evict_last();
+                        for (int cb = 0; cb < P.r / BK; ++cb)
+                            tma_load_3d(sbase + L::OFF_A + cb * (BM * 128), &tmA, cb * BK, mt * BM,
+                                        (int)(blockIdx.x % A_REPLICAS), a_full, pol);
                     }
-                    tmem_st32(tmem_base + ((uint32_t)(q4 * 32) << 16) + A_TMEM_COL + (uint32_t)(g * 32), a);
-                    tc_fence_before();
+                } else {
+                    // A = W_1[prev] rows into TMEM: warpgroup g writes K elements [64g, 64g + 64) of
+                    // its four warps' lanes (32 columns of bf16 pairs), loaded with 8 independent
+                    // 16-byte reads per thread
+                    if (live && g * BK < P.r) {
+                        const RowMeta& mr = s_meta[m];
+                        uint32_t a[32];
+                        if (mr.active && mr.use_bias) {
+                            const __nv_bfloat16* rows = E;
+                            const uint4* src = reinterpret_cast<const uint4*>(rows + (size_t)mr.prev * P.r + g * BK);
+                            uint4 c8[8];
+    #pragma unroll
+                            for (int c = 0; c < 8; ++c) c8[c] = __ldg(src + c);
+    #pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                a[4 * c] = c8[c].x;
+                                a[4 * c + 1] = c8[c].y;
+                                a[4 * c + 2] = c8[c].z;
+                                a[4 * c + 3] = c8[c].w;
+                            }
+                        } else {
+    #pragma unroll
+                            for (int c = 0; c < 32; ++c) a[c] = 0u;
+                        }
+                        tmem_st32(tmem_base + ((uint32_t)(q4 * 32) << 16) + A_TMEM_COL + (uint32_t)(g * 32), a);
+                        tc_fence_before();
+                    }
+                    epi_barrier();
+                    if (e == 0 && live) mbar_arrive(a_full);
                 }
-                epi_barrier();
-                if (e == 0 && live) mbar_arrive(a_full);
                 rm = s_meta[m];
                 cur_tile = tile;
             }
@@ -687,8 +728,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     const int j = c * 8 + h * 2;
-                    x[j] = __uint_as_float(w4[h] << 16) + __uint_as_float(acc[j]);
-                    x[j + 1] = __uint_as_float(w4[h] & 0xFFFF0000u) + __uint_as_float(acc[j + 1]);
+                    x[j] = __uint_as_float(w4[h] << 16) + (rm.use_bias ? __uint_as_float(acc[j]) : 0.f);
+                    x[j + 1] = __uint_as_float(w4[h] & 0xFFFF0000u) + (rm.use_bias ? __uint_as_float(acc[j + 1]) : 0.f);
                 }
             }
             const bool tail = v0 + 32 > P.V;
@@ -853,8 +894,23 @@ cudaError_t encode_u(CUtensorMap* m, const void* U, int V, int G, int R)
                : cudaErrorInvalidValue;
 }
 
+// the draft A rows a_next, A_REPLICAS copies of [R][r]: boxes of 64 columns x 128 rows
+cudaError_t encode_a(CUtensorMap* m, const void* A, int R, int r)
+{
+    const cuuint64_t dims[3] = {(cuuint64_t)r, (cuuint64_t)R, (cuuint64_t)A_REPLICAS};
+    const cuuint64_t strides[2] = {(cuuint64_t)r * 2, (cuuint64_t)R * r * 2};
+    const cuuint32_t box[3] = {BK, BM, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(A), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? cudaSuccess
+               : cudaErrorInvalidValue;
+}
+
 template <int MODE>
-cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorMap& tmU, cudaStream_t s)
+cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorMap& tmU, const CUtensorMap& tmA,
+                      cudaStream_t s)
 {
     constexpr uint32_t SMEM_BYTES = Lay<MODE>::SMEM_BYTES;
     static bool smem_set = false;
@@ -876,7 +932,7 @@ cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorM
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t le = cudaLaunchKernelEx(&cfg, stats_tc_kernel<MODE>, P, tmW, tmU);
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, stats_tc_kernel<MODE>, P, tmW, tmU, tmA);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -886,9 +942,10 @@ cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorM
 cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s)
 {
     if (!encode_fn()) return cudaErrorNotSupported;
-    CUtensorMap tmW, tmU;
+    CUtensorMap tmW, tmU, tmA;
     cudaError_t e = encode_w(&tmW, p.W, p.V, p.r);
     if (e == cudaSuccess) e = encode_u(&tmU, p.U, p.V, p.G, p.R);
+    if (e == cudaSuccess) e = encode_a(&tmA, p.a_next, p.R, p.r);
     if (e != cudaSuccess) return e;
     TcParams P;
     memset(&P, 0, sizeof P);
@@ -900,7 +957,7 @@ cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s)
     P.nblk = p.nblk;
     P.k = p.k;
     P.status = p.status;
-    return launch_tc<kDraftMode>(P, tmW, tmU, s);
+    return launch_tc<kDraftMode>(P, tmW, tmU, tmA, s);
 }
 
 cudaError_t launch_residual_stats_tc(const VerifyParams& p, cudaStream_t s)
@@ -919,7 +976,7 @@ cudaError_t launch_residual_stats_tc(const VerifyParams& p, cudaStream_t s)
     P.nblk = p.nblk;
     P.k = 0;
     P.status = p.status;
-    return launch_tc<kResidualMode>(P, tmW, tmW, s);
+    return launch_tc<kResidualMode>(P, tmW, tmW, tmW, s);
 }
 
 }  // namespace dspark
