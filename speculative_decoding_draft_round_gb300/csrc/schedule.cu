@@ -10,12 +10,17 @@
 //   full   m* = smallest arg-max of Theta_m;
 //   async  K  = full-scan count over the survivals two rounds old,
 //          m* = min(K, |pool|) over the current ranking.
-// GB300 mapping: up to 8192 slots live in shared memory. A positive float's bit
-// pattern orders like an unsigned integer, so the sort is a stable LSD radix
-// sort (four 8-bit digits, warp-aggregated ranks via __match_any_sync) of the
-// complemented bits; stability in slot order gives the (r, j) tie-break for
-// free. Prefix sums are exact 64-bit fixed-point sums (a in units of 2^-48),
-// so they do not depend on the summation order; Theta is formed in double.
+// GB300 mapping: up to 8192 slots live in shared memory, spread over all 32
+// warps. A positive float's bit pattern orders like an unsigned integer, so the
+// sort is a stable LSD radix sort (four 8-bit digits, warp-aggregated ranks via
+// __match_any_sync, digit offsets from one block-wide scan of the [digit][warp]
+// counts) of the complemented bits; stability in slot order gives the (r, j)
+// tie-break for free. Prefix sums are exact 64-bit fixed-point sums (a in units
+// of 2^-48), so they do not depend on the summation order, and every Theta
+// comparison is exact: tau * 2^48 is an integer below 2^62 and SPS(B) a float,
+// so Theta is compared through the 128-bit product of the integer and the
+// float's 24-bit significand (normalised to 64 bits: ties closer than 2^-63
+// relative compare equal). Only the reported Theta_best is formed in double.
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,18 +28,23 @@ namespace dspark {
 
 constexpr int kSchedThreads = 1024;
 constexpr int kSchedWarps = kSchedThreads / 32;
-constexpr int kKeysPerWarp = DSPARK_MAX_SLOTS / kSchedWarps;   // 256
-constexpr int kItems = kKeysPerWarp / 32;                      // 8 per lane
+constexpr int kMaxItems = DSPARK_MAX_SLOTS / kSchedThreads;   // keys per thread, at most 8
+
+struct ThetaKey {
+    int e;                  // Theta = m * 2^e with m normalised (bit 63 set); zero: e = INT_MIN, m = 0
+    unsigned long long m;
+};
+
 constexpr int kDigits = 256;
+constexpr int kHist = kDigits * kSchedWarps;                  // [digit][warp] counts
 
 struct SchedSmem {
     uint32_t key[2][DSPARK_MAX_SLOTS];
     uint16_t val[2][DSPARK_MAX_SLOTS];
-    uint32_t hist[kSchedWarps * kDigits];   // per-warp digit counts, then offsets; reused for keep counts
-    uint32_t dbase[kDigits];
-    uint32_t wtot[kDigits / 32];
+    uint32_t hist[kHist];                   // digit counts, then offsets; reused for keep counts
+    uint32_t wpart[kSchedWarps];
     unsigned long long wsum[kSchedWarps];
-    double wbest[kSchedWarps];
+    ThetaKey wbest[kSchedWarps];
     int wbest_m[kSchedWarps];
     int n_pool;
     int first_bad;
@@ -49,28 +59,44 @@ __device__ __forceinline__ uint32_t lanemask_lt()
     return m;
 }
 
-// Load the pool keys of `src` ([R][G] survivals) into key[0]/val[0]; returns |pool|.
-__device__ int load_pool(SchedSmem& sm, const ScheduleParams& p, const float* src, int n_slots, int n_pad)
+// Sorting position of (warp, item, lane): warp-major, then item, then lane; with ni items per
+// lane, position order equals slot order when the keys are loaded.
+__device__ __forceinline__ int striped(int warp, int it, int lane, int ni) { return (warp * ni + it) * 32 + lane; }
+
+// Load the pool keys of `src` ([R][G] survivals) into key[0]/val[0]; returns |pool|. Every load
+// of a thread is issued before any is used.
+__device__ int load_pool(SchedSmem& sm, const ScheduleParams& p, const float* src, int n_slots, int ni)
 {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) sm.n_pool = 0;
-    __syncthreads();
+    float a[kMaxItems];
+    int g[kMaxItems];
+#pragma unroll
+    for (int it = 0; it < kMaxItems; ++it) {
+        const int s = striped(warp, it, lane, ni);
+        const bool in = it < ni && s < n_slots;
+        a[it] = in ? src[s] : 0.f;
+        g[it] = in ? (p.gamma ? p.gamma[s / p.G] : p.G) : 0;
+    }
     int cnt = 0;
-    for (int s = threadIdx.x; s < n_pad; s += kSchedThreads) {
+#pragma unroll
+    for (int it = 0; it < kMaxItems; ++it) {
+        if (it >= ni) break;
+        const int s = striped(warp, it, lane, ni);
         uint32_t key = 0xFFFFFFFFu;
         if (s < n_slots) {
-            const int q = s / p.G, j = s % p.G;
-            int g = p.gamma ? p.gamma[q] : p.G;
-            if (g < 0 || g > p.G) {
+            int gg = g[it];
+            if (gg < 0 || gg > p.G) {
                 raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
-                g = g < 0 ? 0 : p.G;
+                gg = gg < 0 ? 0 : p.G;
             }
-            float a = src[s];
-            if (j < g && a > 0.f) {   // NaN and non-positive survivals are not in the pool
-                if (!(a <= 1.f)) {
+            float av = a[it];
+            if (s % p.G < gg && av > 0.f) {   // NaN and non-positive survivals are not in the pool
+                if (!(av <= 1.f)) {
                     raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
-                    a = 1.f;
+                    av = 1.f;
                 }
-                key = ~__float_as_uint(a);
+                key = ~__float_as_uint(av);
                 ++cnt;
             }
         }
@@ -78,88 +104,142 @@ __device__ int load_pool(SchedSmem& sm, const ScheduleParams& p, const float* sr
         sm.val[0][s] = (uint16_t)s;
     }
     cnt = __reduce_add_sync(0xffffffffu, cnt);
-    if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(&sm.n_pool, cnt);
+    __syncthreads();
+    if (lane == 0 && cnt) atomicAdd(&sm.n_pool, cnt);
     __syncthreads();
     return sm.n_pool;
 }
 
-// One stable counting pass on 8 bits of the key, buffer `in` -> 1 - in.
-__device__ void radix_pass(SchedSmem& sm, int in, int shift, int active_warps)
+// Exclusive prefix over the kHist counts in [digit][warp] order, in place (1024 threads, 8 each).
+__device__ void scan_hist(SchedSmem& sm)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int i = tid; i < kSchedWarps * kDigits; i += kSchedThreads) sm.hist[i] = 0;
-    __syncthreads();
-    uint32_t key[kItems], dig[kItems], rank[kItems];
-    uint16_t val[kItems];
-    if (warp < active_warps) {
-        uint32_t* h = sm.hist + warp * kDigits;
+    constexpr int per = kHist / kSchedThreads;   // 8
+    const uint4 c0 = reinterpret_cast<uint4*>(sm.hist)[2 * tid];
+    const uint4 c1 = reinterpret_cast<uint4*>(sm.hist)[2 * tid + 1];
+    uint32_t c[per] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    uint32_t run = 0;
 #pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const int idx = warp * kKeysPerWarp + it * 32 + lane;   // striped: order = (warp, it, lane)
-            key[it] = sm.key[in][idx];
-            val[it] = sm.val[in][idx];
-            dig[it] = (key[it] >> shift) & (kDigits - 1);
-            const uint32_t peers = __match_any_sync(0xffffffffu, dig[it]);
-            const uint32_t base = h[dig[it]];
-            __syncwarp();
-            if (lane == __ffs(peers) - 1) h[dig[it]] = base + __popc(peers);
-            __syncwarp();
-            rank[it] = base + __popc(peers & lanemask_lt());
-        }
+    for (int i = 0; i < per; ++i) {
+        const uint32_t v = c[i];
+        c[i] = run;
+        run += v;
     }
+    uint32_t inc = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) sm.wpart[warp] = inc;
     __syncthreads();
-    // exclusive offsets in digit-major, warp-minor order: thread d turns the
-    // per-warp counts of digit d into offsets within the digit, then the 256
-    // digit totals are scanned (8 warps: shuffle scan + warp totals)
-    uint32_t tot = 0, inc = 0;
-    if (tid < kDigits) {
-        for (int w = 0; w < kSchedWarps; ++w) {
-            const uint32_t c = sm.hist[w * kDigits + tid];
-            sm.hist[w * kDigits + tid] = tot;
-            tot += c;
-        }
-        inc = tot;
+    if (warp == 0) {
+        const uint32_t w = sm.wpart[lane];
+        uint32_t wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += y;
+            const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
         }
-        if (lane == 31) sm.wtot[warp] = inc;
+        sm.wpart[lane] = wi - w;
     }
     __syncthreads();
-    if (tid < kDigits) {
-        uint32_t add = 0;
-        for (int w = 0; w < warp; ++w) add += sm.wtot[w];
-        sm.dbase[tid] = add + inc - tot;
+    const uint32_t base = sm.wpart[warp] + inc - run;
+    reinterpret_cast<uint4*>(sm.hist)[2 * tid] = make_uint4(base + c[0], base + c[1], base + c[2], base + c[3]);
+    reinterpret_cast<uint4*>(sm.hist)[2 * tid + 1] = make_uint4(base + c[4], base + c[5], base + c[6], base + c[7]);
+}
+
+// One stable counting pass on 8 bits of the key, buffer `in` -> 1 - in.
+__device__ void radix_pass(SchedSmem& sm, int in, int shift, int ni)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    reinterpret_cast<uint4*>(sm.hist)[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(sm.hist)[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    uint32_t key[kMaxItems], dig[kMaxItems], rank[kMaxItems];
+    uint16_t val[kMaxItems];
+#pragma unroll
+    for (int it = 0; it < kMaxItems; ++it) {
+        if (it >= ni) break;
+        const int idx = striped(warp, it, lane, ni);
+        key[it] = sm.key[in][idx];
+        val[it] = sm.val[in][idx];
     }
+#pragma unroll
+    for (int it = 0; it < kMaxItems; ++it) {
+        if (it >= ni) break;
+        dig[it] = (key[it] >> shift) & (kDigits - 1);
+        uint32_t* h = sm.hist + dig[it] * kSchedWarps + warp;
+        const uint32_t peers = __match_any_sync(0xffffffffu, dig[it]);
+        const uint32_t base = *h;
+        __syncwarp();
+        if (lane == __ffs(peers) - 1) *h = base + __popc(peers);
+        __syncwarp();
+        rank[it] = base + __popc(peers & lanemask_lt());
+    }
+    __syncthreads();
+    scan_hist(sm);
     __syncthreads();
     const int out = 1 - in;
-    if (warp < active_warps) {
 #pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const uint32_t pos = sm.dbase[dig[it]] + sm.hist[warp * kDigits + dig[it]] + rank[it];
-            sm.key[out][pos] = key[it];
-            sm.val[out][pos] = val[it];
-        }
+    for (int it = 0; it < kMaxItems; ++it) {
+        if (it >= ni) break;
+        const uint32_t pos = sm.hist[dig[it] * kSchedWarps + warp] + rank[it];
+        sm.key[out][pos] = key[it];
+        sm.val[out][pos] = val[it];
     }
     __syncthreads();
 }
 
 // Sort key[0]/val[0] ascending (a descending); result in buffer 0.
-__device__ void sort_pool(SchedSmem& sm, int n_pad)
+__device__ void sort_pool(SchedSmem& sm, int ni)
 {
-    const int active_warps = n_pad / kKeysPerWarp;
-    radix_pass(sm, 0, 0, active_warps);
-    radix_pass(sm, 1, 8, active_warps);
-    radix_pass(sm, 0, 16, active_warps);
-    radix_pass(sm, 1, 24, active_warps);
+    radix_pass(sm, 0, 0, ni);
+    radix_pass(sm, 1, 8, ni);
+    radix_pass(sm, 0, 16, ni);
+    radix_pass(sm, 1, 24, ni);
 }
 
+// a * 2^48 rounded to nearest (ties to even), a in (0, 1] from its word, with integer operations
 __device__ __forceinline__ unsigned long long fixed48(uint32_t key)
 {
-    const float a = __uint_as_float(~key);
-    return __float2ull_rn(a * 281474976710656.0f);   // a * 2^48, exact scaling
+    const uint32_t b = ~key;
+    const uint32_t ex = (b >> 23) & 0xFFu;
+    const unsigned long long M = ex ? ((b & 0x7FFFFFu) | 0x800000u) : (b & 0x7FFFFFu);
+    const int sh = (ex ? (int)ex - 150 : -149) + 48;   // a * 2^48 = M * 2^sh
+    if (sh >= 0) return M << sh;
+    if (sh < -25) return 0ull;
+    const unsigned long long q = M >> -sh, rem = M & ((1ull << -sh) - 1ull), half = 1ull << (-sh - 1);
+    return q + ((rem > half || (rem == half && (q & 1ull))) ? 1ull : 0ull);
 }
+
+// Exact Theta_m = (R + S * 2^-48) * SPS(R + m) as a normalised key (see the header comment).
+__device__ __forceinline__ ThetaKey theta_key(int R, int m, unsigned long long S, const float* sps, int* status)
+{
+    const unsigned long long T = ((unsigned long long)R << 48) + S;   // < 2^62
+    const float sv = sps[R + m - 1];
+    if (!(sv > 0.f) || sv == INFINITY) {
+        raise_status(status, DSPARK_ERR_DEVICE_INPUT);   // a throughput table entry must be positive and finite
+        return ThetaKey{INT32_MIN, 0ull};
+    }
+    const uint32_t b = __float_as_uint(sv);
+    const uint32_t ex = (b >> 23) & 0xFFu;
+    const unsigned long long M = ex ? ((b & 0x7FFFFFu) | 0x800000u) : (b & 0x7FFFFFu);
+    const int E = ex ? (int)ex - 150 : -149;   // SPS = M * 2^E
+    const unsigned long long lo = T * M, hi = __umul64hi(T, M);
+    if (hi == 0ull && lo == 0ull) return ThetaKey{INT32_MIN, 0ull};
+    // Theta = (hi * 2^64 + lo) * 2^(E - 48)
+    if (hi) {
+        const int lz = __clzll(hi);
+        const unsigned long long m64 = (hi << lz) | (lz ? lo >> (64 - lz) : 0ull);
+        // m64 holds bits [127 - lz - 63, 127 - lz] of the product: Theta = m64 * 2^(64 - lz + E - 48)
+        return ThetaKey{64 - lz + E - 48, m64};
+    }
+    const int lz = __clzll(lo);
+    return ThetaKey{E - 48 - lz, lo << lz};   // Theta = (lo << lz) * 2^(E - 48 - lz)
+}
+
+__device__ __forceinline__ bool key_gt(ThetaKey a, ThetaKey b) { return a.e > b.e || (a.e == b.e && a.m > b.m); }
 
 __device__ __forceinline__ double theta_of(int R, int m, unsigned long long S, const float* sps)
 {
@@ -167,16 +247,16 @@ __device__ __forceinline__ double theta_of(int R, int m, unsigned long long S, c
     return tau * (double)sps[R + m - 1];
 }
 
-// Inclusive prefix sums S_i (i = sorted index) of the fixed-point a's for the
-// `kItems` consecutive indices this thread owns, plus the exclusive prefix.
-__device__ void prefix_sums(SchedSmem& sm, int n, unsigned long long S[kItems], unsigned long long& excl)
+// Inclusive prefix sums S (sorted index tid * ni + it) of the fixed-point a's, and the exclusive
+// prefix of the thread's first index.
+__device__ void prefix_sums(SchedSmem& sm, int n, int ni, unsigned long long (&S)[kMaxItems], unsigned long long& excl)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     unsigned long long run = 0;
 #pragma unroll
-    for (int it = 0; it < kItems; ++it) {
-        const int i = tid * kItems + it;
-        run += i < n ? fixed48(sm.key[0][i]) : 0ull;
+    for (int it = 0; it < kMaxItems; ++it) {
+        const int i = tid * ni + it;
+        run += (it < ni && i < n) ? fixed48(sm.key[0][i]) : 0ull;
         S[it] = run;
     }
     unsigned long long inc = run;
@@ -187,32 +267,39 @@ __device__ void prefix_sums(SchedSmem& sm, int n, unsigned long long S[kItems], 
     }
     if (lane == 31) sm.wsum[warp] = inc;
     __syncthreads();
-    unsigned long long wbase = 0;
-    for (int w = 0; w < warp; ++w) wbase += sm.wsum[w];
-    excl = wbase + inc - run;
+    if (warp == 0) {
+        const unsigned long long w = sm.wsum[lane];
+        unsigned long long wi = w;
 #pragma unroll
-    for (int it = 0; it < kItems; ++it) S[it] += excl;
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        sm.wsum[lane] = wi - w;
+    }
+    __syncthreads();
+    excl = sm.wsum[warp] + inc - run;
+#pragma unroll
+    for (int it = 0; it < kMaxItems; ++it) S[it] += excl;
     __syncthreads();
 }
 
-// Smallest arg-max of Theta_m over m = 0..n (full scan).
-__device__ int full_scan(SchedSmem& sm, int R, int n, const float* sps)
+// Smallest arg-max of Theta_m over m = 0..n (full scan), from the prefix sums.
+__device__ int full_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, const unsigned long long (&S)[kMaxItems])
 {
-    unsigned long long S[kItems], excl;
-    prefix_sums(sm, n, S, excl);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    double best = -1.0;
+    ThetaKey best{INT32_MIN, 0ull};
     int bm = INT32_MAX;
     if (tid == 0) {
-        best = theta_of(R, 0, 0ull, sps);
+        best = theta_key(p.R, 0, 0ull, p.sps, p.status);
         bm = 0;
     }
 #pragma unroll
-    for (int it = 0; it < kItems; ++it) {
-        const int i = tid * kItems + it;
-        if (i < n) {
-            const double th = theta_of(R, i + 1, S[it], sps);
-            if (th > best) {
+    for (int it = 0; it < kMaxItems; ++it) {
+        const int i = tid * ni + it;
+        if (it < ni && i < n) {
+            const ThetaKey th = theta_key(p.R, i + 1, S[it], p.sps, p.status);
+            if (key_gt(th, best) || bm == INT32_MAX) {
                 best = th;
                 bm = i + 1;
             }
@@ -220,9 +307,9 @@ __device__ int full_scan(SchedSmem& sm, int R, int n, const float* sps)
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const ThetaKey ob{__shfl_xor_sync(0xffffffffu, best.e, o), __shfl_xor_sync(0xffffffffu, best.m, o)};
         const int om = __shfl_xor_sync(0xffffffffu, bm, o);
-        if (ob > best || (ob == best && om < bm)) {
+        if (om != INT32_MAX && (bm == INT32_MAX || key_gt(ob, best) || (!key_gt(best, ob) && om < bm))) {
             best = ob;
             bm = om;
         }
@@ -232,12 +319,14 @@ __device__ int full_scan(SchedSmem& sm, int R, int n, const float* sps)
         sm.wbest_m[warp] = bm;
     }
     __syncthreads();
-    double b = -1.0;
+    ThetaKey b{INT32_MIN, 0ull};
     int m = INT32_MAX;
     for (int w = 0; w < kSchedWarps; ++w) {
-        if (sm.wbest[w] > b || (sm.wbest[w] == b && sm.wbest_m[w] < m)) {
-            b = sm.wbest[w];
-            m = sm.wbest_m[w];
+        const ThetaKey wb = sm.wbest[w];
+        const int wm = sm.wbest_m[w];
+        if (wm != INT32_MAX && (m == INT32_MAX || key_gt(wb, b) || (!key_gt(b, wb) && wm < m))) {
+            b = wb;
+            m = wm;
         }
     }
     __syncthreads();
@@ -245,22 +334,23 @@ __device__ int full_scan(SchedSmem& sm, int R, int n, const float* sps)
 }
 
 // First m >= 1 with Theta_m <= Theta_{m-1}, minus one (|pool| if none).
-__device__ int sync_scan(SchedSmem& sm, int R, int n, const float* sps)
+__device__ int sync_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, const unsigned long long (&S)[kMaxItems],
+                         unsigned long long excl)
 {
-    unsigned long long S[kItems], excl;
-    prefix_sums(sm, n, S, excl);
     const int tid = threadIdx.x;
     if (tid == 0) sm.first_bad = INT32_MAX;
     __syncthreads();
     int bad = INT32_MAX;
-    double prev = (tid * kItems < n) ? theta_of(R, tid * kItems, excl, sps) : 0.0;
+    if (tid * ni < n) {
+        ThetaKey prev = theta_key(p.R, tid * ni, excl, p.sps, p.status);
 #pragma unroll
-    for (int it = 0; it < kItems; ++it) {
-        const int i = tid * kItems + it;
-        if (i < n) {
-            const double th = theta_of(R, i + 1, S[it], sps);
-            if (!(th > prev) && bad == INT32_MAX) bad = i + 1;
-            prev = th;
+        for (int it = 0; it < kMaxItems; ++it) {
+            const int i = tid * ni + it;
+            if (it < ni && i < n) {
+                const ThetaKey th = theta_key(p.R, i + 1, S[it], p.sps, p.status);
+                if (!key_gt(th, prev) && bad == INT32_MAX) bad = i + 1;
+                prev = th;
+            }
         }
     }
     bad = __reduce_min_sync(0xffffffffu, bad);
@@ -276,21 +366,24 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedulePara
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SchedSmem& sm = *reinterpret_cast<SchedSmem*>(smem_raw);
     const int n_slots = p.R * p.G;
-    const int n_pad = (n_slots + kKeysPerWarp - 1) / kKeysPerWarp * kKeysPerWarp;
+    const int ni = (n_slots + kSchedThreads - 1) / kSchedThreads;   // keys per thread, 1..8
 
+    unsigned long long S[kMaxItems], excl;
     int capacity = -1;
     if (p.mode == DSPARK_SCHED_ASYNC_CAPACITY) {
-        const int n_old = load_pool(sm, p, p.surv_capacity, n_slots, n_pad);
-        sort_pool(sm, n_pad);
-        capacity = full_scan(sm, p.R, n_old, p.sps);
+        const int n_old = load_pool(sm, p, p.surv_capacity, n_slots, ni);
+        sort_pool(sm, ni);
+        prefix_sums(sm, n_old, ni, S, excl);
+        capacity = full_scan(sm, p, n_old, ni, S);
     }
-    const int n = load_pool(sm, p, p.surv, n_slots, n_pad);
-    sort_pool(sm, n_pad);
+    const int n = load_pool(sm, p, p.surv, n_slots, ni);
+    sort_pool(sm, ni);
+    prefix_sums(sm, n, ni, S, excl);
     int m_star;
     if (p.mode == DSPARK_SCHED_SYNC)
-        m_star = sync_scan(sm, p.R, n, p.sps);
+        m_star = sync_scan(sm, p, n, ni, S, excl);
     else if (p.mode == DSPARK_SCHED_FULL_SCAN)
-        m_star = full_scan(sm, p.R, n, p.sps);
+        m_star = full_scan(sm, p, n, ni, S);
     else
         m_star = min(capacity, n);
 
@@ -306,14 +399,12 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedulePara
     __syncthreads();
     for (int q = threadIdx.x; q < p.R; q += kSchedThreads) p.keep[q] = (int32_t)cnt[q];
 
-    // Theta of the admitted set with the current survivals
-    unsigned long long S[kItems], excl;
-    prefix_sums(sm, m_star, S, excl);
+    // Theta of the admitted set with the current survivals, from the prefix sums
     const int last = m_star - 1;
     if (m_star == 0 && threadIdx.x == 0) {
         p.stats->theta_best = theta_of(p.R, 0, 0ull, p.sps);
-    } else if (last >= 0 && last / kItems == (int)threadIdx.x) {
-        p.stats->theta_best = theta_of(p.R, m_star, S[last % kItems], p.sps);
+    } else if (last >= 0 && last / ni == (int)threadIdx.x) {
+        p.stats->theta_best = theta_of(p.R, m_star, S[last % ni], p.sps);
     }
     if (threadIdx.x == 0) {
         p.stats->admitted = m_star;
@@ -325,9 +416,14 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedulePara
 
 cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s)
 {
+    static bool smem_set = false;
     const size_t smem = sizeof(SchedSmem);
-    cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    if (!smem_set) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set = true;
+    }
     schedule_kernel<<<1, kSchedThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
