@@ -25,7 +25,7 @@ _SRC = os.path.join(_HERE, "dspark_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libdspark_oracle.so")
 
 F32, BF16, F64 = 0, 1, 2
-SCHED_SYNC, SCHED_ASYNC_CAPACITY, SCHED_FULL_SCAN = 0, 1, 2
+SCHED_SYNC, SCHED_ASYNC_CAPACITY, SCHED_FULL_SCAN, SCHED_THRESHOLD = 0, 1, 2, 3
 
 _lib = None
 _lock = threading.Lock()
@@ -59,6 +59,7 @@ class _SampleArgs(C.Structure):
         ("forced_tokens", C.c_void_p),
         ("tokens", C.c_void_p), ("conf", C.c_void_p), ("surv", C.c_void_p), ("lse", C.c_void_p),
         ("logit", C.c_void_p), ("gap1", C.c_void_p), ("gap2", C.c_void_p),
+        ("sts_temp", C.c_void_p),
     ]
 
 
@@ -69,7 +70,16 @@ class _ScheduleArgs(C.Structure):
         ("sps", C.c_void_p), ("n_sps", C.c_int), ("mode", C.c_int),
         ("keep", C.c_void_p), ("theta_best", C.c_void_p), ("admitted", C.c_void_p),
         ("capacity", C.c_void_p), ("pool", C.c_void_p), ("min_margin", C.c_void_p),
-        ("theta_curve", C.c_void_p),
+        ("theta_curve", C.c_void_p), ("threshold", C.c_double),
+    ]
+
+
+class _AssembleArgs(C.Structure):
+    _fields_ = [
+        ("R", C.c_int), ("gamma_max", C.c_int),
+        ("keep", C.c_void_p), ("anchor", C.c_void_p), ("tokens", C.c_void_p),
+        ("flat_tokens", C.c_void_p), ("flat_request", C.c_void_p), ("flat_position", C.c_void_p),
+        ("offsets", C.c_void_p),
     ]
 
 
@@ -104,6 +114,8 @@ def lib():
             L.dso_schedule.argtypes = [C.POINTER(_ScheduleArgs)]
             L.dso_schedule.restype = C.c_int
             L.dso_verify.argtypes = [C.POINTER(_VerifyArgs)]
+            L.dso_assemble.argtypes = [C.POINTER(_AssembleArgs)]
+            L.dso_assemble.restype = C.c_int
             L.dso_verify.restype = C.c_int
             _lib = L
     return _lib
@@ -160,7 +172,7 @@ def _run(fn, parts, threads):
 
 def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamma=None,
                  req_ids=None, conf_token=0, bias_first=1, noise_block=128, forced_tokens=None,
-                 threads=1):
+                 sts_temp=None, threads=1):
     """Markov-head serial sampling, confidence head and survival products for R requests.
 
     U [R][G][V], E [V][r], W [r][V], h [R][G][d] share one element type
@@ -177,6 +189,7 @@ def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gam
     gamma = None if gamma is None else _c(gamma, np.int32)
     req_ids = np.arange(R, dtype=np.int32) if req_ids is None else _c(req_ids, np.int32)
     forced = None if forced_tokens is None else _c(forced_tokens, np.int32)
+    sts = None if sts_temp is None else _c(sts_temp, np.float64)
     out = {
         "tokens": np.zeros((R, G), np.int32), "conf": np.zeros((R, G)), "surv": np.zeros((R, G)),
         "lse": np.zeros((R, G)), "logit": np.zeros((R, G)), "gap1": np.zeros((R, G)),
@@ -195,6 +208,7 @@ def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gam
         a.seed, a.round = int(seed), int(rnd)
         a.conf_token, a.bias_first, a.noise_block = int(conf_token), int(bias_first), int(noise_block)
         a.forced_tokens = _p(None if forced is None else forced[s:e])
+        a.sts_temp = _p(sts)
         for k, arr in out.items():
             setattr(a, k, _p(arr[s:e]))
         rc = lib().dso_sample_block(C.byref(a))
@@ -207,9 +221,10 @@ def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gam
 
 # ----------------------------------------------------------------- scheduler
 
-def schedule(surv, sps, mode=SCHED_SYNC, *, gamma=None, surv_capacity=None):
+def schedule(surv, sps, mode=SCHED_SYNC, *, gamma=None, surv_capacity=None, threshold=0.0):
     """Algorithm 1 over P independent problems. surv: [R][G] or [P][R][G] (any float),
-    sps: [n_sps] with sps[B-1] = SPS(B)."""
+    sps: [n_sps] with sps[B-1] = SPS(B). SCHED_THRESHOLD admits every candidate whose survival
+    reaches `threshold`."""
     surv = np.asarray(surv, dtype=np.float64)
     squeeze = surv.ndim == 2
     if squeeze:
@@ -233,6 +248,7 @@ def schedule(surv, sps, mode=SCHED_SYNC, *, gamma=None, surv_capacity=None):
     a.P, a.R, a.gamma_max = P, R, G
     a.gamma, a.surv, a.surv_capacity = _p(gamma), _p(surv), _p(cap)
     a.sps, a.n_sps, a.mode = _p(sps), int(sps.shape[0]), int(mode)
+    a.threshold = float(threshold)
     for k, arr in out.items():
         setattr(a, k, _p(arr))
     rc = lib().dso_schedule(C.byref(a))
@@ -285,4 +301,24 @@ def verify(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temper
             raise RuntimeError("dso_verify failed: %d" % rc)
 
     _run(part, _chunks(R, threads), threads)
+    return out
+
+
+# ----------------------------------------------------------------- ragged verify batch
+
+def assemble(keep, anchor, tokens):
+    """Flatten the admitted prefixes: per request its anchor, then keep[r] draft tokens."""
+    keep, anchor, tokens = _c(keep, np.int32), _c(anchor, np.int32), _c(tokens, np.int32)
+    R, G = tokens.shape
+    cap = R * (G + 1)
+    out = {"flat_tokens": np.zeros(cap, np.int32), "flat_request": np.zeros(cap, np.int32),
+           "flat_position": np.zeros(cap, np.int32), "offsets": np.zeros(R + 1, np.int32)}
+    a = _AssembleArgs()
+    a.R, a.gamma_max = R, G
+    a.keep, a.anchor, a.tokens = _p(keep), _p(anchor), _p(tokens)
+    for k, arr in out.items():
+        setattr(a, k, _p(arr))
+    rc = lib().dso_assemble(C.byref(a))
+    if rc:
+        raise ValueError("dso_assemble: keep outside [0, gamma_max]")
     return out

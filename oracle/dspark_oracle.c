@@ -233,6 +233,8 @@ int dso_sample_block(const dso_sample_args* a)
             double dot = (double)a->b;
             for (int j = 0; j < d; ++j) dot += (double)a->w_h[j] * load(a->h, a->dtype, idx * d + j);
             for (int i = 0; i < r; ++i) dot += (double)a->w_e[i] * load(a->E, a->dtype, (size_t)xc * r + i);
+            /* sequential temperature scaling: the logit of position k over its temperature */
+            if (a->sts_temp) dot /= a->sts_temp[k];
             const double c = 1.0 / (1.0 + exp(-dot));
             s *= c;
             a->conf[idx] = c;
@@ -352,7 +354,22 @@ int dso_schedule(const dso_schedule_args* a)
         double theta, margin;
         int admitted;
         a->capacity[p] = -1;
-        if (a->mode == DSO_SCHED_SYNC) {
+        if (a->mode == DSO_SCHED_THRESHOLD) {
+            /* static confidence threshold: every candidate whose survival reaches the threshold,
+             * l_r the largest such position; no throughput model decides anything */
+            double tau = (double)R;
+            admitted = 0;
+            for (int q = 0; q < R; ++q) keep[q] = 0;
+            for (int i = 0; i < n; ++i) {
+                if (pool[i].a >= a->threshold) {
+                    ++admitted;
+                    tau += pool[i].a;
+                    if (pool[i].j > keep[pool[i].r]) keep[pool[i].r] = pool[i].j;
+                }
+            }
+            theta = tau * sps_at(a->sps, R + admitted);
+            margin = INFINITY;
+        } else if (a->mode == DSO_SCHED_SYNC) {
             admitted = greedy_scan(pool, n, R, a->sps, 1, keep, &theta, &margin);
         } else if (a->mode == DSO_SCHED_FULL_SCAN) {
             admitted = greedy_scan(pool, n, R, a->sps, 0, keep, &theta, &margin);
@@ -505,5 +522,29 @@ int dso_verify(const dso_verify_args* a)
     free(zt);
     free(ld);
     free(lw);
+    return 0;
+}
+
+/* ------------------------------------------------------------- ragged verify batch */
+
+int dso_assemble(const dso_assemble_args* a)
+{
+    if (!a || a->R < 0 || a->gamma_max < 1) return 1;
+    const int R = a->R, G = a->gamma_max;
+    const size_t cap = (size_t)R * (G + 1);
+    for (size_t f = 0; f < cap; ++f) a->flat_tokens[f] = a->flat_request[f] = a->flat_position[f] = -1;
+    int32_t off = 0;
+    for (int q = 0; q < R; ++q) {
+        const int ell = a->keep[q];
+        if (ell < 0 || ell > G) return 1;
+        a->offsets[q] = off;
+        for (int j = 0; j <= ell; ++j) {
+            a->flat_tokens[off + j] = j == 0 ? a->anchor[q] : a->tokens[(size_t)q * G + j - 1];
+            a->flat_request[off + j] = q;
+            a->flat_position[off + j] = j;
+        }
+        off += ell + 1;
+    }
+    a->offsets[R] = off;
     return 0;
 }

@@ -14,7 +14,12 @@
  *     capacity variant (section 5.2 of the paper);
  *   - rejection-sampling verification (Leviathan et al. 2023), the residual
  *     norm(max(0, p_t - p_d)) and the bonus token (dspark_cycle sketch,
- *     steps 5-6, on the caijizhuo.github.io page).
+ *     steps 5-6, on the caijizhuo.github.io page);
+ *   - the static confidence-threshold admission used as the ablation baseline
+ *     (zhongzhuzhou.org notes, figure 5 threshold sweep);
+ *   - sequential temperature scaling of the confidences (same notes, "STS");
+ *   - the flattened variable-length verify batch (same notes, physical
+ *     execution without padding).
  * Every pointer is a host pointer owned by the caller.
  */
 #ifndef DSPARK_ORACLE_H
@@ -29,7 +34,7 @@ extern "C" {
 enum { DSO_F32 = 0, DSO_BF16 = 1, DSO_F64 = 2 };
 
 /* scheduler modes */
-enum { DSO_SCHED_SYNC = 0, DSO_SCHED_ASYNC_CAPACITY = 1, DSO_SCHED_FULL_SCAN = 2 };
+enum { DSO_SCHED_SYNC = 0, DSO_SCHED_ASYNC_CAPACITY = 1, DSO_SCHED_FULL_SCAN = 2, DSO_SCHED_THRESHOLD = 3 };
 
 /* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): out = Philox(ctr, key). */
 void dso_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
@@ -65,6 +70,8 @@ typedef struct {
     double* logit;                      /* (U_k + B_k)(x_k) / T at the committed token */
     double* gap1;                       /* top-two gap of the block-level perturbed values */
     double* gap2;                       /* top-two gap of the element-level perturbed values */
+    const double* sts_temp;             /* [gamma_max] or NULL: per-position temperature of the confidence
+                                           logit (sequential temperature scaling), c_k = sigmoid(l_k / t_k) */
 } dso_sample_args;
 
 int dso_sample_block(const dso_sample_args* a);
@@ -87,6 +94,7 @@ typedef struct {
     double* min_margin;                 /* [P] smallest relative margin of a decisive comparison */
     double* theta_curve;                /* [P][R*gamma_max+1] Theta_m of the (current) sorted pool for
                                            m = 0..|pool|, NaN beyond; may be NULL */
+    double threshold;                   /* DSO_SCHED_THRESHOLD: admit (r, j) iff a_{r,j} >= threshold */
 } dso_schedule_args;
 
 int dso_schedule(const dso_schedule_args* a);
@@ -120,6 +128,24 @@ typedef struct {
 } dso_verify_args;
 
 int dso_verify(const dso_verify_args* a);
+
+/* Ragged verify batch: the admitted prefixes of all requests flattened into one token stream
+ * (request r contributes its anchor, then its keep[r] admitted draft tokens), with the request
+ * id and the causal position (0 for the anchor, j for draft token j) of every flat token and
+ * the start offset of every request (offsets[R] = total). Entries past the total are -1.
+ * Returns 1 if a keep value lies outside [0, gamma_max]. */
+typedef struct {
+    int R, gamma_max;
+    const int32_t* keep;                /* [R] */
+    const int32_t* anchor;              /* [R] */
+    const int32_t* tokens;              /* [R][gamma_max] */
+    int32_t* flat_tokens;               /* [R*(gamma_max+1)] */
+    int32_t* flat_request;              /* [R*(gamma_max+1)] */
+    int32_t* flat_position;             /* [R*(gamma_max+1)] */
+    int32_t* offsets;                   /* [R+1] */
+} dso_assemble_args;
+
+int dso_assemble(const dso_assemble_args* a);
 
 #ifdef __cplusplus
 }
