@@ -264,6 +264,30 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def time_next_rows(ds, rnd, res, n=20):
+    """Kernel times of the calls beyond the headline round, on this round's outputs: the flat
+    verify batch, the static-threshold admission, and the sampler with per-position confidence
+    temperatures (its extra work is one division per confidence, inside the commit kernel)."""
+    def per_launch(family, fn):
+        timer = ds.KernelTimer(family, n)
+        with timer:
+            for _ in range(n):
+                fn()
+        d = timer.durations_ms()
+        return round(1e3 * float(np.median(d)), 2) if d else None
+
+    tokens = torch.where(res["tokens"] < 0, torch.zeros_like(res["tokens"]), res["tokens"])
+    a_out = ds.assemble(res["keep"], rnd.anchor, tokens)
+    s_out = ds.schedule(res["surv"], rnd.sps, ds.SCHED_THRESHOLD, gamma=rnd.gamma, threshold=0.5)
+    flat = per_launch("assemble", lambda: ds.assemble(res["keep"], rnd.anchor, tokens, out=a_out,
+                                                     workspace=a_out["workspace"]))
+    thr = per_launch("schedule", lambda: ds.schedule(res["surv"], rnd.sps, ds.SCHED_THRESHOLD, gamma=rnd.gamma,
+                                                    threshold=0.5, out=s_out, workspace=s_out["workspace"]))
+    torch.cuda.synchronize()
+    return {"assemble_us": flat, "threshold_schedule_us": thr,
+            "flat_tokens": int(res["keep"].sum().item()) + rnd.R, "note": "median of %d isolated launches" % n}
+
+
 def bench_ours(args):
     import speculative_decoding_draft_round_gb300 as ds
     from speculative_decoding_draft_round_gb300 import build as dsbuild
@@ -367,6 +391,7 @@ def bench_ours(args):
         e_stops[s].record(stream)
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_starts, e_stops))
+    next_rows = time_next_rows(ds, rnd, res)
     clock = clocks.stop()
 
     drafted = rnd.draft_tokens()
@@ -412,6 +437,7 @@ def bench_ours(args):
                 "steps": n_e2e, "note": "per-round inputs (U, h, target, T, anchor, SPS) copied in, results "
                                         "copied out; E, W, w_h, w_e stay resident"},
         "gpu_launches": launches,
+        "next_rows": next_rows,
         "clocks": clock,
     }
     if rank == 0 and not args.no_cpu_baseline:

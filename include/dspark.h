@@ -67,7 +67,8 @@ enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 };
 enum {
     DSPARK_SCHED_SYNC = 0,           /* Algorithm 1: stop at the first Theta <= Theta_best */
     DSPARK_SCHED_ASYNC_CAPACITY = 1, /* section 5.2: capacity K from old survivals, current ranking */
-    DSPARK_SCHED_FULL_SCAN = 2       /* arg-max of Theta over every prefix of the sorted pool */
+    DSPARK_SCHED_FULL_SCAN = 2,      /* arg-max of Theta over every prefix of the sorted pool */
+    DSPARK_SCHED_THRESHOLD = 3       /* static confidence threshold: admit every a_{r,j} >= threshold */
 };
 
 enum {
@@ -84,8 +85,10 @@ enum {
  *   B_k  = W_1[x_{k-1}] W_2        (E row times W; zero for k = 0 when bias_first = 0)
  *   l_k  = (U[r][k] + B_k) / temperature[r]
  *   x_k  ~ softmax(l_k)            (two-level Gumbel-max, purposes 0 and 3)
- *   c_k  = sigmoid(w_h . h[r][k] + w_e . W_1[x] + b), x = x_{k-1} (conf_token 0, eq. 7)
- *          or x_k (conf_token 1)
+ *   c_k  = sigmoid((w_h . h[r][k] + w_e . W_1[x] + b) / t_k), x = x_{k-1} (conf_token 0,
+ *          eq. 7) or x_k (conf_token 1); t_k = sts_temp[k] (sequential temperature scaling of
+ *          the confidences, zhongzhuzhou.org notes "STS": the temperatures are fitted
+ *          elsewhere and only applied here) or 1 when sts_temp is NULL
  *   a_k  = a_{k-1} c_k             (a_0 = 1)
  * Outputs for k >= gamma_r are token -1 and zeros.
  */
@@ -117,6 +120,7 @@ typedef struct {
     float* surv;              /* out [R][gamma_max] a_k */
     float* draft_lse;         /* out [R][gamma_max] log sum_v exp(l_k(v)) */
     float* draft_logit;       /* out [R][gamma_max] l_k(x_k) */
+    const float* sts_temp;    /* [gamma_max] per-position confidence temperatures (> 0), or NULL */
 } dspark_sample_args;
 
 dspark_status dspark_sample_workspace_size(const dspark_sample_args* args, size_t* bytes);
@@ -163,6 +167,10 @@ dspark_status dspark_sample_block_static(const dspark_sample_args* args, void* s
  * products of confidences in (0,1)) it is the number of admitted slots.
  * The prefix sums are exact fixed-point sums of the fp32 a's (2^-48 units) and
  * Theta is formed in double from them.
+ *   threshold  (the static confidence-threshold admission the paper compares against,
+ *          zhongzhuzhou.org notes figure 5): admit every candidate (r, j) of the pool
+ *          with a_{r,j} >= threshold; no throughput model is consulted. keep and the
+ *          stats follow the same definitions (Theta of the admitted set, capacity -1).
  * Unsupported: R * gamma_max > DSPARK_MAX_SLOTS.
  */
 typedef struct {
@@ -185,6 +193,7 @@ typedef struct {
     const float* sps;             /* [n_sps] SPS(B) at index B-1 */
     int32_t* keep;                /* out [R] */
     dspark_schedule_stats* stats; /* out, one device struct */
+    float threshold;              /* DSPARK_SCHED_THRESHOLD only */
 } dspark_schedule_args;
 
 dspark_status dspark_schedule_workspace_size(const dspark_schedule_args* args, size_t* bytes);
@@ -241,6 +250,34 @@ dspark_status dspark_verify(const dspark_verify_args* args, void* workspace, siz
                             void* stream);
 
 /*
+ * dspark_assemble -- the verify batch as one flat token stream (zhongzhuzhou.org notes,
+ * physical execution of variable-length batches without padding): every request contributes
+ * its anchor followed by its keep[r] admitted draft tokens, the runs laid end to end in request
+ * order. Alongside each flat token: its request id and its causal position inside the request's
+ * run (0 for the anchor, j for draft token j) -- the marker tensor a target forward consumes.
+ *   offsets[r] = sum_{q < r} (keep[q] + 1),  offsets[R] = total
+ *   flat_*[offsets[r] + j] for j = 0 .. keep[r];  entries from total to R*(gamma_max+1) are -1.
+ * keep[r] outside [0, gamma_max] is clamped and DSPARK_ERR_DEVICE_INPUT recorded in the
+ * workspace status word. Unsupported: R > DSPARK_MAX_SLOTS.
+ */
+typedef struct {
+    uint32_t struct_size;
+    int32_t R;
+    int32_t gamma_max;
+    const int32_t* keep;         /* [R] admitted lengths (dspark_schedule) */
+    const int32_t* anchor;       /* [R] the token each request's block follows */
+    const int32_t* tokens;       /* [R][gamma_max] draft tokens */
+    int32_t* flat_tokens;        /* out [R*(gamma_max+1)] */
+    int32_t* flat_request;       /* out [R*(gamma_max+1)] */
+    int32_t* flat_position;      /* out [R*(gamma_max+1)] */
+    int32_t* offsets;            /* out [R+1] */
+} dspark_assemble_args;
+
+dspark_status dspark_assemble_workspace_size(const dspark_assemble_args* args, size_t* bytes);
+dspark_status dspark_assemble(const dspark_assemble_args* args, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
  * Launch accounting and timing (measurement support, not part of the method).
  *
  * dspark_launch_count: number of kernels this library has launched in this
@@ -262,7 +299,8 @@ enum {
     DSPARK_KERNEL_VERIFY_ROWS = 4,
     DSPARK_KERNEL_VERIFY_DECIDE = 5,
     DSPARK_KERNEL_RESIDUAL_STATS = 6,
-    DSPARK_KERNEL_RESIDUAL_PICK = 7
+    DSPARK_KERNEL_RESIDUAL_PICK = 7,
+    DSPARK_KERNEL_ASSEMBLE = 8
 };
 
 typedef struct {

@@ -22,7 +22,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdspark.so")
 
 F32, BF16 = 0, 1
-SCHED_SYNC, SCHED_ASYNC_CAPACITY, SCHED_FULL_SCAN = 0, 1, 2
+SCHED_SYNC, SCHED_ASYNC_CAPACITY, SCHED_FULL_SCAN, SCHED_THRESHOLD = 0, 1, 2, 3
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
 NOISE_BLOCK = 128
 MAX_GAMMA = 32
@@ -43,6 +43,7 @@ class SampleArgs(C.Structure):
         ("b", C.c_float), ("temperature", _vp), ("anchor", _vp),
         ("seed", C.c_uint64), ("round", C.c_uint64),
         ("tokens", _vp), ("conf", _vp), ("surv", _vp), ("draft_lse", _vp), ("draft_logit", _vp),
+        ("sts_temp", _vp),
     ]
 
 
@@ -56,6 +57,7 @@ class ScheduleArgs(C.Structure):
         ("struct_size", C.c_uint32), ("R", C.c_int32), ("gamma_max", C.c_int32), ("mode", C.c_int32),
         ("n_sps", C.c_int32),
         ("gamma", _vp), ("surv", _vp), ("surv_capacity", _vp), ("sps", _vp), ("keep", _vp), ("stats", _vp),
+        ("threshold", C.c_float),
     ]
 
 
@@ -70,13 +72,22 @@ class VerifyArgs(C.Structure):
     ]
 
 
+class AssembleArgs(C.Structure):
+    _fields_ = [
+        ("struct_size", C.c_uint32), ("R", C.c_int32), ("gamma_max", C.c_int32),
+        ("keep", _vp), ("anchor", _vp), ("tokens", _vp),
+        ("flat_tokens", _vp), ("flat_request", _vp), ("flat_position", _vp), ("offsets", _vp),
+    ]
+
+
 EXPORTS = ("dspark_sample_workspace_size", "dspark_sample_block", "dspark_schedule_workspace_size",
            "dspark_schedule", "dspark_verify_workspace_size", "dspark_verify", "dspark_check",
            "dspark_status_string", "dspark_abi_version", "dspark_launch_count", "dspark_time_kernel",
-           "dspark_last_error", "dspark_sample_path", "dspark_sample_block_static")
+           "dspark_last_error", "dspark_sample_path", "dspark_sample_block_static",
+           "dspark_assemble_workspace_size", "dspark_assemble")
 
 KERNELS = {"conf_hidden": 0, "draft_stats": 1, "draft_commit": 2, "schedule": 3, "verify_rows": 4,
-           "verify_decide": 5, "residual_stats": 6, "residual_pick": 7}
+           "verify_decide": 5, "residual_stats": 6, "residual_pick": 7, "assemble": 8}
 
 
 class EventPair(C.Structure):
@@ -108,6 +119,8 @@ def lib():
                            ("dspark_schedule", [C.POINTER(ScheduleArgs), _vp, C.c_size_t, _vp]),
                            ("dspark_verify_workspace_size", [C.POINTER(VerifyArgs), C.POINTER(C.c_size_t)]),
                            ("dspark_verify", [C.POINTER(VerifyArgs), _vp, C.c_size_t, _vp]),
+                           ("dspark_assemble_workspace_size", [C.POINTER(AssembleArgs), C.POINTER(C.c_size_t)]),
+                           ("dspark_assemble", [C.POINTER(AssembleArgs), _vp, C.c_size_t, _vp]),
                            ("dspark_check", [_vp, _vp])):
             f = getattr(L, name)
             f.argtypes = argt
@@ -240,7 +253,7 @@ def check(workspace, stream=None) -> int:
 # ----------------------------------------------------------------- calls
 
 def sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamma=None, conf_token=0,
-                bias_first=1, path=PATH_AUTO, out=None):
+                bias_first=1, path=PATH_AUTO, out=None, sts_temp=None):
     R, G, V = U.shape
     r = E.shape[1]
     d = h.shape[2]
@@ -254,6 +267,7 @@ def sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamm
     _dev(temperature, "temperature", torch.float32, (R,))
     _dev(anchor, "anchor", torch.int32, (R,))
     _dev(gamma, "gamma", torch.int32, (R,))
+    _dev(sts_temp, "sts_temp", torch.float32, (G,))
     dev = U.device
     if out is None:
         out = {"tokens": torch.empty((R, G), dtype=torch.int32, device=dev)}
@@ -270,14 +284,15 @@ def sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamm
     a.seed, a.round = int(seed), int(rnd)
     a.tokens, a.conf, a.surv = _ptr(out["tokens"]), _ptr(out["conf"]), _ptr(out["surv"])
     a.draft_lse, a.draft_logit = _ptr(out["draft_lse"]), _ptr(out["draft_logit"])
+    a.sts_temp = _ptr(sts_temp)
     return a, out
 
 
 def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamma=None, conf_token=0,
-                 bias_first=1, path=PATH_AUTO, out=None, workspace=None, stream=None):
+                 bias_first=1, path=PATH_AUTO, out=None, workspace=None, stream=None, sts_temp=None):
     """dspark_sample_block on the current (or given) stream; returns the output tensors."""
     a, out = sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, gamma=gamma,
-                         conf_token=conf_token, bias_first=bias_first, path=path, out=out)
+                         conf_token=conf_token, bias_first=bias_first, path=path, out=out, sts_temp=sts_temp)
     ws = _workspace("dspark_sample_workspace_size", a, workspace, U.device)
     _call("dspark_sample_block", C.byref(a), _ptr(ws), ws.numel(), _stream(stream))
     out["workspace"] = ws
@@ -298,7 +313,7 @@ def sample_block_static(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd,
     return out
 
 
-def schedule_args(surv, sps, mode=SCHED_SYNC, *, gamma=None, surv_capacity=None, out=None):
+def schedule_args(surv, sps, mode=SCHED_SYNC, *, gamma=None, surv_capacity=None, out=None, threshold=0.0):
     R, G = surv.shape
     _dev(surv, "surv", torch.float32)
     _dev(sps, "sps", torch.float32)
@@ -313,15 +328,48 @@ def schedule_args(surv, sps, mode=SCHED_SYNC, *, gamma=None, surv_capacity=None,
     a.R, a.gamma_max, a.mode, a.n_sps = R, G, int(mode), int(sps.numel())
     a.gamma, a.surv, a.surv_capacity, a.sps = _ptr(gamma), _ptr(surv), _ptr(surv_capacity), _ptr(sps)
     a.keep, a.stats = _ptr(out["keep"]), _ptr(out["stats"])
+    a.threshold = float(threshold)
     return a, out
 
 
 def schedule(surv, sps, mode=SCHED_SYNC, *, gamma=None, surv_capacity=None, out=None, workspace=None,
-             stream=None):
-    """dspark_schedule; returns {"keep": [R] int32, "stats": raw device bytes of dspark_schedule_stats}."""
-    a, out = schedule_args(surv, sps, mode, gamma=gamma, surv_capacity=surv_capacity, out=out)
+             stream=None, threshold=0.0):
+    """dspark_schedule; returns {"keep": [R] int32, "stats": raw device bytes of dspark_schedule_stats}.
+    SCHED_THRESHOLD admits every candidate whose survival reaches `threshold`."""
+    a, out = schedule_args(surv, sps, mode, gamma=gamma, surv_capacity=surv_capacity, out=out,
+                           threshold=threshold)
     ws = _workspace("dspark_schedule_workspace_size", a, workspace, surv.device)
     _call("dspark_schedule", C.byref(a), _ptr(ws), ws.numel(), _stream(stream))
+    out["workspace"] = ws
+    return out
+
+
+def assemble_args(keep, anchor, tokens, out=None):
+    R, G = tokens.shape
+    _dev(keep, "keep", torch.int32, (R,))
+    _dev(anchor, "anchor", torch.int32, (R,))
+    _dev(tokens, "tokens", torch.int32, (R, G))
+    dev = tokens.device
+    if out is None:
+        n = R * (G + 1)
+        out = {k: torch.empty(n, dtype=torch.int32, device=dev)
+               for k in ("flat_tokens", "flat_request", "flat_position")}
+        out["offsets"] = torch.empty(R + 1, dtype=torch.int32, device=dev)
+    a = AssembleArgs()
+    a.struct_size = C.sizeof(AssembleArgs)
+    a.R, a.gamma_max = R, G
+    a.keep, a.anchor, a.tokens = _ptr(keep), _ptr(anchor), _ptr(tokens)
+    a.flat_tokens, a.flat_request = _ptr(out["flat_tokens"]), _ptr(out["flat_request"])
+    a.flat_position, a.offsets = _ptr(out["flat_position"]), _ptr(out["offsets"])
+    return a, out
+
+
+def assemble(keep, anchor, tokens, *, out=None, workspace=None, stream=None):
+    """dspark_assemble: the admitted prefixes as one flat token stream with request ids, causal
+    positions and per-request offsets (entries past offsets[R] are -1)."""
+    a, out = assemble_args(keep, anchor, tokens, out=out)
+    ws = _workspace("dspark_assemble_workspace_size", a, workspace, tokens.device)
+    _call("dspark_assemble", C.byref(a), _ptr(ws), ws.numel(), _stream(stream))
     out["workspace"] = ws
     return out
 

@@ -29,8 +29,9 @@ bool timing(int kernel) { return g_timer.kernel == kernel && g_timer.count && *g
 const char* kernel_name(int kernel)
 {
     static const char* names[] = {"conf_hidden", "draft_stats", "draft_commit", "schedule",
-                                  "verify_rows", "verify_decide", "residual_stats", "residual_pick"};
-    return kernel >= 0 && kernel <= DSPARK_KERNEL_RESIDUAL_PICK ? names[kernel] : "?";
+                                  "verify_rows", "verify_decide", "residual_stats", "residual_pick",
+                                  "assemble"};
+    return kernel >= 0 && kernel <= DSPARK_KERNEL_ASSEMBLE ? names[kernel] : "?";
 }
 
 thread_local char g_last_error[256] = "no error";
@@ -167,7 +168,8 @@ dspark_status check_schedule(const dspark_schedule_args* a)
     if (!a || a->struct_size != sizeof(dspark_schedule_args)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (a->R < 1 || a->gamma_max < 1 || a->gamma_max > DSPARK_MAX_GAMMA) return DSPARK_ERR_INVALID_ARGUMENT;
     if ((long long)a->R * a->gamma_max > DSPARK_MAX_SLOTS) return DSPARK_ERR_UNSUPPORTED_SHAPE;
-    if (a->mode < DSPARK_SCHED_SYNC || a->mode > DSPARK_SCHED_FULL_SCAN) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->mode < DSPARK_SCHED_SYNC || a->mode > DSPARK_SCHED_THRESHOLD) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->mode == DSPARK_SCHED_THRESHOLD && !(a->threshold == a->threshold)) return DSPARK_ERR_INVALID_ARGUMENT;
     if ((long long)a->n_sps < (long long)a->R * (1 + a->gamma_max)) return DSPARK_ERR_INVALID_ARGUMENT;
     if (!a->surv || !a->sps || !a->keep || !a->stats) return DSPARK_ERR_INVALID_ARGUMENT;
     if (a->mode == DSPARK_SCHED_ASYNC_CAPACITY && !a->surv_capacity) return DSPARK_ERR_INVALID_ARGUMENT;
@@ -254,6 +256,7 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.surv = a->surv;
     p.draft_lse = a->draft_lse;
     p.draft_logit = a->draft_logit;
+    p.sts_temp = a->sts_temp;
     p.status = at<int>(ws, 0);
     p.x_cur = at<int32_t>(ws, L.x_cur);
     p.hw = at<float>(ws, L.hw);
@@ -298,9 +301,42 @@ dspark_status dspark_schedule(const dspark_schedule_args* a, void* ws, size_t ws
     p.sps = a->sps;
     p.keep = a->keep;
     p.stats = a->stats;
+    p.threshold = a->threshold;
     p.status = at<int>(ws, 0);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return cuda_status(launch(DSPARK_KERNEL_SCHEDULE, s, [&] { return launch_schedule(p, s); }));
+}
+
+dspark_status dspark_assemble_workspace_size(const dspark_assemble_args* a, size_t* bytes)
+{
+    if (!a || a->struct_size != sizeof(dspark_assemble_args) || !bytes) return DSPARK_ERR_INVALID_ARGUMENT;
+    *bytes = kStatusBytes;
+    return DSPARK_OK;
+}
+
+dspark_status dspark_assemble(const dspark_assemble_args* a, void* ws, size_t ws_bytes, void* stream)
+{
+    clear_stale_error();
+    if (!a || a->struct_size != sizeof(dspark_assemble_args)) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->R < 1 || a->gamma_max < 1 || a->gamma_max > DSPARK_MAX_GAMMA) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->R > DSPARK_MAX_SLOTS) return DSPARK_ERR_UNSUPPORTED_SHAPE;
+    if (!a->keep || !a->anchor || !a->tokens || !a->flat_tokens || !a->flat_request || !a->flat_position ||
+        !a->offsets)
+        return DSPARK_ERR_INVALID_ARGUMENT;
+    if (!ws || ws_bytes < kStatusBytes) return DSPARK_ERR_WORKSPACE;
+    AssembleParams p;
+    p.R = a->R;
+    p.G = a->gamma_max;
+    p.keep = a->keep;
+    p.anchor = a->anchor;
+    p.tokens = a->tokens;
+    p.flat_tokens = a->flat_tokens;
+    p.flat_request = a->flat_request;
+    p.flat_position = a->flat_position;
+    p.offsets = a->offsets;
+    p.status = at<int>(ws, 0);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(launch(DSPARK_KERNEL_ASSEMBLE, s, [&] { return launch_assemble(p, s); }));
 }
 
 dspark_status dspark_verify_workspace_size(const dspark_verify_args* a, size_t* bytes)
@@ -372,7 +408,7 @@ dspark_status dspark_time_kernel(int32_t kernel, dspark_event_pair* events, int3
         g_timer = KernelTimer();
         return DSPARK_OK;
     }
-    if (kernel > DSPARK_KERNEL_RESIDUAL_PICK || !events || capacity < 0 || !count) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (kernel > DSPARK_KERNEL_ASSEMBLE || !events || capacity < 0 || !count) return DSPARK_ERR_INVALID_ARGUMENT;
     g_timer.kernel = kernel;
     g_timer.events = events;
     g_timer.capacity = capacity;

@@ -34,6 +34,7 @@ struct DraftStep {
     float* surv;
     float* draft_lse;
     float* draft_logit;
+    const float* sts_temp;   // [G] confidence temperatures or NULL
     // workspace
     int* status;
     int32_t* x_cur;      // [R] token committed at the previous step
@@ -80,6 +81,20 @@ struct ScheduleParams {
     const float* sps;
     int32_t* keep;
     dspark_schedule_stats* stats;
+    float threshold;
+    int* status;
+};
+
+// The flattened verify batch (dspark_assemble).
+struct AssembleParams {
+    int R, G;
+    const int32_t* keep;
+    const int32_t* anchor;
+    const int32_t* tokens;
+    int32_t* flat_tokens;
+    int32_t* flat_request;
+    int32_t* flat_position;
+    int32_t* offsets;
     int* status;
 };
 
@@ -104,6 +119,9 @@ cudaError_t launch_residual_pick(const VerifyParams& p, cudaStream_t s);
 // schedule.cu
 size_t schedule_smem_bytes();
 cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
+
+// assemble.cu
+cudaError_t launch_assemble(const AssembleParams& p, cudaStream_t s);
 
 inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -354,7 +354,8 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     (void)e_prev;
     dot = block_sum<kCommitThreads>(dot, red);
     if (t == 0) {
-        const float logit = hw + dot + p.b;
+        // sequential temperature scaling of the confidence: the head's logit over t_k
+        const float logit = (hw + dot + p.b) / (p.sts_temp ? p.sts_temp[p.k] : 1.f);
         const float c = 1.f / (1.f + expf(-logit));
         p.tokens[o] = s_tok;
         p.conf[o] = c;

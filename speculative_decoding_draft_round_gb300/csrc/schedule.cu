@@ -361,11 +361,73 @@ __device__ int sync_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, 
     return fb == INT32_MAX ? n : fb - 1;
 }
 
+// Static confidence threshold: every pool candidate with a_{r,j} >= threshold, no sort and no
+// throughput model; keep and the stats as for the other modes.
+__device__ void threshold_admit(SchedSmem& sm, const ScheduleParams& p, int n_slots)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint32_t* cnt = sm.hist;
+    for (int q = tid; q < p.R; q += kSchedThreads) cnt[q] = 0;
+    if (tid == 0) {
+        sm.n_pool = 0;
+        sm.first_bad = 0;   // admitted count
+    }
+    __syncthreads();
+    int n_pool = 0, n_adm = 0;
+    unsigned long long sum = 0;
+    for (int s = tid; s < n_slots; s += kSchedThreads) {
+        const int q = s / p.G, j = s % p.G;
+        int g = p.gamma ? p.gamma[q] : p.G;
+        if (g < 0 || g > p.G) {
+            raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+            g = g < 0 ? 0 : p.G;
+        }
+        float a = p.surv[s];
+        if (j < g && a > 0.f) {   // the pool, as for the other modes
+            if (!(a <= 1.f)) {
+                raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+                a = 1.f;
+            }
+            ++n_pool;
+            if (a >= p.threshold) {
+                ++n_adm;
+                sum += fixed48(~__float_as_uint(a));
+                atomicMax(&cnt[q], (uint32_t)(j + 1));   // l_r = the largest admitted j
+            }
+        }
+    }
+    n_pool = __reduce_add_sync(0xffffffffu, n_pool);
+    n_adm = __reduce_add_sync(0xffffffffu, n_adm);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) {
+        sm.wsum[warp] = sum;
+        if (n_pool) atomicAdd(&sm.n_pool, n_pool);
+        if (n_adm) atomicAdd(&sm.first_bad, n_adm);
+    }
+    __syncthreads();
+    for (int q = tid; q < p.R; q += kSchedThreads) p.keep[q] = (int32_t)cnt[q];
+    if (tid == 0) {
+        unsigned long long S = 0;
+        for (int w = 0; w < kSchedWarps; ++w) S += sm.wsum[w];
+        const int m = sm.first_bad;
+        p.stats->theta_best = theta_of(p.R, m, S, p.sps);
+        p.stats->admitted = m;
+        p.stats->capacity = -1;
+        p.stats->batch = p.R + m;
+        p.stats->pool = sm.n_pool;
+    }
+}
+
 __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleParams p)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SchedSmem& sm = *reinterpret_cast<SchedSmem*>(smem_raw);
     const int n_slots = p.R * p.G;
+    if (p.mode == DSPARK_SCHED_THRESHOLD) {
+        threshold_admit(sm, p, n_slots);
+        return;
+    }
     const int ni = (n_slots + kSchedThreads - 1) / kSchedThreads;   // keys per thread, 1..8
 
     unsigned long long S[kMaxItems], excl;

@@ -38,8 +38,9 @@ def rows(t: torch.Tensor, ids) -> np.ndarray:
     return to_np(t.index_select(0, idx))
 
 
-def check_sample(rnd, out, ids, threads=8):
-    """Compare dspark_sample_block outputs with the oracle on requests `ids`."""
+def check_sample(rnd, out, ids, threads=8, sts_temp=None):
+    """Compare dspark_sample_block outputs with the oracle on requests `ids` (sts_temp: the
+    per-position confidence temperatures the call was given, if any)."""
     ids = np.asarray(ids)
     tok = to_np(out["tokens"])[ids]
     gamma = None if rnd.gamma is None else to_np(rnd.gamma)[ids]
@@ -47,6 +48,7 @@ def check_sample(rnd, out, ids, threads=8):
                             to_np(rnd.w_e), rnd.b, to_np(rnd.temperature)[ids], to_np(rnd.anchor)[ids],
                             rnd.seed, rnd.round, gamma=gamma, req_ids=ids, conf_token=rnd.conf_token,
                             bias_first=rnd.bias_first, forced_tokens=np.where(tok < 0, 0, tok),
+                            sts_temp=None if sts_temp is None else to_np(sts_temp).astype(np.float64),
                             threads=threads)
     G = rnd.gamma_max
     g = np.full(len(ids), G) if gamma is None else gamma

@@ -120,8 +120,32 @@ def test_schedule_validation(L):
     assert L.dspark_schedule_workspace_size(C.byref(a), C.byref(n)) == 1   # SPS table too short
     a.n_sps, a.mode = 512 * 17, 1
     assert L.dspark_schedule_workspace_size(C.byref(a), C.byref(n)) == 1   # async needs old survivals
-    a.mode = 3
+    a.mode = 3                                                                 # static threshold
+    assert L.dspark_schedule_workspace_size(C.byref(a), C.byref(n)) == 0
+    a.threshold = float("nan")
     assert L.dspark_schedule_workspace_size(C.byref(a), C.byref(n)) == 1
+    a.mode, a.threshold = 4, 0.5
+    assert L.dspark_schedule_workspace_size(C.byref(a), C.byref(n)) == 1
+
+
+def test_assemble_validation(L):
+    a = ds.AssembleArgs()
+    a.struct_size = C.sizeof(ds.AssembleArgs)
+    a.R, a.gamma_max = 128, 16
+    for f in ("keep", "anchor", "tokens", "flat_tokens", "flat_request", "flat_position", "offsets"):
+        setattr(a, f, 0x10000)
+    n = C.c_size_t(0)
+    assert L.dspark_assemble_workspace_size(C.byref(a), C.byref(n)) == 0 and n.value == 256
+    # refused on the host before any launch
+    assert L.dspark_assemble(C.byref(a), None, 0, None) == 3                  # no workspace
+    a.R = 8193
+    assert L.dspark_assemble(C.byref(a), C.c_void_p(0x10000), 256, None) == 2
+    a.R, a.gamma_max = 128, 33
+    assert L.dspark_assemble(C.byref(a), C.c_void_p(0x10000), 256, None) == 1
+    a.gamma_max, a.offsets = 16, 0
+    assert L.dspark_assemble(C.byref(a), C.c_void_p(0x10000), 256, None) == 1
+    a.struct_size = 4
+    assert L.dspark_assemble_workspace_size(C.byref(a), C.byref(n)) == 1
 
 
 def test_verify_validation(L):

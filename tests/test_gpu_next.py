@@ -1,0 +1,138 @@
+"""GPU parity of the widening calls through the C ABI against the CPU oracle: the flattened
+verify batch (dspark_assemble), the static confidence-threshold admission (scheduler mode 3)
+and sequential temperature scaling of the confidences (dspark_sample_block's sts_temp)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_draft_round_gb300 as ds
+from speculative_decoding_draft_round_gb300 import workloads as wl
+from parity import check_sample, to_np
+from conftest import load_golden
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    ds.lib()
+    oracle.build()
+
+
+def _i32(a):
+    return torch.as_tensor(np.asarray(a), dtype=torch.int32, device=DEV)
+
+
+# ------------------------------------------------------------------ flattened verify batch
+
+def _check_assemble(keep, anchor, tokens):
+    out = ds.assemble(_i32(keep), _i32(anchor), _i32(tokens))
+    torch.cuda.synchronize()
+    assert ds.check(out["workspace"]) == 0
+    o = oracle.assemble(keep, anchor, tokens)
+    for k in ("flat_tokens", "flat_request", "flat_position", "offsets"):
+        np.testing.assert_array_equal(to_np(out[k]), o[k], err_msg=k)   # index work: bit-exact
+
+
+@pytest.mark.parametrize("R,G", [(1, 1), (3, 3), (37, 6), (1000, 7), (8192, 1), (512, 16)])
+def test_assemble_matches_oracle(R, G):
+    rng = np.random.default_rng(R * 31 + G)
+    keep = rng.integers(0, G + 1, R)
+    anchor = rng.integers(0, 151936, R)
+    tokens = rng.integers(0, 151936, (R, G))
+    _check_assemble(keep, anchor, tokens)
+    _check_assemble(np.zeros(R, np.int64), anchor, tokens)        # nothing admitted
+    _check_assemble(np.full(R, G), anchor, tokens)                # everything admitted
+
+
+def test_assemble_clamps_out_of_range_keep():
+    R, G = 5, 4
+    keep = np.array([1, -3, 9, 4, 0])
+    anchor, tokens = np.arange(R), np.arange(R * G).reshape(R, G) + 100
+    out = ds.assemble(_i32(keep), _i32(anchor), _i32(tokens))
+    torch.cuda.synchronize()
+    assert ds.check(out["workspace"]) == 6   # DSPARK_ERR_DEVICE_INPUT: clamped
+    o = oracle.assemble(np.clip(keep, 0, G), anchor, tokens)
+    np.testing.assert_array_equal(to_np(out["flat_tokens"]), o["flat_tokens"])
+    np.testing.assert_array_equal(to_np(out["offsets"]), o["offsets"])
+
+
+def test_assemble_after_a_full_round():
+    rnd = wl.CONFIGS[3](device=DEV)
+    runner = ds.RoundRunner(rnd)
+    runner.set_round(4)
+    runner.run()
+    assert runner.check() == 0
+    res = runner.results()
+    tokens = to_np(res["tokens"])
+    keep = to_np(res["keep"])
+    anchor = to_np(rnd.anchor)
+    _check_assemble(keep, anchor, np.where(tokens < 0, 0, tokens))
+
+
+# ------------------------------------------------------------------ static threshold admission
+
+def _check_threshold(surv, sps, thr, gamma=None):
+    s32 = torch.as_tensor(surv, dtype=torch.float32, device=DEV)
+    g = None if gamma is None else _i32(gamma)
+    sp = torch.as_tensor(sps, dtype=torch.float32, device=DEV)
+    out = ds.schedule(s32, sp, ds.SCHED_THRESHOLD, gamma=g, threshold=thr)
+    torch.cuda.synchronize()
+    assert ds.check(out["workspace"]) == 0
+    thr32 = float(np.float32(thr))   # the call compares against the fp32 threshold
+    o = oracle.schedule(to_np(s32).astype(np.float64), to_np(sp).astype(np.float64), oracle.SCHED_THRESHOLD,
+                        gamma=None if gamma is None else np.asarray(gamma), threshold=thr32)
+    st = ds.decode_stats(out["stats"])
+    np.testing.assert_array_equal(to_np(out["keep"]), o["keep"])   # exact comparisons: bit-exact
+    assert st["admitted"] == o["admitted"] and st["pool"] == o["pool"] and st["capacity"] == -1
+    assert st["batch"] == s32.shape[0] + o["admitted"]
+    assert abs(st["theta_best"] - o["theta_best"]) <= 1e-9 * abs(o["theta_best"])
+    return st
+
+
+def test_threshold_worked_example_on_gpu():
+    ex = load_golden("worked_examples.json")["single_request"]
+    surv = np.cumprod(np.array(ex["c"]))[None, :]
+    sps = np.array(ex["sps"] + [ex["sps"][-1] * 0.9 ** i for i in range(1, 16)])
+    for thr, keep in ((0.96, 0), (0.9, 1), (0.8, 2), (0.5, 3), (0.2, 4)):
+        st = _check_threshold(surv, sps, thr)
+        assert st["admitted"] == keep
+
+
+@pytest.mark.parametrize("R,G", [(9, 5), (128, 16), (512, 16)])
+def test_threshold_matches_oracle(R, G):
+    rng = np.random.default_rng(R + G)
+    surv = np.cumprod(rng.uniform(0.3, 1.0, (R, G)), axis=1)
+    gamma = rng.integers(0, G + 1, R)
+    sps = wl.sps_staircase(R * (1 + G)).numpy()
+    for thr in (0.0, 0.25, 0.6, 0.95, 1.5):
+        _check_threshold(surv, sps, thr, gamma)
+    # survivals exactly at the threshold are admitted (>=)
+    surv[0, :] = np.float32(0.5)
+    _check_threshold(surv, sps, 0.5, gamma)
+
+
+# ------------------------------------------------------------------ sequential temperature scaling
+
+@pytest.mark.parametrize("spec", [
+    dict(name="sts_f32", R=11, G=5, V=300, r=24, d=20, dtype="f32", ew_std=0.2, gamma=[5, 0, 3, 5, 1, 2, 5, 4, 5, 0, 5]),
+    dict(name="sts_bf16", R=160, G=3, V=1000, r=64, d=96, dtype="bf16", ew_std=0.15),
+], ids=["cuda_core_f32", "tensor_core_bf16"])
+def test_sts_temperatures_match_oracle(spec):
+    spec = dict(spec)
+    name = spec.pop("name")
+    R, G, V, r, d, dtype = (spec.pop(k) for k in ("R", "G", "V", "r", "d", "dtype"))
+    rnd = wl.make_round(name, R, G, V, r, d, dtype, seed=77, device=DEV, sps=wl.sps_hyperbolic(R * (1 + G)),
+                        **spec)
+    rnd.round = 3
+    t = torch.tensor([0.5, 1.7, 3.0, 0.8, 1.1][:G], dtype=torch.float32, device=DEV)
+    out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                          rnd.seed, rnd.round, gamma=rnd.gamma, sts_temp=t)
+    torch.cuda.synchronize()
+    assert ds.check(out["workspace"]) == 0
+    check_sample(rnd, out, np.arange(R), sts_temp=t)   # the oracle gets the same temperatures
