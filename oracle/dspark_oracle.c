@@ -189,7 +189,28 @@ static void draft_logits(double* l, const void* U, int dtype, size_t u_off, int 
             for (int v = 0; v < V; ++v) l[v] += e * wrow[v];
         }
     }
-    for (int v = 0; v < V; ++v) l[v] = (load(U, dtype, u_off + v) + l[v]) / T;
+    /* temperature 0 (greedy decoding) keeps the raw logits */
+    const double div = T > 0.0 ? T : 1.0;
+    for (int v = 0; v < V; ++v) l[v] = (load(U, dtype, u_off + v) + l[v]) / div;
+}
+
+/* Greedy decoding (temperature 0): the arg-max (lowest index on ties) and the gap between the
+ * two largest values (both gaps of a draw report it). */
+static draw_t argmax_draw(const double* l, int V)
+{
+    draw_t dr;
+    memset(&dr, 0, sizeof dr);
+    int best = 0;
+    for (int v = 1; v < V; ++v)
+        if (l[v] > l[best]) best = v;
+    double second = -INFINITY;
+    for (int v = 0; v < V; ++v)
+        if (v != best && l[v] > second) second = l[v];
+    dr.token = best;
+    dr.second_token = -1;
+    dr.block = dr.second_block = -1;
+    dr.gap1 = dr.gap2 = l[best] - second;
+    return dr;
 }
 
 int dso_sample_block(const dso_sample_args* a)
@@ -220,13 +241,14 @@ int dso_sample_block(const dso_sample_args* a)
             }
             const int use_bias = (k > 0) || a->bias_first;
             draft_logits(l, a->U, a->dtype, idx * V, V, r, Wd, a->E, use_bias, prev, T);
-            draw_t dr = two_level_draw(l, V, a->noise_block, a->seed, a->round, PUR_DRAFT_BLOCK,
+            draw_t dr = T == 0.0 ? argmax_draw(l, V) : two_level_draw(l, V, a->noise_block, a->seed, a->round, PUR_DRAFT_BLOCK,
                                        PUR_DRAFT_ELEM, rid, (uint32_t)k);
             const int commit = a->forced_tokens ? a->forced_tokens[idx] : dr.token;
             a->tokens[idx] = dr.token;
             a->gap1[idx] = dr.gap1;
             a->gap2[idx] = dr.gap2;
-            a->lse[idx] = logsumexp(l, V);
+            /* temperature 0: the draft is a point mass, reported as lse = logit (log p_d = 0) */
+            a->lse[idx] = T == 0.0 ? l[commit] : logsumexp(l, V);
             a->logit[idx] = l[commit];
             /* eq. (7): c_k = sigmoid(w^T [h_k; W_1[x]]) + b */
             const int xc = a->conf_token ? commit : prev;
@@ -436,6 +458,30 @@ int dso_verify(const dso_verify_args* a)
         const int ell = a->keep[q];
         for (int k = 0; k < G; ++k) a->accept_margin[(size_t)q * G + k] = NAN;
         for (int i = 0; i <= G; ++i) a->lse_t[(size_t)q * (G + 1) + i] = NAN;
+        if (T == 0.0) {
+            /* greedy decoding: acceptance is an exact match with the target's arg-max; the first
+             * mismatch is replaced by that arg-max, and if every admitted token matches, the
+             * arg-max of row l_r is the bonus token */
+            int n = ell, next = -1;
+            double gap = INFINITY;
+            for (int j = 0; j <= ell; ++j) {
+                const size_t row = ((size_t)q * (G + 1) + j) * V;
+                for (int v = 0; v < V; ++v) zt[v] = load(a->target, a->dtype, row + v);
+                const draw_t t = argmax_draw(zt, V);
+                if (j == ell || a->tokens[(size_t)q * G + j] != t.token) {
+                    n = j;
+                    next = t.token;
+                    gap = t.gap1;
+                    break;
+                }
+            }
+            a->accepted[q] = n;
+            a->next_token[q] = next;
+            a->resampled[q] = n < ell ? 1 : 0;
+            a->gap1[q] = a->gap2[q] = gap;
+            a->slack1[q] = a->slack2[q] = 0.0;
+            continue;
+        }
         /* longest accepted prefix: accept x_j with probability min(1, p_t/p_d) */
         int n = ell;
         for (int j = 1; j <= ell; ++j) {

@@ -19,7 +19,10 @@
  *     (zhongzhuzhou.org notes, figure 5 threshold sweep);
  *   - sequential temperature scaling of the confidences (same notes, "STS");
  *   - the flattened variable-length verify batch (same notes, physical
- *     execution without padding).
+ *     execution without padding);
+ *   - greedy decoding at temperature 0 (same notes, FAQ on temperature 0):
+ *     the draft takes the arg-max of its logits, and acceptance is an exact
+ *     match with the target's arg-max.
  * Every pointer is a host pointer owned by the caller.
  */
 #ifndef DSPARK_ORACLE_H
