@@ -91,6 +91,9 @@ enum {
  *          elsewhere and only applied here) or 1 when sts_temp is NULL
  *   a_k  = a_{k-1} c_k             (a_0 = 1)
  * Outputs for k >= gamma_r are token -1 and zeros.
+ * temperature[r] = 0 is greedy decoding (zhongzhuzhou.org notes, FAQ on temperature 0):
+ *   x_k = arg-max of U[r][k] + B_k (lowest index on ties), draft_lse = draft_logit = its value
+ *   (the draft is a point mass).
  */
 typedef struct {
     uint32_t struct_size;
@@ -111,7 +114,7 @@ typedef struct {
     const float* w_h;     /* [d] */
     const float* w_e;     /* [r] */
     float b;
-    const float* temperature; /* [R], > 0 */
+    const float* temperature; /* [R], > 0, or 0 for greedy decoding */
     const int32_t* anchor;    /* [R] x_0 in 0..V-1 */
     uint64_t seed;
     uint64_t round;
@@ -217,6 +220,10 @@ dspark_status dspark_schedule(const dspark_schedule_args* args, void* workspace,
  *     next_token ~ p_t of row n.
  *   n = keep[r]: next_token ~ p_t of row keep[r]; resampled[r] = 0.
  * Committed tokens: tokens[r][0:n] followed by next_token[r] (the next anchor).
+ * temperature[r] = 0 (greedy decoding): tokens[r][j] is accepted iff it equals the arg-max of
+ *   target row j (lowest index on ties); the first mismatch is replaced by that arg-max
+ *   (resampled 1), and when every admitted token matches, the arg-max of row keep[r] is the
+ *   bonus token (resampled 0). No random numbers are drawn.
  */
 typedef struct {
     uint32_t struct_size;

@@ -87,12 +87,13 @@ constexpr int kSimtReq = 8;   // requests per block of the CUDA-core contraction
 
 struct StepRequest {
     int active, prev, use_bias;
-    float scale;              // log2(e) / T
+    float scale;              // log2(e) / T (log2(e) for greedy requests)
+    int greedy;               // temperature 0: the draw is the arg-max (no noise)
 };
 
 __device__ __forceinline__ StepRequest draft_request(const DraftStep& p, int q)
 {
-    StepRequest s{0, 0, 0, 0.f};
+    StepRequest s{0, 0, 0, 0.f, 0};
     if (q >= p.R) return s;
     int g = p.gamma ? p.gamma[q] : p.G;
     if (g < 0 || g > p.G) {
@@ -103,14 +104,15 @@ __device__ __forceinline__ StepRequest draft_request(const DraftStep& p, int q)
     s.active = 1;
     s.prev = checked_index(p.k == 0 ? p.anchor[q] : p.x_cur[q], p.V, p.status);
     s.use_bias = (p.k > 0) || p.bias_first;
-    s.scale = kLog2e / p.temperature[q];
+    s.greedy = p.temperature[q] == 0.f;
+    s.scale = s.greedy ? kLog2e : kLog2e / p.temperature[q];
     return s;
 }
 
 // the part of draft_request that reads only inputs (no earlier kernel's output)
 __device__ __forceinline__ StepRequest draft_request_inputs(const DraftStep& p, int q)
 {
-    StepRequest s{0, 0, 0, 0.f};
+    StepRequest s{0, 0, 0, 0.f, 0};
     if (q >= p.R) return s;
     int g = p.gamma ? p.gamma[q] : p.G;
     if (g < 0 || g > p.G) {
@@ -120,7 +122,8 @@ __device__ __forceinline__ StepRequest draft_request_inputs(const DraftStep& p, 
     if (p.k >= g) return s;
     s.active = 1;
     s.use_bias = (p.k > 0) || p.bias_first;
-    s.scale = kLog2e / p.temperature[q];
+    s.greedy = p.temperature[q] == 0.f;
+    s.scale = s.greedy ? kLog2e : kLog2e / p.temperature[q];
     return s;
 }
 
@@ -165,9 +168,11 @@ __global__ void __launch_bounds__(kNoiseBlock) draft_stats_simt_kernel(DraftStep
         const float s = block_sum<kNoiseBlock>(e, red);
         if (t == 0) {
             p.stats[(size_t)q * p.nblk + b] = make_float2(m, s);
-            const float z = (m + log2f(s)) * kLn2 -
-                            logf(-logf(uniform_at(make_key(p.seed), p.round, kDraftBlock, (uint32_t)q, (uint32_t)p.k,
-                                                  (uint32_t)b)));
+            // block key of the two-level draw; greedy requests take the block holding the maximum
+            const float z = req[j].greedy ? m
+                                          : (m + log2f(s)) * kLn2 -
+                                                logf(-logf(uniform_at(make_key(p.seed), p.round, kDraftBlock,
+                                                                      (uint32_t)q, (uint32_t)p.k, (uint32_t)b)));
             atomicMax(p.pick + (size_t)p.k * p.R + q, pack_pick(z, b));
         }
     }
@@ -219,7 +224,8 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     // inputs that no earlier kernel writes can be read before the dependency wait
     const StepRequest rq = draft_request_inputs(p, q);
     const size_t o = (size_t)q * p.G + p.k;
-    const float invT = 1.f / p.temperature[q];
+    const bool greedy = p.temperature[q] == 0.f;   // temperature 0: arg-max draft
+    const float invT = greedy ? 1.f : 1.f / p.temperature[q];
     const float hw = p.hw[o];
     pdl_wait();      // block statistics, pick slots and x_cur come from the kernels before this one
     pdl_trigger();   // the next step's statistics kernel may start its prefetch
@@ -329,7 +335,7 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     float lv = 0.f;
     if (t < kNoiseBlock && v < p.V) {
         lv = (u_v + bias) * invT;
-        cand = ArgMax{lv + gumbel_at(key, p.round, kDraftElem, (uint32_t)q, (uint32_t)p.k, (uint32_t)v), v};
+        cand = ArgMax{greedy ? lv : lv + gumbel_at(key, p.round, kDraftElem, (uint32_t)q, (uint32_t)p.k, (uint32_t)v), v};
     }
     const ArgMax win = block_argmax<kCommitThreads>(cand, sv, si);
     int tok = win.i;
@@ -360,7 +366,8 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
         p.tokens[o] = s_tok;
         p.conf[o] = c;
         p.surv[o] = surv_prev * c;
-        p.draft_lse[o] = (tot.m + log2f(tot.s)) * kLn2;
+        // greedy: the draft is a point mass, reported as lse = logit (log p_d(x_k) = 0)
+        p.draft_lse[o] = greedy ? s_logit : (tot.m + log2f(tot.s)) * kLn2;
         p.draft_logit[o] = s_logit;
         p.x_cur[q] = s_tok;
     }

@@ -304,7 +304,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // Per-row metadata of the current request tile (shared memory, 32 bytes per row).
 struct RowMeta {
     int prev;         // token whose W_1 row forms this A row
-    int active;       // row takes part (draft: k < gamma_q; residual: request rejected)
+    int active;       // row takes part (draft: k < gamma_q; residual: request rejected); draft: 2 = greedy
     int use_bias;     // A row is W_1[prev] (else zero)
     float scale;      // log2(e) / T
     float lse_d2;     // residual: draft log-normaliser of the rejected position, log2 units
@@ -347,10 +347,10 @@ __device__ __forceinline__ RowMeta row_meta(const TcParams& P, int q)
             g = g < 0 ? 0 : p.G;
         }
         if (p.k >= g) return m;
-        m.active = 1;
+        m.active = p.temperature[q] == 0.f ? 2 : 1;   // temperature 0: arg-max draft
         m.prev = q;   // row of a_next
         m.use_bias = (p.k > 0) || p.bias_first;
-        m.scale = kLog2e / p.temperature[q];
+        m.scale = m.active == 2 ? kLog2e : kLog2e / p.temperature[q];
     } else {
         const VerifyParams& p = P.v;
         const int n = p.rej[q];
@@ -796,9 +796,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     P.d.stats[o] = make_float2(M, S);
                     // block-level Gumbel-max of the two-level draw, folded into a packed key
                     const int q = mt * BM + m;
-                    const float z = (M + log2f(S)) * kLn2 -
-                                    logf(-logf(uniform_at(make_key(P.d.seed), P.d.round, kDraftBlock, (uint32_t)q,
-                                                          (uint32_t)P.k, (uint32_t)b)));
+                    // greedy requests take the block holding the maximum
+                    const float z = rm.active == 2 ? M
+                                                   : (M + log2f(S)) * kLn2 -
+                                                         logf(-logf(uniform_at(make_key(P.d.seed), P.d.round, kDraftBlock,
+                                                                               (uint32_t)q, (uint32_t)P.k, (uint32_t)b)));
                     atomicMax(P.d.pick + (size_t)P.k * P.R + q, pack_pick(z, b));
                 } else {
                     P.v.res_stats[o] = pp[m].x + pp[BM + m].x + pp[2 * BM + m].x + pp[3 * BM + m].x;

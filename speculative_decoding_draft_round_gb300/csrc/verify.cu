@@ -114,6 +114,28 @@ __device__ __forceinline__ void row_block_stats8(const T* row, int V, int b0, fl
     }
 }
 
+// Greedy requests (temperature 0): per 128-wide block the maximum of the raw target logits and
+// the lowest index attaining it, stored as (max, index) in the statistics slot.
+template <typename T>
+__device__ __forceinline__ float2 row_block_argmax(const T* row, int V, int b, int lane)
+{
+    float m = -INFINITY;
+    int mi = -1;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {   // lane's columns in increasing order: a later equal value never wins
+        const int v = b * kNoiseBlock + e * 32 + lane;
+        if (v < V) {
+            const float x = ld(row, v);
+            if (x > m || mi < 0) {
+                m = x;
+                mi = v;
+            }
+        }
+    }
+    const ArgMax best = warp_argmax(ArgMax{m, mi});
+    return make_float2(best.v, (float)best.i);   // indices below 2^24 are exact in fp32
+}
+
 // grid (vocabulary chunks, R): the CTA walks target rows 0..keep[r] of its request
 template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParams p)
@@ -121,10 +143,22 @@ __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParam
     const int q = blockIdx.y;
     const int ell = request_keep(p, q);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float scale = kLog2e / p.temperature[q];
+    const bool greedy = p.temperature[q] == 0.f;
+    const float scale = greedy ? 1.f : kLog2e / p.temperature[q];
     const bool vec = (p.V % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.target) & 15u) == 0);
     const int b0 = (blockIdx.x * kRowWarps + warp) * kRowBlocksPerWarp;
     if (b0 >= p.nblk) return;
+    if (greedy) {
+        for (int i = 0; i <= ell; ++i) {
+            const T* row = static_cast<const T*>(p.target) + ((size_t)q * (p.G + 1) + i) * p.V;
+            float2* out = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
+            for (int bb = 0; bb < kRowBlocksPerWarp && b0 + bb < p.nblk; ++bb) {
+                const float2 st = row_block_argmax<T>(row, p.V, b0 + bb, lane);
+                if (lane == 0) out[b0 + bb] = st;
+            }
+        }
+        return;
+    }
     for (int i = 0; i <= ell; ++i) {
         const T* row = static_cast<const T*>(p.target) + ((size_t)q * (p.G + 1) + i) * p.V;
         float2* out = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
@@ -153,8 +187,34 @@ __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyPar
     __shared__ float lse_s[DSPARK_MAX_GAMMA + 1];
     const int q = blockIdx.x, t = threadIdx.x;
     const int ell = request_keep(p, q);
-    const float invT = 1.f / p.temperature[q];
     const T* target = static_cast<const T*>(p.target);
+    if (p.temperature[q] == 0.f) {
+        // greedy decoding: accept while the draft token equals the target's arg-max; the first
+        // mismatch is replaced by that arg-max, else the arg-max of row ell is the bonus token
+        __shared__ int s_next;
+        int n = ell;
+        for (int j = 0; j <= ell; ++j) {
+            const float2* st = p.row_stats + ((size_t)q * (p.G + 1) + j) * p.nblk;
+            ArgMax best{-INFINITY, -1};
+            for (int b = t; b < p.nblk; b += kDecideThreads) best = argmax_better(best, ArgMax{st[b].x, (int)st[b].y});
+            best = block_argmax<kDecideThreads>(best, sv, si);
+            const int tgt = best.i < 0 ? 0 : best.i;
+            if (j == ell || checked_index(p.tokens[(size_t)q * p.G + j], p.V, p.status) != tgt) {
+                n = j;
+                if (t == 0) s_next = tgt;
+                break;   // uniform: every thread sees the same reduction
+            }
+        }
+        __syncthreads();
+        if (t == 0) {
+            p.accepted[q] = n;
+            p.rej[q] = -1;   // nothing for the residual kernels
+            p.next_token[q] = s_next;
+            p.resampled[q] = n < ell ? 1 : 0;
+        }
+        return;
+    }
+    const float invT = 1.f / p.temperature[q];
 
     // log-normalisers of target rows 0..ell (natural log)
     for (int i = 0; i <= ell; ++i) {

@@ -136,3 +136,69 @@ def test_sts_temperatures_match_oracle(spec):
     torch.cuda.synchronize()
     assert ds.check(out["workspace"]) == 0
     check_sample(rnd, out, np.arange(R), sts_temp=t)   # the oracle gets the same temperatures
+
+
+# ------------------------------------------------------------------ greedy decoding (temperature 0)
+
+GREEDY_SPECS = [
+    dict(name="greedy_f32", R=11, G=5, V=300, r=24, d=20, dtype="f32", ew_std=0.2),
+    dict(name="greedy_bf16", R=160, G=3, V=1000, r=64, d=96, dtype="bf16", ew_std=0.15),
+]
+
+
+def _greedy_round(spec, seed):
+    spec = dict(spec)
+    name = spec.pop("name")
+    R, G, V, r, d, dtype = (spec.pop(k) for k in ("R", "G", "V", "r", "d", "dtype"))
+    # every third request decodes greedily, the others sample at T in [0.5, 1.5)
+    temp = lambda R_, g, dev: torch.where(torch.arange(R_, device=dev) % 3 == 0, torch.zeros(R_, device=dev),
+                                          0.5 + torch.rand((R_,), generator=g, device=dev))
+    rnd = wl.make_round(name, R, G, V, r, d, dtype, seed=seed, device=DEV, temperature=temp,
+                        sps=wl.sps_hyperbolic(R * (1 + G)), **spec)
+    rnd.round = 5
+    return rnd
+
+
+@pytest.mark.parametrize("spec", GREEDY_SPECS, ids=["cuda_core_f32", "tensor_core_bf16"])
+def test_greedy_draft_matches_oracle(spec):
+    rnd = _greedy_round(spec, 31)
+    out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                          rnd.seed, rnd.round, gamma=rnd.gamma)
+    torch.cuda.synchronize()
+    assert ds.check(out["workspace"]) == 0
+    check_sample(rnd, out, np.arange(rnd.R))
+    g = to_np(rnd.temperature) == 0
+    np.testing.assert_array_equal(to_np(out["draft_lse"])[g], to_np(out["draft_logit"])[g])
+
+
+@pytest.mark.parametrize("spec", GREEDY_SPECS, ids=["cuda_core_f32", "tensor_core_bf16"])
+def test_greedy_verify_matches_oracle(spec):
+    from parity import check_verify
+    rnd = _greedy_round(spec, 32)
+    out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                          rnd.seed, rnd.round, gamma=rnd.gamma)
+    torch.cuda.synchronize()
+    R, G, V = rnd.R, rnd.gamma_max, rnd.V
+    # make the target's arg-max agree with the draft on about 60% of the positions
+    tok = out["tokens"].long()
+    agree = torch.rand((R, G), device=DEV) < 0.6
+    tgt = rnd.target.float()
+    rowmax = tgt[:, :G].amax(dim=2)
+    bump = torch.where(agree, rowmax + 4.0, tgt[:, :G].gather(2, tok.unsqueeze(2)).squeeze(2))
+    tgt[:, :G].scatter_(2, tok.unsqueeze(2), bump.unsqueeze(2))
+    rnd.target = tgt.to(rnd.target.dtype)
+    keep = torch.randint(0, G + 1, (R,), device=DEV, dtype=torch.int32)
+    v = ds.verify(rnd.target, rnd.U, rnd.E, rnd.W, rnd.anchor, out["tokens"], out["draft_lse"],
+                  out["draft_logit"], keep, rnd.temperature, rnd.seed, rnd.round, gamma=rnd.gamma)
+    torch.cuda.synchronize()
+    assert ds.check(v["workspace"]) == 0
+    n_exc = check_verify(rnd, out, keep, v, np.arange(R))
+    # greedy verification compares raw target values exactly: no excusal on those requests
+    g = np.where(to_np(rnd.temperature) == 0)[0]
+    o = oracle.verify(to_np(rnd.target)[g], to_np(rnd.U)[g], to_np(rnd.E), to_np(rnd.W), to_np(rnd.anchor)[g],
+                      to_np(out["tokens"])[g], to_np(out["draft_lse"])[g].astype(np.float64),
+                      to_np(out["draft_logit"])[g].astype(np.float64), to_np(keep)[g],
+                      to_np(rnd.temperature)[g], rnd.seed, rnd.round, req_ids=g)
+    np.testing.assert_array_equal(to_np(v["accepted"])[g], o["accepted"])
+    np.testing.assert_array_equal(to_np(v["next_token"])[g], o["next_token"])
+    np.testing.assert_array_equal(to_np(v["resampled"])[g], o["resampled"])
