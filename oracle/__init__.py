@@ -26,6 +26,7 @@ _LIB_PATH = os.path.join(_HERE, "libdspark_oracle.so")
 
 F32, BF16, F64 = 0, 1, 2
 SCHED_SYNC, SCHED_ASYNC_CAPACITY, SCHED_FULL_SCAN, SCHED_THRESHOLD = 0, 1, 2, 3
+HEAD_MARKOV, HEAD_RNN = 0, 1
 
 _lib = None
 _lock = threading.Lock()
@@ -59,7 +60,7 @@ class _SampleArgs(C.Structure):
         ("forced_tokens", C.c_void_p),
         ("tokens", C.c_void_p), ("conf", C.c_void_p), ("surv", C.c_void_p), ("lse", C.c_void_p),
         ("logit", C.c_void_p), ("gap1", C.c_void_p), ("gap2", C.c_void_p),
-        ("sts_temp", C.c_void_p),
+        ("sts_temp", C.c_void_p), ("head", C.c_int), ("W_rnn", C.c_void_p), ("a_rows", C.c_void_p),
     ]
 
 
@@ -92,7 +93,7 @@ class _VerifyArgs(C.Structure):
         ("draft_lse", C.c_void_p), ("draft_logit", C.c_void_p),
         ("keep", C.c_void_p), ("temperature", C.c_void_p),
         ("seed", C.c_uint64), ("round", C.c_uint64),
-        ("bias_first", C.c_int), ("noise_block", C.c_int),
+        ("bias_first", C.c_int), ("noise_block", C.c_int), ("a_rows", C.c_void_p),
         ("accepted", C.c_void_p), ("next_token", C.c_void_p), ("resampled", C.c_void_p),
         ("accept_margin", C.c_void_p), ("lse_t", C.c_void_p),
         ("gap1", C.c_void_p), ("gap2", C.c_void_p), ("slack1", C.c_void_p), ("slack2", C.c_void_p),
@@ -172,7 +173,7 @@ def _run(fn, parts, threads):
 
 def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamma=None,
                  req_ids=None, conf_token=0, bias_first=1, noise_block=128, forced_tokens=None,
-                 sts_temp=None, threads=1):
+                 sts_temp=None, head=HEAD_MARKOV, W_rnn=None, threads=1):
     """Markov-head serial sampling, confidence head and survival products for R requests.
 
     U [R][G][V], E [V][r], W [r][V], h [R][G][d] share one element type
@@ -190,10 +191,14 @@ def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gam
     req_ids = np.arange(R, dtype=np.int32) if req_ids is None else _c(req_ids, np.int32)
     forced = None if forced_tokens is None else _c(forced_tokens, np.int32)
     sts = None if sts_temp is None else _c(sts_temp, np.float64)
+    if head == HEAD_RNN:
+        W_rnn = _c(W_rnn)
+        if _dtype_code(W_rnn) != dt or W_rnn.shape != (3 * r, 2 * r + d):
+            raise TypeError("W_rnn must be [3r][2r+d] of the inputs' element type")
     out = {
         "tokens": np.zeros((R, G), np.int32), "conf": np.zeros((R, G)), "surv": np.zeros((R, G)),
         "lse": np.zeros((R, G)), "logit": np.zeros((R, G)), "gap1": np.zeros((R, G)),
-        "gap2": np.zeros((R, G)),
+        "gap2": np.zeros((R, G)), "a_rows": np.zeros((R, G, r)),
     }
 
     def part(se):
@@ -209,6 +214,8 @@ def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gam
         a.conf_token, a.bias_first, a.noise_block = int(conf_token), int(bias_first), int(noise_block)
         a.forced_tokens = _p(None if forced is None else forced[s:e])
         a.sts_temp = _p(sts)
+        a.head = int(head)
+        a.W_rnn = _p(W_rnn if head == HEAD_RNN else None)
         for k, arr in out.items():
             setattr(a, k, _p(arr[s:e]))
         rc = lib().dso_sample_block(C.byref(a))
@@ -262,7 +269,7 @@ def schedule(surv, sps, mode=SCHED_SYNC, *, gamma=None, surv_capacity=None, thre
 # ----------------------------------------------------------------- verifier
 
 def verify(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temperature, seed, rnd, *,
-           gamma=None, req_ids=None, bias_first=1, noise_block=128, threads=1):
+           gamma=None, req_ids=None, bias_first=1, noise_block=128, a_rows=None, threads=1):
     """Rejection-sampling verification of the admitted prefixes of R requests."""
     target, U, E, W = _c(target), _c(U), _c(E), _c(W)
     dt = _dtype_code(U)
@@ -275,6 +282,7 @@ def verify(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temper
     temperature = _c(temperature, np.float32)
     gamma = None if gamma is None else _c(gamma, np.int32)
     req_ids = np.arange(R, dtype=np.int32) if req_ids is None else _c(req_ids, np.int32)
+    arows = None if a_rows is None else _c(a_rows, np.float64)
     out = {
         "accepted": np.zeros(R, np.int32), "next_token": np.zeros(R, np.int32),
         "resampled": np.zeros(R, np.int32), "accept_margin": np.zeros((R, G)),
@@ -294,6 +302,7 @@ def verify(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temper
         a.keep, a.temperature = _p(keep[s:e]), _p(temperature[s:e])
         a.seed, a.round = int(seed), int(rnd)
         a.bias_first, a.noise_block = int(bias_first), int(noise_block)
+        a.a_rows = _p(None if arows is None else arows[s:e])
         for k, arr in out.items():
             setattr(a, k, _p(arr[s:e]))
         rc = lib().dso_verify(C.byref(a))

@@ -178,13 +178,14 @@ static draw_t two_level_draw(const double* logw, int V, int nb, uint64_t seed, u
 /* -------------------------------------------------------------- sampler */
 
 /* logits l[v] = (U_k(v) + B_k(v)) / T with B_k = W_1[prev] W_2 (eq. 4-5), or 0 */
+/* l = (U + B) / T with B = a^T W_2, a = arow if given, else W_1[prev] (Markov head) */
 static void draft_logits(double* l, const void* U, int dtype, size_t u_off, int V, int r,
-                         const double* Wd, const void* E, int use_bias, int prev, double T)
+                         const double* Wd, const void* E, int use_bias, int prev, double T, const double* arow)
 {
     for (int v = 0; v < V; ++v) l[v] = 0.0;
     if (use_bias) {
         for (int i = 0; i < r; ++i) {
-            double e = load(E, dtype, (size_t)prev * r + i);
+            double e = arow ? arow[i] : load(E, dtype, (size_t)prev * r + i);
             const double* wrow = Wd + (size_t)i * V;
             for (int v = 0; v < V; ++v) l[v] += e * wrow[v];
         }
@@ -218,11 +219,20 @@ int dso_sample_block(const dso_sample_args* a)
     if (!a || a->R < 0 || a->gamma_max < 1 || a->V < 1 || a->r < 1 || a->d < 1 || a->noise_block < 1)
         return 1;
     const int R = a->R, G = a->gamma_max, V = a->V, r = a->r, d = a->d;
+    const int rnn = a->head == DSO_HEAD_RNN;
+    if (rnn && !a->W_rnn) return 1;
+    const int Z = 2 * r + d;
     double* Wd = to_double(a->W, a->dtype, (size_t)r * V);
     double* l = (double*)malloc((size_t)V * sizeof(double));
-    if (!Wd || !l) {
+    double* st = (double*)malloc((size_t)r * sizeof(double));   /* RNN state s */
+    double* z = (double*)malloc((size_t)Z * sizeof(double));
+    double* o = (double*)malloc((size_t)r * sizeof(double));
+    if (!Wd || !l || !st || !z || !o) {
         free(Wd);
         free(l);
+        free(st);
+        free(z);
+        free(o);
         return 2;
     }
     for (int q = 0; q < R; ++q) {
@@ -231,16 +241,41 @@ int dso_sample_block(const dso_sample_args* a)
         const double T = (double)a->temperature[q];
         int prev = a->anchor[q];
         double s = 1.0;
+        for (int i = 0; i < r; ++i) st[i] = 0.0;   /* s_0 = 0 */
         for (int k = 0; k < G; ++k) {
             const size_t idx = (size_t)q * G + k;
             if (k >= g) {
                 a->tokens[idx] = -1;
                 a->conf[idx] = a->surv[idx] = a->lse[idx] = a->logit[idx] = 0.0;
                 a->gap1[idx] = a->gap2[idx] = INFINITY;
+                if (a->a_rows)
+                    for (int i = 0; i < r; ++i) a->a_rows[idx * r + i] = 0.0;
                 continue;
             }
             const int use_bias = (k > 0) || a->bias_first;
-            draft_logits(l, a->U, a->dtype, idx * V, V, r, Wd, a->E, use_bias, prev, T);
+            if (rnn) {
+                /* eq. (6): one packed projection of z_k = [s_{k-1}; W_1[x_{k-1}]; h_k], split into the
+                 * gate, candidate and output parts */
+                for (int i = 0; i < r; ++i) z[i] = st[i];
+                for (int i = 0; i < r; ++i) z[r + i] = load(a->E, a->dtype, (size_t)prev * r + i);
+                for (int j = 0; j < d; ++j) z[2 * r + j] = load(a->h, a->dtype, idx * d + j);
+                for (int i = 0; i < r; ++i) {
+                    double yg = 0.0, yc = 0.0, yo = 0.0;
+                    for (int j = 0; j < Z; ++j) {
+                        yg += load(a->W_rnn, a->dtype, (size_t)i * Z + j) * z[j];
+                        yc += load(a->W_rnn, a->dtype, (size_t)(r + i) * Z + j) * z[j];
+                        yo += load(a->W_rnn, a->dtype, (size_t)(2 * r + i) * Z + j) * z[j];
+                    }
+                    const double gate = 1.0 / (1.0 + exp(-yg));
+                    st[i] = gate * st[i] + (1.0 - gate) * tanh(yc);   /* z keeps s_{k-1} for the other rows */
+                    o[i] = tanh(yo);
+                }
+            } else {
+                for (int i = 0; i < r; ++i) o[i] = load(a->E, a->dtype, (size_t)prev * r + i);
+            }
+            if (a->a_rows)
+                for (int i = 0; i < r; ++i) a->a_rows[idx * r + i] = o[i];
+            draft_logits(l, a->U, a->dtype, idx * V, V, r, Wd, a->E, use_bias, prev, T, o);
             draw_t dr = T == 0.0 ? argmax_draw(l, V) : two_level_draw(l, V, a->noise_block, a->seed, a->round, PUR_DRAFT_BLOCK,
                                        PUR_DRAFT_ELEM, rid, (uint32_t)k);
             const int commit = a->forced_tokens ? a->forced_tokens[idx] : dr.token;
@@ -266,6 +301,9 @@ int dso_sample_block(const dso_sample_args* a)
     }
     free(Wd);
     free(l);
+    free(st);
+    free(z);
+    free(o);
     return 0;
 }
 
@@ -514,7 +552,8 @@ int dso_verify(const dso_verify_args* a)
             /* rejected at draft position n: resample from norm(max(0, p_t - p_d)) */
             const int prev = n == 0 ? a->anchor[q] : a->tokens[(size_t)q * G + n - 1];
             const int use_bias = (n > 0) || a->bias_first;
-            draft_logits(ld, a->U, a->dtype, ((size_t)q * G + n) * V, V, r, Wd, a->E, use_bias, prev, T);
+            draft_logits(ld, a->U, a->dtype, ((size_t)q * G + n) * V, V, r, Wd, a->E, use_bias, prev, T,
+                         a->a_rows ? a->a_rows + ((size_t)q * G + n) * r : NULL);
             const double lse_d = logsumexp(ld, V);
             int any = 0;
             for (int v = 0; v < V; ++v) {

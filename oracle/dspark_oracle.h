@@ -9,6 +9,8 @@
  * "DSpark: Confidence-Scheduled Speculative Decoding with Semi-Autoregressive
  * Generation" (arXiv:2607.05147) as described on the pages it was built from:
  *   - semi-autoregressive factorisation, eq. (4); Markov bias, eq. (5);
+ *     RNN head, eq. (6): z_k = [s_{k-1}; W_1[x_{k-1}]; h_k], s_k = g s_{k-1} + (1 - g) tanh(W_c z_k)
+ *     with g = sigmoid(W_g z_k), s_0 = 0, B_k = W_2^T tanh(W_o z_k);
  *   - confidence head, eq. (7); survival products a_j = prod c_i;
  *   - Algorithm 1 (hardware-aware prefix scheduler) and the asynchronous
  *     capacity variant (section 5.2 of the paper);
@@ -35,6 +37,9 @@ extern "C" {
 
 /* element types accepted for tensor inputs */
 enum { DSO_F32 = 0, DSO_BF16 = 1, DSO_F64 = 2 };
+
+/* sequential heads: the Markov bias of eq. (5) or the gated recurrent state of eq. (6) */
+enum { DSO_HEAD_MARKOV = 0, DSO_HEAD_RNN = 1 };
 
 /* scheduler modes */
 enum { DSO_SCHED_SYNC = 0, DSO_SCHED_ASYNC_CAPACITY = 1, DSO_SCHED_FULL_SCAN = 2, DSO_SCHED_THRESHOLD = 3 };
@@ -75,6 +80,10 @@ typedef struct {
     double* gap2;                       /* top-two gap of the element-level perturbed values */
     const double* sts_temp;             /* [gamma_max] or NULL: per-position temperature of the confidence
                                            logit (sequential temperature scaling), c_k = sigmoid(l_k / t_k) */
+    int head;                           /* DSO_HEAD_MARKOV (eq. 5) or DSO_HEAD_RNN (eq. 6) */
+    const void* W_rnn;                  /* [3r][2r+d] (dtype): rows W_g, then W_c, then W_o (RNN head) */
+    double* a_rows;                     /* [R][gamma_max][r] or NULL: out, the bias operand of each step
+                                           (W_1[x_{k-1}] for the Markov head, tanh(W_o z_k) for the RNN head) */
 } dso_sample_args;
 
 int dso_sample_block(const dso_sample_args* a);
@@ -118,6 +127,8 @@ typedef struct {
     const float* temperature;           /* [R] */
     uint64_t seed, round;
     int bias_first, noise_block;
+    const double* a_rows;               /* [R][gamma_max][r] or NULL: bias operand of each draft position
+                                           (from dso_sample_block); NULL = W_1[x_{k-1}] (Markov head) */
     /* outputs */
     int32_t* accepted;                  /* [R] n_r */
     int32_t* next_token;                /* [R] residual or bonus token */
