@@ -13,7 +13,8 @@
  *  - Every tensor pointer is a caller-owned DEVICE pointer (for example the
  *    storage of a torch tensor) in row-major layout with the shape stated. The
  *    library allocates nothing, keeps nothing between calls and never writes
- *    an input.
+ *    an input -- except that the RNN head's GEMM runs through one cuBLAS handle
+ *    per device, created (and allocating) on that device's first RNN-head call.
  *  - Scratch memory is a caller-owned device buffer of at least the size the
  *    matching *_workspace_size call reports; distinct concurrent calls need
  *    distinct workspaces. The workspace's first 256 bytes hold a device status
@@ -65,6 +66,11 @@ enum {
 enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 };
 
 enum {
+    DSPARK_HEAD_MARKOV = 0,          /* eq. 5: B_k = W_1[x_{k-1}] W_2 */
+    DSPARK_HEAD_RNN = 1              /* eq. 6: gated recurrent state, B_k = W_2^T tanh(W_o z_k) */
+};
+
+enum {
     DSPARK_SCHED_SYNC = 0,           /* Algorithm 1: stop at the first Theta <= Theta_best */
     DSPARK_SCHED_ASYNC_CAPACITY = 1, /* section 5.2: capacity K from old survivals, current ranking */
     DSPARK_SCHED_FULL_SCAN = 2,      /* arg-max of Theta over every prefix of the sorted pool */
@@ -91,6 +97,16 @@ enum {
  *          elsewhere and only applied here) or 1 when sts_temp is NULL
  *   a_k  = a_{k-1} c_k             (a_0 = 1)
  * Outputs for k >= gamma_r are token -1 and zeros.
+ * head = DSPARK_HEAD_RNN replaces the bias operand W_1[x_{k-1}] by the RNN head's output
+ * (zhongzhuzhou.org notes, eq. 6):
+ *   z_k = [s_{k-1}; W_1[x_{k-1}]; h[r][k]],  [y_g; y_c; y_o] = W_rnn z_k,  s_0 = 0,
+ *   s_k = sigmoid(y_g) * s_{k-1} + (1 - sigmoid(y_g)) * tanh(y_c),  B_k = tanh(y_o) W_2.
+ *   The h part of W_rnn z_k is one GEMM over all positions (cuBLAS, fp32 accumulation), the
+ *   rest a per-step kernel in fp32; on the tensor-core path tanh(y_o) enters the contraction
+ *   as two bf16 operands (its bf16 rounding and the rounding of the remainder), so the bias
+ *   keeps about 16 significant bits.
+ * a_rows (optional output) receives each step's bias operand in fp32 (W_1[x_{k-1}] or
+ * tanh(y_o)); dspark_verify needs them for an RNN-head draft.
  * temperature[r] = 0 is greedy decoding (zhongzhuzhou.org notes, FAQ on temperature 0):
  *   x_k = arg-max of U[r][k] + B_k (lowest index on ties), draft_lse = draft_logit = its value
  *   (the draft is a point mass).
@@ -124,6 +140,9 @@ typedef struct {
     float* draft_lse;         /* out [R][gamma_max] log sum_v exp(l_k(v)) */
     float* draft_logit;       /* out [R][gamma_max] l_k(x_k) */
     const float* sts_temp;    /* [gamma_max] per-position confidence temperatures (> 0), or NULL */
+    int32_t head;             /* DSPARK_HEAD_MARKOV or DSPARK_HEAD_RNN */
+    const void* W_rnn;        /* [3r][2r+d] (dtype of E): rows W_g, W_c, W_o (RNN head only) */
+    float* a_rows;            /* out [R][gamma_max][r] bias operand of each step, or NULL */
 } dspark_sample_args;
 
 dspark_status dspark_sample_workspace_size(const dspark_sample_args* args, size_t* bytes);
@@ -144,7 +163,8 @@ dspark_status dspark_sample_block(const dspark_sample_args* args, void* workspac
  * process exits. It calls no cudaMalloc, cudaFree or allocating library routine.
  *  - Arguments and results are those of dspark_sample_block.
  *  - Shapes whose dspark_sample_workspace_size exceeds DSPARK_STATIC_WORKSPACE_BYTES return
- *    DSPARK_ERR_UNSUPPORTED_SHAPE before any launch.
+ *    DSPARK_ERR_UNSUPPORTED_SHAPE before any launch, and so does head = DSPARK_HEAD_RNN (its
+ *    GEMM runs through a cuBLAS handle, which allocates).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *    that device current; make that first call before any stream capture.
  *  - Every call on a device shares the one array, which keeps the previous call's contents (the
@@ -219,6 +239,8 @@ dspark_status dspark_schedule(const dspark_schedule_args* args, void* workspace,
  *     If that residual is zero everywhere (possible only through rounding)
  *     next_token ~ p_t of row n.
  *   n = keep[r]: next_token ~ p_t of row keep[r]; resampled[r] = 0.
+ * The residual's p_d is rebuilt with the bias operand W_1[x_{n-1}] (Markov head) or, when
+ *   a_rows is given, with a_rows[r][n] (the RNN head's operand reported by the sampler).
  * Committed tokens: tokens[r][0:n] followed by next_token[r] (the next anchor).
  * temperature[r] = 0 (greedy decoding): tokens[r][j] is accepted iff it equals the arg-max of
  *   target row j (lowest index on ties); the first mismatch is replaced by that arg-max
@@ -250,6 +272,7 @@ typedef struct {
     int32_t* accepted;           /* out [R] */
     int32_t* next_token;         /* out [R] */
     uint8_t* resampled;          /* out [R] */
+    const float* a_rows;         /* [R][gamma_max][r] bias operands from dspark_sample_block, or NULL */
 } dspark_verify_args;
 
 dspark_status dspark_verify_workspace_size(const dspark_verify_args* args, size_t* bytes);
@@ -307,7 +330,8 @@ enum {
     DSPARK_KERNEL_VERIFY_DECIDE = 5,
     DSPARK_KERNEL_RESIDUAL_STATS = 6,
     DSPARK_KERNEL_RESIDUAL_PICK = 7,
-    DSPARK_KERNEL_ASSEMBLE = 8
+    DSPARK_KERNEL_ASSEMBLE = 8,
+    DSPARK_KERNEL_RNN_STEP = 9       /* RNN head: the per-step state update (and its hidden-state GEMM) */
 };
 
 typedef struct {

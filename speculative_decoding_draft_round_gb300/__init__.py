@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_PKG, "libdspark.so")
 F32, BF16 = 0, 1
 SCHED_SYNC, SCHED_ASYNC_CAPACITY, SCHED_FULL_SCAN, SCHED_THRESHOLD = 0, 1, 2, 3
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
+HEAD_MARKOV, HEAD_RNN = 0, 1
 NOISE_BLOCK = 128
 MAX_GAMMA = 32
 MAX_SLOTS = 8192
@@ -43,7 +44,7 @@ class SampleArgs(C.Structure):
         ("b", C.c_float), ("temperature", _vp), ("anchor", _vp),
         ("seed", C.c_uint64), ("round", C.c_uint64),
         ("tokens", _vp), ("conf", _vp), ("surv", _vp), ("draft_lse", _vp), ("draft_logit", _vp),
-        ("sts_temp", _vp),
+        ("sts_temp", _vp), ("head", C.c_int32), ("W_rnn", _vp), ("a_rows", _vp),
     ]
 
 
@@ -68,7 +69,7 @@ class VerifyArgs(C.Structure):
         ("gamma", _vp), ("target", _vp), ("U", _vp), ("E", _vp), ("W", _vp), ("anchor", _vp), ("tokens", _vp),
         ("draft_lse", _vp), ("draft_logit", _vp), ("keep", _vp), ("temperature", _vp),
         ("seed", C.c_uint64), ("round", C.c_uint64),
-        ("accepted", _vp), ("next_token", _vp), ("resampled", _vp),
+        ("accepted", _vp), ("next_token", _vp), ("resampled", _vp), ("a_rows", _vp),
     ]
 
 
@@ -87,7 +88,7 @@ EXPORTS = ("dspark_sample_workspace_size", "dspark_sample_block", "dspark_schedu
            "dspark_assemble_workspace_size", "dspark_assemble")
 
 KERNELS = {"conf_hidden": 0, "draft_stats": 1, "draft_commit": 2, "schedule": 3, "verify_rows": 4,
-           "verify_decide": 5, "residual_stats": 6, "residual_pick": 7, "assemble": 8}
+           "verify_decide": 5, "residual_stats": 6, "residual_pick": 7, "assemble": 8, "rnn_step": 9}
 
 
 class EventPair(C.Structure):
@@ -253,7 +254,8 @@ def check(workspace, stream=None) -> int:
 # ----------------------------------------------------------------- calls
 
 def sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamma=None, conf_token=0,
-                bias_first=1, path=PATH_AUTO, out=None, sts_temp=None):
+                bias_first=1, path=PATH_AUTO, out=None, sts_temp=None, head=HEAD_MARKOV, W_rnn=None,
+                a_rows=False):
     R, G, V = U.shape
     r = E.shape[1]
     d = h.shape[2]
@@ -268,11 +270,15 @@ def sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamm
     _dev(anchor, "anchor", torch.int32, (R,))
     _dev(gamma, "gamma", torch.int32, (R,))
     _dev(sts_temp, "sts_temp", torch.float32, (G,))
+    if head == HEAD_RNN:
+        _dev(W_rnn, "W_rnn", dt, (3 * r, 2 * r + d))
     dev = U.device
     if out is None:
         out = {"tokens": torch.empty((R, G), dtype=torch.int32, device=dev)}
         for k in ("conf", "surv", "draft_lse", "draft_logit"):
             out[k] = torch.empty((R, G), dtype=torch.float32, device=dev)
+        if a_rows:
+            out["a_rows"] = torch.empty((R, G, r), dtype=torch.float32, device=dev)
     a = SampleArgs()
     a.struct_size = C.sizeof(SampleArgs)
     a.R, a.gamma_max, a.V, a.r, a.d = R, G, V, r, d
@@ -285,14 +291,20 @@ def sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamm
     a.tokens, a.conf, a.surv = _ptr(out["tokens"]), _ptr(out["conf"]), _ptr(out["surv"])
     a.draft_lse, a.draft_logit = _ptr(out["draft_lse"]), _ptr(out["draft_logit"])
     a.sts_temp = _ptr(sts_temp)
+    a.head = int(head)
+    a.W_rnn = _ptr(W_rnn if head == HEAD_RNN else None)
+    a.a_rows = _ptr(out.get("a_rows"))
     return a, out
 
 
 def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamma=None, conf_token=0,
-                 bias_first=1, path=PATH_AUTO, out=None, workspace=None, stream=None, sts_temp=None):
-    """dspark_sample_block on the current (or given) stream; returns the output tensors."""
+                 bias_first=1, path=PATH_AUTO, out=None, workspace=None, stream=None, sts_temp=None,
+                 head=HEAD_MARKOV, W_rnn=None, a_rows=False):
+    """dspark_sample_block on the current (or given) stream; returns the output tensors (with
+    a_rows=True also each step's bias operand, which dspark_verify needs for an RNN-head draft)."""
     a, out = sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, gamma=gamma,
-                         conf_token=conf_token, bias_first=bias_first, path=path, out=out, sts_temp=sts_temp)
+                         conf_token=conf_token, bias_first=bias_first, path=path, out=out, sts_temp=sts_temp,
+                         head=head, W_rnn=W_rnn, a_rows=a_rows)
     ws = _workspace("dspark_sample_workspace_size", a, workspace, U.device)
     _call("dspark_sample_block", C.byref(a), _ptr(ws), ws.numel(), _stream(stream))
     out["workspace"] = ws
@@ -303,12 +315,14 @@ STATIC_WORKSPACE_BYTES = 8 << 20
 
 
 def sample_block_static(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamma=None, conf_token=0,
-                        bias_first=1, path=PATH_AUTO, out=None, stream=None):
+                        bias_first=1, path=PATH_AUTO, out=None, stream=None, sts_temp=None, head=HEAD_MARKOV,
+                        W_rnn=None):
     """dspark_sample_block_static: the sampler with its scratch in the library's static device
     array (for callers that cannot allocate device memory). Only the output tensors are
-    allocated here, by torch, when `out` is not given."""
+    allocated here, by torch, when `out` is not given. The RNN head is refused here."""
     a, out = sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, gamma=gamma,
-                         conf_token=conf_token, bias_first=bias_first, path=path, out=out)
+                         conf_token=conf_token, bias_first=bias_first, path=path, out=out, sts_temp=sts_temp,
+                         head=head, W_rnn=W_rnn)
     _call("dspark_sample_block_static", C.byref(a), _stream(stream))
     return out
 
@@ -383,7 +397,7 @@ def decode_stats(stats_bytes) -> dict:
 
 
 def verify_args(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temperature, seed, rnd, *,
-                gamma=None, bias_first=1, path=PATH_AUTO, out=None):
+                gamma=None, bias_first=1, path=PATH_AUTO, out=None, a_rows=None):
     R, G, V = U.shape
     r = E.shape[1]
     dt = U.dtype
@@ -398,6 +412,7 @@ def verify_args(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, t
     _dev(keep, "keep", torch.int32, (R,))
     _dev(temperature, "temperature", torch.float32, (R,))
     _dev(gamma, "gamma", torch.int32, (R,))
+    _dev(a_rows, "a_rows", torch.float32, (R, G, r))
     dev = U.device
     if out is None:
         out = {"accepted": torch.empty(R, dtype=torch.int32, device=dev),
@@ -412,14 +427,16 @@ def verify_args(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, t
     a.keep, a.temperature = _ptr(keep), _ptr(temperature)
     a.seed, a.round = int(seed), int(rnd)
     a.accepted, a.next_token, a.resampled = _ptr(out["accepted"]), _ptr(out["next_token"]), _ptr(out["resampled"])
+    a.a_rows = _ptr(a_rows)
     return a, out
 
 
 def verify(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temperature, seed, rnd, *,
-           gamma=None, bias_first=1, path=PATH_AUTO, out=None, workspace=None, stream=None):
-    """dspark_verify; returns accepted lengths, next tokens and residual flags."""
+           gamma=None, bias_first=1, path=PATH_AUTO, out=None, workspace=None, stream=None, a_rows=None):
+    """dspark_verify; returns accepted lengths, next tokens and residual flags (a_rows: the
+    sampler's bias operands, needed for an RNN-head draft)."""
     a, out = verify_args(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temperature, seed, rnd,
-                         gamma=gamma, bias_first=bias_first, path=path, out=out)
+                         gamma=gamma, bias_first=bias_first, path=path, out=out, a_rows=a_rows)
     ws = _workspace("dspark_verify_workspace_size", a, workspace, U.device)
     _call("dspark_verify", C.byref(a), _ptr(ws), ws.numel(), _stream(stream))
     out["workspace"] = ws

@@ -30,8 +30,8 @@ const char* kernel_name(int kernel)
 {
     static const char* names[] = {"conf_hidden", "draft_stats", "draft_commit", "schedule",
                                   "verify_rows", "verify_decide", "residual_stats", "residual_pick",
-                                  "assemble"};
-    return kernel >= 0 && kernel <= DSPARK_KERNEL_ASSEMBLE ? names[kernel] : "?";
+                                  "assemble", "rnn_step"};
+    return kernel >= 0 && kernel <= DSPARK_KERNEL_RNN_STEP ? names[kernel] : "?";
 }
 
 thread_local char g_last_error[256] = "no error";
@@ -68,7 +68,7 @@ dspark_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK :
 // ------------------------------------------------------------ sample_block
 
 struct SampleLayout {
-    size_t x_cur, hw, stats, pick, a_next, total;
+    size_t x_cur, hw, stats, pick, a_next, yh, state, a_rows, a_lo, total;
 };
 
 dspark_status check_sample(const dspark_sample_args* a)
@@ -78,6 +78,8 @@ dspark_status check_sample(const dspark_sample_args* a)
     if (a->V < 1 || a->V > (1 << 24) || a->r < 1 || a->r > 1024 || a->d < 1) return DSPARK_ERR_INVALID_ARGUMENT;
     if (a->dtype != DSPARK_F32 && a->dtype != DSPARK_BF16) return DSPARK_ERR_INVALID_ARGUMENT;
     if ((a->conf_token | 1) != 1 || (a->bias_first | 1) != 1) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->head != DSPARK_HEAD_MARKOV && a->head != DSPARK_HEAD_RNN) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (a->head == DSPARK_HEAD_RNN && !a->W_rnn) return DSPARK_ERR_INVALID_ARGUMENT;
     if (a->path < DSPARK_PATH_AUTO || a->path > DSPARK_PATH_TENSOR_CORE) return DSPARK_ERR_INVALID_ARGUMENT;
     if (a->round >= (1ull << 29)) return DSPARK_ERR_INVALID_ARGUMENT;
     if ((long long)a->R * a->gamma_max * a->V >= (1ll << 40)) return DSPARK_ERR_UNSUPPORTED_SHAPE;
@@ -110,6 +112,15 @@ SampleLayout sample_layout(const dspark_sample_args* a)
     L.a_next = o;   // the tensor-core path keeps kAReplicas copies of the next step's A rows
     o = align_up(o + (sample_uses_tc(a) ? kAReplicas : 1) * (a->dtype == DSPARK_BF16 ? 2 : 4) * (size_t)a->R * a->r,
                  kAlign);
+    const bool rnn = a->head == DSPARK_HEAD_RNN;
+    L.yh = o;   // RNN head: the h part of the projection, every position
+    o = align_up(o + (rnn ? sizeof(float) * (size_t)a->R * a->gamma_max * 3 * a->r : 0), kAlign);
+    L.state = o;
+    o = align_up(o + (rnn ? sizeof(float) * 2 * (size_t)a->R * a->r : 0), kAlign);
+    L.a_rows = o;   // used when the caller does not take the bias operands
+    o = align_up(o + (rnn && !a->a_rows ? sizeof(float) * (size_t)a->R * a->gamma_max * a->r : 0), kAlign);
+    L.a_lo = o;
+    o = align_up(o + (rnn ? 2 * (size_t)a->R * a->r : 0), kAlign);
     L.total = o;
     return L;
 }
@@ -140,6 +151,7 @@ dspark_status check_verify(const dspark_verify_args* a)
 bool verify_uses_tc(const dspark_verify_args* a)
 {
     if (a->path == DSPARK_PATH_CUDA_CORE) return false;
+    if (a->a_rows) return false;   // fp32 bias operands (RNN head): the CUDA-core residual keeps them exact
     return tc_residual_supported(a->dtype, a->R, a->V, a->r, a->U, a->E, a->W);
 }
 
@@ -265,11 +277,27 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.a_next = at<unsigned char>(ws, L.a_next);
     const bool tc = sample_uses_tc(a);
     p.a_replicas = tc ? kAReplicas : 1;
+    p.head = a->head;
+    p.W_rnn = a->W_rnn;
+    const bool rnn = a->head == DSPARK_HEAD_RNN;
+    p.a_rows = rnn ? (a->a_rows ? a->a_rows : at<float>(ws, L.a_rows)) : a->a_rows;
+    p.yh = rnn ? at<float>(ws, L.yh) : nullptr;
+    p.state = rnn ? at<float>(ws, L.state) : nullptr;
+    p.a_lo = rnn && tc ? at<unsigned char>(ws, L.a_lo) : nullptr;
     cudaError_t e = launch(DSPARK_KERNEL_CONF_HIDDEN, s, [&] { return launch_conf_hidden(p, s); });
+    if (rnn && e == cudaSuccess) {
+        // the h part of the RNN projection: a cuBLAS GEMM, not one of this library's kernels
+        e = launch_rnn_hidden(p, s);
+        if (e != cudaSuccess)
+            snprintf(g_last_error, sizeof g_last_error, "rnn hidden GEMM: %s (%s)", cudaGetErrorName(e),
+                     cudaGetErrorString(e));
+    }
     for (int k = 0; k < a->gamma_max && e == cudaSuccess; ++k) {
         p.k = k;
-        e = launch(DSPARK_KERNEL_DRAFT_STATS, s,
-                   [&] { return tc ? launch_draft_stats_tc(p, s) : launch_draft_stats_simt(p, s); });
+        if (rnn) e = launch(DSPARK_KERNEL_RNN_STEP, s, [&] { return launch_rnn_step(p, s); });
+        if (e == cudaSuccess)
+            e = launch(DSPARK_KERNEL_DRAFT_STATS, s,
+                       [&] { return tc ? launch_draft_stats_tc(p, s) : launch_draft_stats_simt(p, s); });
         if (e == cudaSuccess) e = launch(DSPARK_KERNEL_DRAFT_COMMIT, s, [&] { return launch_draft_commit(p, s); });
     }
     return cuda_status(e);
@@ -375,6 +403,7 @@ dspark_status dspark_verify(const dspark_verify_args* a, void* ws, size_t ws_byt
     p.anchor = a->anchor;
     p.tokens = a->tokens;
     p.draft_lse = a->draft_lse;
+    p.a_rows = a->a_rows;
     p.draft_logit = a->draft_logit;
     p.keep = a->keep;
     p.temperature = a->temperature;
@@ -408,7 +437,7 @@ dspark_status dspark_time_kernel(int32_t kernel, dspark_event_pair* events, int3
         g_timer = KernelTimer();
         return DSPARK_OK;
     }
-    if (kernel > DSPARK_KERNEL_ASSEMBLE || !events || capacity < 0 || !count) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (kernel > DSPARK_KERNEL_RNN_STEP || !events || capacity < 0 || !count) return DSPARK_ERR_INVALID_ARGUMENT;
     g_timer.kernel = kernel;
     g_timer.events = events;
     g_timer.capacity = capacity;

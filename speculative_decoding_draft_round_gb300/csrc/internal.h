@@ -42,8 +42,16 @@ struct DraftStep {
     float2* stats;       // [R_pad][nblk] (max, sum) of exp2 over each vocabulary block, log2 units
     unsigned long long* pick;   // [G][R] packed block-level arg-max of each step (cleared per call)
     void* a_next;        // [a_replicas][R][r] (element type of E): W_1 row of the token each request
-                         // conditions on next, in a_replicas identical copies
+                         // conditions on next, in a_replicas identical copies (RNN head on the tensor-core
+                         // path: the bf16 rounding of the step's bias operand)
     int a_replicas;      // 1 (CUDA-core path) or kAReplicas (tensor-core path: each CTA reads one copy)
+    // RNN head (eq. 6)
+    int head;            // DSPARK_HEAD_*
+    const void* W_rnn;   // [3r][2r+d]
+    float* a_rows;       // [R][G][r] fp32 bias operand of each step (RNN head: tanh(W_o z_k))
+    float* yh;           // [R*G][3r] W_rnn[:, 2r:] h_k for every position
+    float* state;        // [2][R][r] s_{k-1} / s_k by step parity
+    void* a_lo;          // [R][r] bf16: operand minus its bf16 rounding (tensor-core path)
 };
 
 // Verification (dspark_verify).
@@ -71,6 +79,7 @@ struct VerifyParams {
     float* lse_t;        // [R][G+1]
     int32_t* rej;        // [R] rejected position, -1 if every admitted token was accepted
     float* res_stats;    // [R_pad][nblk] block sums of max(0, p_t - p_d)
+    const float* a_rows; // [R][G][r] bias operands reported by the sampler, or NULL (W_1[x_{n-1}])
 };
 
 struct ScheduleParams {
@@ -122,6 +131,10 @@ cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
 
 // assemble.cu
 cudaError_t launch_assemble(const AssembleParams& p, cudaStream_t s);
+
+// rnn.cu (RNN head)
+cudaError_t launch_rnn_hidden(const DraftStep& p, cudaStream_t s);   // yh = W_rnn[:, 2r:] h for all positions
+cudaError_t launch_rnn_step(const DraftStep& p, cudaStream_t s);     // step k: state, bias operand
 
 inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

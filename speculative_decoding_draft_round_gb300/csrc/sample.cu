@@ -142,7 +142,11 @@ __global__ void __launch_bounds__(kNoiseBlock) draft_stats_simt_kernel(DraftStep
     const T* W = static_cast<const T*>(p.W);
     for (int i = t; i < kSimtReq * p.r; i += blockDim.x) {
         const int j = i / p.r, c = i % p.r;
-        es[i] = (req[j].active && req[j].use_bias) ? ld(E, (size_t)req[j].prev * p.r + c) : 0.f;
+        // the bias operand: W_1[x_{k-1}] (Markov head) or the RNN head's tanh(W_o z_k) row
+        const size_t ar = ((size_t)(q0 + j) * p.G + p.k) * p.r + c;
+        es[i] = (req[j].active && req[j].use_bias)
+                    ? (p.head == DSPARK_HEAD_RNN ? p.a_rows[ar] : ld(E, (size_t)req[j].prev * p.r + c))
+                    : 0.f;
     }
     __syncthreads();
     const int v = b * kNoiseBlock + t;
@@ -230,6 +234,8 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     pdl_wait();      // block statistics, pick slots and x_cur come from the kernels before this one
     pdl_trigger();   // the next step's statistics kernel may start its prefetch
     if (!rq.active) {
+        if (p.a_rows && p.head != DSPARK_HEAD_RNN)
+            for (int i = t; i < p.r; i += kCommitThreads) p.a_rows[o * p.r + i] = 0.f;
         if (t == 0) {
             p.tokens[o] = -1;
             p.conf[o] = p.surv[o] = p.draft_lse[o] = p.draft_logit[o] = 0.f;
@@ -256,12 +262,18 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
             ms[u] = b < p.nblk ? st[b] : make_float2(-INFINITY, 1.f);
         }
     }
-    float e_prev = 0.f;
     const bool need_prev_row = rq.use_bias || !p.conf_token;
+    const bool rnn = p.head == DSPARK_HEAD_RNN;
+    // RNN head: the bias operand is the step's tanh(W_o z_k); W_1[x_{k-1}] feeds eq. (7) only
+    const int prevtok = rnn ? checked_index(p.k == 0 ? p.anchor[q] : p.x_cur[q], p.V, p.status) : 0;
     for (int i = t; i < p.r; i += kCommitThreads) {
-        const float ev = need_prev_row ? ld(prev_row, i) : 0.f;
-        if (i == t) e_prev = ev;
+        float ev;
+        if (rnn)
+            ev = rq.use_bias ? p.a_rows[o * p.r + i] : 0.f;
+        else
+            ev = need_prev_row ? ld(prev_row, i) : 0.f;
         erow[i] = ev;
+        if (!rnn && p.a_rows) p.a_rows[o * p.r + i] = ld(prev_row, i);   // Markov operand W_1[x_{k-1}]
     }
     int bstar = pk == 0ull ? -1 : unpack_pick_index(pk);
     if (bstar < 0 || bstar >= p.nblk) {
@@ -354,10 +366,11 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     const size_t rep_stride = (size_t)p.R * p.r;
     for (int i = t; i < p.r; i += kCommitThreads) {
         const T et = E[(size_t)tok * p.r + i];
-        for (int rp = 0; rp < p.a_replicas; ++rp) an[rp * rep_stride + i] = et;
-        dot = fmaf(p.w_e[i], p.conf_token ? to_f32<T>(et) : erow[i], dot);   // eq. (7) reads W_1[x_{k-1}]
+        if (!rnn)   // the RNN head's next operand comes from its state update
+            for (int rp = 0; rp < p.a_replicas; ++rp) an[rp * rep_stride + i] = et;
+        const float xprev = rnn ? (p.conf_token ? 0.f : ld(E, (size_t)prevtok * p.r + i)) : erow[i];
+        dot = fmaf(p.w_e[i], p.conf_token ? to_f32<T>(et) : xprev, dot);   // eq. (7) reads W_1[x_{k-1}]
     }
-    (void)e_prev;
     dot = block_sum<kCommitThreads>(dot, red);
     if (t == 0) {
         // sequential temperature scaling of the confidence: the head's logit over t_k

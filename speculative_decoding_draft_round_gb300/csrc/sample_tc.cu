@@ -588,6 +588,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // A: box kc of the tile in shared memory, K-major; 16 K elements = 32 bytes per step
                         const uint64_t ad = sw128_desc(sbase + L::OFF_A + kc * (BM * 128) + kk * 32, 16, 1024);
                         mma_bf16_ss(d_tmem, ad, bd, (kc | kk) != 0);
+                        if (P.d.a_lo)   // RNN head: + the operand's bf16 remainder, from TMEM
+                            mma_bf16_ts(d_tmem, tmem_base + A_TMEM_COL + (uint32_t)(kc * (BK / 2) + kk * 8), bd, 1u);
                     } else {
                         const uint32_t a_tmem = tmem_base + A_TMEM_COL + (uint32_t)(kc * (BK / 2) + kk * 8);
                         mma_bf16_ts(d_tmem, a_tmem, bd, (kc | kk) != 0);
@@ -634,6 +636,34 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 epi_barrier();
                 if (MODE == kDraftMode) {
+                    // RNN head: the bf16 remainder of the operand rows goes to TMEM (the second A
+                    // operand), warpgroup g covering K elements [64g, 64g + 64) of its lanes' rows
+                    if (P.d.a_lo) {
+                        if (live && g * BK < P.r) {
+                            uint32_t a[32];
+                            const int q = mt * BM + m;
+                            if (q < P.R) {
+                                const uint4* src = reinterpret_cast<const uint4*>(
+                                    static_cast<const __nv_bfloat16*>(P.d.a_lo) + (size_t)q * P.r + g * BK);
+                                uint4 c8[8];
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) c8[c] = src[c];
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    a[4 * c] = c8[c].x;
+                                    a[4 * c + 1] = c8[c].y;
+                                    a[4 * c + 2] = c8[c].z;
+                                    a[4 * c + 3] = c8[c].w;
+                                }
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < 32; ++c) a[c] = 0u;
+                            }
+                            tmem_st32(tmem_base + ((uint32_t)(q4 * 32) << 16) + A_TMEM_COL + (uint32_t)(g * 32), a);
+                            tc_fence_before();
+                        }
+                        epi_barrier();
+                    }
                     // A = the tile's rows of a_next (W_1 of the previous tokens, written by the
                     // previous kernel) from this CTA's replica, one TMA tile per 64 columns
                     if (e == 0 && live) {

@@ -328,7 +328,11 @@ __global__ void __launch_bounds__(kNoiseBlock) residual_stats_simt_kernel(Verify
     const T* W = static_cast<const T*>(p.W);
     for (int i = t; i < kResReq * p.r; i += blockDim.x) {
         const int j = i / p.r, c = i % p.r;
-        es[i] = (req[j].active && req[j].use_bias) ? ld(E, (size_t)req[j].prev * p.r + c) : 0.f;
+        // the bias operand of the rejected position: the sampler's reported row, else W_1[x_{n-1}]
+        es[i] = (req[j].active && req[j].use_bias)
+                    ? (p.a_rows ? p.a_rows[((size_t)(q0 + j) * p.G + req[j].n) * p.r + c]
+                                : ld(E, (size_t)req[j].prev * p.r + c))
+                    : 0.f;
     }
     __syncthreads();
     const int v = b * kNoiseBlock + t;
@@ -382,7 +386,9 @@ __global__ void __launch_bounds__(kPickThreads) residual_pick_kernel(VerifyParam
     const float2* st = p.row_stats + ((size_t)q * (p.G + 1) + rq.n) * p.nblk;
     const T* E = static_cast<const T*>(p.E);
     const T* W = static_cast<const T*>(p.W);
-    for (int i = t; i < p.r; i += kPickThreads) erow[i] = rq.use_bias ? ld(E, (size_t)rq.prev * p.r + i) : 0.f;
+    for (int i = t; i < p.r; i += kPickThreads)
+        erow[i] = rq.use_bias ? (p.a_rows ? p.a_rows[((size_t)q * p.G + rq.n) * p.r + i] : ld(E, (size_t)rq.prev * p.r + i))
+                              : 0.f;
     // residual mass anywhere?
     float tot = 0.f;
     for (int b = t; b < p.nblk; b += kPickThreads) tot += rs[b];

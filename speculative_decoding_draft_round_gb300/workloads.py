@@ -217,3 +217,12 @@ def config5(device="cpu") -> Round:
 
 
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+
+
+def rnn_weights(rnd: Round, seed: int = 99) -> torch.Tensor:
+    """Seeded weights W_rnn [3r][2r+d] (rows W_g, W_c, W_o) for the RNN head, N(0, 1/sqrt(2r+d)) so
+    that the projections of z = [s; W_1[x]; h] are of order one; the element type of the round."""
+    g = _gen(seed, rnd.U.device)
+    Z = 2 * rnd.r + rnd.d
+    w = _normal((3 * rnd.r, Z), 1.0 / math.sqrt(Z), g, rnd.U.device)
+    return w.to(rnd.U.dtype)

@@ -24,6 +24,7 @@ ACC_TOL = 1e-4      # accept-test margin below which a decision is excused
 THETA_TOL = 1e-12   # relative Theta margin below which a scheduler decision is excused
 CONF_TOL = 1e-5     # c_k and a_k, absolute
 LSE_TOL = 1e-5      # log-normalisers and logits, relative to max(1, |value|)
+ROW_TOL = 1e-5      # bias operand rows (W_1 rows, or tanh outputs of the RNN head), absolute
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
@@ -38,7 +39,7 @@ def rows(t: torch.Tensor, ids) -> np.ndarray:
     return to_np(t.index_select(0, idx))
 
 
-def check_sample(rnd, out, ids, threads=8, sts_temp=None):
+def check_sample(rnd, out, ids, threads=8, sts_temp=None, head=0, W_rnn=None):
     """Compare dspark_sample_block outputs with the oracle on requests `ids` (sts_temp: the
     per-position confidence temperatures the call was given, if any)."""
     ids = np.asarray(ids)
@@ -49,7 +50,10 @@ def check_sample(rnd, out, ids, threads=8, sts_temp=None):
                             rnd.seed, rnd.round, gamma=gamma, req_ids=ids, conf_token=rnd.conf_token,
                             bias_first=rnd.bias_first, forced_tokens=np.where(tok < 0, 0, tok),
                             sts_temp=None if sts_temp is None else to_np(sts_temp).astype(np.float64),
-                            threads=threads)
+                            head=head, W_rnn=None if W_rnn is None else to_np(W_rnn), threads=threads)
+    if "a_rows" in out:   # the bias operand of each step
+        g_rows = to_np(out["a_rows"])[ids].astype(np.float64)
+        np.testing.assert_allclose(g_rows, o["a_rows"], rtol=0, atol=ROW_TOL)
     G = rnd.gamma_max
     g = np.full(len(ids), G) if gamma is None else gamma
     active = np.arange(G)[None, :] < g[:, None]
@@ -90,7 +94,7 @@ def check_schedule(surv, sps, mode, out, *, gamma=None, surv_capacity=None):
     return 0
 
 
-def check_verify(rnd, sout, keep, vout, ids, threads=8):
+def check_verify(rnd, sout, keep, vout, ids, threads=8, a_rows=None):
     """Compare dspark_verify with the oracle on requests `ids`, fed the GPU's draft outputs."""
     ids = np.asarray(ids)
     gamma = None if rnd.gamma is None else to_np(rnd.gamma)[ids]
@@ -100,7 +104,8 @@ def check_verify(rnd, sout, keep, vout, ids, threads=8):
                       to_np(rnd.anchor)[ids], np.where(tok < 0, 0, tok),
                       to_np(sout["draft_lse"])[ids].astype(np.float64),
                       to_np(sout["draft_logit"])[ids].astype(np.float64), kp, to_np(rnd.temperature)[ids],
-                      rnd.seed, rnd.round, gamma=gamma, req_ids=ids, bias_first=rnd.bias_first, threads=threads)
+                      rnd.seed, rnd.round, gamma=gamma, req_ids=ids, bias_first=rnd.bias_first,
+                      a_rows=None if a_rows is None else to_np(a_rows)[ids].astype(np.float64), threads=threads)
     acc = to_np(vout["accepted"])[ids]
     nxt = to_np(vout["next_token"])[ids]
     res = to_np(vout["resampled"])[ids]

@@ -1,6 +1,7 @@
 """GPU parity of the widening calls through the C ABI against the CPU oracle: the flattened
-verify batch (dspark_assemble), the static confidence-threshold admission (scheduler mode 3)
-and sequential temperature scaling of the confidences (dspark_sample_block's sts_temp)."""
+verify batch (dspark_assemble), the static confidence-threshold admission (scheduler mode 3),
+sequential temperature scaling of the confidences (dspark_sample_block's sts_temp) and the RNN
+sequential head (head = HEAD_RNN, with the verifier rebuilding rejected positions from a_rows)."""
 import numpy as np
 import pytest
 import torch
@@ -202,3 +203,61 @@ def test_greedy_verify_matches_oracle(spec):
     np.testing.assert_array_equal(to_np(v["accepted"])[g], o["accepted"])
     np.testing.assert_array_equal(to_np(v["next_token"])[g], o["next_token"])
     np.testing.assert_array_equal(to_np(v["resampled"])[g], o["resampled"])
+
+
+# ------------------------------------------------------------------ RNN sequential head (eq. 6)
+
+RNN_SPECS = [
+    dict(name="rnn_f32", R=11, G=5, V=300, r=24, d=20, dtype="f32", ew_std=0.2, gamma=[5, 0, 3, 5, 1, 2, 5, 4, 5, 0, 5]),
+    dict(name="rnn_tiles_bf16", R=160, G=3, V=1000, r=64, d=96, dtype="bf16", ew_std=0.15),
+    dict(name="rnn_wide_bf16", R=37, G=4, V=2056, r=256, d=64, dtype="bf16", ew_std=0.05, gamma=[4, 2] * 18 + [3]),
+]
+
+
+def _rnn_round(spec, seed):
+    spec = dict(spec)
+    name = spec.pop("name")
+    R, G, V, r, d, dtype = (spec.pop(k) for k in ("R", "G", "V", "r", "d", "dtype"))
+    rnd = wl.make_round(name, R, G, V, r, d, dtype, seed=seed, device=DEV, sps=wl.sps_hyperbolic(R * (1 + G)),
+                        **spec)
+    rnd.round = 6
+    return rnd, wl.rnn_weights(rnd)
+
+
+@pytest.mark.parametrize("spec", RNN_SPECS, ids=[s["name"] for s in RNN_SPECS])
+def test_rnn_head_matches_oracle(spec):
+    from parity import check_verify
+    rnd, W_rnn = _rnn_round(spec, 41)
+    paths = [ds.PATH_CUDA_CORE] + ([ds.PATH_TENSOR_CORE] if rnd.dtype == "bf16" else [])
+    for path in paths:
+        out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                              rnd.seed, rnd.round, gamma=rnd.gamma, path=path, head=ds.HEAD_RNN, W_rnn=W_rnn,
+                              a_rows=True)
+        torch.cuda.synchronize()
+        assert ds.check(out["workspace"]) == 0
+        check_sample(rnd, out, np.arange(rnd.R), head=ds.HEAD_RNN, W_rnn=W_rnn)
+        # verification rebuilds a rejected position's draft with the reported operands
+        g = np.full(rnd.R, rnd.gamma_max) if rnd.gamma is None else to_np(rnd.gamma)
+        keep = _i32(g)
+        v = ds.verify(rnd.target, rnd.U, rnd.E, rnd.W, rnd.anchor, out["tokens"].clamp(min=0), out["draft_lse"],
+                      out["draft_logit"], keep, rnd.temperature, rnd.seed, rnd.round, gamma=rnd.gamma,
+                      a_rows=out["a_rows"])
+        torch.cuda.synchronize()
+        assert ds.check(v["workspace"]) == 0
+        check_verify(rnd, out, keep, v, np.arange(rnd.R), a_rows=out["a_rows"])
+
+
+def test_markov_head_reports_its_operand_rows():
+    rnd, _ = _rnn_round(RNN_SPECS[1], 42)
+    out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                          rnd.seed, rnd.round, gamma=rnd.gamma, a_rows=True)
+    torch.cuda.synchronize()
+    check_sample(rnd, out, np.arange(rnd.R))   # compares a_rows with W_1[x_{k-1}]
+
+
+def test_static_entry_refuses_the_rnn_head():
+    rnd, W_rnn = _rnn_round(RNN_SPECS[0], 43)
+    with pytest.raises(ds.DsparkError) as err:
+        ds.sample_block_static(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                               rnd.seed, rnd.round, gamma=rnd.gamma, head=ds.HEAD_RNN, W_rnn=W_rnn)
+    assert err.value.code == 2
