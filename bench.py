@@ -264,17 +264,33 @@ def bench_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def time_next_rows(ds, rnd, res, n=20):
-    """Kernel times of the calls beyond the headline round, on this round's outputs: the flat
-    verify batch, the static-threshold admission, and the sampler with per-position confidence
-    temperatures (its extra work is one division per confidence, inside the commit kernel)."""
-    def per_launch(family, fn):
-        timer = ds.KernelTimer(family, n)
+def time_next_rows(ds, rnd, res, flush, n=20):
+    """Times of the calls beyond the headline round, on this round's inputs and outputs: the
+    flat verify batch and the static-threshold admission (median of isolated launches), and the
+    sampler call in its variants -- the Markov head as in the headline, the RNN sequential head,
+    greedy decoding at temperature 0 and per-position confidence temperatures -- each a whole
+    dspark_sample_block call between CUDA events with L2 flushed before it, plus the median
+    launch of the per-step kernels the variant changes."""
+    from speculative_decoding_draft_round_gb300 import workloads as wl
+
+    def per_launch(family, fn, reps=n):
+        timer = ds.KernelTimer(family, reps * max(1, rnd.gamma_max))
         with timer:
-            for _ in range(n):
+            for _ in range(reps):
                 fn()
         d = timer.durations_ms()
         return round(1e3 * float(np.median(d)), 2) if d else None
+
+    def call_us(fn, reps=5):
+        fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return round(1e3 * float(np.median([a.elapsed_time(b) for a, b in ev])), 1)
 
     tokens = torch.where(res["tokens"] < 0, torch.zeros_like(res["tokens"]), res["tokens"])
     a_out = ds.assemble(res["keep"], rnd.anchor, tokens)
@@ -283,9 +299,36 @@ def time_next_rows(ds, rnd, res, n=20):
                                                      workspace=a_out["workspace"]))
     thr = per_launch("schedule", lambda: ds.schedule(res["surv"], rnd.sps, ds.SCHED_THRESHOLD, gamma=rnd.gamma,
                                                     threshold=0.5, out=s_out, workspace=s_out["workspace"]))
+    rows = {"assemble_us": flat, "threshold_schedule_us": thr,
+            "flat_tokens": int(res["keep"].sum().item()) + rnd.R}
+
+    base = (rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b)
+    variants = {
+        "markov": dict(temperature=rnd.temperature),
+        "rnn": dict(temperature=rnd.temperature, head=ds.HEAD_RNN, W_rnn=wl.rnn_weights(rnd)),
+        "greedy": dict(temperature=torch.zeros_like(rnd.temperature)),
+        "sts": dict(temperature=rnd.temperature,
+                    sts_temp=torch.linspace(0.8, 1.6, rnd.gamma_max, device=rnd.U.device)),
+    }
+    for name, kw in variants.items():
+        temp = kw.pop("temperature")
+        out = ds.sample_block(*base, temp, rnd.anchor, rnd.seed, 7, gamma=rnd.gamma, **kw)
+        ws = out.pop("workspace")
+        fn = lambda: ds.sample_block(*base, temp, rnd.anchor, rnd.seed, 7, gamma=rnd.gamma, out=out, workspace=ws,
+                                     **kw)
+        row = {"sampler_us": call_us(fn), "draft_stats_us": per_launch("draft_stats", fn, reps=2),
+               "draft_commit_us": per_launch("draft_commit", fn, reps=2)}
+        if name == "rnn":
+            row["rnn_step_us"] = per_launch("rnn_step", fn, reps=2)
+            row["W_rnn"] = [3 * rnd.r, 2 * rnd.r + rnd.d]
+        status = ds.check(ws)
+        if status:
+            raise RuntimeError("device status %d in the %s sampler" % (status, name))
+        rows["sampler_" + name] = row
     torch.cuda.synchronize()
-    return {"assemble_us": flat, "threshold_schedule_us": thr,
-            "flat_tokens": int(res["keep"].sum().item()) + rnd.R, "note": "median of %d isolated launches" % n}
+    rows["note"] = ("kernel times: medians of isolated launches under per-kernel events; sampler_us: median of "
+                    "5 whole calls, L2 flushed before each")
+    return rows
 
 
 def bench_ours(args):
@@ -391,7 +434,7 @@ def bench_ours(args):
         e_stops[s].record(stream)
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_starts, e_stops))
-    next_rows = time_next_rows(ds, rnd, res)
+    next_rows = time_next_rows(ds, rnd, res, flush)
     clock = clocks.stop()
 
     drafted = rnd.draft_tokens()

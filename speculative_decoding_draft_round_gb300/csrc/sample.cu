@@ -212,7 +212,7 @@ __device__ __forceinline__ LseAcc lse_merge(LseAcc a, LseAcc b)
 constexpr int kStatsPerThread = 8;       // block statistics held in registers per thread (nblk <= 2048)
 constexpr int kBiasRows = 16;            // W rows per thread in the fast path (r <= 256)
 
-template <typename T>
+template <typename T, bool RNN>
 __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep p)
 {
     extern __shared__ float sm_dyn[];   // [r] W_1[prev], then [16][128] K-slice partials
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     pdl_wait();      // block statistics, pick slots and x_cur come from the kernels before this one
     pdl_trigger();   // the next step's statistics kernel may start its prefetch
     if (!rq.active) {
-        if (p.a_rows && p.head != DSPARK_HEAD_RNN)
+        if (p.a_rows && !RNN)
             for (int i = t; i < p.r; i += kCommitThreads) p.a_rows[o * p.r + i] = 0.f;
         if (t == 0) {
             p.tokens[o] = -1;
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
         }
     }
     const bool need_prev_row = rq.use_bias || !p.conf_token;
-    const bool rnn = p.head == DSPARK_HEAD_RNN;
+    constexpr bool rnn = RNN;
     // RNN head: the bias operand is the step's tanh(W_o z_k); W_1[x_{k-1}] feeds eq. (7) only
     const int prevtok = rnn ? checked_index(p.k == 0 ? p.anchor[q] : p.x_cur[q], p.V, p.status) : 0;
     for (int i = t; i < p.r; i += kCommitThreads) {
@@ -427,8 +427,13 @@ cudaError_t launch_draft_commit(const DraftStep& p, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.dtype == DSPARK_BF16) return cudaLaunchKernelEx(&cfg, draft_commit_kernel<__nv_bfloat16>, p);
-    return cudaLaunchKernelEx(&cfg, draft_commit_kernel<float>, p);
+    // the RNN head takes its own instance: the Markov head's commit carries none of its branches
+    const bool rnn = p.head == DSPARK_HEAD_RNN;
+    if (p.dtype == DSPARK_BF16)
+        return rnn ? cudaLaunchKernelEx(&cfg, draft_commit_kernel<__nv_bfloat16, true>, p)
+                   : cudaLaunchKernelEx(&cfg, draft_commit_kernel<__nv_bfloat16, false>, p);
+    return rnn ? cudaLaunchKernelEx(&cfg, draft_commit_kernel<float, true>, p)
+               : cudaLaunchKernelEx(&cfg, draft_commit_kernel<float, false>, p);
 }
 
 }  // namespace dspark

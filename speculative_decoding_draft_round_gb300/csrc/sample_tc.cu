@@ -379,7 +379,9 @@ struct Ring {
     }
 };
 
-template <int MODE>
+// SPLIT (draft mode only): the A operand is a bf16 tile plus its bf16 remainder in TMEM (the RNN
+// head's fp32 rows); a separate instance so that the Markov head's kernel carries none of it
+template <int MODE, bool SPLIT = false>
 __global__ void __launch_bounds__(THREADS, 1)
     stats_tc_kernel(const TcParams P, const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU,
                     const __grid_constant__ CUtensorMap tmA)
@@ -588,7 +590,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // A: box kc of the tile in shared memory, K-major; 16 K elements = 32 bytes per step
                         const uint64_t ad = sw128_desc(sbase + L::OFF_A + kc * (BM * 128) + kk * 32, 16, 1024);
                         mma_bf16_ss(d_tmem, ad, bd, (kc | kk) != 0);
-                        if (P.d.a_lo)   // RNN head: + the operand's bf16 remainder, from TMEM
+                        if (SPLIT)   // RNN head: + the operand's bf16 remainder, from TMEM
                             mma_bf16_ts(d_tmem, tmem_base + A_TMEM_COL + (uint32_t)(kc * (BK / 2) + kk * 8), bd, 1u);
                     } else {
                         const uint32_t a_tmem = tmem_base + A_TMEM_COL + (uint32_t)(kc * (BK / 2) + kk * 8);
@@ -638,7 +640,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (MODE == kDraftMode) {
                     // RNN head: the bf16 remainder of the operand rows goes to TMEM (the second A
                     // operand), warpgroup g covering K elements [64g, 64g + 64) of its lanes' rows
-                    if (P.d.a_lo) {
+                    if (SPLIT) {
                         if (live && g * BK < P.r) {
                             uint32_t a[32];
                             const int q = mt * BM + m;
@@ -940,7 +942,7 @@ cudaError_t encode_a(CUtensorMap* m, const void* A, int R, int r)
                : cudaErrorInvalidValue;
 }
 
-template <int MODE>
+template <int MODE, bool SPLIT = false>
 cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorMap& tmU, const CUtensorMap& tmA,
                       cudaStream_t s)
 {
@@ -948,7 +950,8 @@ cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorM
     static bool smem_set = false;
     if (!smem_set) {
         const cudaError_t e =
-            cudaFuncSetAttribute(stats_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+            cudaFuncSetAttribute(stats_tc_kernel<MODE, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         smem_set = true;
     }
@@ -964,7 +967,7 @@ cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorM
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t le = cudaLaunchKernelEx(&cfg, stats_tc_kernel<MODE>, P, tmW, tmU, tmA);
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, stats_tc_kernel<MODE, SPLIT>, P, tmW, tmU, tmA);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
@@ -989,7 +992,7 @@ cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s)
     P.nblk = p.nblk;
     P.k = p.k;
     P.status = p.status;
-    return launch_tc<kDraftMode>(P, tmW, tmU, tmA, s);
+    return p.a_lo ? launch_tc<kDraftMode, true>(P, tmW, tmU, tmA, s) : launch_tc<kDraftMode>(P, tmW, tmU, tmA, s);
 }
 
 cudaError_t launch_residual_stats_tc(const VerifyParams& p, cudaStream_t s)
