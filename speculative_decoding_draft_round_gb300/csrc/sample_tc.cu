@@ -84,6 +84,25 @@ struct Lay {
     static_assert(OFF_A % 1024 == 0, "A tile on a 1024-byte boundary (128-byte swizzle atoms)");
 };
 
+// A CTA's items it = i0, i0 + istep, ... in block-major order (block it / nt of tile it % nt),
+// walked without a division per step; n counts the items visited
+struct ItemIter {
+    int it, tile, b, n, dq, dr, nt;
+    __device__ ItemIter(int i0, int istep, int nt_)
+        : it(i0), tile(i0 % nt_), b(i0 / nt_), n(0), dq(istep / nt_), dr(istep % nt_), nt(nt_) {}
+    __device__ void next(int istep)
+    {
+        it += istep;
+        ++n;
+        b += dq;
+        tile += dr;
+        if (tile >= nt) {
+            tile -= nt;
+            ++b;
+        }
+    }
+};
+
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;   // 4 s
 
 // instruction descriptor, kind::f16: D fp32, A = B = bf16, A K-major (shared memory in draft mode,
@@ -456,9 +475,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     pdl_trigger();
     const int nblk = P.nblk;
-    const int n_items = *s_ntiles * nblk;
-    // items are dealt round-robin: at any moment the CTAs work on adjacent vocabulary blocks, so
-    // their U and W reads fall in the same DRAM pages
+    const int nt = *s_ntiles;
+    const int n_items = nt * nblk;
+    // items are dealt round-robin in block-major order (item it = block it / nt of tile it % nt):
+    // at any moment the CTAs work on adjacent vocabulary blocks, so their U and W reads fall in the
+    // same DRAM pages, and the nt tiles of one W block are read at the same time, by nt
+    // neighbouring CTAs, so that W comes from DRAM once per step however many tiles there are.
+    // The grid is a multiple of the tile count, so a CTA keeps one tile (one A load) throughout.
     const int i0 = blockIdx.x, istep = gridDim.x;
     const int KC = P.r / BK;
 
@@ -468,8 +491,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         Ring ws;
         uint32_t last_par[W_STAGES];
         bool filled[W_STAGES] = {};
-        for (int it = i0; it < n_items && !*s_abort; it += istep) {
-            const int b = it % nblk;
+        for (ItemIter I(i0, istep, nt); I.it < n_items && !*s_abort; I.next(istep)) {
+            const int b = I.b;
             for (int kc = 0; kc < KC; ++kc) {
                 if (!mbar_wait(w_empty(ws.idx), ws.phase ^ 1u, ctl)) break;
                 const uint32_t dst = sbase + OFF_W + ws.idx * W_STAGE_BYTES;
@@ -490,8 +513,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         Ring us;
         uint32_t last_par[U_STAGES];
         bool filled[U_STAGES] = {false, false};
-        for (int it = i0; it < n_items && !*s_abort; it += istep) {
-            const int mt = s_tiles[it / nblk], b = it % nblk;
+        for (ItemIter I(i0, istep, nt); I.it < n_items && !*s_abort; I.next(istep)) {
+            const int mt = s_tiles[I.tile], b = I.b;
             if (!mbar_wait(u_empty(us.idx), us.phase ^ 1u, ctl)) break;
             const uint32_t dst = sbase + OFF_U + us.idx * U_STAGE_BYTES;
             mbar_expect_tx(u_full(us.idx), U_STAGE_BYTES);
@@ -517,8 +540,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int cur_tile = -1, cur_mt = 0, n_act = 0;
         bool act[4] = {false, false, false, false};
         uint32_t urow[4] = {0, 0, 0, 0};   // U row index q * G + n; the target row is urow + q
-        for (int it = i0; it < n_items && !*s_abort; it += istep) {
-            const int tile = it / nblk, b = it % nblk;
+        for (ItemIter I(i0, istep, nt); I.it < n_items && !*s_abort; I.next(istep)) {
+            const int tile = I.tile, b = I.b;
             if (tile != cur_tile) {
                 const int mt = s_tiles[tile];
                 int cnt = 0;
@@ -563,8 +586,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         Ring ws, tb;
         uint32_t a_par = 0;
         int cur_tile = -1;
-        for (int it = i0; it < n_items; it += istep) {
-            const int tile = it / nblk;
+        for (ItemIter I(i0, istep, nt); I.it < n_items; I.next(istep)) {
+            const int tile = I.tile;
             if (tile != cur_tile) {
                 if (cur_tile >= 0) mma_commit(a_empty);   // old A is free once its MMAs retire
                 if (!mbar_wait(a_full, a_par, ctl)) break;
@@ -623,8 +646,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int cur_tile = -1;
         RowMeta rm{};
         bool live = true;
-        for (int it = i0; it < n_items; it += istep) {
-            const int tile = it / nblk, b = it % nblk;
+        for (ItemIter I(i0, istep, nt); I.it < n_items; I.next(istep)) {
+            const int tile = I.tile, b = I.b;
             const int mt = s_tiles[tile];
             if (tile != cur_tile) {
                 if (cur_tile >= 0) {
@@ -810,7 +833,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 partial = make_float2(rs, 0.f);
             }
-            float2* pp = part + (((it - i0) / istep) & 1) * 4 * BM;
+            float2* pp = part + (I.n & 1) * 4 * BM;
             pp[g * BM + m] = partial;
             epi_barrier();
             if (g == 0 && rm.active && live) {
@@ -955,8 +978,11 @@ cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorM
         if (e != cudaSuccess) return e;
         smem_set = true;
     }
-    const int items = ((P.R + BM - 1) / BM) * P.nblk;
-    const int grid = items < num_sms() ? items : num_sms();
+    // a multiple of the tile count (when every tile takes part, each CTA keeps one tile)
+    const int n_mt = (P.R + BM - 1) / BM, items = n_mt * P.nblk;
+    int grid = num_sms();
+    if (n_mt <= grid) grid -= grid % n_mt;
+    if (items < grid) grid = items;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(THREADS);
