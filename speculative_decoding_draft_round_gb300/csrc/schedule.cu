@@ -38,9 +38,14 @@ struct ThetaKey {
 constexpr int kDigits = 256;
 constexpr int kHist = kDigits * kSchedWarps;                  // [digit][warp] counts
 
+// Position x of a key array lives at sk(x) = x + x / 32: a thread's run of 2, 4 or 8 consecutive
+// positions and a warp's 32 consecutive positions both fall in distinct banks.
+__device__ __forceinline__ int sk(int x) { return x + (x >> 5); }
+constexpr int kSkewed = DSPARK_MAX_SLOTS + DSPARK_MAX_SLOTS / 32;
+
 struct SchedSmem {
-    uint32_t key[2][DSPARK_MAX_SLOTS];
-    uint16_t val[2][DSPARK_MAX_SLOTS];
+    uint32_t key[2][kSkewed];
+    uint16_t val[2][kSkewed];
     uint32_t hist[kHist];                   // digit counts, then offsets; reused for keep counts
     uint32_t wpart[kSchedWarps];
     unsigned long long wsum[kSchedWarps];
@@ -100,8 +105,8 @@ __device__ int load_pool(SchedSmem& sm, const ScheduleParams& p, const float* sr
                 ++cnt;
             }
         }
-        sm.key[0][s] = key;
-        sm.val[0][s] = (uint16_t)s;
+        sm.key[0][sk(s)] = key;
+        sm.val[0][sk(s)] = (uint16_t)s;
     }
     cnt = __reduce_add_sync(0xffffffffu, cnt);
     __syncthreads();
@@ -162,8 +167,8 @@ __device__ void radix_pass(SchedSmem& sm, int in, int shift, int ni)
     for (int it = 0; it < kMaxItems; ++it) {
         if (it >= ni) break;
         const int idx = striped(warp, it, lane, ni);
-        key[it] = sm.key[in][idx];
-        val[it] = sm.val[in][idx];
+        key[it] = sm.key[in][sk(idx)];
+        val[it] = sm.val[in][sk(idx)];
     }
 #pragma unroll
     for (int it = 0; it < kMaxItems; ++it) {
@@ -185,19 +190,110 @@ __device__ void radix_pass(SchedSmem& sm, int in, int shift, int ni)
     for (int it = 0; it < kMaxItems; ++it) {
         if (it >= ni) break;
         const uint32_t pos = sm.hist[dig[it] * kSchedWarps + warp] + rank[it];
-        sm.key[out][pos] = key[it];
-        sm.val[out][pos] = val[it];
+        sm.key[out][sk(pos)] = key[it];
+        sm.val[out][sk(pos)] = val[it];
     }
     __syncthreads();
 }
 
-// Sort key[0]/val[0] ascending (a descending); result in buffer 0.
-__device__ void sort_pool(SchedSmem& sm, int ni)
+// (key, slot) order: the sort order of the pool (a descending, then slot ascending)
+__device__ __forceinline__ bool kv_less(uint32_t ka, uint16_t va, uint32_t kb, uint16_t vb)
 {
-    radix_pass(sm, 0, 0, ni);
-    radix_pass(sm, 1, 8, ni);
-    radix_pass(sm, 0, 16, ni);
-    radix_pass(sm, 1, 24, ni);
+    return ka < kb || (ka == kb && va < vb);
+}
+
+// One level of a merge sort: the sorted runs [2pL, 2pL + L) and [2pL + L, 2pL + 2L) of buffer `in`
+// (clipped to n) merge into [2pL, 2pL + 2L) of buffer 1 - in. Thread t writes outputs
+// t*ni .. t*ni + ni - 1; it finds where its first output of each pair starts on the merge path by
+// a binary search, then merges element by element with the two candidates held in registers.
+__device__ void merge_level(SchedSmem& sm, int in, int n, int L, int ni)
+{
+    const uint32_t* ka = sm.key[in];
+    const uint16_t* va = sm.val[in];
+    uint32_t* ko = sm.key[1 - in];
+    uint16_t* vo = sm.val[1 - in];
+    const int o0 = threadIdx.x * ni, o1 = min(o0 + ni, n);
+    if (o0 >= o1) return;
+    int p0 = o0 / (2 * L) * (2 * L);
+    int a = 0, a_end = 0, b = 0, b_end = 0;
+    uint32_t kA = 0, kB = 0;
+    uint16_t vA = 0, vB = 0;
+    for (int o = o0; o < o1; ++o) {
+        if (o == p0 + 2 * L) p0 = o;   // the chunk runs into the next pair
+        if (o == o0 || o == p0) {      // locate on the merge path of this pair
+            const int a0 = p0, a1 = min(p0 + L, n), b0 = a1, b1 = min(p0 + 2 * L, n);
+            const int na = a1 - a0, nb = b1 - b0, k = o - p0;
+            int lo = max(0, k - nb), hi = min(k, na);
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                const int ai = sk(a0 + mid), bj = sk(b0 + k - mid - 1);
+                if (kv_less(ka[ai], va[ai], ka[bj], va[bj]))
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+            a = a0 + lo;
+            a_end = a1;
+            b = b0 + k - lo;
+            b_end = b1;
+            if (a < a_end) {
+                kA = ka[sk(a)];
+                vA = va[sk(a)];
+            }
+            if (b < b_end) {
+                kB = ka[sk(b)];
+                vB = va[sk(b)];
+            }
+        }
+        const bool take_a = b >= b_end || (a < a_end && kv_less(kA, vA, kB, vB));
+        const int w = sk(o);
+        if (take_a) {
+            ko[w] = kA;
+            vo[w] = vA;
+            if (++a < a_end) {
+                kA = ka[sk(a)];
+                vA = va[sk(a)];
+            }
+        } else {
+            ko[w] = kB;
+            vo[w] = vB;
+            if (++b < b_end) {
+                kB = ka[sk(b)];
+                vB = va[sk(b)];
+            }
+        }
+    }
+}
+
+// Sort key[0]/val[0] ascending (a descending, then slot); result in buffer 0. When every
+// request's G slots are already in order -- the sampler's survivals are running products of
+// confidences below one, so they never increase along a request -- the R runs are merged
+// pairwise (log2 R levels); any other input takes the stable LSD radix sort.
+__device__ void sort_pool(SchedSmem& sm, int n, int G, int ni)
+{
+    bool unsorted = false;
+    for (int s = threadIdx.x; s < n; s += kSchedThreads)
+        if (s % G != G - 1 && s + 1 < n && sm.key[0][sk(s + 1)] < sm.key[0][sk(s)]) unsorted = true;
+    if (__syncthreads_or(unsorted)) {
+        radix_pass(sm, 0, 0, ni);
+        radix_pass(sm, 1, 8, ni);
+        radix_pass(sm, 0, 16, ni);
+        radix_pass(sm, 1, 24, ni);
+        return;
+    }
+    int in = 0;
+    for (int L = G; L < n; L *= 2) {
+        merge_level(sm, in, n, L, ni);
+        __syncthreads();
+        in = 1 - in;
+    }
+    if (in == 1) {
+        for (int s = threadIdx.x; s < n; s += kSchedThreads) {
+            sm.key[0][sk(s)] = sm.key[1][sk(s)];
+            sm.val[0][sk(s)] = sm.val[1][sk(s)];
+        }
+        __syncthreads();
+    }
 }
 
 // a * 2^48 rounded to nearest (ties to even), a in (0, 1] from its word, with integer operations
@@ -256,7 +352,7 @@ __device__ void prefix_sums(SchedSmem& sm, int n, int ni, unsigned long long (&S
 #pragma unroll
     for (int it = 0; it < kMaxItems; ++it) {
         const int i = tid * ni + it;
-        run += (it < ni && i < n) ? fixed48(sm.key[0][i]) : 0ull;
+        run += (it < ni && i < n) ? fixed48(sm.key[0][sk(i)]) : 0ull;
         S[it] = run;
     }
     unsigned long long inc = run;
@@ -434,12 +530,12 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedulePara
     int capacity = -1;
     if (p.mode == DSPARK_SCHED_ASYNC_CAPACITY) {
         const int n_old = load_pool(sm, p, p.surv_capacity, n_slots, ni);
-        sort_pool(sm, ni);
+        sort_pool(sm, n_slots, p.G, ni);
         prefix_sums(sm, n_old, ni, S, excl);
         capacity = full_scan(sm, p, n_old, ni, S);
     }
     const int n = load_pool(sm, p, p.surv, n_slots, ni);
-    sort_pool(sm, ni);
+    sort_pool(sm, n_slots, p.G, ni);
     prefix_sums(sm, n, ni, S, excl);
     int m_star;
     if (p.mode == DSPARK_SCHED_SYNC)
@@ -455,7 +551,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedulePara
     for (int q = threadIdx.x; q < p.R; q += kSchedThreads) cnt[q] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < m_star; i += kSchedThreads) {
-        const int slot = sm.val[0][i];
+        const int slot = sm.val[0][sk(i)];
         atomicMax(&cnt[slot / p.G], (uint32_t)(slot % p.G + 1));
     }
     __syncthreads();

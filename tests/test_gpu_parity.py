@@ -112,6 +112,28 @@ def test_schedule_matches_oracle(mode):
     assert n_exc <= 2
 
 
+@pytest.mark.parametrize("mode", [ds.SCHED_SYNC, ds.SCHED_FULL_SCAN, ds.SCHED_ASYNC_CAPACITY])
+def test_schedule_monotone_runs_match_oracle(mode):
+    # survivals that never increase along a request (the sampler's running products, zeros only
+    # as a tail) take the kernel's merge of per-request runs instead of the radix sort
+    gen = torch.Generator().manual_seed(78)
+    cases = [(1, 1), (3, 2), (5, 3), (32, 16), (128, 16), (100, 7), (512, 16), (8192, 1), (256, 32), (37, 5)]
+    n_exc = 0
+    for R, G in cases:
+        sps = wl.sps_hyperbolic(R * (1 + G), a=1e-3, b=2e-6 * 32 / R)
+        for ties in (False, True):
+            surv = _rand_surv(R, G, gen, zero_frac=0.0, ties=ties)
+            tail = torch.randint(0, G + 1, (R,), generator=gen)
+            surv[torch.arange(G)[None, :] >= tail[:, None]] = 0.0   # underflowed tails
+            surv = surv.to(DEV)
+            old = _rand_surv(R, G, gen, zero_frac=0.0).to(DEV) if mode == ds.SCHED_ASYNC_CAPACITY else None
+            gamma = torch.randint(0, G + 1, (R,), generator=gen, dtype=torch.int32).to(DEV) if ties else None
+            out = ds.schedule(surv, sps.to(DEV), mode, gamma=gamma, surv_capacity=old)
+            assert ds.check(out["workspace"]) == 0
+            n_exc += check_schedule(surv, sps, mode, out, gamma=gamma, surv_capacity=old)
+    assert n_exc <= 2
+
+
 def test_schedule_worked_examples_on_gpu():
     ex = load_golden("worked_examples.json")
     s = ex["single_request"]
