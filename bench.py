@@ -520,6 +520,18 @@ def bench_profile(args):
     if rnd.mode == wl.SCHED_ASYNC_CAPACITY:
         cap = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
                               rnd.seed, 0, gamma=rnd.gamma, path=path)["surv"].clone()
+    if args.head == "rnn":
+        W_rnn = wl.rnn_weights(rnd)
+        status = 0
+        for i in range(args.warmup + args.steps):
+            out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                                  rnd.seed, 2 + i, gamma=rnd.gamma, path=path, head=ds.HEAD_RNN, W_rnn=W_rnn)
+            status = status or ds.check(out["workspace"])
+        print(json.dumps({"profile_rounds": args.warmup + args.steps, "workload": rnd.name, "head": "rnn",
+                          "status": status, "launches": ds.launch_count()}))
+        if status:
+            raise SystemExit(1)
+        return
     runner = ds.RoundRunner(rnd, surv_capacity=cap, path=path)
     for i in range(args.warmup + args.steps):
         runner.set_round(2 + i)
@@ -542,6 +554,8 @@ def main():
     ap.add_argument("--path", choices=["auto", "cuda_core", "tensor_core"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true", help="plain rounds for ncu (no timing, no baselines)")
+    ap.add_argument("--head", choices=["markov", "rnn"], default="markov",
+                    help="with --profile: rnn runs only the sampler, with the RNN sequential head")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

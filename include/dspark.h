@@ -331,7 +331,7 @@ enum {
     DSPARK_KERNEL_RESIDUAL_STATS = 6,
     DSPARK_KERNEL_RESIDUAL_PICK = 7,
     DSPARK_KERNEL_ASSEMBLE = 8,
-    DSPARK_KERNEL_RNN_STEP = 9       /* RNN head: the per-step state update (and its hidden-state GEMM) */
+    DSPARK_KERNEL_RNN_STEP = 9       /* RNN head: the per-step state update (the cuBLAS hidden GEMM is not timed) */
 };
 
 typedef struct {
