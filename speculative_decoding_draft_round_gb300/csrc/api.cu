@@ -128,7 +128,7 @@ SampleLayout sample_layout(const dspark_sample_args* a)
 // ------------------------------------------------------------ verify
 
 struct VerifyLayout {
-    size_t row_stats, lse_t, rej, res_stats, total;
+    size_t row_stats, lse_t, rej, n_rej, rej_list, res_stats, total;
 };
 
 dspark_status check_verify(const dspark_verify_args* a)
@@ -166,6 +166,10 @@ VerifyLayout verify_layout(const dspark_verify_args* a)
     L.lse_t = o;
     o = align_up(o + sizeof(float) * (size_t)a->R * (a->gamma_max + 1), kAlign);
     L.rej = o;
+    o = align_up(o + sizeof(int32_t) * a->R, kAlign);
+    L.n_rej = o;
+    o = align_up(o + sizeof(int), kAlign);
+    L.rej_list = o;
     o = align_up(o + sizeof(int32_t) * a->R, kAlign);
     L.res_stats = o;
     o = align_up(o + sizeof(float) * rows * nblk, kAlign);
@@ -416,6 +420,8 @@ dspark_status dspark_verify(const dspark_verify_args* a, void* ws, size_t ws_byt
     p.row_stats = at<float2>(ws, L.row_stats);
     p.lse_t = at<float>(ws, L.lse_t);
     p.rej = at<int32_t>(ws, L.rej);
+    p.n_rej = at<int>(ws, L.n_rej);
+    p.rej_list = at<int32_t>(ws, L.rej_list);
     p.res_stats = at<float>(ws, L.res_stats);
     const bool tc = verify_uses_tc(a);
     cudaError_t e = launch(DSPARK_KERNEL_VERIFY_ROWS, s, [&] { return launch_verify_rows(p, s); });

@@ -78,6 +78,8 @@ struct VerifyParams {
     float2* row_stats;   // [R][G+1][nblk] block (max, sum) of the target rows, log2 units
     float* lse_t;        // [R][G+1]
     int32_t* rej;        // [R] rejected position, -1 if every admitted token was accepted
+    int* n_rej;          // number of rejected requests (zeroed by verify_rows, counted by verify_decide)
+    int32_t* rej_list;   // [R] the rejected requests, in the order verify_decide found them
     float* res_stats;    // [R_pad][nblk] block sums of max(0, p_t - p_d)
     const float* a_rows; // [R][G][r] bias operands reported by the sampler, or NULL (W_1[x_{n-1}])
 };

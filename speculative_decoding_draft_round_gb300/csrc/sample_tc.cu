@@ -56,19 +56,16 @@ enum Mode { kDraftMode = 0, kResidualMode = 1 };
 constexpr int A_REPLICAS = kAReplicas;   // copies of the draft A rows, so that ~19 CTAs share one
 
 constexpr int MAX_TILES = 64;                                              // R <= 8192
-constexpr uint32_t META_BYTES = BM * 32;
-constexpr uint32_t RES_ROW_BYTES = 272;   // residual stage row: 256 bytes of 128 bf16 + 16 bytes padding
-
+constexpr uint32_t META_BYTES = BM * 40;
 // Shared-memory layout of one mode. Draft mode: 5 W stages, U stages of two 128-byte-swizzled
 // [128 x 64] boxes, and the A tile (the W_1 rows of the tile's previous tokens, K-major,
-// 128-byte swizzle, r/64 boxes of [128 x 64]) loaded by TMA. Residual mode: 4 W stages; a U
-// stage holds 128 U rows then 128 target rows of one item, RES_ROW_BYTES apart (the padding
-// keeps the thread-per-row reads conflict-free); A lives in TMEM.
+// 128-byte swizzle, r/64 boxes of [128 x 64]) loaded by TMA. Residual mode: 8 W stages and no U
+// stages (each epilogue thread loads its own U and target columns); A lives in TMEM.
 template <int MODE>
 struct Lay {
-    static constexpr int W_ST = MODE == kDraftMode ? 5 : 4;
+    static constexpr int W_ST = MODE == kDraftMode ? 5 : 8;
     static constexpr int U_ST = 2;
-    static constexpr uint32_t U_ST_BYTES = MODE == kDraftMode ? 2 * U_BOX_BYTES : 2 * BM * RES_ROW_BYTES;
+    static constexpr uint32_t U_ST_BYTES = MODE == kDraftMode ? 2 * U_BOX_BYTES : 0;   // residual: no U stages
     static constexpr uint32_t A_BYTES = MODE == kDraftMode ? BM * KMAX * 2 : 0;   // draft: A tile in shared memory
     static constexpr uint32_t OFF_W = 0;
     static constexpr uint32_t OFF_U = OFF_W + W_ST * W_STAGE_BYTES;
@@ -310,14 +307,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-            "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-        : "memory");
-}
-
 // ------------------------------------------------------------------ kernel
 
 // Per-row metadata of the current request tile (shared memory, 32 bytes per row).
@@ -330,8 +319,10 @@ struct RowMeta {
     float lse_t2;     // residual: target log-normaliser of the same row, log2 units
     uint32_t u_row;   // residual: row index q*G + n of U (row of V elements)
     uint32_t t_row;   // residual: row index q*(G+1) + n of the target
+    int q;            // the request of this row (residual rows are the rejected requests, packed)
+    int pad;
 };
-static_assert(sizeof(RowMeta) == 32, "RowMeta is 32 bytes");
+static_assert(sizeof(RowMeta) == 40, "RowMeta is 40 bytes");
 
 struct TcParams {
     DraftStep d;      // draft mode
@@ -352,11 +343,31 @@ __device__ __forceinline__ bool row_takes_part(const TcParams& P, int q)
     return P.v.rej[q] >= 0;
 }
 
+// Request of row e of tile mt: the row itself in draft mode. In residual mode the n_act rejected
+// requests are dealt over the ceil(n_act / 128) tiles round-robin, so the tiles fill evenly, and
+// inside a tile the j-th row sits at e = (j % 4) * 32 + j / 4, so that a part-filled tile spreads
+// its rows over the four TMEM lane quarters (the four epilogue warps of each column group); -1
+// past the end of the list.
+template <int MODE>
+__device__ __forceinline__ int row_request(const TcParams& P, int mt, int e, int n_act)
+{
+    if (MODE == kDraftMode) return mt * BM + e;
+    const int nt = (n_act + BM - 1) / BM;
+    const int idx = ((e & 31) * 4 + (e >> 5)) * nt + mt;
+    if (idx >= n_act) return -1;
+    const int q = P.v.rej_list[idx];
+    if (q < 0 || q >= P.R) {
+        raise_status(P.status, DSPARK_ERR_DEVICE_INPUT);
+        return -1;
+    }
+    return q;
+}
+
 template <int MODE>
 __device__ __forceinline__ RowMeta row_meta(const TcParams& P, int q)
 {
-    RowMeta m{0, 0, 0, 0.f, 0.f, 0.f, 0u, 0u};
-    if (q >= P.R) return m;
+    RowMeta m{0, 0, 0, 0.f, 0.f, 0.f, 0u, 0u, q, 0};
+    if (q < 0 || q >= P.R) return m;
     if (MODE == kDraftMode) {
         // inputs only (no output of the previous kernel): the A row itself comes from a_next
         const DraftStep& p = P.d;
@@ -384,6 +395,23 @@ __device__ __forceinline__ RowMeta row_meta(const TcParams& P, int q)
         m.t_row = (uint32_t)(q * (p.G + 1) + n);
     }
     return m;
+}
+
+// Residual mode: this thread's 32 columns v0.. of its row of U and of the target, straight from
+// global memory (8 x 16 bytes; V % 8 == 0 keeps every 8-column chunk wholly inside or outside).
+__device__ __forceinline__ void load_res_cols(uint4 (&uv)[4], uint4 (&tv)[4], const VerifyParams& p, const RowMeta& rm,
+                                              int v0, int V)
+{
+    const uint4* up = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.U) + (size_t)rm.u_row * V + v0);
+    const uint4* tp =
+        reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.target) + (size_t)rm.t_row * V + v0);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (v0 + 8 * c < V) {
+            uv[c] = __ldg(up + c);
+            tv[c] = __ldg(tp + c);
+        }
+    }
 }
 
 struct Ring {
@@ -427,22 +455,36 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     int* s_ntiles = reinterpret_cast<int*>(smem + OFF_MISC + 8);
     int* s_tiles = reinterpret_cast<int*>(smem + OFF_MISC + 16);
+    int* s_nact = reinterpret_cast<int*>(smem + OFF_MISC + 12);   // residual: rejected requests
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const Ctl ctl{s_abort, P.status};
     const int n_mt = (P.R + BM - 1) / BM;
 
-    // tiles with at least one request taking part (residual mode: which requests were rejected
-    // comes from the previous kernel)
-    if (MODE == kResidualMode) pdl_wait();
+    // Tiles with at least one request taking part. Residual mode: the rows are the rejected
+    // requests, packed in the order the previous kernel listed them, so ceil(n / 128) tiles.
+    int n_act = 0;
+    if (MODE == kResidualMode) {
+        pdl_wait();
+        n_act = min(max(*P.v.n_rej, 0), P.R);
+    }
     if (tid == 0) {
         *s_ntiles = 0;
         *s_abort = 0;
+        *s_nact = n_act;
     }
     __syncthreads();
-    for (int mt = 0; mt < n_mt; ++mt) {
-        const bool act = tid < BM && row_takes_part<MODE>(P, mt * BM + tid);
-        if (__syncthreads_or(act) && tid == 0) s_tiles[(*s_ntiles)++] = mt;
+    if (MODE == kResidualMode) {
+        if (tid == 0) {
+            for (int mt = 0; mt * BM < n_act; ++mt) s_tiles[mt] = mt;
+            *s_ntiles = (n_act + BM - 1) / BM;
+        }
+        __syncthreads();
+    } else {
+        for (int mt = 0; mt < n_mt; ++mt) {
+            const bool act = tid < BM && row_takes_part<MODE>(P, mt * BM + tid);
+            if (__syncthreads_or(act) && tid == 0) s_tiles[(*s_ntiles)++] = mt;
+        }
     }
     if (tid == 0) {
         for (int i = 0; i < W_STAGES; ++i) {
@@ -482,7 +524,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     // same DRAM pages, and the nt tiles of one W block are read at the same time, by nt
     // neighbouring CTAs, so that W comes from DRAM once per step however many tiles there are.
     // The grid is a multiple of the tile count, so a CTA keeps one tile (one A load) throughout.
-    const int i0 = blockIdx.x, istep = gridDim.x;
+    // a CTA keeps one tile when the item stride is a multiple of the tile count: the CTAs past
+    // the largest such stride (fewer than nt of them) sit this launch out
+    const int i0 = blockIdx.x, istep = nt > 0 ? (int)gridDim.x - (int)gridDim.x % nt : (int)gridDim.x;
+    const int n_items_cta = i0 < istep ? n_items : 0;
+    const int nt_walk = nt > 0 ? nt : 1;   // no tiles: no items, and no division by zero in the walk
     const int KC = P.r / BK;
 
     if (warp == 0 && lane == 0) {
@@ -491,7 +537,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         Ring ws;
         uint32_t last_par[W_STAGES];
         bool filled[W_STAGES] = {};
-        for (ItemIter I(i0, istep, nt); I.it < n_items && !*s_abort; I.next(istep)) {
+        for (ItemIter I(i0, istep, nt_walk); I.it < n_items_cta && !*s_abort; I.next(istep)) {
             const int b = I.b;
             for (int kc = 0; kc < KC; ++kc) {
                 if (!mbar_wait(w_empty(ws.idx), ws.phase ^ 1u, ctl)) break;
@@ -513,7 +559,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         Ring us;
         uint32_t last_par[U_STAGES];
         bool filled[U_STAGES] = {false, false};
-        for (ItemIter I(i0, istep, nt); I.it < n_items && !*s_abort; I.next(istep)) {
+        for (ItemIter I(i0, istep, nt_walk); I.it < n_items_cta && !*s_abort; I.next(istep)) {
             const int mt = s_tiles[I.tile], b = I.b;
             if (!mbar_wait(u_empty(us.idx), us.phase ^ 1u, ctl)) break;
             const uint32_t dst = sbase + OFF_U + us.idx * U_STAGE_BYTES;
@@ -527,66 +573,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (*s_abort)
             for (int i = 0; i < U_STAGES; ++i)
                 if (filled[i]) mbar_drain(u_full(i), last_par[i]);
-    } else if (MODE == kResidualMode && warp == 3) {
-        // ---------------- residual U / target producer: lane l copies rows l, l+32, l+64, l+96 of
-        // the tile (256 bytes of U and of the target per active row) with 1-D bulk copies
-        pdl_wait();   // rej (rejected positions) comes from the previous kernel
-        const uint64_t pol = l2_policy_evict_first();
-        const char* Ub = static_cast<const char*>(P.v.U);
-        const char* Tb = static_cast<const char*>(P.v.target);
-        Ring us;
-        uint32_t last_par[U_STAGES];
-        bool filled[U_STAGES] = {};
-        int cur_tile = -1, cur_mt = 0, n_act = 0;
-        bool act[4] = {false, false, false, false};
-        uint32_t urow[4] = {0, 0, 0, 0};   // U row index q * G + n; the target row is urow + q
-        for (ItemIter I(i0, istep, nt); I.it < n_items && !*s_abort; I.next(istep)) {
-            const int tile = I.tile, b = I.b;
-            if (tile != cur_tile) {
-                const int mt = s_tiles[tile];
-                int cnt = 0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int q = mt * BM + lane + 32 * j;
-                    const int n = q < P.R ? P.v.rej[q] : -1;
-                    act[j] = n >= 0 && n < P.G;
-                    urow[j] = act[j] ? (uint32_t)(q * P.G + n) : 0u;
-                    cnt += act[j] ? 1 : 0;
-                }
-                n_act = __reduce_add_sync(0xffffffffu, cnt);
-                cur_tile = tile;
-                cur_mt = mt;
-            }
-            const int cols = min(BN, P.V - b * BN);   // V % 8 == 0: a multiple of 16 bytes
-            const uint32_t row_bytes = (uint32_t)cols * 2;
-            if (!warp_wait(u_empty(us.idx), us.phase ^ 1u, ctl)) break;
-            const uint32_t dst = sbase + OFF_U + us.idx * U_STAGE_BYTES;
-            if (lane == 0) mbar_expect_tx(u_full(us.idx), (uint32_t)n_act * 2u * row_bytes);
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (!act[j]) continue;
-                const uint32_t m = lane + 32 * j;
-                const uint32_t trow = urow[j] + (uint32_t)(cur_mt * BM) + m;   // q * (G + 1) + n
-                const size_t col_off = (size_t)b * BN * 2;
-                bulk_load(dst + m * RES_ROW_BYTES, Ub + (size_t)urow[j] * P.V * 2 + col_off, row_bytes,
-                          u_full(us.idx), pol);
-                bulk_load(dst + BM * RES_ROW_BYTES + m * RES_ROW_BYTES, Tb + (size_t)trow * P.V * 2 + col_off,
-                          row_bytes, u_full(us.idx), pol);
-            }
-            filled[us.idx] = true;
-            last_par[us.idx] = us.phase;
-            us.next(U_STAGES);
-        }
-        if (*s_abort && lane == 0)
-            for (int i = 0; i < U_STAGES; ++i)
-                if (filled[i]) mbar_drain(u_full(i), last_par[i]);
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
         Ring ws, tb;
         uint32_t a_par = 0;
         int cur_tile = -1;
-        for (ItemIter I(i0, istep, nt); I.it < n_items; I.next(istep)) {
+        for (ItemIter I(i0, istep, nt_walk); I.it < n_items_cta; I.next(istep)) {
             const int tile = I.tile;
             if (tile != cur_tile) {
                 if (cur_tile >= 0) mma_commit(a_empty);   // old A is free once its MMAs retire
@@ -644,9 +636,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         Ring us, tb;
         uint32_t a_par = 0;
         int cur_tile = -1;
-        RowMeta rm{};
         bool live = true;
-        for (ItemIter I(i0, istep, nt); I.it < n_items; I.next(istep)) {
+        uint4 uv[4] = {}, tv[4] = {};
+        RowMeta rm_reg{};
+        bool have_next = false;   // residual: uv / tv already hold this item's columns
+        for (ItemIter I(i0, istep, nt_walk); I.it < n_items_cta; I.next(istep)) {
             const int tile = I.tile, b = I.b;
             const int mt = s_tiles[tile];
             if (tile != cur_tile) {
@@ -654,7 +648,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     live = live && warp_wait(a_empty, a_par, ctl);
                     a_par ^= 1u;
                 }
-                if (e < BM) s_meta[e] = row_meta<MODE>(P, mt * BM + e);
+                if (e < BM) s_meta[e] = row_meta<MODE>(P, row_request<MODE>(P, mt, e, *s_nact));
                 if (!waited) {
                     pdl_wait();
                     waited = true;
@@ -729,12 +723,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     epi_barrier();
                     if (e == 0 && live) mbar_arrive(a_full);
                 }
-                rm = s_meta[m];
+                if (MODE == kDraftMode) rm_reg = s_meta[m];
                 cur_tile = tile;
             }
+            // this row's metadata for the current tile: a register copy in draft mode, read from shared
+            // memory in residual mode (whose epilogue has no registers to spare)
+            const RowMeta& rm = MODE == kDraftMode ? rm_reg : s_meta[m];
             const int v0 = b * BN + g * 32;
             // this thread's 32 columns of the row's input logits: U (draft) or U and target (residual)
-            uint4 uv[4] = {}, tv[4] = {};
             bool u_ok = live;
             if (MODE == kDraftMode) {
                 u_ok = live && warp_wait(u_full(us.idx), us.phase, ctl);
@@ -748,18 +744,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 us.next(U_STAGES);
             } else {
-                u_ok = live && warp_wait(u_full(us.idx), us.phase, ctl);
-                if (u_ok) {
-                    const uint32_t ubase = sbase + OFF_U + us.idx * U_STAGE_BYTES + m * RES_ROW_BYTES + g * 64;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uv[c] = ld_shared_v4(ubase + c * 16);
-                        tv[c] = ld_shared_v4(ubase + BM * RES_ROW_BYTES + c * 16);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(u_empty(us.idx));
-                }
-                us.next(U_STAGES);
+                // rows of U and the target at the rejected positions: scattered 64-byte pieces, loaded by
+                // the thread that uses them (one TMA copy per row and item was issue-bound in the copy
+                // engine); the next item's are requested before this item's combine
+                if (!have_next && live && rm.active) load_res_cols(uv, tv, P.v, rm, v0, P.V);
+                have_next = false;
             }
             // accumulator columns 32g .. 32g+31 of this row
             uint32_t acc[32];
@@ -835,9 +824,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             float2* pp = part + (I.n & 1) * 4 * BM;
             pp[g * BM + m] = partial;
+            if (MODE == kResidualMode && live && rm.active) {
+                ItemIter J = I;
+                J.next(istep);
+                if (J.it < n_items && J.tile == I.tile) {
+                    load_res_cols(uv, tv, P.v, rm, J.b * BN + g * 32, P.V);
+                    have_next = true;
+                }
+            }
             epi_barrier();
             if (g == 0 && rm.active && live) {
-                const size_t o = (size_t)(mt * BM + m) * nblk + b;
+                const size_t o = (size_t)(MODE == kDraftMode ? mt * BM + m : rm.q) * nblk + b;
                 if (MODE == kDraftMode) {
                     float M = pp[m].x;
 #pragma unroll

@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParam
     const bool greedy = p.temperature[q] == 0.f;
     const float scale = greedy ? 1.f : kLog2e / p.temperature[q];
     const bool vec = (p.V % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.target) & 15u) == 0);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.n_rej = 0;   // verify_decide counts from zero
     const int b0 = (blockIdx.x * kRowWarps + warp) * kRowBlocksPerWarp;
     if (b0 >= p.nblk) return;
     if (greedy) {
@@ -248,6 +249,7 @@ __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyPar
     if (t == 0) {
         p.accepted[q] = n;
         p.rej[q] = n < ell ? n : -1;
+        if (n < ell) p.rej_list[atomicAdd(p.n_rej, 1)] = q;   // the residual kernel tiles these rows
     }
     if (n < ell) return;   // residual draw happens in residual_pick
 
