@@ -19,6 +19,7 @@ constexpr int kAsmPer = DSPARK_MAX_SLOTS / kAsmThreads;   // requests per thread
 
 __global__ void __launch_bounds__(kAsmThreads) assemble_kernel(AssembleParams p)
 {
+    pdl_enter();   // keep comes from the scheduler
     __shared__ int32_t s_off[DSPARK_MAX_SLOTS + 1];
     __shared__ int32_t s_warp[kAsmThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -99,7 +100,8 @@ __global__ void __launch_bounds__(kAsmThreads) assemble_kernel(AssembleParams p)
 
 cudaError_t launch_assemble(const AssembleParams& p, cudaStream_t s)
 {
-    assemble_kernel<<<1, kAsmThreads, 0, s>>>(p);
+    const cudaError_t e = launch_pdl(assemble_kernel, 1, kAsmThreads, 0, s, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

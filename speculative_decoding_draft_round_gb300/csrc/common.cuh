@@ -86,6 +86,32 @@ __host__ __device__ inline PhiloxKey make_key(uint64_t seed)
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
+// Kernels that do nothing before the dependency: wait for the previous kernel, then let the next
+// one be scheduled, so that its launch overlaps this kernel's work.
+__device__ __forceinline__ void pdl_enter()
+{
+    pdl_wait();
+    pdl_trigger();
+}
+
+// Launch with the programmatic-serialization attribute (the kernel calls pdl_wait / pdl_enter).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ------------------------------------------------------------------ element loads
 
 template <typename T>

@@ -27,6 +27,7 @@ namespace dspark {
 template <typename T>
 __global__ void __launch_bounds__(256) conf_hidden_kernel(DraftStep p)
 {
+    pdl_enter();   // the previous call's kernels read the slots and rows written here
     // clear the per-step block-draw slots of this call, and set the first step's conditioning rows
     // (W_1[x_0], x_0 = anchor) for the tensor-core statistics kernel
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.R * p.G; i += gridDim.x * blockDim.x) p.pick[i] = 0ull;
@@ -130,6 +131,7 @@ __device__ __forceinline__ StepRequest draft_request_inputs(const DraftStep& p, 
 template <typename T>
 __global__ void __launch_bounds__(kNoiseBlock) draft_stats_simt_kernel(DraftStep p)
 {
+    pdl_enter();   // x_cur, the operand rows and the pick slots come from the previous kernels
     extern __shared__ float es[];   // [kSimtReq][r]
     __shared__ StepRequest req[kSimtReq];
     __shared__ float red[8];
@@ -392,11 +394,9 @@ cudaError_t launch_conf_hidden(const DraftStep& p, cudaStream_t s)
 {
     const int rows = p.R * p.G;
     const int blocks = cdiv(rows, 8);
-    if (p.dtype == DSPARK_BF16)
-        conf_hidden_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(p);
-    else
-        conf_hidden_kernel<float><<<blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    const cudaError_t e = p.dtype == DSPARK_BF16 ? launch_pdl(conf_hidden_kernel<__nv_bfloat16>, blocks, 256, 0, s, p)
+                                                 : launch_pdl(conf_hidden_kernel<float>, blocks, 256, 0, s, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_draft_stats_simt(const DraftStep& p, cudaStream_t s)
@@ -406,10 +406,12 @@ cudaError_t launch_draft_stats_simt(const DraftStep& p, cudaStream_t s)
     if (p.dtype == DSPARK_BF16) {
         cudaFuncSetAttribute(draft_stats_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
-        draft_stats_simt_kernel<__nv_bfloat16><<<grid, kNoiseBlock, smem, s>>>(p);
+        const cudaError_t e = launch_pdl(draft_stats_simt_kernel<__nv_bfloat16>, grid, kNoiseBlock, smem, s, p);
+        if (e != cudaSuccess) return e;
     } else {
         cudaFuncSetAttribute(draft_stats_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        draft_stats_simt_kernel<float><<<grid, kNoiseBlock, smem, s>>>(p);
+        const cudaError_t e = launch_pdl(draft_stats_simt_kernel<float>, grid, kNoiseBlock, smem, s, p);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

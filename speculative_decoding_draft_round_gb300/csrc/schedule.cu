@@ -517,6 +517,7 @@ __device__ void threshold_admit(SchedSmem& sm, const ScheduleParams& p, int n_sl
 
 __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleParams p)
 {
+    pdl_enter();   // the survivals come from the sampler's last commit
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SchedSmem& sm = *reinterpret_cast<SchedSmem*>(smem_raw);
     const int n_slots = p.R * p.G;
@@ -582,8 +583,8 @@ cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s)
         if (e != cudaSuccess) return e;
         smem_set = true;
     }
-    schedule_kernel<<<1, kSchedThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(schedule_kernel, 1, kSchedThreads, smem, s, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace dspark

@@ -140,6 +140,7 @@ __device__ __forceinline__ float2 row_block_argmax(const T* row, int V, int b, i
 template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParams p)
 {
+    pdl_enter();   // keep comes from the scheduler; the workspace is read by the previous call
     const int q = blockIdx.y;
     const int ell = request_keep(p, q);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -182,6 +183,7 @@ constexpr int kDecideThreads = 128;
 template <typename T>
 __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyParams p)
 {
+    pdl_enter();   // the row statistics and the zeroed rejection counter come from verify_rows
     __shared__ float red[8];
     __shared__ float sv[8];
     __shared__ int si[8];
@@ -316,6 +318,7 @@ __device__ __forceinline__ ResRequest residual_request(const VerifyParams& p, in
 template <typename T>
 __global__ void __launch_bounds__(kNoiseBlock) residual_stats_simt_kernel(VerifyParams p)
 {
+    pdl_enter();   // the rejected positions come from verify_decide
     extern __shared__ float es[];   // [kResReq][r]
     __shared__ ResRequest req[kResReq];
     __shared__ float red[8];
@@ -374,6 +377,7 @@ constexpr int kPickThreads = kBlockGemvThreads;
 template <typename T>
 __global__ void __launch_bounds__(kPickThreads) residual_pick_kernel(VerifyParams p)
 {
+    pdl_enter();   // the residual block sums come from the residual statistics kernel
     extern __shared__ float sm_dyn[];   // [r] W_1[prev], then [16][128] K-slice partials
     float* erow = sm_dyn;
     float* part = sm_dyn + ((p.r + 3) & ~3);
@@ -454,20 +458,18 @@ cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s)
 {
     const int per_cta = kRowWarps * kRowBlocksPerWarp;
     const dim3 grid(cdiv(p.nblk, per_cta), p.R);
-    if (p.dtype == DSPARK_BF16)
-        verify_rows_kernel<__nv_bfloat16><<<grid, kRowWarps * 32, 0, s>>>(p);
-    else
-        verify_rows_kernel<float><<<grid, kRowWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
+    const cudaError_t e = p.dtype == DSPARK_BF16
+                              ? launch_pdl(verify_rows_kernel<__nv_bfloat16>, grid, kRowWarps * 32, 0, s, p)
+                              : launch_pdl(verify_rows_kernel<float>, grid, kRowWarps * 32, 0, s, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_verify_decide(const VerifyParams& p, cudaStream_t s)
 {
-    if (p.dtype == DSPARK_BF16)
-        verify_decide_kernel<__nv_bfloat16><<<p.R, kDecideThreads, 0, s>>>(p);
-    else
-        verify_decide_kernel<float><<<p.R, kDecideThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    const cudaError_t e = p.dtype == DSPARK_BF16
+                              ? launch_pdl(verify_decide_kernel<__nv_bfloat16>, p.R, kDecideThreads, 0, s, p)
+                              : launch_pdl(verify_decide_kernel<float>, p.R, kDecideThreads, 0, s, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_residual_stats_simt(const VerifyParams& p, cudaStream_t s)
@@ -477,11 +479,13 @@ cudaError_t launch_residual_stats_simt(const VerifyParams& p, cudaStream_t s)
     if (p.dtype == DSPARK_BF16) {
         cudaFuncSetAttribute(residual_stats_simt_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
-        residual_stats_simt_kernel<__nv_bfloat16><<<grid, kNoiseBlock, smem, s>>>(p);
+        const cudaError_t e = launch_pdl(residual_stats_simt_kernel<__nv_bfloat16>, grid, kNoiseBlock, smem, s, p);
+        if (e != cudaSuccess) return e;
     } else {
         cudaFuncSetAttribute(residual_stats_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
-        residual_stats_simt_kernel<float><<<grid, kNoiseBlock, smem, s>>>(p);
+        const cudaError_t e = launch_pdl(residual_stats_simt_kernel<float>, grid, kNoiseBlock, smem, s, p);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -489,11 +493,10 @@ cudaError_t launch_residual_stats_simt(const VerifyParams& p, cudaStream_t s)
 cudaError_t launch_residual_pick(const VerifyParams& p, cudaStream_t s)
 {
     const size_t smem = (size_t)(((p.r + 3) & ~3) + 16 * kNoiseBlock) * sizeof(float);
-    if (p.dtype == DSPARK_BF16)
-        residual_pick_kernel<__nv_bfloat16><<<p.R, kPickThreads, smem, s>>>(p);
-    else
-        residual_pick_kernel<float><<<p.R, kPickThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    const cudaError_t e = p.dtype == DSPARK_BF16
+                              ? launch_pdl(residual_pick_kernel<__nv_bfloat16>, p.R, kPickThreads, smem, s, p)
+                              : launch_pdl(residual_pick_kernel<float>, p.R, kPickThreads, smem, s, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace dspark
