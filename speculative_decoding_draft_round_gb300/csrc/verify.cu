@@ -64,24 +64,26 @@ __device__ __forceinline__ void row_block_stats8(const T* row, int V, int b0, fl
         for (int j = 0; j < 4; ++j) {
             const int v = b0 * kNoiseBlock + j * 256 + lane * 8;
             const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-            float x[8];
+            float x[8];   // raw logits: the maximum is taken before scaling (scale > 0)
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                x[2 * h] = __uint_as_float(w4[h] << 16) * scale;
-                x[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u) * scale;
+                x[2 * h] = __uint_as_float(w4[h] << 16);
+                x[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
             }
             const bool in = v < V;   // V % 8 == 0: 8 columns all in or all out
-            float m = -INFINITY;
+            float mr = -INFINITY;
             if (in) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m = fmaxf(m, x[e]);
+                for (int e = 0; e < 8; ++e) mr = fmaxf(mr, x[e]);
             }
 #pragma unroll
-            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            for (int o = 8; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+            const float m = mr * scale;   // the block maximum of z/T in log2 units
             float sacc = 0.f;
             if (in && m > -INFINITY) {
+                // one fused multiply-add and one SFU exponential per element: 2^(x*scale - m)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) sacc += exp2f(x[e] - m);
+                for (int e = 0; e < 8; ++e) sacc += ex2(fmaf(x[e], scale, -m));
             }
 #pragma unroll
             for (int o = 8; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
