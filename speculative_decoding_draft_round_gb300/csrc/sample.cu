@@ -24,6 +24,9 @@ namespace dspark {
 
 // ----------------------------------------------------------------- w_h . h
 
+constexpr int kHwRows = 2;    // confidence-head rows per CTA of conf_hidden_kernel
+constexpr int kHwSplit = 4;   // warps per row
+
 template <typename T>
 __global__ void __launch_bounds__(256) conf_hidden_kernel(DraftStep p)
 {
@@ -43,43 +46,56 @@ __global__ void __launch_bounds__(256) conf_hidden_kernel(DraftStep p)
             for (int rp = 0; rp < p.a_replicas; ++rp) an[rp * n + i] = v;
         }
     }
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (warp >= p.R * p.G) return;
-    const int q = warp / p.G, k = warp % p.G;
-    const int g = p.gamma ? p.gamma[q] : p.G;
-    if (k >= g) return;
-    const T* h = static_cast<const T*>(p.h) + (size_t)warp * p.d;
+    // hw[q][k] = w_h . h[q][k]: kHwRows rows per CTA, each split over kHwSplit warps along d (more
+    // warps in flight than one per row), the parts summed through shared memory
+    __shared__ float s_part[kHwRows * kHwSplit];
+    const int wic = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kHwRows + wic / kHwSplit, part = wic % kHwSplit;
+    bool on = row < p.R * p.G;
+    if (on) {
+        const int q = row / p.G, k = row % p.G;
+        const int g = p.gamma ? p.gamma[q] : p.G;
+        on = k < g;
+    }
     float acc = 0.f;
-    const bool vec = (p.d % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.h) & 15u) == 0) &&
-                     ((reinterpret_cast<uintptr_t>(p.w_h) & 15u) == 0);
-    if (vec) {
-        // 8 elements (16 bytes of bf16, 32 of fp32) per lane per step, four steps' loads in flight
-        int j = lane * 8;
-        for (; j + 3 * 256 < p.d; j += 4 * 256) {
-            float w[4][8], x[4][8];
+    if (on) {
+        const T* h = static_cast<const T*>(p.h) + (size_t)row * p.d;
+        const bool vec = (p.d % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.h) & 15u) == 0) &&
+                         ((reinterpret_cast<uintptr_t>(p.w_h) & 15u) == 0);
+        if (vec) {
+            // step s covers columns 256 s + 8 lane .. +7; this warp takes steps part, part + 4, ...,
+            // four of them in flight (d % 8 == 0: a lane's 8 columns are all inside or all outside)
+            for (int s0 = part; s0 * 256 < p.d; s0 += 4 * kHwSplit) {
+                float w[4][8], x[4][8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                load8<T>(h + j + u * 256, x[u]);
-                load8<float>(p.w_h + j + u * 256, w[u]);
+                for (int u = 0; u < 4; ++u) {
+                    const int jj = (s0 + u * kHwSplit) * 256 + lane * 8;
+                    if (jj < p.d) {
+                        load8<T>(h + jj, x[u]);
+                        load8<float>(p.w_h + jj, w[u]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) w[u][e] = x[u][e] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc = fmaf(w[u][e], x[u][e], acc);
             }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc = fmaf(w[u][e], x[u][e], acc);
+        } else {
+            for (int jj = part * 32 + lane; jj < p.d; jj += 32 * kHwSplit) acc += p.w_h[jj] * ld(h, jj);
         }
-        for (; j < p.d; j += 256) {
-            float w[8], x[8];
-            load8<T>(h + j, x);
-            load8<float>(p.w_h + j, w);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc = fmaf(w[e], x[e], acc);
-        }
-    } else {
-        for (int j = lane; j < p.d; j += 32) acc += p.w_h[j] * ld(h, j);
     }
     acc = warp_sum(acc);
-    if (lane == 0) p.hw[warp] = acc;
+    if (lane == 0) s_part[wic] = acc;
+    __syncthreads();
+    if (on && part == 0 && lane == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int u = 0; u < kHwSplit; ++u) t += s_part[wic + u];
+        p.hw[row] = t;
+    }
 }
 
 // ----------------------------------------------------------------- block statistics (CUDA cores)
@@ -393,7 +409,7 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
 cudaError_t launch_conf_hidden(const DraftStep& p, cudaStream_t s)
 {
     const int rows = p.R * p.G;
-    const int blocks = cdiv(rows, 8);
+    const int blocks = cdiv(rows, kHwRows);
     const cudaError_t e = p.dtype == DSPARK_BF16 ? launch_pdl(conf_hidden_kernel<__nv_bfloat16>, blocks, 256, 0, s, p)
                                                  : launch_pdl(conf_hidden_kernel<float>, blocks, 256, 0, s, p);
     return e != cudaSuccess ? e : cudaGetLastError();
