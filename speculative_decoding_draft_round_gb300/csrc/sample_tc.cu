@@ -190,6 +190,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_normal()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last()
 {
     uint64_t p;
@@ -527,7 +534,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp == 0 && lane == 0) {
         // ---------------- W producer
-        const uint64_t pol = l2_policy_evict_last();
+        // W takes the default L2 policy: measured against evict-last and evict-first hints, it keeps
+        // the most of the other kernels' working set (and of W) in L2 from one step to the next
+        const uint64_t pol = l2_policy_evict_normal();
         Ring ws;
         uint32_t last_par[W_STAGES];
         bool filled[W_STAGES] = {};

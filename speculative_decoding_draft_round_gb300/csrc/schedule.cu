@@ -70,7 +70,7 @@ __device__ __forceinline__ int striped(int warp, int it, int lane, int ni) { ret
 
 // Load the pool keys of `src` ([R][G] survivals) into key[0]/val[0]; returns |pool|. Every load
 // of a thread is issued before any is used.
-__device__ int load_pool(SchedSmem& sm, const ScheduleParams& p, const float* src, int n_slots, int ni)
+__device__ __noinline__ int load_pool(SchedSmem& sm, const ScheduleParams& p, const float* src, int n_slots, int ni)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) sm.n_pool = 0;
@@ -116,7 +116,7 @@ __device__ int load_pool(SchedSmem& sm, const ScheduleParams& p, const float* sr
 }
 
 // Exclusive prefix over the kHist counts in [digit][warp] order, in place (1024 threads, 8 each).
-__device__ void scan_hist(SchedSmem& sm)
+__device__ __noinline__ void scan_hist(SchedSmem& sm)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int per = kHist / kSchedThreads;   // 8
@@ -155,7 +155,7 @@ __device__ void scan_hist(SchedSmem& sm)
 }
 
 // One stable counting pass on 8 bits of the key, buffer `in` -> 1 - in.
-__device__ void radix_pass(SchedSmem& sm, int in, int shift, int ni)
+__device__ __noinline__ void radix_pass(SchedSmem& sm, int in, int shift, int ni)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     reinterpret_cast<uint4*>(sm.hist)[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
@@ -206,7 +206,7 @@ __device__ __forceinline__ bool kv_less(uint32_t ka, uint16_t va, uint32_t kb, u
 // (clipped to n) merge into [2pL, 2pL + 2L) of buffer 1 - in. Thread t writes outputs
 // t*ni .. t*ni + ni - 1; it finds where its first output of each pair starts on the merge path by
 // a binary search, then merges element by element with the two candidates held in registers.
-__device__ void merge_level(SchedSmem& sm, int in, int n, int L, int ni)
+__device__ __noinline__ void merge_level(SchedSmem& sm, int in, int n, int L, int ni)
 {
     const uint32_t* ka = sm.key[in];
     const uint16_t* va = sm.val[in];
@@ -269,7 +269,7 @@ __device__ void merge_level(SchedSmem& sm, int in, int n, int L, int ni)
 // request's G slots are already in order -- the sampler's survivals are running products of
 // confidences below one, so they never increase along a request -- the R runs are merged
 // pairwise (log2 R levels); any other input takes the stable LSD radix sort.
-__device__ void sort_pool(SchedSmem& sm, int n, int G, int ni)
+__device__ __noinline__ void sort_pool(SchedSmem& sm, int n, int G, int ni)
 {
     bool unsorted = false;
     for (int s = threadIdx.x; s < n; s += kSchedThreads)
@@ -310,10 +310,9 @@ __device__ __forceinline__ unsigned long long fixed48(uint32_t key)
 }
 
 // Exact Theta_m = (R + S * 2^-48) * SPS(R + m) as a normalised key (see the header comment).
-__device__ __forceinline__ ThetaKey theta_key(int R, int m, unsigned long long S, const float* sps, int* status)
+__device__ __forceinline__ ThetaKey theta_key(int R, unsigned long long S, float sv, int* status)
 {
     const unsigned long long T = ((unsigned long long)R << 48) + S;   // < 2^62
-    const float sv = sps[R + m - 1];
     if (!(sv > 0.f) || sv == INFINITY) {
         raise_status(status, DSPARK_ERR_DEVICE_INPUT);   // a throughput table entry must be positive and finite
         return ThetaKey{INT32_MIN, 0ull};
@@ -345,7 +344,7 @@ __device__ __forceinline__ double theta_of(int R, int m, unsigned long long S, c
 
 // Inclusive prefix sums S (sorted index tid * ni + it) of the fixed-point a's, and the exclusive
 // prefix of the thread's first index.
-__device__ void prefix_sums(SchedSmem& sm, int n, int ni, unsigned long long (&S)[kMaxItems], unsigned long long& excl)
+__device__ __noinline__ void prefix_sums(SchedSmem& sm, int n, int ni, unsigned long long (&S)[kMaxItems], unsigned long long& excl)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     unsigned long long run = 0;
@@ -381,20 +380,21 @@ __device__ void prefix_sums(SchedSmem& sm, int n, int ni, unsigned long long (&S
 }
 
 // Smallest arg-max of Theta_m over m = 0..n (full scan), from the prefix sums.
-__device__ int full_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, const unsigned long long (&S)[kMaxItems])
+__device__ __noinline__ int full_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, const unsigned long long (&S)[kMaxItems],
+                         const float (&sv)[kMaxItems + 1])
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     ThetaKey best{INT32_MIN, 0ull};
     int bm = INT32_MAX;
     if (tid == 0) {
-        best = theta_key(p.R, 0, 0ull, p.sps, p.status);
+        best = theta_key(p.R, 0ull, sv[0], p.status);
         bm = 0;
     }
 #pragma unroll
     for (int it = 0; it < kMaxItems; ++it) {
         const int i = tid * ni + it;
         if (it < ni && i < n) {
-            const ThetaKey th = theta_key(p.R, i + 1, S[it], p.sps, p.status);
+            const ThetaKey th = theta_key(p.R, S[it], sv[it + 1], p.status);
             if (key_gt(th, best) || bm == INT32_MAX) {
                 best = th;
                 bm = i + 1;
@@ -430,20 +430,20 @@ __device__ int full_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, 
 }
 
 // First m >= 1 with Theta_m <= Theta_{m-1}, minus one (|pool| if none).
-__device__ int sync_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, const unsigned long long (&S)[kMaxItems],
-                         unsigned long long excl)
+__device__ __noinline__ int sync_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, const unsigned long long (&S)[kMaxItems],
+                         unsigned long long excl, const float (&sv)[kMaxItems + 1])
 {
     const int tid = threadIdx.x;
     if (tid == 0) sm.first_bad = INT32_MAX;
     __syncthreads();
     int bad = INT32_MAX;
     if (tid * ni < n) {
-        ThetaKey prev = theta_key(p.R, tid * ni, excl, p.sps, p.status);
+        ThetaKey prev = theta_key(p.R, excl, sv[0], p.status);
 #pragma unroll
         for (int it = 0; it < kMaxItems; ++it) {
             const int i = tid * ni + it;
             if (it < ni && i < n) {
-                const ThetaKey th = theta_key(p.R, i + 1, S[it], p.sps, p.status);
+                const ThetaKey th = theta_key(p.R, S[it], sv[it + 1], p.status);
                 if (!key_gt(th, prev) && bad == INT32_MAX) bad = i + 1;
                 prev = th;
             }
@@ -517,15 +517,24 @@ __device__ void threshold_admit(SchedSmem& sm, const ScheduleParams& p, int n_sl
 
 __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(ScheduleParams p)
 {
-    pdl_enter();   // the survivals come from the sampler's last commit
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SchedSmem& sm = *reinterpret_cast<SchedSmem*>(smem_raw);
     const int n_slots = p.R * p.G;
+    const int ni = (n_slots + kSchedThreads - 1) / kSchedThreads;   // keys per thread, 1..8
+    // The throughput-table entries of this thread's scan positions, SPS(R + m) for
+    // m = tid*ni .. tid*ni + ni (index R + m - 1; n_sps >= R (1 + G) covers every m <= R G). The
+    // table is an input: it is read before the dependency wait, so the scans never wait on memory.
+    float sv[kMaxItems + 1];
+#pragma unroll
+    for (int u = 0; u <= kMaxItems; ++u) {
+        const int m = (int)threadIdx.x * ni + u;
+        sv[u] = (u <= ni && m <= n_slots && p.R + m >= 1) ? p.sps[p.R + m - 1] : 0.f;
+    }
+    pdl_enter();   // the survivals come from the sampler's last commit
     if (p.mode == DSPARK_SCHED_THRESHOLD) {
         threshold_admit(sm, p, n_slots);
         return;
     }
-    const int ni = (n_slots + kSchedThreads - 1) / kSchedThreads;   // keys per thread, 1..8
 
     unsigned long long S[kMaxItems], excl;
     int capacity = -1;
@@ -533,16 +542,16 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedulePara
         const int n_old = load_pool(sm, p, p.surv_capacity, n_slots, ni);
         sort_pool(sm, n_slots, p.G, ni);
         prefix_sums(sm, n_old, ni, S, excl);
-        capacity = full_scan(sm, p, n_old, ni, S);
+        capacity = full_scan(sm, p, n_old, ni, S, sv);
     }
     const int n = load_pool(sm, p, p.surv, n_slots, ni);
     sort_pool(sm, n_slots, p.G, ni);
     prefix_sums(sm, n, ni, S, excl);
     int m_star;
     if (p.mode == DSPARK_SCHED_SYNC)
-        m_star = sync_scan(sm, p, n, ni, S, excl);
+        m_star = sync_scan(sm, p, n, ni, S, excl, sv);
     else if (p.mode == DSPARK_SCHED_FULL_SCAN)
-        m_star = full_scan(sm, p, n, ni, S);
+        m_star = full_scan(sm, p, n, ni, S, sv);
     else
         m_star = min(capacity, n);
 
