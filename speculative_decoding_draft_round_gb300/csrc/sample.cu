@@ -248,9 +248,10 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     const size_t o = (size_t)q * p.G + p.k;
     const bool greedy = p.temperature[q] == 0.f;   // temperature 0: arg-max draft
     const float invT = greedy ? 1.f : 1.f / p.temperature[q];
-    const float hw = p.hw[o];
     pdl_wait();      // block statistics, pick slots and x_cur come from the kernels before this one
     pdl_trigger();   // the next step's statistics kernel may start its prefetch
+    // hw comes from conf_hidden, which the chain of waits orders before this point only
+    const float hw = p.hw[o];
     if (!rq.active) {
         if (p.a_rows && !RNN)
             for (int i = t; i < p.r; i += kCommitThreads) p.a_rows[o * p.r + i] = 0.f;
