@@ -105,8 +105,8 @@ SampleLayout sample_layout(const dspark_sample_args* a)
     o = align_up(o + sizeof(int32_t) * a->R, kAlign);
     L.hw = o;
     o = align_up(o + sizeof(float) * (size_t)a->R * a->gamma_max, kAlign);
-    L.stats = o;
-    o = align_up(o + sizeof(float2) * rows * nblk, kAlign);
+    L.stats = o;   // per block (CUDA-core path) or per CTA of the tensor-core kernel
+    o = align_up(o + sizeof(float2) * rows * (sample_uses_tc(a) ? tc_grid(a->R, nblk) : nblk), kAlign);
     L.pick = o;
     o = align_up(o + sizeof(unsigned long long) * (size_t)a->R * a->gamma_max, kAlign);
     L.a_next = o;   // the tensor-core path keeps kAReplicas copies of the next step's A rows
@@ -277,6 +277,7 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.x_cur = at<int32_t>(ws, L.x_cur);
     p.hw = at<float>(ws, L.hw);
     p.stats = at<float2>(ws, L.stats);
+    p.n_stats = sample_uses_tc(a) ? tc_grid(a->R, p.nblk) : p.nblk;
     p.pick = at<unsigned long long>(ws, L.pick);
     p.a_next = at<unsigned char>(ws, L.a_next);
     const bool tc = sample_uses_tc(a);
@@ -296,13 +297,19 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
             snprintf(g_last_error, sizeof g_last_error, "rnn hidden GEMM: %s (%s)", cudaGetErrorName(e),
                      cudaGetErrorString(e));
     }
+    // the commit copies the winning W block with one bulk copy when W admits the block map
+    CUtensorMap wmap;
+    memset(&wmap, 0, sizeof wmap);
+    const bool use_wmap = a->dtype == DSPARK_BF16 && a->r % 16 == 0 && a->r <= 256 &&
+                          encode_w_block_map(&wmap, a->W, a->V, a->r) == cudaSuccess;
     for (int k = 0; k < a->gamma_max && e == cudaSuccess; ++k) {
         p.k = k;
         if (rnn) e = launch(DSPARK_KERNEL_RNN_STEP, s, [&] { return launch_rnn_step(p, s); });
         if (e == cudaSuccess)
             e = launch(DSPARK_KERNEL_DRAFT_STATS, s,
                        [&] { return tc ? launch_draft_stats_tc(p, s) : launch_draft_stats_simt(p, s); });
-        if (e == cudaSuccess) e = launch(DSPARK_KERNEL_DRAFT_COMMIT, s, [&] { return launch_draft_commit(p, s); });
+        if (e == cudaSuccess)
+            e = launch(DSPARK_KERNEL_DRAFT_COMMIT, s, [&] { return launch_draft_commit(p, use_wmap ? &wmap : nullptr, s); });
     }
     return cuda_status(e);
 }

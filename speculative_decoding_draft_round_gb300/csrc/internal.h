@@ -2,6 +2,7 @@
 // translation units (host side). Not part of the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -39,7 +40,9 @@ struct DraftStep {
     int* status;
     int32_t* x_cur;      // [R] token committed at the previous step
     float* hw;           // [R][G] w_h . h[r][k]
-    float2* stats;       // [R_pad][nblk] (max, sum) of exp2 over each vocabulary block, log2 units
+    float2* stats;       // [R][n_stats] (max, sum) of exp2, log2 units: per vocabulary block (CUDA-core
+                         // path) or per CTA of the tensor-core kernel (its blocks merged), row-major
+    int n_stats;         // entries per row of stats: nblk, or the tensor-core grid
     unsigned long long* pick;   // [G][R] packed block-level arg-max of each step (cleared per call)
     void* a_next;        // [a_replicas][R][r] (element type of E): W_1 row of the token each request
                          // conditions on next, in a_replicas identical copies (RNN head on the tensor-core
@@ -112,12 +115,17 @@ struct AssembleParams {
 // sample.cu
 cudaError_t launch_conf_hidden(const DraftStep& p, cudaStream_t s);
 cudaError_t launch_draft_stats_simt(const DraftStep& p, cudaStream_t s);
-cudaError_t launch_draft_commit(const DraftStep& p, cudaStream_t s);
+// wmap: the W block map of encode_w_block_map, or NULL (the commit then loads W with plain loads)
+cudaError_t launch_draft_commit(const DraftStep& p, const CUtensorMap* wmap, cudaStream_t s);
+// Tensor map of W [r][V] bf16 with one [r x 128] box per vocabulary block (r <= 256, V % 8 == 0,
+// W 16-byte aligned): the commit's copy of the winning block.
+cudaError_t encode_w_block_map(CUtensorMap* m, const void* W, int V, int r);
 
 // sample_tc.cu
 bool tc_supported(int dtype, int R, int V, int r, const void* U, const void* E, const void* W);
 bool tc_residual_supported(int dtype, int R, int V, int r, const void* U, const void* E, const void* W);
 size_t tc_stats_rows(int R);  // rows of the block-statistics workspace the tensor-core path writes
+int tc_grid(int R, int nblk); // CTAs of the tensor-core statistics kernel
 cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s);
 cudaError_t launch_residual_stats_tc(const VerifyParams& p, cudaStream_t s);
 

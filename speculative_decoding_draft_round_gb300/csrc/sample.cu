@@ -17,8 +17,11 @@
 //                    previous token.
 // w_h . h_k does not depend on the draws, so conf_hidden computes it for every
 // (request, position) in one pass before the serial loop.
+#include <string.h>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace dspark {
 
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(kNoiseBlock) draft_stats_simt_kernel(DraftStep
         const float e = v < p.V ? exp2f(x - m) : 0.f;
         const float s = block_sum<kNoiseBlock>(e, red);
         if (t == 0) {
-            p.stats[(size_t)q * p.nblk + b] = make_float2(m, s);
+            p.stats[(size_t)q * p.n_stats + b] = make_float2(m, s);
             // block key of the two-level draw; greedy requests take the block holding the maximum
             const float z = req[j].greedy ? m
                                           : (m + log2f(s)) * kLn2 -
@@ -230,12 +233,44 @@ __device__ __forceinline__ LseAcc lse_merge(LseAcc a, LseAcc b)
 constexpr int kStatsPerThread = 8;       // block statistics held in registers per thread (nblk <= 2048)
 constexpr int kBiasRows = 16;            // W rows per thread in the fast path (r <= 256)
 
-template <typename T, bool RNN>
-__global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep p)
+constexpr unsigned long long kCommitWaitNs = 4000000000ull;   // 4 s
+
+// Bounded wait for phase `parity` of a shared-memory barrier; false (and DSPARK_ERR_TIMEOUT
+// recorded) when it runs out.
+__device__ __noinline__ bool commit_wait(uint32_t bar, uint32_t parity, int* status)
 {
-    extern __shared__ float sm_dyn[];   // [r] W_1[prev], then [16][128] K-slice partials
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > kCommitWaitNs) {
+            raise_status(status, DSPARK_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Shared memory of the commit: [r] W_1[prev] (padded to 4), [16][128] K-slice partials, and with
+// the W block map the block's W columns [r][128] bf16 (128-byte aligned for the copy) and the
+// copy's barrier.
+__host__ __device__ inline size_t commit_smem_wtile(int r) { return (size_t)(((r + 3) & ~3) + 16 * kNoiseBlock) * 4; }
+constexpr size_t kCommitTmaSlack = 128 + 16;   // alignment of the tile, then the barrier
+
+template <typename T, bool RNN>
+__global__ void __launch_bounds__(kCommitThreads)
+    draft_commit_kernel(DraftStep p, const __grid_constant__ CUtensorMap wmap, int use_wmap)
+{
+    extern __shared__ __align__(16) float sm_dyn[];
     float* erow = sm_dyn;
     float* part = sm_dyn + ((p.r + 3) & ~3);
+    unsigned char* wtile = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(sm_dyn) + commit_smem_wtile(p.r) + 127) & ~uintptr_t(127));
+    const uint32_t wbar = smem_addr(wtile + (size_t)p.r * kNoiseBlock * 2);
+    if (use_wmap && threadIdx.x == 0) {
+        mbar_init(wbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
     __shared__ float sv[kCommitThreads / 32];
     __shared__ int si[kCommitThreads / 32];
     __shared__ float lm_s[kCommitThreads / 32], ls_s[kCommitThreads / 32];
@@ -267,32 +302,38 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     const T* W = static_cast<const T*>(p.W);
     const T* U = static_cast<const T*>(p.U);
     const PhiloxKey key = make_key(p.seed);
-    const float2* st = p.stats + (size_t)q * p.nblk;
+    const float2* st = p.stats + (size_t)q * p.n_stats;
 
     // ---- phase A
     const unsigned long long pk = p.pick[(size_t)p.k * p.R + q];
     const float surv_prev = p.k == 0 ? 1.f : p.surv[o - 1];
-    const bool fast_stats = p.nblk <= kStatsPerThread * kCommitThreads;
+    const bool fast_stats = p.n_stats <= kStatsPerThread * kCommitThreads;
     float2 ms[kStatsPerThread];
     if (fast_stats) {
 #pragma unroll
         for (int u = 0; u < kStatsPerThread; ++u) {
             const int b = t + u * kCommitThreads;
-            ms[u] = b < p.nblk ? st[b] : make_float2(-INFINITY, 1.f);
+            ms[u] = b < p.n_stats ? st[b] : make_float2(-INFINITY, 0.f);
         }
     }
     const bool need_prev_row = rq.use_bias || !p.conf_token;
     constexpr bool rnn = RNN;
     // RNN head: the bias operand is the step's tanh(W_o z_k); W_1[x_{k-1}] feeds eq. (7) only
     const int prevtok = rnn ? checked_index(p.k == 0 ? p.anchor[q] : p.x_cur[q], p.V, p.status) : 0;
-    for (int i = t; i < p.r; i += kCommitThreads) {
-        float ev;
-        if (rnn)
-            ev = rq.use_bias ? p.a_rows[o * p.r + i] : 0.f;
-        else
-            ev = need_prev_row ? ld(prev_row, i) : 0.f;
-        erow[i] = ev;
-        if (!rnn && p.a_rows) p.a_rows[o * p.r + i] = ld(prev_row, i);   // Markov operand W_1[x_{k-1}]
+    // the conditioning row is loaded now and stored to shared memory after the phase-B loads are
+    // issued, so that no use of a load holds up the next one (r <= 4 * kCommitThreads here)
+    constexpr int kErowPer = 4;
+    float ev[kErowPer];
+#pragma unroll
+    for (int j = 0; j < kErowPer; ++j) {
+        const int i = t + j * kCommitThreads;
+        ev[j] = 0.f;
+        if (i < p.r) {
+            if (rnn)
+                ev[j] = rq.use_bias ? p.a_rows[o * p.r + i] : 0.f;
+            else
+                ev[j] = (need_prev_row || p.a_rows) ? ld(prev_row, i) : 0.f;
+        }
     }
     int bstar = pk == 0ull ? -1 : unpack_pick_index(pk);
     if (bstar < 0 || bstar >= p.nblk) {
@@ -302,13 +343,19 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
 
     // ---- phase B: the chosen block's W columns and U values
     const int v = bstar * kNoiseBlock + t;
-    const float u_v = (t < kNoiseBlock && v < p.V) ? ld(U, o * p.V + v) : 0.f;
     const bool fast_bias = rq.use_bias && sizeof(T) == 2 && p.V % 8 == 0 && p.r % 16 == 0 &&
                            p.r <= 16 * kBiasRows && ((reinterpret_cast<uintptr_t>(W) & 15u) == 0);
     const int cg = t & 15, ks = t >> 4;
     const int c0 = bstar * kNoiseBlock + cg * 8;
     uint4 wv[kBiasRows];
-    if (fast_bias) {
+    // With the W block map one bulk copy brings the block's [r x 128] columns into shared memory
+    // (64 KB at r = 256: more than per-thread loads keep in flight); columns past V read as zero.
+    const bool tma_w = fast_bias && use_wmap;
+    if (tma_w && t == 0) {
+        mbar_expect_tx(wbar, (uint32_t)p.r * kNoiseBlock * 2);
+        tma_load_2d(smem_addr(wtile), &wmap, bstar * kNoiseBlock, 0, wbar, l2_policy_evict_normal());
+    }
+    if (fast_bias && !tma_w) {
 #pragma unroll
         for (int j = 0; j < kBiasRows; ++j) {
             const int i = ks + 16 * j;
@@ -316,14 +363,26 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
                                           : make_uint4(0, 0, 0, 0);
         }
     }
+    // U at this thread's column of the block, kept in its own type until it is used
+    T u_raw = T(0.f);
+    if (t < kNoiseBlock && v < p.V) u_raw = U[o * p.V + v];
+#pragma unroll
+    for (int j = 0; j < kErowPer; ++j) {
+        const int i = t + j * kCommitThreads;
+        if (i < p.r) {
+            erow[i] = (rnn || need_prev_row) ? ev[j] : 0.f;
+            if (!rnn && p.a_rows) p.a_rows[o * p.r + i] = ev[j];   // Markov operand W_1[x_{k-1}]
+        }
+    }
     // log-normaliser from phase A while the phase-B loads fly
     LseAcc acc{-INFINITY, 0.f};
     if (fast_stats) {
 #pragma unroll
         for (int u = 0; u < kStatsPerThread; ++u)
-            if (t + u * kCommitThreads < p.nblk) acc = lse_add(acc, ms[u].x + log2f(ms[u].y));
+            if (ms[u].y > 0.f) acc = lse_add(acc, ms[u].x + log2f(ms[u].y));   // empty entries hold zero mass
     } else {
-        for (int b = t; b < p.nblk; b += kCommitThreads) acc = lse_add(acc, st[b].x + log2f(st[b].y));
+        for (int b = t; b < p.n_stats; b += kCommitThreads)
+            if (st[b].y > 0.f) acc = lse_add(acc, st[b].x + log2f(st[b].y));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -339,6 +398,16 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
 #pragma unroll
     for (int w = 0; w < kCommitThreads / 32; ++w) tot = lse_merge(tot, LseAcc{lm_s[w], ls_s[w]});
     float bias = 0.f;
+    bool w_ok = true;
+    if (tma_w) {
+        w_ok = commit_wait(wbar, 0u, p.status);
+        const uint4* wt = reinterpret_cast<const uint4*>(wtile);
+#pragma unroll
+        for (int j = 0; j < kBiasRows; ++j) {
+            const int i = ks + 16 * j;
+            wv[j] = (w_ok && i < p.r) ? wt[i * (kNoiseBlock / 8) + cg] : make_uint4(0, 0, 0, 0);
+        }
+    }
     if (fast_bias) {
         float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -365,7 +434,7 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
     ArgMax cand{-INFINITY, -1};
     float lv = 0.f;
     if (t < kNoiseBlock && v < p.V) {
-        lv = (u_v + bias) * invT;
+        lv = (to_f32<T>(u_raw) + bias) * invT;
         cand = ArgMax{greedy ? lv : lv + gumbel_at(key, p.round, kDraftElem, (uint32_t)q, (uint32_t)p.k, (uint32_t)v), v};
     }
     const ArgMax win = block_argmax<kCommitThreads>(cand, sv, si);
@@ -403,6 +472,8 @@ __global__ void __launch_bounds__(kCommitThreads) draft_commit_kernel(DraftStep 
         p.draft_logit[o] = s_logit;
         p.x_cur[q] = s_tok;
     }
+    // a copy whose wait gave up may still be writing shared memory: let it land before exit
+    if (tma_w && !w_ok && t == 0) (void)commit_wait(wbar, 0u, p.status);
 }
 
 // ----------------------------------------------------------------- launchers
@@ -433,26 +504,32 @@ cudaError_t launch_draft_stats_simt(const DraftStep& p, cudaStream_t s)
     return cudaGetLastError();
 }
 
-cudaError_t launch_draft_commit(const DraftStep& p, cudaStream_t s)
+template <typename T, bool RNN>
+cudaError_t launch_commit_instance(const DraftStep& p, const CUtensorMap* wmap, cudaStream_t s)
 {
-    const size_t smem = (size_t)(((p.r + 3) & ~3) + 16 * kNoiseBlock) * sizeof(float);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.R);
-    cfg.blockDim = dim3(kCommitThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const bool use = wmap != nullptr;
+    const size_t smem = commit_smem_wtile(p.r) + (use ? (size_t)p.r * kNoiseBlock * 2 + kCommitTmaSlack : 0);
+    static size_t smem_set = 0;   // the largest dynamic shared memory this instance was opened to
+    if (smem > 48 * 1024 && smem > smem_set) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(draft_commit_kernel<T, RNN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set = smem;
+    }
+    CUtensorMap none;
+    memset(&none, 0, sizeof none);
+    return launch_pdl(draft_commit_kernel<T, RNN>, dim3(p.R), dim3(kCommitThreads), smem, s, p, use ? *wmap : none,
+                      use ? 1 : 0);
+}
+
+cudaError_t launch_draft_commit(const DraftStep& p, const CUtensorMap* wmap, cudaStream_t s)
+{
     // the RNN head takes its own instance: the Markov head's commit carries none of its branches
     const bool rnn = p.head == DSPARK_HEAD_RNN;
     if (p.dtype == DSPARK_BF16)
-        return rnn ? cudaLaunchKernelEx(&cfg, draft_commit_kernel<__nv_bfloat16, true>, p)
-                   : cudaLaunchKernelEx(&cfg, draft_commit_kernel<__nv_bfloat16, false>, p);
-    return rnn ? cudaLaunchKernelEx(&cfg, draft_commit_kernel<float, true>, p)
-               : cudaLaunchKernelEx(&cfg, draft_commit_kernel<float, false>, p);
+        return rnn ? launch_commit_instance<__nv_bfloat16, true>(p, wmap, s)
+                   : launch_commit_instance<__nv_bfloat16, false>(p, wmap, s);
+    return rnn ? launch_commit_instance<float, true>(p, nullptr, s) : launch_commit_instance<float, false>(p, nullptr, s);
 }
 
 }  // namespace dspark

@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace dspark {
 namespace {
@@ -109,43 +110,6 @@ constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u
 
 // ------------------------------------------------------------------ PTX wrappers
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ unsigned long long globaltimer()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 struct Ctl {
     volatile int* abort;
     int* status;
@@ -183,48 +147,6 @@ __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity)
     }
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_first()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_normal()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar,
-                                            uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -278,8 +200,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-
-
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -299,7 +219,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
 {
@@ -643,10 +562,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint4 uv[4] = {}, tv[4] = {};
         RowMeta rm_reg{};
         bool have_next = false;   // residual: uv / tv already hold this item's columns
+        // draft: this CTA's running (max, sum) of its row over the blocks it has processed, log2
+        // units, written to stats[q][blockIdx.x] when the CTA leaves the tile (g == 0 threads)
+        float run_m = -INFINITY, run_s = 0.f;
+        uint64_t done_tiles = 0ull;   // request tiles whose rows this CTA has written
+        const auto flush_run = [&](int mt_old) {
+            const int q = mt_old * BM + m;
+            if (MODE == kDraftMode && g == 0 && q < P.R) P.d.stats[(size_t)q * P.d.n_stats + blockIdx.x] = make_float2(run_m, run_s);
+            done_tiles |= 1ull << mt_old;
+            run_m = -INFINITY;
+            run_s = 0.f;
+        };
         for (ItemIter I(i0, istep, nt_walk); I.it < n_items_cta; I.next(istep)) {
             const int tile = I.tile, b = I.b;
             const int mt = s_tiles[tile];
             if (tile != cur_tile) {
+                if (MODE == kDraftMode && cur_tile >= 0) flush_run(s_tiles[cur_tile]);
                 if (cur_tile >= 0) {
                     live = live && warp_wait(a_empty, a_par, ctl);
                     a_par ^= 1u;
@@ -848,7 +779,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float2 t = pp[gg * BM + m];
                         if (t.y > 0.f) S += t.y * ex2(t.x - M);
                     }
-                    P.d.stats[o] = make_float2(M, S);
+                    // merge the block into this CTA's running log-normaliser of the row
+                    if (M > run_m) {
+                        run_s = run_s * ex2(run_m - M) + S;
+                        run_m = M;
+                    } else {
+                        run_s += S * ex2(M - run_m);
+                    }
                     // block-level Gumbel-max of the two-level draw, folded into a packed key
                     const int q = mt * BM + m;
                     // greedy requests take the block holding the maximum
@@ -861,6 +798,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     P.v.res_stats[o] = pp[m].x + pp[BM + m].x + pp[2 * BM + m].x + pp[3 * BM + m].x;
                 }
             }
+        }
+        if (MODE == kDraftMode) {
+            // the last tile's partials, then empty ones for every other tile's rows: the commit
+            // merges all n_stats entries of a row
+            if (cur_tile >= 0) flush_run(s_tiles[cur_tile]);
+            for (int mt2 = 0; mt2 * BM < P.R; ++mt2)
+                if (!((done_tiles >> mt2) & 1ull)) flush_run(mt2);
         }
     }
     __syncwarp();
@@ -923,6 +867,17 @@ bool tc_residual_supported(int dtype, int R, int V, int r, const void* U, const 
 
 size_t tc_stats_rows(int R) { return (size_t)R; }
 
+// a multiple of the tile count (when every tile takes part, each CTA keeps one tile), at most
+// one CTA per SM
+int tc_grid(int R, int nblk)
+{
+    const int n_mt = (R + BM - 1) / BM, items = n_mt * nblk;
+    int grid = num_sms();
+    if (n_mt <= grid) grid -= grid % n_mt;
+    if (items < grid) grid = items;
+    return grid;
+}
+
 namespace {
 
 cudaError_t encode_w(CUtensorMap* m, const void* W, int V, int r)
@@ -937,6 +892,24 @@ cudaError_t encode_w(CUtensorMap* m, const void* W, int V, int r)
                ? cudaSuccess
                : cudaErrorInvalidValue;
 }
+
+}  // namespace
+
+cudaError_t encode_w_block_map(CUtensorMap* m, const void* W, int V, int r)
+{
+    if (!encode_fn() || r < 1 || r > 256 || V % 8 != 0 || !aligned16(W)) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)V, (cuuint64_t)r};
+    const cuuint64_t strides[1] = {(cuuint64_t)V * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BN, (cuuint32_t)r};
+    const cuuint32_t es[2] = {1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? cudaSuccess
+               : cudaErrorInvalidValue;
+}
+
+namespace {
 
 cudaError_t encode_u(CUtensorMap* m, const void* U, int V, int G, int R)
 {
@@ -978,11 +951,7 @@ cudaError_t launch_tc(const TcParams& P, const CUtensorMap& tmW, const CUtensorM
         if (e != cudaSuccess) return e;
         smem_set = true;
     }
-    // a multiple of the tile count (when every tile takes part, each CTA keeps one tile)
-    const int n_mt = (P.R + BM - 1) / BM, items = n_mt * P.nblk;
-    int grid = num_sms();
-    if (n_mt <= grid) grid -= grid % n_mt;
-    if (items < grid) grid = items;
+    const int grid = tc_grid(P.R, P.nblk);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(THREADS);
