@@ -158,16 +158,17 @@ def round_bytes(rnd, keep_sum: int, n_rejected: int) -> dict:
 
 def draft_stats_launch_bytes(rnd, w_every_step: bool = False) -> float:
     """Algorithmic bytes of one draft_stats launch: that step's U slice, the
-    conditioning E rows and the block statistics written, plus W counted once per
-    round (its share per step), as the round's compulsory traffic counts it. With
-    w_every_step, W is counted whole in every step instead: the L2 cannot keep a
+    conditioning E rows and the partial statistics written (one (max, sum) pair per
+    request for each of the kernel's CTAs, one per SM: 152 on GB300), plus W counted
+    once per round (its share per step), as the round's compulsory traffic counts it.
+    With w_every_step, W is counted whole in every step instead: the L2 cannot keep a
     78 MB operand between steps on this GPU (measured retention 32-48 MB)."""
     es = 2 if rnd.dtype == "bf16" else 4
     g = rnd.gamma.cpu().numpy() if rnd.gamma is not None else np.full(rnd.R, rnd.gamma_max)
     drafted = int(g.sum())
-    nblk = -(-rnd.V // 128)
+    ctas = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
     w = rnd.r * rnd.V * es
-    per_round = drafted * rnd.V * es + drafted * rnd.r * es + drafted * nblk * 8
+    per_round = drafted * rnd.V * es + drafted * rnd.r * es + rnd.R * rnd.gamma_max * ctas * 8
     return (per_round + (w * rnd.gamma_max if w_every_step else w)) / rnd.gamma_max
 
 
