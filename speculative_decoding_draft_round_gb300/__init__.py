@@ -471,10 +471,17 @@ class RoundRunner:
         self.va.round = int(rnd_index)
 
     def run(self, stream=None):
+        self.run_draft(stream)
+        self.run_verify(stream)
+
+    def run_draft(self, stream=None):
+        """The sampler and the scheduler: keep is known (on the device) when these have run."""
         s = _stream(stream)
         _call("dspark_sample_block", C.byref(self.sa), _ptr(self.sws), self.sws.numel(), s)
         _call("dspark_schedule", C.byref(self.ca), _ptr(self.cws), self.cws.numel(), s)
-        _call("dspark_verify", C.byref(self.va), _ptr(self.vws), self.vws.numel(), s)
+
+    def run_verify(self, stream=None):
+        _call("dspark_verify", C.byref(self.va), _ptr(self.vws), self.vws.numel(), _stream(stream))
 
     def check(self, stream=None) -> int:
         codes = [check(w, stream) for w in (self.sws, self.cws, self.vws)]
