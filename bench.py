@@ -196,6 +196,30 @@ def host_to_device_copier():
     return copy
 
 
+def host_to_device_copier_2d():
+    """cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, host-to-device, stream)."""
+    import ctypes
+    rt = None
+    for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            continue
+    if rt is None:
+        raise RuntimeError("the CUDA runtime library is not loadable")
+    fn = rt.cudaMemcpy2DAsync
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_size_t,
+                   ctypes.c_int, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+
+    def copy(dst, dpitch, src, spitch, width, height, stream):
+        rc = fn(dst, dpitch, src, spitch, width, height, 1, stream)
+        if rc:
+            raise RuntimeError("cudaMemcpy2DAsync failed (%d)" % rc)
+    return copy
+
+
 def kernel_hash(files) -> str:
     h = hashlib.sha1()
     for f in files:
@@ -435,10 +459,17 @@ def bench_ours(args):
     n_rej = int(res["resampled"].to(torch.int32).sum())
 
     # end to end through the public API: per-round inputs copied from pinned host memory,
-    # results read back, every step. The target logits are copied after the scheduler, and only
-    # the rows verification reads (rows 0..keep[r] of each request: what the target model would
-    # have scored), one copy per request; the host reads keep back to know them.
-    host_in = {k: getattr(rnd, k).cpu().pin_memory() for k in ("U", "h", "temperature", "anchor", "sps")}
+    # results read back, every step. U is copied one position at a time on a second stream and
+    # the sampler's step k waits for its slice (step_ready events), so the draft steps run under
+    # the copy. The target logits are copied after the scheduler, and only the rows verification
+    # reads (rows 0..keep[r] of each request: what the target model would have scored), one copy
+    # per request; the host reads keep back to know them.
+    host_in = {k: getattr(rnd, k).cpu().pin_memory() for k in ("h", "temperature", "anchor", "sps")}
+    U_h = rnd.U.cpu().pin_memory()
+    copy_stream = torch.cuda.Stream()
+    slice_ready = [torch.cuda.Event() for _ in range(rnd.gamma_max)]
+    es_u = rnd.U.element_size()
+    memcpy_2d = host_to_device_copier_2d()
     if rnd.gamma is not None:
         host_in["gamma"] = rnd.gamma.cpu().pin_memory()
     dev_in = {k: getattr(rnd, k) for k in host_in}
@@ -446,7 +477,7 @@ def bench_ours(args):
     keep_h = torch.empty(rnd.R, dtype=torch.int32).pin_memory()
     outs = [res["tokens"], res["keep"], res["accepted"], res["next_token"], res["stats"]]
     host_out = [o.cpu().pin_memory() for o in outs]
-    h2d_fixed = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d_fixed = sum(t.numel() * t.element_size() for t in host_in.values()) + U_h.numel() * es_u
     d2h = sum(t.numel() * t.element_size() for t in host_out) + keep_h.numel() * 4
     row_bytes = rnd.V * rnd.target.element_size()
     req_bytes = (rnd.gamma_max + 1) * row_bytes
@@ -460,8 +491,15 @@ def bench_ours(args):
         e_starts[s].record(stream)
         for k, t in host_in.items():
             dev_in[k].copy_(t, non_blocking=True)
+        # U[:, k, :] for every request: R rows of V elements, G*V apart, on the copy stream
+        copy_stream.wait_stream(stream)
+        for k in range(rnd.gamma_max):
+            memcpy_2d(rnd.U.data_ptr() + k * rnd.V * es_u, rnd.gamma_max * rnd.V * es_u,
+                      U_h.data_ptr() + k * rnd.V * es_u, rnd.gamma_max * rnd.V * es_u, rnd.V * es_u, rnd.R,
+                      copy_stream.cuda_stream)
+            slice_ready[k].record(copy_stream)
         runner.set_round(5000 + s)
-        runner.run_draft()
+        runner.run_draft(step_ready=slice_ready)
         keep_h.copy_(res["keep"], non_blocking=True)
         stream.synchronize()
         for q, kq in enumerate(keep_h.tolist()):
@@ -519,7 +557,8 @@ def bench_ours(args):
                            "bias_gemm_tflops": 2.0 * rnd.r * rnd.V * drafted / round_s / 1e12,
                            "breakdown": rb},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": n_e2e, "note": "per-round inputs (U, h, T, anchor, SPS) copied in before the round, the "
+                "steps": n_e2e, "note": "per-round inputs copied in: h, T, anchor, SPS before the round, U one position at a "
+                                        "time on a second stream with the sampler's step k waiting for its slice, the "
                                         "target rows verification reads (rows 0..keep[r], after keep is read back) "
                                         "copied in after the scheduler, results copied out; E, W, w_h, w_e stay "
                                         "resident"},

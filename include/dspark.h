@@ -143,6 +143,9 @@ typedef struct {
     int32_t head;             /* DSPARK_HEAD_MARKOV or DSPARK_HEAD_RNN */
     const void* W_rnn;        /* [3r][2r+d] (dtype of E): rows W_g, W_c, W_o (RNN head only) */
     float* a_rows;            /* out [R][gamma_max][r] bias operand of each step, or NULL */
+    const void* const* step_ready; /* [gamma_max] cudaEvent_t (host array), or NULL: step k's kernels
+                                      wait for step_ready[k] (NULL entries: no wait), so that U[:, k, :]
+                                      may still be arriving when the call is made */
 } dspark_sample_args;
 
 dspark_status dspark_sample_workspace_size(const dspark_sample_args* args, size_t* bytes);

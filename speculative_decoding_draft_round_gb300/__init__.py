@@ -44,7 +44,7 @@ class SampleArgs(C.Structure):
         ("b", C.c_float), ("temperature", _vp), ("anchor", _vp),
         ("seed", C.c_uint64), ("round", C.c_uint64),
         ("tokens", _vp), ("conf", _vp), ("surv", _vp), ("draft_lse", _vp), ("draft_logit", _vp),
-        ("sts_temp", _vp), ("head", C.c_int32), ("W_rnn", _vp), ("a_rows", _vp),
+        ("sts_temp", _vp), ("head", C.c_int32), ("W_rnn", _vp), ("a_rows", _vp), ("step_ready", _vp),
     ]
 
 
@@ -474,10 +474,18 @@ class RoundRunner:
         self.run_draft(stream)
         self.run_verify(stream)
 
-    def run_draft(self, stream=None):
-        """The sampler and the scheduler: keep is known (on the device) when these have run."""
+    def run_draft(self, stream=None, step_ready=None):
+        """The sampler and the scheduler: keep is known (on the device) when these have run.
+        step_ready: optional list of gamma_max torch.cuda.Event; step k's kernels wait for
+        step_ready[k] (for inputs still being copied in)."""
         s = _stream(stream)
-        _call("dspark_sample_block", C.byref(self.sa), _ptr(self.sws), self.sws.numel(), s)
+        if step_ready is not None:
+            handles = (C.c_void_p * len(step_ready))(*[ev.cuda_event for ev in step_ready])
+            self.sa.step_ready = C.cast(handles, C.c_void_p)
+        try:
+            _call("dspark_sample_block", C.byref(self.sa), _ptr(self.sws), self.sws.numel(), s)
+        finally:
+            self.sa.step_ready = None
         _call("dspark_schedule", C.byref(self.ca), _ptr(self.cws), self.cws.numel(), s)
 
     def run_verify(self, stream=None):

@@ -304,6 +304,14 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
                           encode_w_block_map(&wmap, a->W, a->V, a->r) == cudaSuccess;
     for (int k = 0; k < a->gamma_max && e == cudaSuccess; ++k) {
         p.k = k;
+        // the caller may still be delivering this step's inputs (U[:, k, :]): wait for its event
+        if (a->step_ready && a->step_ready[k]) {
+            e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(const_cast<void*>(a->step_ready[k])), 0);
+            if (e != cudaSuccess) {
+                snprintf(g_last_error, sizeof g_last_error, "step_ready[%d]: %s", k, cudaGetErrorName(e));
+                break;
+            }
+        }
         if (rnn) e = launch(DSPARK_KERNEL_RNN_STEP, s, [&] { return launch_rnn_step(p, s); });
         if (e == cudaSuccess)
             e = launch(DSPARK_KERNEL_DRAFT_STATS, s,

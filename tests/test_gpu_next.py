@@ -261,3 +261,25 @@ def test_static_entry_refuses_the_rnn_head():
         ds.sample_block_static(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
                                rnd.seed, rnd.round, gamma=rnd.gamma, head=ds.HEAD_RNN, W_rnn=W_rnn)
     assert err.value.code == 2
+
+
+def test_step_ready_events_keep_the_results():
+    # the sampler waits on per-step events (inputs still arriving); the draws do not change
+    rnd, _ = _rnn_round(RNN_SPECS[1], 44)
+    runner = ds.RoundRunner(rnd)
+    runner.set_round(3)
+    runner.run()
+    torch.cuda.synchronize()
+    ref = {k: v.clone() for k, v in runner.results().items() if torch.is_tensor(v)}
+    side = torch.cuda.Stream()
+    events = [torch.cuda.Event() for _ in range(rnd.gamma_max)]
+    side.wait_stream(torch.cuda.current_stream())
+    for ev in events:
+        ev.record(side)
+    runner.run_draft(step_ready=events)
+    runner.run_verify()
+    torch.cuda.synchronize()
+    assert runner.check() == 0
+    got = runner.results()
+    for k in ("tokens", "conf", "surv", "keep", "accepted", "next_token"):
+        assert torch.equal(got[k], ref[k]), k
