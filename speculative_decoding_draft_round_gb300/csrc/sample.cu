@@ -8,13 +8,15 @@
 //   c_k = sigmoid(w_h . h_k + w_e . W_1[x] + b), a_k = a_{k-1} c_k.
 // The step runs as two launches:
 //   draft_stats   -- per (request, 128-wide vocabulary block): the bias
-//                    contraction, then (max, sum exp2) of l_k over the block.
-//                    The V-wide bias never reaches global memory.
-//   draft_commit  -- per request: block-level Gumbel-max over the block
-//                    log-masses, element-level Gumbel-max inside the winning
-//                    block (its 128 logits recomputed), log-normaliser,
-//                    confidence and survival; x_k becomes the next step's
-//                    previous token.
+//                    contraction, then (max, sum exp2) of l_k over the block and
+//                    the block's key of the two-level Gumbel-max, folded into one
+//                    packed atomicMax per request. The V-wide bias never reaches
+//                    global memory. (CUDA-core version here; tensor-core version in
+//                    sample_tc.cu.)
+//   draft_commit  -- per request: the winning block, the element-level Gumbel-max
+//                    inside it (its 128 logits recomputed from W's block columns),
+//                    the log-normaliser from the statistics, confidence and
+//                    survival; x_k becomes the next step's previous token.
 // w_h . h_k does not depend on the draws, so conf_hidden computes it for every
 // (request, position) in one pass before the serial loop.
 #include <string.h>

@@ -1,30 +1,34 @@
-// sample_tc.cu -- the per-step bias contraction of the draft sampler on the
-// 5th-generation tensor cores (tcgen05 + TMEM + TMA), with the softmax
-// statistics fused into the epilogue.
+// sample_tc.cu -- the per-step bias contraction of the draft sampler, and the residual
+// recompute of verification, on the 5th-generation tensor cores (tcgen05 + TMEM + TMA),
+// with the softmax statistics fused into the epilogue.
 //
-// For draft step k of "DSpark" (Markov head, zhongzhuzhou.org notes eq. 4-5;
-// caijizhuo.github.io section 4 step 3), every request tile of 128 rows and
-// every 128-wide vocabulary block b:
-//   D[m][n]  = sum_i W_1[x_{k-1}(m)][i] * W_2[i][b*128 + n]        (bf16 x bf16 -> fp32 in TMEM)
+// Draft mode, for step k of "DSpark" (Markov head, zhongzhuzhou.org notes eq. 4-5;
+// caijizhuo.github.io section 4 step 3), every request tile of 128 rows and every 128-wide
+// vocabulary block b (one item):
+//   D[m][n]  = sum_i A[m][i] * W_2[i][b*128 + n]      A = W_1[x_{k-1}(m)] (bf16 x bf16 -> fp32 in TMEM)
 //   x[m][n]  = (U[m][k][b*128 + n] + D[m][n]) * log2(e) / T_m
-//   stats[m][b] = (max_n x, sum_n 2^(x - max))                       (log2 units)
+//   block b: (max_n x, sum_n 2^(x - max)) (log2 units) -> the block key of the two-level draw
+//            (packed 64-bit atomicMax per request) and the CTA's running (max, sum) of the row,
+//            written once per CTA as its partial log-normaliser.
+// Residual mode (verification, rejected requests packed into tiles): the same contraction at
+// the rejected position and per block sum_n max(0, p_t(n) - p_d(n)).
 // The V-wide bias lives only in TMEM; it never reaches global memory.
 //
-// Layout and roles (one persistent CTA per SM, 640 threads):
-//   warp 0      TMA producer of W tiles: per item 4 K-chunks of [64 K x 128 N]
-//               bf16, two 64-column boxes each, 128-byte swizzle (MN-major B).
-//   warp 1      TMEM allocator (512 columns = 4 accumulators of 128 x 128 fp32)
-//               and the single MMA-issuing thread (tcgen05.mma kind::f16,
-//               M=128, N=128, K=16 per instruction, cta_group::1).
-//   warp 3      TMA producer of U tiles: [128 requests x 128 columns] per item
-//               via a 3-D map (V, gamma, R), evict-first L2 policy.
-//   warps 4-19  epilogue: four warpgroups, each owns 32 of the 128 accumulator
-//               columns; a thread owns one request row (TMEM lane). They also
-//               gather the A operand (rows W_1[x_{k-1}] of the tile's requests)
-//               into shared memory in the 128-byte-swizzled K-major layout.
-// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
-// DSPARK_ERR_TIMEOUT, stops issuing work, waits (bounded) for its own TMA copies
-// and frees its TMEM.
+// Layout and roles (one persistent CTA per SM, 640 threads; items dealt round-robin in
+// block-major order):
+//   warp 0      TMA producer of W tiles: per item 4 K-chunks of [64 K x 128 N] bf16, two
+//               64-column boxes each, 128-byte swizzle (MN-major B).
+//   warp 1      TMEM allocator (512 columns: 3 accumulators of 128 x 128 fp32 and an A region)
+//               and the single MMA-issuing thread (tcgen05.mma kind::f16, M=128, N=128, K=16
+//               per instruction, cta_group::1).
+//   warp 3      draft: TMA producer of U tiles [128 requests x 128 columns] via a 3-D map
+//               (V, gamma, R), evict-first L2 policy.
+//   warps 4-19  epilogue: four warpgroups, each owns 32 of the 128 accumulator columns; a
+//               thread owns one request row (TMEM lane). Draft: the A tile arrives by TMA from
+//               one of eight copies of the rows (K-major, 128-byte swizzle, shared memory).
+//               Residual: the threads write A into TMEM and load their own U and target columns.
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records DSPARK_ERR_TIMEOUT,
+// stops issuing work, waits (bounded) for its own TMA copies and frees its TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
