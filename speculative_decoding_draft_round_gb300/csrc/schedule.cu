@@ -11,11 +11,16 @@
 //   async  K  = full-scan count over the survivals two rounds old,
 //          m* = min(K, |pool|) over the current ranking.
 // GB300 mapping: up to 8192 slots live in shared memory, spread over all 32
-// warps. A positive float's bit pattern orders like an unsigned integer, so the
-// sort is a stable LSD radix sort (four 8-bit digits, warp-aggregated ranks via
-// __match_any_sync, digit offsets from one block-wide scan of the [digit][warp]
-// counts) of the complemented bits; stability in slot order gives the (r, j)
-// tie-break for free. Prefix sums are exact 64-bit fixed-point sums (a in units
+// warps. A positive float's bit pattern orders like an unsigned integer, so keys
+// are the complemented bits. When every request's keys are already in order (the
+// sampler's survivals are running products of confidences) the R runs are merged
+// pairwise on merge paths; any other input takes a stable LSD radix sort (four
+// 8-bit digits, warp-aggregated ranks via __match_any_sync, digit offsets from one
+// block-wide scan of the [digit][warp] counts); stability in slot order gives the
+// (r, j) tie-break for free. Sync mode with a table that forces the first decrease
+// within 64 admissions (a staircase edge) takes only the top 64 keys, selected
+// by bitonic networks in registers, instead of sorting the whole pool.
+// Prefix sums are exact 64-bit fixed-point sums (a in units
 // of 2^-48), so they do not depend on the summation order, and every Theta
 // comparison is exact: tau * 2^48 is an integer below 2^62 and SPS(B) a float,
 // so Theta is compared through the 128-bit product of the integer and the
@@ -35,6 +40,8 @@ struct ThetaKey {
     unsigned long long m;
 };
 
+constexpr int kTopMax = 64;      // sync mode: the latest forced first decrease that takes the top-keys path
+
 constexpr int kDigits = 256;
 constexpr int kHist = kDigits * kSchedWarps;                  // [digit][warp] counts
 
@@ -53,6 +60,14 @@ struct SchedSmem {
     int wbest_m[kSchedWarps];
     int n_pool;
     int first_bad;
+    // sync mode, top-keys path
+    unsigned long long tlist[kSchedWarps][kTopMax];   // per-warp top lists, (key << 32) | slot ascending
+    float tsps[kTopMax + 1];                           // SPS(R + m), m = 0 .. kTopMax
+    unsigned long long s_star;                         // fixed-point sum of the admitted a's
+    int m_bound;   // first m at which the throughput table forces Theta down
+    // the table entries SPS(R + m) of each thread's scan positions m = tid*ni + u, read before the
+    // dependency wait; kept here, not in registers, so that no out-of-line call has to save them
+    float sv[kMaxItems + 1][kSchedThreads];
 };
 
 size_t schedule_smem_bytes() { return sizeof(SchedSmem); }
@@ -69,8 +84,10 @@ __device__ __forceinline__ uint32_t lanemask_lt()
 __device__ __forceinline__ int striped(int warp, int it, int lane, int ni) { return (warp * ni + it) * 32 + lane; }
 
 // Load the pool keys of `src` ([R][G] survivals) into key[0]/val[0]; returns |pool|. Every load
-// of a thread is issued before any is used.
-__device__ __noinline__ int load_pool(SchedSmem& sm, const ScheduleParams& p, const float* src, int n_slots, int ni)
+// of a thread is issued before any is used. (Scalar arguments: a reference to the kernel's
+// parameter block would put a copy of it in local memory.)
+__device__ __noinline__ int load_pool(SchedSmem& sm, const int32_t* gamma, int G, int* status, const float* src,
+                                      int n_slots, int ni)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) sm.n_pool = 0;
@@ -81,7 +98,7 @@ __device__ __noinline__ int load_pool(SchedSmem& sm, const ScheduleParams& p, co
         const int s = striped(warp, it, lane, ni);
         const bool in = it < ni && s < n_slots;
         a[it] = in ? src[s] : 0.f;
-        g[it] = in ? (p.gamma ? p.gamma[s / p.G] : p.G) : 0;
+        g[it] = in ? (gamma ? gamma[s / G] : G) : 0;
     }
     int cnt = 0;
 #pragma unroll
@@ -91,14 +108,14 @@ __device__ __noinline__ int load_pool(SchedSmem& sm, const ScheduleParams& p, co
         uint32_t key = 0xFFFFFFFFu;
         if (s < n_slots) {
             int gg = g[it];
-            if (gg < 0 || gg > p.G) {
-                raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
-                gg = gg < 0 ? 0 : p.G;
+            if (gg < 0 || gg > G) {
+                raise_status(status, DSPARK_ERR_DEVICE_INPUT);
+                gg = gg < 0 ? 0 : G;
             }
             float av = a[it];
-            if (s % p.G < gg && av > 0.f) {   // NaN and non-positive survivals are not in the pool
+            if (s % G < gg && av > 0.f) {   // NaN and non-positive survivals are not in the pool
                 if (!(av <= 1.f)) {
-                    raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+                    raise_status(status, DSPARK_ERR_DEVICE_INPUT);
                     av = 1.f;
                 }
                 key = ~__float_as_uint(av);
@@ -265,16 +282,22 @@ __device__ __noinline__ void merge_level(SchedSmem& sm, int in, int n, int L, in
     }
 }
 
-// Sort key[0]/val[0] ascending (a descending, then slot); result in buffer 0. When every
-// request's G slots are already in order -- the sampler's survivals are running products of
-// confidences below one, so they never increase along a request -- the R runs are merged
-// pairwise (log2 R levels); any other input takes the stable LSD radix sort.
-__device__ __noinline__ void sort_pool(SchedSmem& sm, int n, int G, int ni)
+// Are every request's G keys in order? The sampler's survivals are running products of
+// confidences below one, so they never increase along a request.
+__device__ __noinline__ bool runs_sorted(SchedSmem& sm, int n, int G)
 {
     bool unsorted = false;
     for (int s = threadIdx.x; s < n; s += kSchedThreads)
         if (s % G != G - 1 && s + 1 < n && sm.key[0][sk(s + 1)] < sm.key[0][sk(s)]) unsorted = true;
-    if (__syncthreads_or(unsorted)) {
+    return !__syncthreads_or(unsorted);
+}
+
+// Sort key[0]/val[0] ascending (a descending, then slot); result in buffer 0. When the R runs of
+// G keys are in order they are merged pairwise (log2 R levels); any other input takes the
+// stable LSD radix sort.
+__device__ __noinline__ void sort_pool(SchedSmem& sm, int n, int G, int ni)
+{
+    if (!runs_sorted(sm, n, G)) {
         radix_pass(sm, 0, 0, ni);
         radix_pass(sm, 1, 8, ni);
         radix_pass(sm, 0, 16, ni);
@@ -344,7 +367,7 @@ __device__ __forceinline__ double theta_of(int R, int m, unsigned long long S, c
 
 // Inclusive prefix sums S (sorted index tid * ni + it) of the fixed-point a's, and the exclusive
 // prefix of the thread's first index.
-__device__ __noinline__ void prefix_sums(SchedSmem& sm, int n, int ni, unsigned long long (&S)[kMaxItems], unsigned long long& excl)
+__device__ __forceinline__ void prefix_sums(SchedSmem& sm, int n, int ni, unsigned long long (&S)[kMaxItems], unsigned long long& excl)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     unsigned long long run = 0;
@@ -380,9 +403,9 @@ __device__ __noinline__ void prefix_sums(SchedSmem& sm, int n, int ni, unsigned 
 }
 
 // Smallest arg-max of Theta_m over m = 0..n (full scan), from the prefix sums.
-__device__ __noinline__ int full_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, const unsigned long long (&S)[kMaxItems],
-                         const float (&sv)[kMaxItems + 1])
+__device__ __forceinline__ int full_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, const unsigned long long (&S)[kMaxItems])
 {
+    const float* sv = &sm.sv[0][threadIdx.x];   // sv[u * kSchedThreads]: SPS at position tid*ni + u
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     ThetaKey best{INT32_MIN, 0ull};
     int bm = INT32_MAX;
@@ -394,7 +417,7 @@ __device__ __noinline__ int full_scan(SchedSmem& sm, const ScheduleParams& p, in
     for (int it = 0; it < kMaxItems; ++it) {
         const int i = tid * ni + it;
         if (it < ni && i < n) {
-            const ThetaKey th = theta_key(p.R, S[it], sv[it + 1], p.status);
+            const ThetaKey th = theta_key(p.R, S[it], sv[(it + 1) * kSchedThreads], p.status);
             if (key_gt(th, best) || bm == INT32_MAX) {
                 best = th;
                 bm = i + 1;
@@ -430,9 +453,10 @@ __device__ __noinline__ int full_scan(SchedSmem& sm, const ScheduleParams& p, in
 }
 
 // First m >= 1 with Theta_m <= Theta_{m-1}, minus one (|pool| if none).
-__device__ __noinline__ int sync_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, const unsigned long long (&S)[kMaxItems],
-                         unsigned long long excl, const float (&sv)[kMaxItems + 1])
+__device__ __forceinline__ int sync_scan(SchedSmem& sm, const ScheduleParams& p, int n, int ni, const unsigned long long (&S)[kMaxItems],
+                         unsigned long long excl)
 {
+    const float* sv = &sm.sv[0][threadIdx.x];   // sv[u * kSchedThreads]: SPS at position tid*ni + u
     const int tid = threadIdx.x;
     if (tid == 0) sm.first_bad = INT32_MAX;
     __syncthreads();
@@ -443,7 +467,7 @@ __device__ __noinline__ int sync_scan(SchedSmem& sm, const ScheduleParams& p, in
         for (int it = 0; it < kMaxItems; ++it) {
             const int i = tid * ni + it;
             if (it < ni && i < n) {
-                const ThetaKey th = theta_key(p.R, S[it], sv[it + 1], p.status);
+                const ThetaKey th = theta_key(p.R, S[it], sv[(it + 1) * kSchedThreads], p.status);
                 if (!key_gt(th, prev) && bad == INT32_MAX) bad = i + 1;
                 prev = th;
             }
@@ -455,6 +479,138 @@ __device__ __noinline__ int sync_scan(SchedSmem& sm, const ScheduleParams& p, in
     const int fb = sm.first_bad;
     __syncthreads();
     return fb == INT32_MAX ? n : fb - 1;
+}
+
+// ---- sync mode, top-keys path
+// Admitting an m-th key adds a <= 1 to tau >= R, so Theta_m <= Theta_{m-1} whatever the keys are
+// once SPS(R + m - 1) * R >= SPS(R + m) * (R + 1). With M the first such m (the table is an input,
+// so M is known before the dependency wait) the first decrease comes at m <= M, and only the top M
+// keys decide m*. For M <= kTopMax the kernel takes the kTopMax smallest (key, slot) pairs with
+// bitonic networks in registers -- no sort of the whole pool -- and scans Theta over them in one
+// warp. A lane holds elements `lane` and `lane + 32` of a 64-element list in x0 and x1.
+
+__device__ __forceinline__ unsigned long long packed_key(const SchedSmem& sm, int i, int n)
+{
+    return i < n ? ((unsigned long long)sm.key[0][sk(i)] << 32) | sm.val[0][sk(i)] : ~0ull;
+}
+
+// compare-exchange of element i with element i ^ j (j < 32, another lane), in the direction of
+// i's block of size k (ascending when i & k == 0)
+__device__ __forceinline__ unsigned long long cmp_x(unsigned long long x, int i, int j, int k)
+{
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, x, j);
+    return (((i & k) == 0) == ((i & j) == 0)) ? min(x, o) : max(x, o);
+}
+
+// sort 64 values ascending
+__device__ __forceinline__ void bitonic_sort64(unsigned long long& x0, unsigned long long& x1, int lane)
+{
+#pragma unroll
+    for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j == 32) {   // k == 64: the partner is this lane's other element, ascending
+                const unsigned long long lo = min(x0, x1), hi = max(x0, x1);
+                x0 = lo;
+                x1 = hi;
+            } else {
+                x0 = cmp_x(x0, lane, j, k);
+                x1 = cmp_x(x1, lane + 32, j, k);
+            }
+        }
+    }
+}
+
+// (x0, x1) = the 64 smallest of two ascending lists (x0, x1) and (y0, y1), ascending:
+// min(A_i, B_{63-i}) is a bitonic sequence that holds them, then a bitonic merge sorts it
+__device__ __forceinline__ void merge_top64(unsigned long long& x0, unsigned long long& x1, unsigned long long y0,
+                                            unsigned long long y1, int lane)
+{
+    x0 = min(x0, __shfl_sync(0xffffffffu, y1, 31 - lane));   // B_{63 - lane}
+    x1 = min(x1, __shfl_sync(0xffffffffu, y0, 31 - lane));   // B_{31 - lane}
+    const unsigned long long lo = min(x0, x1), hi = max(x0, x1);
+    x0 = lo;
+    x1 = hi;
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+        x0 = cmp_x(x0, lane, j, 64);
+        x1 = cmp_x(x1, lane + 32, j, 64);
+    }
+}
+
+// m* of the sync scan from the top keys of buffer 0 (n_slots positions, n of them in the pool):
+// every warp sorts 64-position chunks and folds them into its own top list, the 32 lists are
+// merged pairwise in five levels, and warp 0 scans Theta over the first min(kTopMax, n). Returns
+// m* to every thread, with the admitted keys' slots at val[0] positions 0 .. m*-1 and their
+// fixed-point sum in s_star; -1 (buffers untouched) when those keys showed no decrease and the pool
+// holds more, so that the full sort decides.
+__device__ __noinline__ int top_scan(SchedSmem& sm, int R, int* status, int n_slots, int n)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned long long x0 = ~0ull, x1 = ~0ull;
+    for (int c = warp * 64; c < n_slots; c += kSchedWarps * 64) {
+        unsigned long long y0 = packed_key(sm, c + lane, n_slots), y1 = packed_key(sm, c + 32 + lane, n_slots);
+        bitonic_sort64(y0, y1, lane);
+        merge_top64(x0, x1, y0, y1, lane);
+    }
+    sm.tlist[warp][lane] = x0;
+    sm.tlist[warp][lane + 32] = x1;
+    __syncthreads();
+    for (int w = kSchedWarps / 2; w >= 1; w >>= 1) {
+        if (warp < w) {
+            merge_top64(x0, x1, sm.tlist[warp + w][lane], sm.tlist[warp + w][lane + 32], lane);
+            sm.tlist[warp][lane] = x0;
+            sm.tlist[warp][lane + 32] = x1;
+        }
+        __syncthreads();
+    }
+    if (warp == 0) {
+        const int nt = min(kTopMax, n);   // pool keys sort before every other position
+        const unsigned long long f0 = lane < nt ? fixed48((uint32_t)(x0 >> 32)) : 0ull;
+        const unsigned long long f1 = lane + 32 < nt ? fixed48((uint32_t)(x1 >> 32)) : 0ull;
+        unsigned long long s0 = f0, s1 = f1;   // inclusive prefix sums over positions lane, lane + 32
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y0 = __shfl_up_sync(0xffffffffu, s0, o), y1 = __shfl_up_sync(0xffffffffu, s1, o);
+            if (lane >= o) {
+                s0 += y0;
+                s1 += y1;
+            }
+        }
+        s1 += __shfl_sync(0xffffffffu, s0, 31);
+        const ThetaKey big{INT32_MAX, ~0ull};
+        const ThetaKey t0 = lane < nt ? theta_key(R, s0, sm.tsps[lane + 1], status) : big;
+        const ThetaKey t1 = lane + 32 < nt ? theta_key(R, s1, sm.tsps[lane + 33], status) : big;
+        ThetaKey p0{__shfl_up_sync(0xffffffffu, t0.e, 1), __shfl_up_sync(0xffffffffu, t0.m, 1)};
+        ThetaKey p1{__shfl_up_sync(0xffffffffu, t1.e, 1), __shfl_up_sync(0xffffffffu, t1.m, 1)};
+        const ThetaKey t0_last{__shfl_sync(0xffffffffu, t0.e, 31), __shfl_sync(0xffffffffu, t0.m, 31)};
+        if (lane == 0) {
+            p0 = theta_key(R, 0ull, sm.tsps[0], status);
+            p1 = t0_last;
+        }
+        const uint32_t b0 = __ballot_sync(0xffffffffu, lane < nt && !key_gt(t0, p0));
+        const uint32_t b1 = __ballot_sync(0xffffffffu, lane + 32 < nt && !key_gt(t1, p1));
+        // first position whose key does not raise Theta: m* keys come before it
+        int m_star = b0 ? __ffs(b0) - 1 : b1 ? 32 + __ffs(b1) - 1 : (nt == n ? n : -1);
+        unsigned long long s_star = 0ull;
+        if (m_star >= 0) {
+            // exclusive prefix at position m* (the sum of all nt keys when m* = nt)
+            const unsigned long long e0 = __shfl_sync(0xffffffffu, s0 - f0, m_star & 31);
+            const unsigned long long e1 = __shfl_sync(0xffffffffu, s1 - f1, m_star & 31);
+            const unsigned long long tot = __shfl_sync(0xffffffffu, s1, 31);
+            s_star = m_star == nt ? (nt > 32 ? tot : __shfl_sync(0xffffffffu, s0, 31)) : (m_star < 32 ? e0 : e1);
+            if (lane < m_star) sm.val[0][sk(lane)] = (uint16_t)(x0 & 0xFFFFu);
+            if (lane + 32 < m_star) sm.val[0][sk(lane + 32)] = (uint16_t)(x1 & 0xFFFFu);
+        }
+        if (lane == 0) {
+            sm.first_bad = m_star;
+            sm.s_star = s_star;
+        }
+    }
+    __syncthreads();
+    const int m = sm.first_bad;
+    __syncthreads();
+    return m;
 }
 
 // Static confidence threshold: every pool candidate with a_{r,j} >= threshold, no sort and no
@@ -524,11 +680,23 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedulePara
     // The throughput-table entries of this thread's scan positions, SPS(R + m) for
     // m = tid*ni .. tid*ni + ni (index R + m - 1; n_sps >= R (1 + G) covers every m <= R G). The
     // table is an input: it is read before the dependency wait, so the scans never wait on memory.
-    float sv[kMaxItems + 1];
 #pragma unroll
     for (int u = 0; u <= kMaxItems; ++u) {
         const int m = (int)threadIdx.x * ni + u;
-        sv[u] = (u <= ni && m <= n_slots && p.R + m >= 1) ? p.sps[p.R + m - 1] : 0.f;
+        sm.sv[u][threadIdx.x] = (u <= ni && m <= n_slots && p.R + m >= 1) ? p.sps[p.R + m - 1] : 0.f;
+    }
+    // sync mode: the table's first forced decrease and its first entries (see top_scan); the table
+    // is an input like the entries above
+    const bool sync_mode = p.mode == DSPARK_SCHED_SYNC;
+    if (sync_mode) {
+        if (threadIdx.x == 0) sm.m_bound = INT32_MAX;
+        __syncthreads();
+        const int t = threadIdx.x, m = t + 1;
+        if (t <= kTopMax && t <= n_slots) sm.tsps[t] = p.sps[p.R + t - 1];
+        if (m <= kTopMax && m <= n_slots) {
+            const double lo = p.sps[p.R + m - 2], hi = p.sps[p.R + m - 1];   // exact products in double
+            if (hi > 0.0 && lo * p.R >= hi * (p.R + 1.0)) atomicMin(&sm.m_bound, m);
+        }
     }
     pdl_enter();   // the survivals come from the sampler's last commit
     if (p.mode == DSPARK_SCHED_THRESHOLD) {
@@ -539,40 +707,64 @@ __global__ void __launch_bounds__(kSchedThreads, 1) schedule_kernel(SchedulePara
     unsigned long long S[kMaxItems], excl;
     int capacity = -1;
     if (p.mode == DSPARK_SCHED_ASYNC_CAPACITY) {
-        const int n_old = load_pool(sm, p, p.surv_capacity, n_slots, ni);
+        const int n_old = load_pool(sm, p.gamma, p.G, p.status, p.surv_capacity, n_slots, ni);
         sort_pool(sm, n_slots, p.G, ni);
         prefix_sums(sm, n_old, ni, S, excl);
-        capacity = full_scan(sm, p, n_old, ni, S, sv);
+        capacity = full_scan(sm, p, n_old, ni, S);
     }
-    const int n = load_pool(sm, p, p.surv, n_slots, ni);
-    sort_pool(sm, n_slots, p.G, ni);
-    prefix_sums(sm, n, ni, S, excl);
-    int m_star;
-    if (p.mode == DSPARK_SCHED_SYNC)
-        m_star = sync_scan(sm, p, n, ni, S, excl, sv);
-    else if (p.mode == DSPARK_SCHED_FULL_SCAN)
-        m_star = full_scan(sm, p, n, ni, S, sv);
-    else
-        m_star = min(capacity, n);
+    const int n = load_pool(sm, p.gamma, p.G, p.status, p.surv, n_slots, ni);
+    int m_star = -1;
+    bool top = false;
+    if (sync_mode && sm.m_bound <= kTopMax) {
+        // the whole scan reads every table entry up to |pool|: flag a bad one the same way
+#pragma unroll
+        for (int u = 0; u <= kMaxItems; ++u) {
+            const int m = (int)threadIdx.x * ni + u;
+            const float v = sm.sv[u][threadIdx.x];
+            if (u <= ni && m <= n && !(v > 0.f && v != INFINITY)) raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+        }
+        m_star = top_scan(sm, p.R, p.status, n_slots, n);
+        top = m_star >= 0;
+    }
+    if (m_star < 0) {
+        sort_pool(sm, n_slots, p.G, ni);
+        prefix_sums(sm, n, ni, S, excl);
+        if (p.mode == DSPARK_SCHED_SYNC)
+            m_star = sync_scan(sm, p, n, ni, S, excl);
+        else if (p.mode == DSPARK_SCHED_FULL_SCAN)
+            m_star = full_scan(sm, p, n, ni, S);
+        else
+            m_star = min(capacity, n);
+    }
 
-    // keep[r] = l_r, the largest admitted position of request r (Algorithm 1 sets l_r = j on
-    // each admission); with survivals non-increasing in j it is also the admitted count
+    // keep[r] = l_r. Algorithm 1 sets l_r = j at each admission in sorted order, so in the sync and
+    // full-scan modes l_r is the position of r's last admitted key (packed behind its sorted index,
+    // so the largest index wins); the asynchronous mode fills its capacity with r's largest admitted
+    // position. With survivals non-increasing in j both are r's admitted count.
     uint32_t* cnt = sm.hist;
     for (int q = threadIdx.x; q < p.R; q += kSchedThreads) cnt[q] = 0;
     __syncthreads();
+    const bool last_wins = p.mode == DSPARK_SCHED_SYNC || p.mode == DSPARK_SCHED_FULL_SCAN;
     for (int i = threadIdx.x; i < m_star; i += kSchedThreads) {
         const int slot = sm.val[0][sk(i)];
-        atomicMax(&cnt[slot / p.G], (uint32_t)(slot % p.G + 1));
+        const uint32_t j1 = (uint32_t)(slot % p.G + 1);   // <= 8192 < 2^14
+        atomicMax(&cnt[slot / p.G], last_wins ? ((uint32_t)i << 14) | j1 : j1);
     }
     __syncthreads();
-    for (int q = threadIdx.x; q < p.R; q += kSchedThreads) p.keep[q] = (int32_t)cnt[q];
+    for (int q = threadIdx.x; q < p.R; q += kSchedThreads) p.keep[q] = (int32_t)(cnt[q] & 0x3FFFu);
 
     // Theta of the admitted set with the current survivals, from the prefix sums
     const int last = m_star - 1;
-    if (m_star == 0 && threadIdx.x == 0) {
+    if (top) {
+        if (threadIdx.x == 0) p.stats->theta_best = theta_of(p.R, m_star, sm.s_star, p.sps);
+    } else if (m_star == 0 && threadIdx.x == 0) {
         p.stats->theta_best = theta_of(p.R, 0, 0ull, p.sps);
     } else if (last >= 0 && last / ni == (int)threadIdx.x) {
-        p.stats->theta_best = theta_of(p.R, m_star, S[last % ni], p.sps);
+        unsigned long long s_last = 0ull;   // S[last % ni], selected without a dynamic index (S stays in registers)
+#pragma unroll
+        for (int it = 0; it < kMaxItems; ++it)
+            if (it == last % ni) s_last = S[it];
+        p.stats->theta_best = theta_of(p.R, m_star, s_last, p.sps);
     }
     if (threadIdx.x == 0) {
         p.stats->admitted = m_star;

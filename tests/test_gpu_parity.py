@@ -134,6 +134,55 @@ def test_schedule_monotone_runs_match_oracle(mode):
     assert n_exc <= 2
 
 
+def _sps_drops(n, drops, base=1000.0):
+    """SPS(B) for B = 1..n: `base`, multiplied by f at every B >= B0 for each (B0, f) in drops."""
+    B = torch.arange(1, n + 1, dtype=torch.float64)
+    v = torch.full((n,), base, dtype=torch.float64)
+    for b0, f in drops:
+        v = torch.where(B >= b0, v * f, v)
+    return v.to(torch.float32)
+
+
+def test_schedule_sync_forced_stop_matches_oracle():
+    # sync mode with a table whose drop at some B forces Theta down whatever the keys (a ratio of at
+    # least 1 + 1/R): the kernel then takes only the top keys, merged from the sorted request runs.
+    # Drops land before, inside and past the pool; a mild earlier drop may stop the scan first;
+    # R past the fast path's limit and unsorted runs take the full sort.
+    gen = torch.Generator().manual_seed(79)
+    cases = [(1, 1), (3, 2), (5, 3), (37, 5), (64, 4), (100, 7), (128, 16), (512, 16), (600, 2)]
+    n_exc = 0
+    for R, G in cases:
+        n = R * (1 + G)
+        stop_at = sorted({1, 2, min(63, R * G), max(1, R * G // 2), min(256, R * G), min(300, R * G)})
+        for m0 in stop_at:
+            for mild in (False, True):
+                drops = [(R + m0, 0.9 * R / (R + 1.0))]           # forced: ratio above 1 + 1/R
+                if mild and m0 > 2:
+                    drops.append((R + m0 // 2, 1.0 / (1.0 + 0.4 / R)))   # may or may not stop first
+                sps = _sps_drops(n, drops)
+                for variant in ("ties", "tails", "sparse", "unsorted"):
+                    # confidences of at least 0.5 keep every a above 1e-5, so no admission changes
+                    # Theta by less than the tie band
+                    c = torch.rand((R, G), generator=gen) * 0.5 + 0.5
+                    if variant == "ties":
+                        c = torch.round(c * 10) / 10
+                    surv = torch.cumprod(c, dim=1).to(torch.float32)
+                    if variant == "tails":
+                        tail = torch.randint(0, G + 1, (R,), generator=gen)
+                        surv[torch.arange(G)[None, :] >= tail[:, None]] = 0.0
+                    elif variant == "sparse":   # most requests empty: the pool can end before the drop
+                        surv[torch.rand((R,), generator=gen) < 0.8] = 0.0
+                    elif variant == "unsorted" and G > 1:
+                        surv[:, [0, G - 1]] = surv[:, [G - 1, 0]]
+                    surv = surv.to(DEV)
+                    gamma = torch.randint(0, G + 1, (R,), generator=gen, dtype=torch.int32).to(DEV) \
+                        if variant == "ties" else None
+                    out = ds.schedule(surv, sps.to(DEV), ds.SCHED_SYNC, gamma=gamma)
+                    assert ds.check(out["workspace"]) == 0
+                    n_exc += check_schedule(surv, sps, ds.SCHED_SYNC, out, gamma=gamma)
+    assert n_exc <= 2
+
+
 def test_schedule_worked_examples_on_gpu():
     ex = load_golden("worked_examples.json")
     s = ex["single_request"]
