@@ -68,7 +68,7 @@ dspark_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK :
 // ------------------------------------------------------------ sample_block
 
 struct SampleLayout {
-    size_t x_cur, hw, stats, pick, a_next, yh, state, a_rows, a_lo, total;
+    size_t x_cur, hw, stats, pick, a_next, yh, state, a_rows, a_lo, zbuf, total;
 };
 
 dspark_status check_sample(const dspark_sample_args* a)
@@ -121,6 +121,8 @@ SampleLayout sample_layout(const dspark_sample_args* a)
     o = align_up(o + (rnn && !a->a_rows ? sizeof(float) * (size_t)a->R * a->gamma_max * a->r : 0), kAlign);
     L.a_lo = o;
     o = align_up(o + (rnn ? 2 * (size_t)a->R * a->r : 0), kAlign);
+    L.zbuf = o;   // RNN head on the tensor cores: the step's operand rows, two parities of [R][3r] bf16
+    o = align_up(o + (rnn && sample_uses_tc(a) ? 2 * 2 * (size_t)a->R * 3 * a->r : 0), kAlign);
     L.total = o;
     return L;
 }
@@ -289,6 +291,7 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.yh = rnn ? at<float>(ws, L.yh) : nullptr;
     p.state = rnn ? at<float>(ws, L.state) : nullptr;
     p.a_lo = rnn && tc ? at<unsigned char>(ws, L.a_lo) : nullptr;
+    p.zbuf = rnn && tc ? at<unsigned char>(ws, L.zbuf) : nullptr;
     cudaError_t e = launch(DSPARK_KERNEL_CONF_HIDDEN, s, [&] { return launch_conf_hidden(p, s); });
     if (rnn && e == cudaSuccess) {
         // the h part of the RNN projection: a cuBLAS GEMM, not one of this library's kernels
@@ -297,6 +300,13 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
             snprintf(g_last_error, sizeof g_last_error, "rnn hidden GEMM: %s (%s)", cudaGetErrorName(e),
                      cudaGetErrorString(e));
     }
+    // RNN head on the tensor cores: operand-row and W_rnn tensor maps, and the step-0 operand rows
+    CUtensorMap zmap, rmap;
+    memset(&zmap, 0, sizeof zmap);
+    memset(&rmap, 0, sizeof rmap);
+    const bool rnn_tc = rnn && e == cudaSuccess && rnn_tc_supported(p) && rnn_tc_maps(p, &zmap, &rmap) == cudaSuccess;
+    if (rnn && !rnn_tc) p.zbuf = nullptr;   // the CUDA-core step: the commit writes no operand rows
+    if (rnn_tc) e = launch(DSPARK_KERNEL_RNN_STEP, s, [&] { return launch_rnn_z0(p, s); });
     // the commit copies the winning W block with one bulk copy when W admits the block map
     CUtensorMap wmap;
     memset(&wmap, 0, sizeof wmap);
@@ -312,7 +322,9 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
                 break;
             }
         }
-        if (rnn) e = launch(DSPARK_KERNEL_RNN_STEP, s, [&] { return launch_rnn_step(p, s); });
+        if (rnn)
+            e = launch(DSPARK_KERNEL_RNN_STEP, s,
+                       [&] { return rnn_tc ? launch_rnn_step_tc(p, zmap, rmap, s) : launch_rnn_step(p, s); });
         if (e == cudaSuccess)
             e = launch(DSPARK_KERNEL_DRAFT_STATS, s,
                        [&] { return tc ? launch_draft_stats_tc(p, s) : launch_draft_stats_simt(p, s); });

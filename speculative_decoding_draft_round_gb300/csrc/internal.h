@@ -55,6 +55,8 @@ struct DraftStep {
     float* yh;           // [R*G][3r] W_rnn[:, 2r:] h_k for every position
     float* state;        // [2][R][r] s_{k-1} / s_k by step parity
     void* a_lo;          // [R][r] bf16: operand minus its bf16 rounding (tensor-core path)
+    void* zbuf;          // [2][R][3r] bf16 by step parity: [hi(s_{k-1}); lo(s_{k-1}); W_1[x_{k-1}]], the
+                         // tensor-core RNN step's operand rows (NULL: the CUDA-core step)
 };
 
 // Verification (dspark_verify).
@@ -145,6 +147,11 @@ cudaError_t launch_assemble(const AssembleParams& p, cudaStream_t s);
 // rnn.cu (RNN head)
 cudaError_t launch_rnn_hidden(const DraftStep& p, cudaStream_t s);   // yh = W_rnn[:, 2r:] h for all positions
 cudaError_t launch_rnn_step(const DraftStep& p, cudaStream_t s);     // step k: state, bias operand
+// rnn_tc.cu (RNN head on the tensor cores)
+bool rnn_tc_supported(const DraftStep& p);
+cudaError_t rnn_tc_maps(const DraftStep& p, CUtensorMap* zmap, CUtensorMap* wmap);
+cudaError_t launch_rnn_z0(const DraftStep& p, cudaStream_t s);      // z[0]: zero state, W_1 of the anchor
+cudaError_t launch_rnn_step_tc(const DraftStep& p, const CUtensorMap& zmap, const CUtensorMap& wmap, cudaStream_t s);
 
 inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -458,6 +458,8 @@ __global__ void __launch_bounds__(kCommitThreads)
         const T et = E[(size_t)tok * p.r + i];
         if (!rnn)   // the RNN head's next operand comes from its state update
             for (int rp = 0; rp < p.a_replicas; ++rp) an[rp * rep_stride + i] = et;
+        else if (p.zbuf)   // the tensor-core RNN step's next operand rows: W_1[x_k]
+            static_cast<T*>(p.zbuf)[(((size_t)((p.k + 1) & 1) * p.R + q) * 3 + 2) * p.r + i] = et;
         const float xprev = rnn ? (p.conf_token ? 0.f : ld(E, (size_t)prevtok * p.r + i)) : erow[i];
         dot = fmaf(p.w_e[i], p.conf_token ? to_f32<T>(et) : xprev, dot);   // eq. (7) reads W_1[x_{k-1}]
     }
