@@ -30,7 +30,9 @@ constexpr uint32_t kRtABytes = kRtM * kRtK * 2;             // 16 KB
 constexpr uint32_t kRtBBox = kRtEl * kRtK * 2;              // 2 KB: one gate's 16 rows
 constexpr uint32_t kRtStageBytes = kRtABytes + 3 * kRtBBox;   // 22 KB, a multiple of 1024
 constexpr uint32_t kRtTmemCols = 64;
-constexpr int kRtThreads = 192;                             // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kRtEpiGroups = 4;                            // epilogue warps per TMEM lane quarter
+constexpr int kRtElT = kRtEl / kRtEpiGroups;                // state elements per epilogue thread
+constexpr int kRtThreads = 64 + 128 * kRtEpiGroups;         // warp 0 TMA, warp 1 MMA, 16 epilogue warps
 constexpr uint32_t kRtSmem = kRtStages * kRtStageBytes + 1024 + 256;
 constexpr unsigned long long kRtWaitNs = 4000000000ull;     // 4 s
 // instruction descriptor, kind::f16: D fp32, A = B = bf16, both K-major, N = 48, M = 128
@@ -102,27 +104,21 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     tc5::fence_after();
     const uint32_t tmem = *s_tmem;
 
-    // epilogue inputs that no earlier kernel of this call writes: the h part of the projection
-    // (the GEMM before the serial loop) and the request's draft length
+    // epilogue: warp w >= 2 takes TMEM lane quarter w % 4 (row q) and elements e0 + 4 ge .. + 3,
+    // ge = (w - 2) / 4. Inputs that no earlier kernel of this call writes, loaded first: the h part
+    // of the projection (the GEMM before the serial loop) and the request's draft length.
     const int row = (warp & 3) * 32 + lane, q = mt * kRtM + row;
     const bool epi = warp >= 2;
+    const int ge = epi ? (warp - 2) / 4 : 0, el = e0 + kRtElT * ge;
     bool active = false;
-    float yh[3][kRtEl];
+    float4 yh[3] = {};
     if (epi && q < R) {
         int g = p.gamma ? p.gamma[q] : G;
         g = g < 0 ? 0 : (g > G ? G : g);
         active = k < g;
         const float* yrow = p.yh + ((size_t)q * G + k) * 3 * r;
 #pragma unroll
-        for (int u = 0; u < 3; ++u)
-#pragma unroll
-            for (int c = 0; c < kRtEl / 4; ++c) {
-                const float4 v = *reinterpret_cast<const float4*>(yrow + u * r + e0 + 4 * c);
-                yh[u][4 * c] = v.x;
-                yh[u][4 * c + 1] = v.y;
-                yh[u][4 * c + 2] = v.z;
-                yh[u][4 * c + 3] = v.w;
-            }
+        for (int u = 0; u < 3; ++u) yh[u] = *reinterpret_cast<const float4*>(yrow + u * r + el);
     }
     pdl_wait();      // the operand rows and the state come from the previous step's kernels
     pdl_trigger();   // the statistics kernel may start its prologue
@@ -166,41 +162,36 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         }
         if (ok) tc5::commit(done);
     } else if (epi) {
-        // ---------------- epilogue: row q, elements e0 .. e0 + 15
-        float sp[kRtEl];
+        // ---------------- epilogue: row q, elements el .. el + 3
         const float* s_prev = p.state + (size_t)(k & 1) * R * r;
         float* s_next = p.state + (size_t)((k + 1) & 1) * R * r;
-        if (q < R) {
-#pragma unroll
-            for (int c = 0; c < kRtEl / 4; ++c) {
-                const float4 v = *reinterpret_cast<const float4*>(s_prev + (size_t)q * r + e0 + 4 * c);
-                sp[4 * c] = v.x;
-                sp[4 * c + 1] = v.y;
-                sp[4 * c + 2] = v.z;
-                sp[4 * c + 3] = v.w;
-            }
-        }
+        float4 sp4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (q < R) sp4 = *reinterpret_cast<const float4*>(s_prev + (size_t)q * r + el);
         const bool ok = rt_wait(done, 0u, s_abort, p.status);
         const bool all_ok = __all_sync(0xffffffffu, ok);
-        uint32_t acc[3][kRtEl];
+        uint32_t acc[3][kRtElT];
         if (all_ok) {
             tc5::fence_after();
-            const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-            tc5::ld16(lane_base + 0, acc[0]);
-            tc5::ld16(lane_base + kRtEl, acc[1]);
-            tc5::ld16(lane_base + 2 * kRtEl, acc[2]);
+            const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(kRtElT * ge);
+            tc5::ld4(lane_base + 0, acc[0]);
+            tc5::ld4(lane_base + kRtEl, acc[1]);
+            tc5::ld4(lane_base + 2 * kRtEl, acc[2]);
         }
         if (all_ok && q < R) {
             const size_t o = (size_t)q * G + k;
-            float sn[kRtEl], op[kRtEl];
+            const float sp[kRtElT] = {sp4.x, sp4.y, sp4.z, sp4.w};
+            const float yg0[kRtElT] = {yh[0].x, yh[0].y, yh[0].z, yh[0].w};
+            const float yc0[kRtElT] = {yh[1].x, yh[1].y, yh[1].z, yh[1].w};
+            const float yo0[kRtElT] = {yh[2].x, yh[2].y, yh[2].z, yh[2].w};
+            float sn[kRtElT], op[kRtElT];
 #pragma unroll
-            for (int j = 0; j < kRtEl; ++j) {
+            for (int j = 0; j < kRtElT; ++j) {
                 sn[j] = sp[j];
                 op[j] = 0.f;
                 if (active) {
-                    const float yg = __uint_as_float(acc[0][j]) + yh[0][j];
-                    const float yc = __uint_as_float(acc[1][j]) + yh[1][j];
-                    const float yo = __uint_as_float(acc[2][j]) + yh[2][j];
+                    const float yg = __uint_as_float(acc[0][j]) + yg0[j];
+                    const float yc = __uint_as_float(acc[1][j]) + yc0[j];
+                    const float yo = __uint_as_float(acc[2][j]) + yo0[j];
                     const float gate = 1.f / (1.f + expf(-yg));
                     sn[j] = gate * sp[j] + (1.f - gate) * tanhf(yc);
                     op[j] = tanhf(yo);
@@ -208,9 +199,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             }
             // the state in fp32 and, for the next step's operand, its bf16 rounding and remainder
             __nv_bfloat16* zn = static_cast<__nv_bfloat16*>(p.zbuf) + ((size_t)((k + 1) & 1) * R + q) * 3 * r;
-            uint32_t hi2[kRtEl / 2], lo2[kRtEl / 2], ohi2[kRtEl / 2], olo2[kRtEl / 2];
+            uint32_t hi2[kRtElT / 2], lo2[kRtElT / 2], ohi2[kRtElT / 2], olo2[kRtElT / 2];
 #pragma unroll
-            for (int j = 0; j < kRtEl; j += 2) {
+            for (int j = 0; j < kRtElT; j += 2) {
                 const float h0 = __bfloat162float(__float2bfloat16_rn(sn[j]));
                 const float h1 = __bfloat162float(__float2bfloat16_rn(sn[j + 1]));
                 hi2[j / 2] = pack_bf16x2(h0, h1);
@@ -220,26 +211,14 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                 ohi2[j / 2] = pack_bf16x2(g0, g1);
                 olo2[j / 2] = pack_bf16x2(op[j] - g0, op[j + 1] - g1);
             }
-#pragma unroll
-            for (int c = 0; c < kRtEl / 4; ++c) {
-                *reinterpret_cast<float4*>(s_next + (size_t)q * r + e0 + 4 * c) =
-                    make_float4(sn[4 * c], sn[4 * c + 1], sn[4 * c + 2], sn[4 * c + 3]);
-                *reinterpret_cast<float4*>(p.a_rows + o * r + e0 + 4 * c) =
-                    make_float4(op[4 * c], op[4 * c + 1], op[4 * c + 2], op[4 * c + 3]);
-            }
-#pragma unroll
-            for (int c = 0; c < kRtEl / 8; ++c) {
-                const uint4 h = make_uint4(hi2[4 * c], hi2[4 * c + 1], hi2[4 * c + 2], hi2[4 * c + 3]);
-                const uint4 l = make_uint4(lo2[4 * c], lo2[4 * c + 1], lo2[4 * c + 2], lo2[4 * c + 3]);
-                const uint4 oh = make_uint4(ohi2[4 * c], ohi2[4 * c + 1], ohi2[4 * c + 2], ohi2[4 * c + 3]);
-                const uint4 ol = make_uint4(olo2[4 * c], olo2[4 * c + 1], olo2[4 * c + 2], olo2[4 * c + 3]);
-                *reinterpret_cast<uint4*>(zn + e0 + 8 * c) = h;
-                *reinterpret_cast<uint4*>(zn + r + e0 + 8 * c) = l;
-                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.a_lo) + (size_t)q * r + e0 + 8 * c) = ol;
-                for (int rp = 0; rp < p.a_replicas; ++rp)
-                    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.a_next) + ((size_t)rp * R + q) * r + e0 +
-                                              8 * c) = oh;
-            }
+            *reinterpret_cast<float4*>(s_next + (size_t)q * r + el) = make_float4(sn[0], sn[1], sn[2], sn[3]);
+            *reinterpret_cast<float4*>(p.a_rows + o * r + el) = make_float4(op[0], op[1], op[2], op[3]);
+            *reinterpret_cast<uint2*>(zn + el) = make_uint2(hi2[0], hi2[1]);
+            *reinterpret_cast<uint2*>(zn + r + el) = make_uint2(lo2[0], lo2[1]);
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.a_lo) + (size_t)q * r + el) = make_uint2(olo2[0], olo2[1]);
+            for (int rp = 0; rp < p.a_replicas; ++rp)
+                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.a_next) + ((size_t)rp * R + q) * r + el) =
+                    make_uint2(ohi2[0], ohi2[1]);
         }
     }
     tc5::fence_before();
@@ -290,6 +269,7 @@ bool rnn_tc_supported(const DraftStep& p)
     const int Z = 2 * p.r + p.d;
     return p.dtype == DSPARK_BF16 && p.a_lo != nullptr && p.zbuf != nullptr && p.r % kRtK == 0 && (Z % 8) == 0 &&
            (reinterpret_cast<uintptr_t>(p.W_rnn) & 15u) == 0 && (reinterpret_cast<uintptr_t>(p.zbuf) & 15u) == 0 &&
+           (reinterpret_cast<uintptr_t>(p.a_rows) & 15u) == 0 &&   // the epilogue's 16-byte stores
            rt_encode_fn() != nullptr;
 }
 

@@ -57,6 +57,15 @@ __device__ __forceinline__ void commit(uint32_t bar)
                  : "memory");
 }
 
+// 4 consecutive 32-bit columns of this thread's TMEM lane (warp-wide, lanes of the warp's quarter)
+__device__ __forceinline__ void ld4(uint32_t taddr, uint32_t (&v)[4])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // 16 consecutive 32-bit columns of this thread's TMEM lane (warp-wide, lanes of the warp's quarter)
 __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&v)[16])
 {
