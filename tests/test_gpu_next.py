@@ -211,6 +211,9 @@ RNN_SPECS = [
     dict(name="rnn_f32", R=11, G=5, V=300, r=24, d=20, dtype="f32", ew_std=0.2, gamma=[5, 0, 3, 5, 1, 2, 5, 4, 5, 0, 5]),
     dict(name="rnn_tiles_bf16", R=160, G=3, V=1000, r=64, d=96, dtype="bf16", ew_std=0.15),
     dict(name="rnn_wide_bf16", R=37, G=4, V=2056, r=256, d=64, dtype="bf16", ew_std=0.05, gamma=[4, 2] * 18 + [3]),
+    # 2r + d = 228 is not a multiple of 8: W_rnn rows do not meet the copy engine's 16-byte pitch, so the
+    # step runs on CUDA cores beside the tensor-core statistics kernel
+    dict(name="rnn_pitch_bf16", R=40, G=3, V=1024, r=64, d=100, dtype="bf16", ew_std=0.15),
 ]
 
 
