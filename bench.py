@@ -1,7 +1,7 @@
 #!/usr/bin/env python
 """Benchmark one DSpark draft round (sample + schedule + verify) on GB300.
 
-Workload (default): config 3 -- R=128 requests, gamma=16, V=151936, r=256,
+Workload (default, --workload 3): R=128 requests, gamma=16, V=151936, r=256,
 d=4096, bf16 inputs, synthetic structured logits (top-1 boosted +6 on 70% of
 positions), T in {0.6, 1.0}, staircase SPS, synchronous scheduler. A step is
 one whole round over one batch; inputs stay resident in HBM, `round` advances
@@ -288,7 +288,7 @@ def bench_reference(args):
         return
     from speculative_decoding_draft_round_gb300 import workloads as wl
     dev = "cuda:%d" % local if torch.cuda.is_available() else "cpu"
-    rnd = wl.CONFIGS[args.workload](device=dev)
+    rnd = wl.WORKLOADS[args.workload](device=dev)
     threads = cpu_threads()
     n_req = threads
     ids = list(range(0, rnd.R, max(1, rnd.R // n_req)))[:n_req]
@@ -393,7 +393,7 @@ def bench_ours(args):
         dist.init_process_group("nccl", device_id=dev)
     dsbuild.build()
     path = {"auto": ds.PATH_AUTO, "cuda_core": ds.PATH_CUDA_CORE, "tensor_core": ds.PATH_TENSOR_CORE}[args.path]
-    rnd = wl.CONFIGS[args.workload](device=dev)
+    rnd = wl.WORKLOADS[args.workload](device=dev)
     if world > 1:   # independent replica per rank
         rnd.seed = replica_seed(rnd.seed, rank)
     cap = None
@@ -598,7 +598,7 @@ def bench_profile(args):
     from speculative_decoding_draft_round_gb300 import workloads as wl
     dsbuild.build()
     path = {"auto": ds.PATH_AUTO, "cuda_core": ds.PATH_CUDA_CORE, "tensor_core": ds.PATH_TENSOR_CORE}[args.path]
-    rnd = wl.CONFIGS[args.workload](device="cuda")
+    rnd = wl.WORKLOADS[args.workload](device="cuda")
     cap = None
     if rnd.mode == wl.SCHED_ASYNC_CAPACITY:
         cap = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,

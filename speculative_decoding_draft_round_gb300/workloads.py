@@ -5,10 +5,11 @@ shapes and value distributions of the workloads the round is measured on, so
 that the CUDA library and the CPU oracle read the same bits. The pages measure
 on benchmark suites and trained DeepSeek / Qwen3 weights; none of those are
 used. The synthetic distributions stand in for their shape: independent
-Gaussian logits (config 2), structured high-acceptance logits with a shared
-boosted top-1 (config 3), a mix of low- and high-entropy requests (config 4),
-and a target that differs from the draft by a controlled total-variation
-distance (config 5).
+Gaussian logits (`small`), structured high-acceptance logits with a shared
+boosted top-1 (`structured`), a mix of low- and high-entropy requests
+(`mixed_entropy`), and a target that differs from the draft by a controlled
+total-variation distance (`controlled_tv`). WORKLOADS numbers them 1-5 from
+`tiny` up, the order of their sizes.
 
 Distribution notation N(mu, s) means mean mu and standard deviation s.
 bf16 tensors are drawn in fp32 and rounded to nearest-even by torch.
@@ -72,7 +73,7 @@ def _normal(shape, std, g, device, mean=0.0):
     return torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std + mean
 
 
-def sps_config1(n: int = 20) -> torch.Tensor:
+def sps_tiny(n: int = 20) -> torch.Tensor:
     """SPS(1..5) = 1000, 520, 400, 340, 280, then x0.9 per extra B."""
     v = [1000.0, 520.0, 400.0, 340.0, 280.0]
     while len(v) < n:
@@ -165,58 +166,58 @@ def make_round(name: str, R: int, gamma_max: int, V: int, r: int, d: int, dtype:
     return rnd
 
 
-def config1(device="cpu") -> Round:
+def tiny(device="cpu") -> Round:
     """R=4, gamma=4, V=64, r=8, d=32, fp32; U, target ~N(0,2); E, W ~N(0,0.1);
     w_h, w_e ~N(0,0.3), b=1.5; T=1; SPS 1000,520,400,340,280 then x0.9 to B=20."""
-    return make_round("config1_R4_g4_V64_f32", 4, 4, 64, 8, 32, "f32", seed=0, device=device,
+    return make_round("R4_g4_V64_f32", 4, 4, 64, 8, 32, "f32", seed=0, device=device,
                       u_std=2.0, t_std=2.0, ew_std=0.1, wh_std=0.3, we_std=0.3, b=1.5,
-                      sps=sps_config1(20), mode=SCHED_SYNC)
+                      sps=sps_tiny(20), mode=SCHED_SYNC)
 
 
-def config2(device="cpu") -> Round:
+def small(device="cpu") -> Round:
     """R=32, gamma=16, V=32768, r=256, d=2048, bf16; U, target ~N(0,3); E, W ~N(0,0.05);
     T=1; SPS(B) = 1/(1e-3 + 2e-6 B), 544 entries."""
-    return make_round("config2_R32_g16_V32768_bf16", 32, 16, 32768, 256, 2048, "bf16", seed=1,
+    return make_round("R32_g16_V32768_bf16", 32, 16, 32768, 256, 2048, "bf16", seed=1,
                       device=device, sps=sps_hyperbolic(544), mode=SCHED_SYNC)
 
 
-def _temp_c3(R, g, dev):
+def _temp_structured(R, g, dev):
     return torch.where(torch.arange(R, device=dev) % 2 == 0, torch.tensor(0.6, device=dev),
                        torch.tensor(1.0, device=dev))
 
 
-def config3(device="cpu") -> Round:
+def structured(device="cpu") -> Round:
     """R=128, gamma=16, V=151936, r=256, d=4096, bf16; U, target ~N(0,3) with the top-1
     boosted by +6 on 70% of positions; T in {0.6, 1.0}; staircase SPS, 2176 entries."""
-    return make_round("config3_R128_g16_V151936_bf16", 128, 16, 151936, 256, 4096, "bf16", seed=2,
-                      device=device, boost=(0.7, 6.0), temperature=_temp_c3,
+    return make_round("R128_g16_V151936_bf16", 128, 16, 151936, 256, 4096, "bf16", seed=2,
+                      device=device, boost=(0.7, 6.0), temperature=_temp_structured,
                       sps=sps_staircase(2176), mode=SCHED_SYNC)
 
 
-def config4(device="cpu") -> Round:
+def mixed_entropy(device="cpu") -> Round:
     """R=256, gamma=16, V=129280, r=256, d=7168, bf16; requests r<128 have logits x4;
     staircase SPS, 4352 entries; asynchronous capacity scheduling."""
-    return make_round("config4_R256_g16_V129280_bf16", 256, 16, 129280, 256, 7168, "bf16", seed=3,
+    return make_round("R256_g16_V129280_bf16", 256, 16, 129280, 256, 7168, "bf16", seed=3,
                       device=device, entropy_split=(128, 4.0), sps=sps_staircase(4352),
                       mode=SCHED_ASYNC_CAPACITY)
 
 
-def _temp_c5(R, g, dev):
+def _temp_controlled_tv(R, g, dev):
     return 0.3 + 0.9 * torch.rand((R,), generator=g, device=dev)
 
 
-def config5(device="cpu") -> Round:
+def controlled_tv(device="cpu") -> Round:
     """R=512, gamma 8 (r < 256) or 16, V=129280, r=256, d=7168, bf16; target differs from
     the draft by TV ~U[0.05, 0.6] per position; T ~U[0.3, 1.2]; staircase SPS, 8704
     entries; full-scan scheduling over 8192 slots."""
     R = 512
     gamma = [8] * (R // 2) + [16] * (R // 2)
-    return make_round("config5_R512_g8-16_V129280_bf16", R, 16, 129280, 256, 7168, "bf16", seed=4,
-                      device=device, temperature=_temp_c5, gamma=gamma, tv_range=(0.05, 0.6),
+    return make_round("R512_g8-16_V129280_bf16", R, 16, 129280, 256, 7168, "bf16", seed=4,
+                      device=device, temperature=_temp_controlled_tv, gamma=gamma, tv_range=(0.05, 0.6),
                       sps=sps_staircase(8704), mode=SCHED_FULL_SCAN)
 
 
-CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+WORKLOADS = {1: tiny, 2: small, 3: structured, 4: mixed_entropy, 5: controlled_tv}
 
 
 def rnn_weights(rnd: Round, seed: int = 99) -> torch.Tensor:

@@ -64,7 +64,7 @@ def test_assemble_clamps_out_of_range_keep():
 
 
 def test_assemble_after_a_full_round():
-    rnd = wl.CONFIGS[3](device=DEV)
+    rnd = wl.WORKLOADS[3](device=DEV)
     runner = ds.RoundRunner(rnd)
     runner.set_round(4)
     runner.run()

@@ -232,10 +232,10 @@ def test_verify_matches_oracle(spec):
             assert n_exc <= max(2, rnd.R // 100)
 
 
-def test_config1_round_end_to_end():
-    """Config 1 exactly: the oracle runs alone from the inputs (its own draws feed its
+def test_tiny_round_end_to_end():
+    """The tiny round exactly: the oracle runs alone from the inputs (its own draws feed its
     scheduler and verifier) and every output must equal the GPU's."""
-    rnd = wl.config1(device=DEV)
+    rnd = wl.tiny(device=DEV)
     runner = ds.RoundRunner(rnd)
     for rnd_idx in range(20):
         runner.set_round(rnd_idx)

@@ -29,10 +29,10 @@ def _capacity_survivals(rnd, rnd_idx):
     return old["surv"].clone()
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
-def test_full_size_round(cfg):
+@pytest.mark.parametrize("workload", [2, 3, 4, 5])
+def test_full_size_round(workload):
     torch.cuda.empty_cache()
-    rnd = wl.CONFIGS[cfg](device=DEV)
+    rnd = wl.WORKLOADS[workload](device=DEV)
     t = 2
     rnd.round = t
     cap = _capacity_survivals(rnd, t - 2) if rnd.mode == wl.SCHED_ASYNC_CAPACITY else None
@@ -42,7 +42,7 @@ def test_full_size_round(cfg):
     assert runner.check() == 0
     res = runner.results()
     R, G = rnd.R, rnd.gamma_max
-    rng = np.random.default_rng(cfg)
+    rng = np.random.default_rng(workload)
     ids = np.unique(np.concatenate([[0, 1, R // 2, R - 1], rng.integers(0, R, 2)]))
     check_sample(rnd, res, ids)
     assert check_schedule(res["surv"], rnd.sps, rnd.mode, res, gamma=rnd.gamma, surv_capacity=cap) <= 1
