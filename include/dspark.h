@@ -102,9 +102,12 @@ enum {
  *   z_k = [s_{k-1}; W_1[x_{k-1}]; h[r][k]],  [y_g; y_c; y_o] = W_rnn z_k,  s_0 = 0,
  *   s_k = sigmoid(y_g) * s_{k-1} + (1 - sigmoid(y_g)) * tanh(y_c),  B_k = tanh(y_o) W_2.
  *   The h part of W_rnn z_k is one GEMM over all positions (cuBLAS, fp32 accumulation), the
- *   rest a per-step kernel in fp32; on the tensor-core path tanh(y_o) enters the contraction
- *   as two bf16 operands (its bf16 rounding and the rounding of the remainder), so the bias
- *   keeps about 16 significant bits.
+ *   rest a per-step kernel. On the tensor-core path (bf16, r a multiple of 64 up to 256,
+ *   (2r + d) a multiple of 8, 16-byte aligned W_rnn and a_rows) that kernel is a tcgen05 GEMM
+ *   whose fp32 state enters as two bf16 operands (its rounding and the rounding of the
+ *   remainder); elsewhere it runs on CUDA cores in fp32. On the tensor-core path tanh(y_o)
+ *   likewise enters the bias contraction as two bf16 operands, so the bias keeps about 16
+ *   significant bits.
  * a_rows (optional output) receives each step's bias operand in fp32 (W_1[x_{k-1}] or
  * tanh(y_o)); dspark_verify needs them for an RNN-head draft.
  * temperature[r] = 0 is greedy decoding (zhongzhuzhou.org notes, FAQ on temperature 0):
