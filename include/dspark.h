@@ -328,7 +328,7 @@ dspark_status dspark_assemble(const dspark_assemble_args* args, void* workspace,
  * thread-safe; it adds one event record before and after each timed launch.
  */
 enum {
-    DSPARK_KERNEL_CONF_HIDDEN = 0,    /* w_h . h for every (request, position) */
+    DSPARK_KERNEL_DRAFT_SETUP = 0,    /* sampler set-up: clears the block-draw slots, writes step 0's conditioning rows */
     DSPARK_KERNEL_DRAFT_STATS = 1,    /* bias contraction + block softmax statistics, one per draft step */
     DSPARK_KERNEL_DRAFT_COMMIT = 2,   /* two-level draw, confidence, survival, one per draft step */
     DSPARK_KERNEL_SCHEDULE = 3,

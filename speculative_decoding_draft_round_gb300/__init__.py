@@ -87,7 +87,7 @@ EXPORTS = ("dspark_sample_workspace_size", "dspark_sample_block", "dspark_schedu
            "dspark_last_error", "dspark_sample_path", "dspark_sample_block_static",
            "dspark_assemble_workspace_size", "dspark_assemble")
 
-KERNELS = {"conf_hidden": 0, "draft_stats": 1, "draft_commit": 2, "schedule": 3, "verify_rows": 4,
+KERNELS = {"draft_setup": 0, "draft_stats": 1, "draft_commit": 2, "schedule": 3, "verify_rows": 4,
            "verify_decide": 5, "residual_stats": 6, "residual_pick": 7, "assemble": 8, "rnn_step": 9}
 
 

@@ -28,7 +28,7 @@ bool timing(int kernel) { return g_timer.kernel == kernel && g_timer.count && *g
 
 const char* kernel_name(int kernel)
 {
-    static const char* names[] = {"conf_hidden", "draft_stats", "draft_commit", "schedule",
+    static const char* names[] = {"draft_setup", "draft_stats", "draft_commit", "schedule",
                                   "verify_rows", "verify_decide", "residual_stats", "residual_pick",
                                   "assemble", "rnn_step"};
     return kernel >= 0 && kernel <= DSPARK_KERNEL_RNN_STEP ? names[kernel] : "?";
@@ -68,7 +68,7 @@ dspark_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK :
 // ------------------------------------------------------------ sample_block
 
 struct SampleLayout {
-    size_t x_cur, hw, stats, pick, a_next, yh, state, a_rows, a_lo, zbuf, total;
+    size_t x_cur, stats, pick, a_next, yh, state, a_rows, a_lo, zbuf, total;
 };
 
 dspark_status check_sample(const dspark_sample_args* a)
@@ -103,8 +103,6 @@ SampleLayout sample_layout(const dspark_sample_args* a)
     size_t o = kStatusBytes;
     L.x_cur = o;
     o = align_up(o + sizeof(int32_t) * a->R, kAlign);
-    L.hw = o;
-    o = align_up(o + sizeof(float) * (size_t)a->R * a->gamma_max, kAlign);
     L.stats = o;   // per block (CUDA-core path) or per CTA of the tensor-core kernel
     o = align_up(o + sizeof(float2) * rows * (sample_uses_tc(a) ? tc_grid(a->R, nblk) : nblk), kAlign);
     L.pick = o;
@@ -277,7 +275,6 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.sts_temp = a->sts_temp;
     p.status = at<int>(ws, 0);
     p.x_cur = at<int32_t>(ws, L.x_cur);
-    p.hw = at<float>(ws, L.hw);
     p.stats = at<float2>(ws, L.stats);
     p.n_stats = sample_uses_tc(a) ? tc_grid(a->R, p.nblk) : p.nblk;
     p.pick = at<unsigned long long>(ws, L.pick);
@@ -292,7 +289,7 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.state = rnn ? at<float>(ws, L.state) : nullptr;
     p.a_lo = rnn && tc ? at<unsigned char>(ws, L.a_lo) : nullptr;
     p.zbuf = rnn && tc ? at<unsigned char>(ws, L.zbuf) : nullptr;
-    cudaError_t e = launch(DSPARK_KERNEL_CONF_HIDDEN, s, [&] { return launch_conf_hidden(p, s); });
+    cudaError_t e = launch(DSPARK_KERNEL_DRAFT_SETUP, s, [&] { return launch_draft_setup(p, s); });
     if (rnn && e == cudaSuccess) {
         // the h part of the RNN projection: a cuBLAS GEMM, not one of this library's kernels
         e = launch_rnn_hidden(p, s);

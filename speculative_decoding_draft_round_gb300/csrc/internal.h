@@ -39,7 +39,6 @@ struct DraftStep {
     // workspace
     int* status;
     int32_t* x_cur;      // [R] token committed at the previous step
-    float* hw;           // [R][G] w_h . h[r][k]
     float2* stats;       // [R][n_stats] (max, sum) of exp2, log2 units: per vocabulary block (CUDA-core
                          // path) or per CTA of the tensor-core kernel (its blocks merged), row-major
     int n_stats;         // entries per row of stats: nblk, or the tensor-core grid
@@ -115,7 +114,7 @@ struct AssembleParams {
 };
 
 // sample.cu
-cudaError_t launch_conf_hidden(const DraftStep& p, cudaStream_t s);
+cudaError_t launch_draft_setup(const DraftStep& p, cudaStream_t s);
 cudaError_t launch_draft_stats_simt(const DraftStep& p, cudaStream_t s);
 // wmap: the W block map of encode_w_block_map, or NULL (the commit then loads W with plain loads)
 cudaError_t launch_draft_commit(const DraftStep& p, const CUtensorMap* wmap, cudaStream_t s);

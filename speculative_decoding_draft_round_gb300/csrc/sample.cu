@@ -17,9 +17,13 @@
 //                    inside it (its 128 logits recomputed from W's block columns),
 //                    the log-normaliser from the statistics, confidence and
 //                    survival; x_k becomes the next step's previous token.
-// w_h . h_k does not depend on the draws, so conf_hidden computes it for every
-// (request, position) in one pass before the serial loop.
+// w_h . h_k does not depend on the draws: each commit forms it from the inputs while the
+// previous kernel finishes, and reduces it with the w_e part of eq. (7).
+//   draft_setup   -- once per call: clears the block-draw slots and writes the first
+//                    step's conditioning rows W_1[x_0].
 #include <string.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -27,13 +31,10 @@
 
 namespace dspark {
 
-// ----------------------------------------------------------------- w_h . h
-
-constexpr int kHwRows = 2;    // confidence-head rows per CTA of conf_hidden_kernel
-constexpr int kHwSplit = 4;   // warps per row
+// ----------------------------------------------------------------- set-up of a call
 
 template <typename T>
-__global__ void __launch_bounds__(256) conf_hidden_kernel(DraftStep p)
+__global__ void __launch_bounds__(256) draft_setup_kernel(DraftStep p)
 {
     pdl_enter();   // the previous call's kernels read the slots and rows written here
     // clear the per-step block-draw slots of this call, and set the first step's conditioning rows
@@ -50,56 +51,6 @@ __global__ void __launch_bounds__(256) conf_hidden_kernel(DraftStep p)
             const T v = E[(size_t)x0 * p.r + c];
             for (int rp = 0; rp < p.a_replicas; ++rp) an[rp * n + i] = v;
         }
-    }
-    // hw[q][k] = w_h . h[q][k]: kHwRows rows per CTA, each split over kHwSplit warps along d (more
-    // warps in flight than one per row), the parts summed through shared memory
-    __shared__ float s_part[kHwRows * kHwSplit];
-    const int wic = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * kHwRows + wic / kHwSplit, part = wic % kHwSplit;
-    bool on = row < p.R * p.G;
-    if (on) {
-        const int q = row / p.G, k = row % p.G;
-        const int g = p.gamma ? p.gamma[q] : p.G;
-        on = k < g;
-    }
-    float acc = 0.f;
-    if (on) {
-        const T* h = static_cast<const T*>(p.h) + (size_t)row * p.d;
-        const bool vec = (p.d % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.h) & 15u) == 0) &&
-                         ((reinterpret_cast<uintptr_t>(p.w_h) & 15u) == 0);
-        if (vec) {
-            // step s covers columns 256 s + 8 lane .. +7; this warp takes steps part, part + 4, ...,
-            // four of them in flight (d % 8 == 0: a lane's 8 columns are all inside or all outside)
-            for (int s0 = part; s0 * 256 < p.d; s0 += 4 * kHwSplit) {
-                float w[4][8], x[4][8];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int jj = (s0 + u * kHwSplit) * 256 + lane * 8;
-                    if (jj < p.d) {
-                        load8<T>(h + jj, x[u]);
-                        load8<float>(p.w_h + jj, w[u]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) w[u][e] = x[u][e] = 0.f;
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc = fmaf(w[u][e], x[u][e], acc);
-            }
-        } else {
-            for (int jj = part * 32 + lane; jj < p.d; jj += 32 * kHwSplit) acc += p.w_h[jj] * ld(h, jj);
-        }
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) s_part[wic] = acc;
-    __syncthreads();
-    if (on && part == 0 && lane == 0) {
-        float t = 0.f;
-#pragma unroll
-        for (int u = 0; u < kHwSplit; ++u) t += s_part[wic + u];
-        p.hw[row] = t;
     }
 }
 
@@ -285,10 +236,27 @@ __global__ void __launch_bounds__(kCommitThreads)
     const size_t o = (size_t)q * p.G + p.k;
     const bool greedy = p.temperature[q] == 0.f;   // temperature 0: arg-max draft
     const float invT = greedy ? 1.f : 1.f / p.temperature[q];
+    // w_h . h[q][k], the confidence head's hidden part (eq. 7): h and w_h are inputs, so this
+    // thread's share of the dot product is formed while the previous kernel finishes, and is
+    // reduced with the w_e part after the draw
+    float hdot = 0.f;
+    if (rq.active) {
+        const T* h = static_cast<const T*>(p.h) + o * p.d;
+        if (sizeof(T) == 2 && p.d % 8 == 0 && ((reinterpret_cast<uintptr_t>(p.h) & 15u) == 0) &&
+            ((reinterpret_cast<uintptr_t>(p.w_h) & 15u) == 0)) {
+            for (int c = t * 8; c < p.d; c += 8 * kCommitThreads) {
+                float x[8], w[8];
+                load8<T>(h + c, x);
+                load8<float>(p.w_h + c, w);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) hdot = fmaf(w[e], x[e], hdot);
+            }
+        } else {
+            for (int c = t; c < p.d; c += kCommitThreads) hdot = fmaf(p.w_h[c], ld(h, c), hdot);
+        }
+    }
     pdl_wait();      // block statistics, pick slots and x_cur come from the kernels before this one
     pdl_trigger();   // the next step's statistics kernel may start its prefetch
-    // hw comes from conf_hidden, which the chain of waits orders before this point only
-    const float hw = p.hw[o];
     if (!rq.active) {
         if (p.a_rows && !RNN)
             for (int i = t; i < p.r; i += kCommitThreads) p.a_rows[o * p.r + i] = 0.f;
@@ -298,7 +266,7 @@ __global__ void __launch_bounds__(kCommitThreads)
         }
         return;
     }
-    // W_1[x_{k-1}] is the conditioning row the previous commit (or conf_hidden for k = 0) wrote
+    // W_1[x_{k-1}] is the conditioning row the previous commit (or draft_setup for k = 0) wrote
     const T* prev_row = static_cast<const T*>(p.a_next) + (size_t)q * p.r;
     const T* E = static_cast<const T*>(p.E);
     const T* W = static_cast<const T*>(p.W);
@@ -463,10 +431,10 @@ __global__ void __launch_bounds__(kCommitThreads)
         const float xprev = rnn ? (p.conf_token ? 0.f : ld(E, (size_t)prevtok * p.r + i)) : erow[i];
         dot = fmaf(p.w_e[i], p.conf_token ? to_f32<T>(et) : xprev, dot);   // eq. (7) reads W_1[x_{k-1}]
     }
-    dot = block_sum<kCommitThreads>(dot, red);
+    dot = block_sum<kCommitThreads>(dot + hdot, red);
     if (t == 0) {
         // sequential temperature scaling of the confidence: the head's logit over t_k
-        const float logit = (hw + dot + p.b) / (p.sts_temp ? p.sts_temp[p.k] : 1.f);
+        const float logit = (dot + p.b) / (p.sts_temp ? p.sts_temp[p.k] : 1.f);
         const float c = 1.f / (1.f + expf(-logit));
         p.tokens[o] = s_tok;
         p.conf[o] = c;
@@ -482,12 +450,11 @@ __global__ void __launch_bounds__(kCommitThreads)
 
 // ----------------------------------------------------------------- launchers
 
-cudaError_t launch_conf_hidden(const DraftStep& p, cudaStream_t s)
+cudaError_t launch_draft_setup(const DraftStep& p, cudaStream_t s)
 {
-    const int rows = p.R * p.G;
-    const int blocks = cdiv(rows, kHwRows);
-    const cudaError_t e = p.dtype == DSPARK_BF16 ? launch_pdl(conf_hidden_kernel<__nv_bfloat16>, blocks, 256, 0, s, p)
-                                                 : launch_pdl(conf_hidden_kernel<float>, blocks, 256, 0, s, p);
+    const int blocks = cdiv(std::max(p.R * p.G, p.R * p.r), 256);
+    const cudaError_t e = p.dtype == DSPARK_BF16 ? launch_pdl(draft_setup_kernel<__nv_bfloat16>, blocks, 256, 0, s, p)
+                                                 : launch_pdl(draft_setup_kernel<float>, blocks, 256, 0, s, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
