@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(t_full(i), 1);
             mbar_init(t_empty(i), EPI_WARPS);
         }
-        mbar_init(a_full, 1);
+        mbar_init(a_full, MODE == kDraftMode && SPLIT ? 2 : 1);   // split operand: the copy and the TMEM half
         mbar_init(a_empty, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
@@ -593,8 +593,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 epi_barrier();
                 if (MODE == kDraftMode) {
+                    // A = the tile's rows of a_next (W_1 of the previous tokens, written by the
+                    // previous kernel) from this CTA's replica, one TMA tile per 64 columns
+                    if (e == 0 && live) {
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        mbar_expect_tx(a_full, (uint32_t)(P.r / BK) * BM * 128u);
+                        const uint64_t pol = l2_policy_evict_last();
+                        for (int cb = 0; cb < P.r / BK; ++cb)
+                            tma_load_3d(sbase + L::OFF_A + cb * (BM * 128), &tmA, cb * BK, mt * BM,
+                                        (int)(blockIdx.x % A_REPLICAS), a_full, pol);
+                    }
                     // RNN head: the bf16 remainder of the operand rows goes to TMEM (the second A
-                    // operand), warpgroup g covering K elements [64g, 64g + 64) of its lanes' rows
+                    // operand) while that copy flies, warpgroup g covering K elements [64g, 64g + 64)
+                    // of its lanes' rows; a_full then takes a second arrival, so that the MMAs wait
+                    // for both halves of the operand
                     if (SPLIT) {
                         if (live && g * BK < P.r) {
                             uint32_t a[32];
@@ -620,16 +632,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             tc_fence_before();
                         }
                         epi_barrier();
-                    }
-                    // A = the tile's rows of a_next (W_1 of the previous tokens, written by the
-                    // previous kernel) from this CTA's replica, one TMA tile per 64 columns
-                    if (e == 0 && live) {
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        mbar_expect_tx(a_full, (uint32_t)(P.r / BK) * BM * 128u);
-                        const uint64_t pol = l2_policy_evict_last();
-                        for (int cb = 0; cb < P.r / BK; ++cb)
-                            tma_load_3d(sbase + L::OFF_A + cb * (BM * 128), &tmA, cb * BK, mt * BM,
-                                        (int)(blockIdx.x % A_REPLICAS), a_full, pol);
+                        if (e == 0 && live) mbar_arrive(a_full);
                     }
                 } else {
                     // A = W_1[prev] rows into TMEM: warpgroup g writes K elements [64g, 64g + 64) of
