@@ -164,3 +164,31 @@ def test_zero_survivals_never_admitted_and_ties_keep_prefixes(oracle_mod):
     out = oracle_mod.schedule(a, sps, oracle_mod.SCHED_SYNC)
     assert out["keep"].tolist() == [3, 4, 0]
     assert int(out["pool"]) == 7
+
+
+def test_sync_stop_comes_by_the_first_forced_decrease(oracle_mod):
+    # Admitting an m-th key adds a <= 1 to tau >= R, so once SPS(R + m - 1) * R >= SPS(R + m) * (R + 1)
+    # Theta cannot rise at m whatever the keys are: the sync scan admits fewer than that m. The GPU
+    # scheduler relies on this to take only the top keys; check the bound on random survivals and
+    # tables with drops of every size, including drops just below and above the forcing ratio.
+    rng = np.random.default_rng(5)
+    n_checked = 0
+    for trial in range(300):
+        R = int(rng.integers(1, 40))
+        G = int(rng.integers(1, 9))
+        n = R * (1 + G)
+        sps = np.full(n, 1000.0)
+        B = np.arange(1, n + 1)
+        for _ in range(int(rng.integers(1, 4))):
+            b0 = int(rng.integers(R + 1, R + R * G + 2))
+            ratio = 1.0 + float(rng.choice([0.2, 0.9, 1.0, 1.1, 5.0])) / R
+            sps = np.where(B >= b0, sps / ratio, sps)
+        c = rng.uniform(0.05, 1.0, size=(R, G))
+        surv = np.cumprod(c, axis=1)
+        surv[rng.random((R, G)) < 0.1] = 0.0
+        out = oracle_mod.schedule(surv, sps, oracle_mod.SCHED_SYNC)
+        forced = [m for m in range(1, R * G + 1) if sps[R + m - 2] * R >= sps[R + m - 1] * (R + 1)]
+        if forced:
+            assert int(out["admitted"]) < forced[0]
+            n_checked += 1
+    assert n_checked > 100
