@@ -60,7 +60,10 @@ enum {
     DSPARK_ERR_WORKSPACE = 3,         /* workspace missing or smaller than *_workspace_size */
     DSPARK_ERR_CUDA = 4,              /* a CUDA runtime / driver call failed */
     DSPARK_ERR_TIMEOUT = 5,           /* a bounded device-side wait ran out (device status word) */
-    DSPARK_ERR_DEVICE_INPUT = 6       /* an out-of-range device value was clamped (device status word) */
+    DSPARK_ERR_DEVICE_INPUT = 6,      /* an out-of-range device value was clamped (device status word) */
+    DSPARK_ERR_NONFINITE_INPUT = 7    /* a NaN or +inf logit (U, target) or a non-finite confidence logit
+                                         (h or a weight) was read (device status word); -inf logits are
+                                         zero-probability entries, not errors */
 };
 
 enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 };
@@ -176,10 +179,17 @@ dspark_status dspark_sample_block(const dspark_sample_args* args, void* workspac
  *  - Every call on a device shares the one array, which keeps the previous call's contents (the
  *    call clears what must start at zero). Calls whose work overlaps on the GPU (other streams,
  *    other host threads) race on it: serialise them.
- *  - Device-side status (clamped out-of-range device inputs) is kept in the array and not
- *    reported; use dspark_sample_block with a workspace and dspark_check to observe it.
+ *  - The status word at the start of the array collects what the kernels record on the device
+ *    (a clamped out-of-range device input, a bounded wait that ran out, a non-finite input).
+ *    The call clears it first; read it with dspark_check_static after the call and before the
+ *    next one.
  */
 dspark_status dspark_sample_block_static(const dspark_sample_args* args, void* stream);
+
+/* Synchronise `stream`, then return the device status word of the static array of
+ * dspark_sample_block_static on the current device (DSPARK_OK or the code a kernel of the last
+ * call recorded) and clear it. Like the array itself, it has no counterpart in the paper. */
+dspark_status dspark_check_static(void* stream);
 
 /*
  * dspark_schedule -- hardware-aware prefix scheduler (Algorithm 1; "admit").
@@ -349,8 +359,17 @@ uint64_t dspark_launch_count(void);
 dspark_status dspark_time_kernel(int32_t kernel, dspark_event_pair* events, int32_t capacity, int32_t* count);
 
 /* Synchronise `stream`, then return the device status word of `workspace`
- * (DSPARK_OK, DSPARK_ERR_TIMEOUT or DSPARK_ERR_DEVICE_INPUT) and clear it. */
+ * (DSPARK_OK, DSPARK_ERR_TIMEOUT, DSPARK_ERR_DEVICE_INPUT or DSPARK_ERR_NONFINITE_INPUT: the
+ * first code a kernel recorded since the last check) and clear it. */
 dspark_status dspark_check(void* workspace, void* stream);
+
+/* Bound, in nanoseconds of the device's global timer, of every device-side wait on another
+ * agent (a copy, an MMA, another CTA) in the calls made after this one, process-wide; 0
+ * restores the default of 4 s. Returns the previous bound. A wait that runs out records
+ * DSPARK_ERR_TIMEOUT in the status word; its kernel stops issuing work, lets its own copies and
+ * MMAs in flight complete, frees its tensor memory and returns, so the context stays usable.
+ * Meant for tests and debugging: results of a call whose wait ran out are not defined. */
+uint64_t dspark_set_wait_limit(uint64_t ns);
 
 /* Description of the last CUDA failure seen by a call on this thread (the kernel
  * family and the CUDA error name and string), or "no error". */

@@ -94,9 +94,10 @@ class _VerifyArgs(C.Structure):
         ("keep", C.c_void_p), ("temperature", C.c_void_p),
         ("seed", C.c_uint64), ("round", C.c_uint64),
         ("bias_first", C.c_int), ("noise_block", C.c_int), ("a_rows", C.c_void_p),
+        ("res_rel_eps", C.c_double),
         ("accepted", C.c_void_p), ("next_token", C.c_void_p), ("resampled", C.c_void_p),
         ("accept_margin", C.c_void_p), ("lse_t", C.c_void_p),
-        ("gap1", C.c_void_p), ("gap2", C.c_void_p), ("slack1", C.c_void_p), ("slack2", C.c_void_p),
+        ("gap1", C.c_void_p), ("gap2", C.c_void_p), ("rgap1", C.c_void_p), ("rgap2", C.c_void_p),
     ]
 
 
@@ -269,8 +270,11 @@ def schedule(surv, sps, mode=SCHED_SYNC, *, gamma=None, surv_capacity=None, thre
 # ----------------------------------------------------------------- verifier
 
 def verify(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temperature, seed, rnd, *,
-           gamma=None, req_ids=None, bias_first=1, noise_block=128, a_rows=None, threads=1):
-    """Rejection-sampling verification of the admitted prefixes of R requests."""
+           gamma=None, req_ids=None, bias_first=1, noise_block=128, a_rows=None, threads=1, res_rel_eps=0.0):
+    """Rejection-sampling verification of the admitted prefixes of R requests.
+
+    res_rel_eps: the relative error of the probabilities assumed by the residual draw's robust
+    margins rgap1 / rgap2 (equal to gap1 / gap2 when 0)."""
     target, U, E, W = _c(target), _c(U), _c(E), _c(W)
     dt = _dtype_code(U)
     if not (_dtype_code(target) == dt and _dtype_code(E) == dt and _dtype_code(W) == dt):
@@ -287,7 +291,7 @@ def verify(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temper
         "accepted": np.zeros(R, np.int32), "next_token": np.zeros(R, np.int32),
         "resampled": np.zeros(R, np.int32), "accept_margin": np.zeros((R, G)),
         "lse_t": np.zeros((R, G + 1)), "gap1": np.zeros(R), "gap2": np.zeros(R),
-        "slack1": np.zeros(R), "slack2": np.zeros(R),
+        "rgap1": np.zeros(R), "rgap2": np.zeros(R),
     }
 
     def part(se):
@@ -303,6 +307,7 @@ def verify(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temper
         a.seed, a.round = int(seed), int(rnd)
         a.bias_first, a.noise_block = int(bias_first), int(noise_block)
         a.a_rows = _p(None if arows is None else arows[s:e])
+        a.res_rel_eps = float(res_rel_eps)
         for k, arr in out.items():
             setattr(a, k, _p(arr[s:e]))
         rc = lib().dso_verify(C.byref(a))

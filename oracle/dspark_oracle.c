@@ -475,6 +475,54 @@ int dso_schedule(const dso_schedule_args* a)
 
 /* ------------------------------------------------------------- verifier */
 
+/* Margins of the residual draw ([P1] section 4 sample_residual) when every probability p_t(v),
+ * p_d(v) is known only to a relative error e: a block's mass sum max(0, p_t - p_d) then lies
+ * within e * sum (p_t + p_d) of its value, and so does each token's residual. m1 is the winning
+ * block's lowest possible perturbed value log(mass) + G minus the highest possible value of any
+ * other block; m2 the same for the tokens of the winning block. With e = 0 they are the draw's
+ * top-two gaps. A negative margin means another candidate could win under such errors. */
+static void residual_margins(const double* zt, double lse_t, const double* ld, double lse_d, int V, int nb,
+                             double e, draw_t dr, uint64_t seed, uint64_t round, uint32_t req, double* m1,
+                             double* m2)
+{
+    const int nblk = (V + nb - 1) / nb;
+    double low_w = -INFINITY, up_o = -INFINITY;
+    for (int b = 0; b < nblk; ++b) {
+        const int v0 = b * nb, v1 = (v0 + nb < V) ? v0 + nb : V;
+        double mass = 0.0, scale = 0.0;
+        for (int v = v0; v < v1; ++v) {
+            const double pt = exp(zt[v] - lse_t), pd = exp(ld[v] - lse_d);
+            if (pt > pd) mass += pt - pd;
+            scale += pt + pd;
+        }
+        const double g = gumbel(dso_uniform(seed, round, PUR_FINAL_BLOCK, req, 0, (uint32_t)b));
+        if (b == dr.block) {
+            const double lo = mass - e * scale;
+            low_w = lo > 0.0 ? log(lo) + g : -INFINITY;
+        } else {
+            const double hi = mass + e * scale;
+            if (hi > 0.0 && log(hi) + g > up_o) up_o = log(hi) + g;
+        }
+    }
+    *m1 = up_o == -INFINITY ? INFINITY : low_w - up_o;
+    low_w = -INFINITY;
+    up_o = -INFINITY;
+    const int v0 = dr.block * nb, v1 = (v0 + nb < V) ? v0 + nb : V;
+    for (int v = v0; v < v1; ++v) {
+        const double pt = exp(zt[v] - lse_t), pd = exp(ld[v] - lse_d);
+        const double res = pt - pd, scale = pt + pd;
+        const double g = gumbel(dso_uniform(seed, round, PUR_FINAL_ELEM, req, 0, (uint32_t)v));
+        if (v == dr.token) {
+            const double lo = res - e * scale;
+            low_w = lo > 0.0 ? log(lo) + g : -INFINITY;
+        } else {
+            const double hi = res + e * scale;
+            if (hi > 0.0 && log(hi) + g > up_o) up_o = log(hi) + g;
+        }
+    }
+    *m2 = up_o == -INFINITY ? INFINITY : low_w - up_o;
+}
+
 int dso_verify(const dso_verify_args* a)
 {
     if (!a || a->R < 0 || a->gamma_max < 1 || a->V < 1 || a->r < 1 || a->noise_block < 1) return 1;
@@ -517,7 +565,7 @@ int dso_verify(const dso_verify_args* a)
             a->next_token[q] = next;
             a->resampled[q] = n < ell ? 1 : 0;
             a->gap1[q] = a->gap2[q] = gap;
-            a->slack1[q] = a->slack2[q] = 0.0;
+            a->rgap1[q] = a->rgap2[q] = gap;
             continue;
         }
         /* longest accepted prefix: accept x_j with probability min(1, p_t/p_d) */
@@ -546,8 +594,6 @@ int dso_verify(const dso_verify_args* a)
         const double lse_t = logsumexp(zt, V);
         a->lse_t[(size_t)q * (G + 1) + n] = lse_t;
         draw_t dr;
-        a->slack1[q] = 0.0;
-        a->slack2[q] = 0.0;
         if (n < ell) {
             /* rejected at draft position n: resample from norm(max(0, p_t - p_d)) */
             const int prev = n == 0 ? a->anchor[q] : a->tokens[(size_t)q * G + n - 1];
@@ -568,35 +614,18 @@ int dso_verify(const dso_verify_args* a)
             }
             dr = two_level_draw(lw, V, nb, a->seed, a->round, PUR_FINAL_BLOCK, PUR_FINAL_ELEM, rid, 0);
             if (any) {
-                /* fp32 error model of a GPU residual: each p carries a relative
-                 * error of about 1e-6, so a block mass sum(max(0,pt-pd)) carries an
-                 * absolute error of 1e-6 * sum(pt+pd); convert to log space for the
-                 * two leading candidates. */
-                const int cand_b[2] = {dr.block, dr.second_block};
-                for (int c = 0; c < 2; ++c) {
-                    const int b = cand_b[c];
-                    if (b < 0) continue;
-                    const int v0 = b * nb, v1 = (v0 + nb < V) ? v0 + nb : V;
-                    double mass = 0.0, scale = 0.0;
-                    for (int v = v0; v < v1; ++v) {
-                        const double pt = exp(zt[v] - lse_t), pd = exp(ld[v] - lse_d);
-                        if (pt > pd) mass += pt - pd;
-                        scale += pt + pd;
-                    }
-                    a->slack1[q] += mass > 0.0 ? 1e-6 * scale / mass : INFINITY;
-                }
-                const int cand_v[2] = {dr.token, dr.second_token};
-                for (int c = 0; c < 2; ++c) {
-                    const int v = cand_v[c];
-                    if (v < 0) continue;
-                    const double pt = exp(zt[v] - lse_t), pd = exp(ld[v] - lse_d);
-                    a->slack2[q] += pt > pd ? 1e-6 * (pt + pd) / (pt - pd) : INFINITY;
-                }
+                residual_margins(zt, lse_t, ld, lse_d, V, nb, a->res_rel_eps, dr, a->seed, a->round, rid,
+                                 &a->rgap1[q], &a->rgap2[q]);
+            } else {
+                a->rgap1[q] = dr.gap1;
+                a->rgap2[q] = dr.gap2;
             }
             a->resampled[q] = 1;
         } else {
             /* every admitted token accepted: bonus token from target row l_r */
             dr = two_level_draw(zt, V, nb, a->seed, a->round, PUR_FINAL_BLOCK, PUR_FINAL_ELEM, rid, 0);
+            a->rgap1[q] = dr.gap1;
+            a->rgap2[q] = dr.gap2;
             a->resampled[q] = 0;
         }
         a->next_token[q] = dr.token;

@@ -129,6 +129,8 @@ typedef struct {
     int bias_first, noise_block;
     const double* a_rows;               /* [R][gamma_max][r] or NULL: bias operand of each draft position
                                            (from dso_sample_block); NULL = W_1[x_{k-1}] (Markov head) */
+    double res_rel_eps;                 /* relative error of the probabilities assumed for rgap1, rgap2 (0:
+                                           rgap equals gap) */
     /* outputs */
     int32_t* accepted;                  /* [R] n_r */
     int32_t* next_token;                /* [R] residual or bonus token */
@@ -137,8 +139,10 @@ typedef struct {
     double* lse_t;                      /* [R][gamma_max+1] target log-normaliser of rows 0..l_r, NaN otherwise */
     double* gap1;                       /* [R] block-level top-two gap of the final draw */
     double* gap2;                       /* [R] element-level top-two gap of the final draw */
-    double* slack1;                     /* [R] bound on the fp32 error of the block-level values (residual only) */
-    double* slack2;                     /* [R] same, element level */
+    double* rgap1;                      /* [R] block-level margin of the final draw when every probability
+                                           carries a relative error up to res_rel_eps (residual draws; gap1
+                                           otherwise): the winner's lowest value minus any other's highest */
+    double* rgap2;                      /* [R] same, element level inside the winning block */
 } dso_verify_args;
 
 int dso_verify(const dso_verify_args* a);

@@ -30,7 +30,8 @@ MAX_GAMMA = 32
 MAX_SLOTS = 8192
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "workspace", 4: "CUDA error",
-          5: "timeout", 6: "out-of-range device input"}
+          5: "timeout", 6: "out-of-range device input", 7: "non-finite input"}
+ERR_TIMEOUT, ERR_DEVICE_INPUT, ERR_NONFINITE_INPUT = 5, 6, 7
 
 _vp = C.c_void_p
 
@@ -84,7 +85,8 @@ class AssembleArgs(C.Structure):
 EXPORTS = ("dspark_sample_workspace_size", "dspark_sample_block", "dspark_schedule_workspace_size",
            "dspark_schedule", "dspark_verify_workspace_size", "dspark_verify", "dspark_check",
            "dspark_status_string", "dspark_abi_version", "dspark_launch_count", "dspark_time_kernel",
-           "dspark_last_error", "dspark_sample_path", "dspark_sample_block_static",
+           "dspark_last_error", "dspark_sample_path", "dspark_sample_block_static", "dspark_check_static",
+           "dspark_set_wait_limit",
            "dspark_assemble_workspace_size", "dspark_assemble")
 
 KERNELS = {"draft_setup": 0, "draft_stats": 1, "draft_commit": 2, "schedule": 3, "verify_rows": 4,
@@ -132,6 +134,10 @@ def lib():
         L.dspark_abi_version.restype = C.c_int32
         L.dspark_sample_block_static.argtypes = [C.POINTER(SampleArgs), _vp]
         L.dspark_sample_block_static.restype = C.c_int32
+        L.dspark_check_static.argtypes = [_vp]
+        L.dspark_check_static.restype = C.c_int32
+        L.dspark_set_wait_limit.argtypes = [C.c_uint64]
+        L.dspark_set_wait_limit.restype = C.c_uint64
         L.dspark_sample_path.argtypes = [C.POINTER(SampleArgs)]
         L.dspark_sample_path.restype = C.c_int32
         L.dspark_last_error.argtypes = []
@@ -325,6 +331,18 @@ def sample_block_static(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd,
                          head=head, W_rnn=W_rnn)
     _call("dspark_sample_block_static", C.byref(a), _stream(stream))
     return out
+
+
+def set_wait_limit(ns: int) -> int:
+    """Bound (ns) of every device-side wait of the calls made after this one (0: the default of
+    4 s); returns the previous bound. A wait that runs out records ERR_TIMEOUT (for tests)."""
+    return int(lib().dspark_set_wait_limit(int(ns)))
+
+
+def check_static(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the status word of the static array that
+    sample_block_static uses on the current device."""
+    return lib().dspark_check_static(_stream(stream))
 
 
 def schedule_args(surv, sps, mode=SCHED_SYNC, *, gamma=None, surv_capacity=None, out=None, threshold=0.0):

@@ -17,6 +17,9 @@ namespace {
 
 std::atomic<unsigned long long> g_launches{0};
 
+constexpr unsigned long long kDefaultWaitNs = 4000000000ull;   // 4 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+
 struct KernelTimer {
     int kernel = -1;
     dspark_event_pair* events = nullptr;
@@ -200,6 +203,8 @@ T* at(void* ws, size_t off)
 
 }  // namespace
 
+unsigned long long dspark::wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 extern "C" {
 
 int32_t dspark_abi_version(void) { return DSPARK_ABI_VERSION; }
@@ -214,6 +219,7 @@ const char* dspark_status_string(dspark_status s)
     case DSPARK_ERR_CUDA: return "CUDA error";
     case DSPARK_ERR_TIMEOUT: return "bounded device wait ran out";
     case DSPARK_ERR_DEVICE_INPUT: return "out-of-range device input (clamped)";
+    case DSPARK_ERR_NONFINITE_INPUT: return "NaN or +inf in a logit or hidden-state input";
     default: return "unknown status";
     }
 }
@@ -273,6 +279,7 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.draft_lse = a->draft_lse;
     p.draft_logit = a->draft_logit;
     p.sts_temp = a->sts_temp;
+    p.wait_ns = wait_limit_ns();
     p.status = at<int>(ws, 0);
     p.x_cur = at<int32_t>(ws, L.x_cur);
     p.stats = at<float2>(ws, L.stats);
@@ -440,6 +447,7 @@ dspark_status dspark_verify(const dspark_verify_args* a, void* ws, size_t ws_byt
     p.accepted = a->accepted;
     p.next_token = a->next_token;
     p.resampled = a->resampled;
+    p.wait_ns = wait_limit_ns();
     p.status = at<int>(ws, 0);
     p.row_stats = at<float2>(ws, L.row_stats);
     p.lse_t = at<float>(ws, L.lse_t);
@@ -458,6 +466,11 @@ dspark_status dspark_verify(const dspark_verify_args* a, void* ws, size_t ws_byt
 }
 
 const char* dspark_last_error(void) { return g_last_error; }
+
+uint64_t dspark_set_wait_limit(uint64_t ns)
+{
+    return g_wait_ns.exchange(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
+}
 
 uint64_t dspark_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

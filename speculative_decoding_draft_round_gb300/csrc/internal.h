@@ -56,6 +56,7 @@ struct DraftStep {
     void* a_lo;          // [R][r] bf16: operand minus its bf16 rounding (tensor-core path)
     void* zbuf;          // [2][R][3r] bf16 by step parity: [hi(s_{k-1}); lo(s_{k-1}); W_1[x_{k-1}]], the
                          // tensor-core RNN step's operand rows (NULL: the CUDA-core step)
+    unsigned long long wait_ns;   // bound of each device-side wait (dspark_set_wait_limit)
 };
 
 // Verification (dspark_verify).
@@ -86,6 +87,7 @@ struct VerifyParams {
     int32_t* rej_list;   // [R] the rejected requests, in the order verify_decide found them
     float* res_stats;    // [R_pad][nblk] block sums of max(0, p_t - p_d)
     const float* a_rows; // [R][G][r] bias operands reported by the sampler, or NULL (W_1[x_{n-1}])
+    unsigned long long wait_ns;   // bound of each device-side wait (dspark_set_wait_limit)
 };
 
 struct ScheduleParams {
@@ -151,6 +153,10 @@ bool rnn_tc_supported(const DraftStep& p);
 cudaError_t rnn_tc_maps(const DraftStep& p, CUtensorMap* zmap, CUtensorMap* wmap);
 cudaError_t launch_rnn_z0(const DraftStep& p, cudaStream_t s);      // z[0]: zero state, W_1 of the anchor
 cudaError_t launch_rnn_step_tc(const DraftStep& p, const CUtensorMap& zmap, const CUtensorMap& wmap, cudaStream_t s);
+
+// Bound of the device-side waits on other agents (copies, MMAs, other CTAs) for the next
+// launches; 4 s unless dspark_set_wait_limit changed it.
+unsigned long long wait_limit_ns();
 
 inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

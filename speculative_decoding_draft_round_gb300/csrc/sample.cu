@@ -145,6 +145,8 @@ __global__ void __launch_bounds__(kNoiseBlock) draft_stats_simt_kernel(DraftStep
         const float e = v < p.V ? exp2f(x - m) : 0.f;
         const float s = block_sum<kNoiseBlock>(e, red);
         if (t == 0) {
+            // a NaN or +inf logit leaves a NaN sum or an infinite maximum (-inf is a zero weight)
+            if (!(s >= 0.f) || m == INFINITY) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
             p.stats[(size_t)q * p.n_stats + b] = make_float2(m, s);
             // block key of the two-level draw; greedy requests take the block holding the maximum
             const float z = req[j].greedy ? m
@@ -186,16 +188,16 @@ __device__ __forceinline__ LseAcc lse_merge(LseAcc a, LseAcc b)
 constexpr int kStatsPerThread = 8;       // block statistics held in registers per thread (nblk <= 2048)
 constexpr int kBiasRows = 16;            // W rows per thread in the fast path (r <= 256)
 
-constexpr unsigned long long kCommitWaitNs = 4000000000ull;   // 4 s
+constexpr unsigned long long kCommitDrainNs = 4000000000ull;   // 4 s: a copy in flight lands long before
 
 // Bounded wait for phase `parity` of a shared-memory barrier; false (and DSPARK_ERR_TIMEOUT
 // recorded) when it runs out.
-__device__ __noinline__ bool commit_wait(uint32_t bar, uint32_t parity, int* status)
+__device__ __noinline__ bool commit_wait(uint32_t bar, uint32_t parity, int* status, unsigned long long limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > kCommitWaitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             raise_status(status, DSPARK_ERR_TIMEOUT);
             return false;
         }
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(kCommitThreads)
     float bias = 0.f;
     bool w_ok = true;
     if (tma_w) {
-        w_ok = commit_wait(wbar, 0u, p.status);
+        w_ok = commit_wait(wbar, 0u, p.status, p.wait_ns);
         const uint4* wt = reinterpret_cast<const uint4*>(wtile);
 #pragma unroll
         for (int j = 0; j < kBiasRows; ++j) {
@@ -435,6 +437,7 @@ __global__ void __launch_bounds__(kCommitThreads)
     if (t == 0) {
         // sequential temperature scaling of the confidence: the head's logit over t_k
         const float logit = (dot + p.b) / (p.sts_temp ? p.sts_temp[p.k] : 1.f);
+        if (!isfinite(logit)) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);   // h, or a weight
         const float c = 1.f / (1.f + expf(-logit));
         p.tokens[o] = s_tok;
         p.conf[o] = c;
@@ -445,7 +448,7 @@ __global__ void __launch_bounds__(kCommitThreads)
         p.x_cur[q] = s_tok;
     }
     // a copy whose wait gave up may still be writing shared memory: let it land before exit
-    if (tma_w && !w_ok && t == 0) (void)commit_wait(wbar, 0u, p.status);
+    if (tma_w && !w_ok && t == 0) (void)commit_wait(wbar, 0u, nullptr, kCommitDrainNs);
 }
 
 // ----------------------------------------------------------------- launchers

@@ -78,7 +78,7 @@ struct Lay {
     static constexpr uint32_t OFF_PART = OFF_A + A_BYTES;                   // [2][4][128] float2
     static constexpr uint32_t OFF_META = OFF_PART + 2 * 4 * BM * 8;        // per-row metadata, see RowMeta
     static constexpr uint32_t OFF_BAR = OFF_META + META_BYTES;
-    static constexpr int N_BARS = 2 * W_ST + 2 * U_ST + 2 * TMEM_BUFS + 2;
+    static constexpr int N_BARS = 2 * W_ST + 2 * U_ST + 2 * TMEM_BUFS + 3;
     static constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM_USED = OFF_MISC + 16 + MAX_TILES * 4;
     static constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;               // alignment slack
@@ -105,7 +105,9 @@ struct ItemIter {
     }
 };
 
-constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;   // 4 s
+// Bound of the waits that drain this CTA's own copies and MMAs before it exits: these complete
+// in microseconds once issued, whatever the limit of the other waits (a launch parameter).
+constexpr unsigned long long DRAIN_LIMIT_NS = 4000000000ull;   // 4 s
 
 // instruction descriptor, kind::f16: D fp32, A = B = bf16, A K-major (shared memory in draft mode,
 // TMEM in residual mode), B MN-major, M = 128, N = 128
@@ -117,6 +119,7 @@ constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (0u << 15) | (1u
 struct Ctl {
     volatile int* abort;
     int* status;
+    unsigned long long limit_ns;   // bound of each wait (dspark_set_wait_limit)
 };
 
 // Wait for the phase of `bar` with the given parity; false if the CTA aborted or the wait ran out.
@@ -127,7 +130,7 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Ctl c)
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*c.abort) return false;
-        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        if (globaltimer() - t0 > c.limit_ns) {
             *c.abort = 1;
             raise_status(c.status, DSPARK_ERR_TIMEOUT);
             return false;
@@ -147,7 +150,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Ctl c)
 __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity)
 {
     const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < WAIT_LIMIT_NS) {
+    while (!mbar_try_wait(bar, parity) && globaltimer() - t0 < DRAIN_LIMIT_NS) {
     }
 }
 
@@ -253,6 +256,7 @@ struct TcParams {
     VerifyParams v;   // residual mode
     int R, G, V, r, nblk, k;
     int* status;
+    unsigned long long wait_ns;   // bound of every wait that depends on another agent
 };
 
 // Does request q take part at this launch?
@@ -375,6 +379,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto t_empty = [&](int i) { return bar0 + 8u * (2 * W_STAGES + 2 * U_STAGES + TMEM_BUFS + i); };
     const uint32_t a_full = bar0 + 8u * (2 * W_STAGES + 2 * U_STAGES + 2 * TMEM_BUFS);
     const uint32_t a_empty = a_full + 8u;
+    const uint32_t mma_done = a_full + 16u;   // every MMA of this CTA has completed (before TMEM is freed)
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
     int* s_ntiles = reinterpret_cast<int*>(smem + OFF_MISC + 8);
@@ -382,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int* s_nact = reinterpret_cast<int*>(smem + OFF_MISC + 12);   // residual: rejected requests
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const Ctl ctl{s_abort, P.status};
+    const Ctl ctl{s_abort, P.status, P.wait_ns};
     const int n_mt = (P.R + BM - 1) / BM;
 
     // Tiles with at least one request taking part. Residual mode: the rows are the rejected
@@ -425,6 +430,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         mbar_init(a_full, MODE == kDraftMode && SPLIT ? 2 : 1);   // split operand: the copy and the TMEM half
         mbar_init(a_empty, 1);
+        mbar_init(mma_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
     }
@@ -545,6 +551,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_commit(t_full(tb.idx));
             tb.next(TMEM_BUFS);
         }
+        // every MMA issued above completes before the CTA frees its TMEM, after an abort too
+        mma_commit(mma_done);
+        mbar_drain(mma_done, 0u);
     } else if (warp >= 4) {
         // ---------------- epilogue (and A gather)
         // The A rows read the previous kernel's output and the block statistics overwrite what it
@@ -563,6 +572,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t a_par = 0;
         int cur_tile = -1;
         bool live = true;
+        int a_fills = 0;   // A-tile copies this thread issued (thread e == 0, draft mode)
         uint4 uv[4] = {}, tv[4] = {};
         RowMeta rm_reg{};
         bool have_next = false;   // residual: uv / tv already hold this item's columns
@@ -596,6 +606,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // A = the tile's rows of a_next (W_1 of the previous tokens, written by the
                     // previous kernel) from this CTA's replica, one TMA tile per 64 columns
                     if (e == 0 && live) {
+                        ++a_fills;
                         asm volatile("fence.proxy.async.global;" ::: "memory");
                         mbar_expect_tx(a_full, (uint32_t)(P.r / BK) * BM * 128u);
                         const uint64_t pol = l2_policy_evict_last();
@@ -786,6 +797,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float2 t = pp[gg * BM + m];
                         if (t.y > 0.f) S += t.y * ex2(t.x - M);
                     }
+                    // a NaN or +inf logit leaves a NaN sum or an infinite maximum (-inf is a zero weight)
+                    if (!(S >= 0.f) || M == INFINITY) raise_status(P.status, DSPARK_ERR_NONFINITE_INPUT);
                     // merge the block into this CTA's running log-normaliser of the row
                     if (M > run_m) {
                         run_s = run_s * ex2(run_m - M) + S;
@@ -812,6 +825,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (cur_tile >= 0) flush_run(s_tiles[cur_tile]);
             for (int mt2 = 0; mt2 * BM < P.R; ++mt2)
                 if (!((done_tiles >> mt2) & 1ull)) flush_run(mt2);
+            // the last A copy lands before the CTA exits (it may be unconsumed after an abort)
+            if (e == 0 && a_fills > 0) mbar_drain(a_full, (uint32_t)(a_fills - 1) & 1u);
         }
     }
     __syncwarp();
@@ -994,6 +1009,7 @@ cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s)
     P.nblk = p.nblk;
     P.k = p.k;
     P.status = p.status;
+    P.wait_ns = p.wait_ns;
     return p.a_lo ? launch_tc<kDraftMode, true>(P, tmW, tmU, tmA, s) : launch_tc<kDraftMode>(P, tmW, tmU, tmA, s);
 }
 
@@ -1013,6 +1029,7 @@ cudaError_t launch_residual_stats_tc(const VerifyParams& p, cudaStream_t s)
     P.nblk = p.nblk;
     P.k = 0;
     P.status = p.status;
+    P.wait_ns = p.wait_ns;
     return launch_tc<kResidualMode>(P, tmW, tmW, tmW, s);
 }
 

@@ -11,6 +11,8 @@
 // exits. It calls no cudaMalloc, cudaFree or allocating library routine.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -19,7 +21,9 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_workspace[DSPARK_STATIC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_static_ptr[kMaxDevices] = {};   // device address of g_static_workspace, per device
+// device address of g_static_workspace, per device; host threads may call concurrently, and
+// each stores the same value, so a relaxed atomic slot is enough
+std::atomic<void*> g_static_ptr[kMaxDevices] = {};
 
 // Device address of the static array on the current device. The host-side name of a
 // __device__ array is only a stand-in, so the address is looked up once per device, with that
@@ -28,12 +32,12 @@ dspark_status static_workspace(void** out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSPARK_ERR_CUDA;
-    if (!g_static_ptr[dev]) {
-        void* p = nullptr;
+    void* p = g_static_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return DSPARK_ERR_CUDA;
-        g_static_ptr[dev] = p;
+        g_static_ptr[dev].store(p, std::memory_order_relaxed);
     }
-    *out = g_static_ptr[dev];
+    *out = p;
     return DSPARK_OK;
 }
 
@@ -54,4 +58,14 @@ extern "C" dspark_status dspark_sample_block_static(const dspark_sample_args* ar
     // other scratch regions are written before they are read within a call)
     if (cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DSPARK_ERR_CUDA;
     return dspark_sample_block(args, ws, (size_t)DSPARK_STATIC_WORKSPACE_BYTES, stream);
+}
+
+// The status word of the static array: clamped device inputs and bounded waits that ran out in
+// the calls since the last check. Synchronises the stream, returns the word and clears it.
+extern "C" dspark_status dspark_check_static(void* stream)
+{
+    void* ws = nullptr;
+    const dspark_status sw = static_workspace(&ws);
+    if (sw != DSPARK_OK) return sw;
+    return dspark_check(ws, stream);
 }

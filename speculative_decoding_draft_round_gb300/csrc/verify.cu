@@ -119,7 +119,7 @@ __device__ __forceinline__ void row_block_stats8(const T* row, int V, int b0, fl
 // Greedy requests (temperature 0): per 128-wide block the maximum of the raw target logits and
 // the lowest index attaining it, stored as (max, index) in the statistics slot.
 template <typename T>
-__device__ __forceinline__ float2 row_block_argmax(const T* row, int V, int b, int lane)
+__device__ __forceinline__ float2 row_block_argmax(const T* row, int V, int b, int lane, bool& nonfinite)
 {
     float m = -INFINITY;
     int mi = -1;
@@ -128,6 +128,7 @@ __device__ __forceinline__ float2 row_block_argmax(const T* row, int V, int b, i
         const int v = b * kNoiseBlock + e * 32 + lane;
         if (v < V) {
             const float x = ld(row, v);
+            if (x != x || x == INFINITY) nonfinite = true;
             if (x > m || mi < 0) {
                 m = x;
                 mi = v;
@@ -156,10 +157,12 @@ __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParam
         for (int i = 0; i <= ell; ++i) {
             const T* row = static_cast<const T*>(p.target) + ((size_t)q * (p.G + 1) + i) * p.V;
             float2* out = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
+            bool nonfinite = false;
             for (int bb = 0; bb < kRowBlocksPerWarp && b0 + bb < p.nblk; ++bb) {
-                const float2 st = row_block_argmax<T>(row, p.V, b0 + bb, lane);
+                const float2 st = row_block_argmax<T>(row, p.V, b0 + bb, lane, nonfinite);
                 if (lane == 0) out[b0 + bb] = st;
             }
+            if (nonfinite) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
         }
         return;
     }
@@ -174,6 +177,8 @@ __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParam
             for (int bb = 1; bb < kRowBlocksPerWarp; ++bb)
                 if (lane == bb) v = st[bb];
             out[b0 + lane] = v;
+            // a NaN or +inf logit leaves a NaN sum or an infinite maximum (-inf is a zero weight)
+            if (!(v.y >= 0.f) || v.x == INFINITY) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
         }
     }
 }

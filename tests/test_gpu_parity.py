@@ -8,7 +8,7 @@ import torch
 import oracle
 import speculative_decoding_draft_round_gb300 as ds
 from speculative_decoding_draft_round_gb300 import workloads as wl
-from parity import check_sample, check_schedule, check_verify, to_np
+from parity import add_counts, check_sample, check_schedule, check_verify, new_counts, report, to_np
 from conftest import load_golden
 
 pytestmark = pytest.mark.gpu
@@ -62,14 +62,16 @@ def test_sample_block_matches_oracle(spec, conf_token):
     rnd = _make(spec, conf_token=conf_token)
     ids = np.arange(rnd.R)
     for path in _paths(rnd):
+        total = new_counts()
         for rnd_idx in (0, 7):
             out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature,
                                   rnd.anchor, rnd.seed, rnd_idx, gamma=rnd.gamma, conf_token=conf_token,
                                   path=path)
             assert ds.check(out["workspace"]) == 0
             rnd.round = rnd_idx
-            n_exc = check_sample(rnd, out, ids)
-            assert n_exc <= max(2, rnd.R * rnd.gamma_max // 1000)
+            add_counts(total, check_sample(rnd, out, ids))
+        report("sample %s conf_token=%d path=%d" % (spec["name"], conf_token, path), total)
+        assert total["draw"] <= max(2, total["checked_tokens"] // 1000)
 
 
 def test_bias_first_off_and_tiny_vocab():
@@ -108,7 +110,7 @@ def test_schedule_matches_oracle(mode):
                 gamma = torch.randint(0, G + 1, (R,), generator=gen, dtype=torch.int32).to(DEV) if ties else None
                 out = ds.schedule(surv, sps.to(DEV), mode, gamma=gamma, surv_capacity=old)
                 assert ds.check(out["workspace"]) == 0
-                n_exc += check_schedule(surv, sps, mode, out, gamma=gamma, surv_capacity=old)
+                n_exc += check_schedule(surv, sps, mode, out, gamma=gamma, surv_capacity=old)["theta"]
     assert n_exc <= 2
 
 
@@ -130,7 +132,7 @@ def test_schedule_monotone_runs_match_oracle(mode):
             gamma = torch.randint(0, G + 1, (R,), generator=gen, dtype=torch.int32).to(DEV) if ties else None
             out = ds.schedule(surv, sps.to(DEV), mode, gamma=gamma, surv_capacity=old)
             assert ds.check(out["workspace"]) == 0
-            n_exc += check_schedule(surv, sps, mode, out, gamma=gamma, surv_capacity=old)
+            n_exc += check_schedule(surv, sps, mode, out, gamma=gamma, surv_capacity=old)["theta"]
     assert n_exc <= 2
 
 
@@ -179,7 +181,7 @@ def test_schedule_sync_forced_stop_matches_oracle():
                         if variant == "ties" else None
                     out = ds.schedule(surv, sps.to(DEV), ds.SCHED_SYNC, gamma=gamma)
                     assert ds.check(out["workspace"]) == 0
-                    n_exc += check_schedule(surv, sps, ds.SCHED_SYNC, out, gamma=gamma)
+                    n_exc += check_schedule(surv, sps, ds.SCHED_SYNC, out, gamma=gamma)["theta"]
     assert n_exc <= 2
 
 
@@ -213,6 +215,7 @@ def test_verify_matches_oracle(spec):
     ids = np.arange(rnd.R)
     gen = torch.Generator().manual_seed(5)
     for path in _paths(rnd):
+        total = new_counts()
         sout = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature,
                                rnd.anchor, rnd.seed, rnd.round, gamma=rnd.gamma, path=path)
         g = torch.full((rnd.R,), rnd.gamma_max) if rnd.gamma is None else rnd.gamma.cpu()
@@ -228,15 +231,20 @@ def test_verify_matches_oracle(spec):
                              sout["draft_logit"], keep, rnd.temperature, rnd.seed, rnd.round, gamma=rnd.gamma,
                              path=path)
             assert ds.check(vout["workspace"]) == 0
-            n_exc = check_verify(rnd, sout, keep, vout, ids)
-            assert n_exc <= max(2, rnd.R // 100)
+            add_counts(total, check_verify(rnd, sout, keep, vout, ids))
+        report("verify %s path=%d" % (spec["name"], path), total)
+        assert total["draw"] + total["accept"] + total["residual_fp32"] <= max(2, 3 * rnd.R // 100)
 
 
 def test_tiny_round_end_to_end():
     """The tiny round exactly: the oracle runs alone from the inputs (its own draws feed its
-    scheduler and verifier) and every output must equal the GPU's."""
+    scheduler and verifier) and every output must equal the GPU's. A round in which one of the
+    oracle's own decisions lies within the tolerance of a tie is counted, not compared; at
+    least 18 of the 20 rounds must be compared in full."""
     rnd = wl.tiny(device=DEV)
     runner = ds.RoundRunner(rnd)
+    skipped = {"draw": 0, "theta": 0, "verify": 0}
+    compared = 0
     for rnd_idx in range(20):
         runner.set_round(rnd_idx)
         runner.run()
@@ -247,11 +255,13 @@ def test_tiny_round_end_to_end():
                                   rnd_idx)
         gap = np.minimum(o_s["gap1"], o_s["gap2"])
         if np.any(gap < 1e-4):
-            continue   # a near-tie draw: covered by the stage-wise tests
+            skipped["draw"] += 1
+            continue
         assert np.array_equal(to_np(res["tokens"]), o_s["tokens"])
         assert np.allclose(to_np(res["surv"]), o_s["surv"], atol=1e-5)
         o_c = oracle.schedule(o_s["surv"], to_np(rnd.sps).astype(np.float64), rnd.mode)
         if o_c["min_margin"] <= 1e-12:
+            skipped["theta"] += 1
             continue
         assert to_np(res["keep"]).tolist() == o_c["keep"].tolist()
         o_v = oracle.verify(to_np(rnd.target), to_np(rnd.U), to_np(rnd.E), to_np(rnd.W), to_np(rnd.anchor),
@@ -259,10 +269,14 @@ def test_tiny_round_end_to_end():
                             rnd.seed, rnd_idx)
         if np.nanmin(o_v["accept_margin"], initial=1.0) < 1e-4 or np.min(o_v["gap1"]) < 1e-4 or \
                 np.min(o_v["gap2"]) < 1e-4:
+            skipped["verify"] += 1
             continue
         assert to_np(res["accepted"]).tolist() == o_v["accepted"].tolist()
         assert to_np(res["next_token"]).tolist() == o_v["next_token"].tolist()
         assert to_np(res["resampled"]).tolist() == o_v["resampled"].tolist()
+        compared += 1
+    print("tiny round end to end: %d of 20 rounds compared in full, near-ties %s" % (compared, skipped))
+    assert compared >= 18
 
 
 def test_out_of_range_device_inputs_are_clamped_and_reported():

@@ -157,3 +157,45 @@ def test_residual_reads_the_bias_of_the_rejected_position(oracle_mod):
     res /= res.sum()
     assert sel.sum() > 5000
     assert _chi2(np.bincount(v["next_token"][sel], minlength=V), res) > 1e-3
+
+
+def test_residual_margins_under_relative_errors(oracle_mod):
+    """The residual draw's robust margins (rgap): equal to the exact top-two gaps when no error
+    is assumed; never larger when one is; and their sign agrees with a brute-force search over
+    perturbed probabilities (each p_t(v), p_d(v) moved by at most the relative error e, in the
+    direction that helps the runner-up) on a three-token residual max(0, p_t - p_d)."""
+    V = 3
+    pd = np.array([0.2, 0.3, 0.5])
+    pt = np.array([0.5, 0.35, 0.15])
+    n = 64
+    U = np.ascontiguousarray(np.broadcast_to(np.log(pd)[None, None], (n, 1, V)))
+    E, W = np.zeros((V, 1)), np.zeros((1, V))
+    T = np.ones(n, np.float32)
+    anchor = np.zeros(n, np.int32)
+    tokens = np.full((n, 1), 2, np.int32)            # p_t(2) / p_d(2) = 0.3: mostly rejected
+    lse = np.zeros((n, 1))
+    logit = np.full((n, 1), np.log(0.5))
+    target = np.ascontiguousarray(np.broadcast_to(np.log(np.stack([pt, pt]))[None], (n, 2, V)))
+    keep = np.ones(n, np.int32)
+    base = oracle_mod.verify(target, U, E, W, anchor, tokens, lse, logit, keep, T, 5, 1)
+    rej = base["resampled"] == 1
+    assert rej.sum() > 20
+    np.testing.assert_array_equal(base["rgap2"], base["gap2"])
+    res = pt - pd
+    for e in (1e-3, 0.05, 0.1, 0.2):
+        o = oracle_mod.verify(target, U, E, W, anchor, tokens, lse, logit, keep, T, 5, 1, res_rel_eps=e)
+        assert np.all(o["rgap2"][rej] <= base["gap2"][rej])
+        for q in np.where(rej)[0]:
+            g = np.array([-np.log(-np.log(oracle_mod.uniform(5, 1, 2, q, 0, v))) for v in range(V)])
+            w = int(o["next_token"][q])
+            # brute force: the winner's p_t down and p_d up, one rival's p_t up and p_d down, by e
+            lo = pt[w] * (1 - e) - pd[w] * (1 + e)
+            beaten = False
+            for v in range(V):
+                if v == w:
+                    continue
+                hi = pt[v] * (1 + e) - pd[v] * (1 - e)
+                if hi > 0 and (lo <= 0 or np.log(hi) + g[v] >= np.log(lo) + g[w]):
+                    beaten = True
+            assert beaten == (o["rgap2"][q] <= 0), (e, q, o["rgap2"][q])
+    assert res[2] < 0

@@ -39,7 +39,7 @@ def test_static_entry_matches_workspace_entry_twice(shape):
         assert ds.check(ref["workspace"]) == 0
         got = ds.sample_block_static(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature,
                                      rnd.anchor, rnd.seed, rnd_idx, gamma=rnd.gamma)
-        torch.cuda.synchronize()
+        assert ds.check_static() == 0   # synchronises; no clamped input, timeout or non-finite value
         _compare(got, ref)
 
 
@@ -59,3 +59,24 @@ def test_static_entry_rejects_shapes_beyond_its_array():
     with pytest.raises(ds.DsparkError) as err:
         ds.sample_block_static(*args)
     assert err.value.code == 2
+
+
+@pytest.mark.parametrize("workload", [1, 2, 3, 4, 5])
+def test_static_array_holds_each_workload(workload):
+    """The scratch each of the five workload shapes needs, from dspark_sample_workspace_size on
+    this device (the tensor-core layout depends on the SM count), fits the static array."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    R, G, V, r, d, dt = wl.SHAPES[workload]
+    dev = "cuda"
+    args = (torch.empty((R, G, V), dtype=dt, device=dev), torch.empty((V, r), dtype=dt, device=dev),
+            torch.empty((r, V), dtype=dt, device=dev), torch.empty((R, G, d), dtype=dt, device=dev),
+            torch.zeros(d, device=dev), torch.zeros(r, device=dev), 0.0, torch.ones(R, device=dev),
+            torch.zeros(R, dtype=torch.int32, device=dev), 1, 0)
+    a, _ = ds.sample_args(*args)
+    need = ds.workspace_bytes("sample", a)
+    print("workload %d (R=%d G=%d V=%d r=%d): sampler scratch %.2f MiB of %.0f MiB" % (
+        workload, R, G, V, r, need / 2**20, ds.STATIC_WORKSPACE_BYTES / 2**20))
+    assert need <= ds.STATIC_WORKSPACE_BYTES
+    del args
+    torch.cuda.empty_cache()
