@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kNoiseBlock) draft_stats_simt_kernel(DraftStep
         const float s = block_sum<kNoiseBlock>(e, red);
         if (t == 0) {
             // a NaN or +inf logit leaves a NaN sum or an infinite maximum (-inf is a zero weight)
-            if (!(s >= 0.f) || m == INFINITY) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
+            if (!(s >= 0.f) || m == INFINITY || m != m) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
             p.stats[(size_t)q * p.n_stats + b] = make_float2(m, s);
             // block key of the two-level draw; greedy requests take the block holding the maximum
             const float z = req[j].greedy ? m

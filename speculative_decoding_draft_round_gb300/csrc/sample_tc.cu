@@ -752,6 +752,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     pm = mx * rm.scale;
                     ps = s0 + s1;
                 }
+                // a NaN logit leaves a NaN sum, a +inf one an infinite maximum (-inf is a zero weight)
+                if (rm.active && (!(ps >= 0.f) || mx == INFINITY || mx != mx))
+                    raise_status(P.status, DSPARK_ERR_NONFINITE_INPUT);
                 partial = make_float2(pm, ps);
             } else {
                 // residual mass: sum of max(0, p_t - p_d), both from log2-unit logits
@@ -797,8 +800,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float2 t = pp[gg * BM + m];
                         if (t.y > 0.f) S += t.y * ex2(t.x - M);
                     }
-                    // a NaN or +inf logit leaves a NaN sum or an infinite maximum (-inf is a zero weight)
-                    if (!(S >= 0.f) || M == INFINITY) raise_status(P.status, DSPARK_ERR_NONFINITE_INPUT);
                     // merge the block into this CTA's running log-normaliser of the row
                     if (M > run_m) {
                         run_s = run_s * ex2(run_m - M) + S;

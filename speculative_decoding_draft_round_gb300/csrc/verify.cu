@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParam
                 if (lane == bb) v = st[bb];
             out[b0 + lane] = v;
             // a NaN or +inf logit leaves a NaN sum or an infinite maximum (-inf is a zero weight)
-            if (!(v.y >= 0.f) || v.x == INFINITY) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
+            if (!(v.y >= 0.f) || v.x == INFINITY || v.x != v.x) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
         }
     }
 }

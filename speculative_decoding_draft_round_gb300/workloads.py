@@ -219,6 +219,11 @@ def controlled_tv(device="cpu") -> Round:
 
 WORKLOADS = {1: tiny, 2: small, 3: structured, 4: mixed_entropy, 5: controlled_tv}
 
+# (R, gamma_max, V, r, d, element type) of each workload, without drawing its tensors
+SHAPES = {1: (4, 4, 64, 8, 32, torch.float32), 2: (32, 16, 32768, 256, 2048, torch.bfloat16),
+          3: (128, 16, 151936, 256, 4096, torch.bfloat16), 4: (256, 16, 129280, 256, 7168, torch.bfloat16),
+          5: (512, 16, 129280, 256, 7168, torch.bfloat16)}
+
 
 def rnn_weights(rnd: Round, seed: int = 99) -> torch.Tensor:
     """Seeded weights W_rnn [3r][2r+d] (rows W_g, W_c, W_o) for the RNN head, N(0, 1/sqrt(2r+d)) so

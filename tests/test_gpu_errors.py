@@ -43,9 +43,9 @@ def test_nonfinite_draft_logit_is_flagged(dtype, bad):
         U = rnd.U.clone()
         U[5 % rnd.R, 1, 17] = bad
         out = _sample(rnd, U=U, path=path)
-        assert ds.check(out["workspace"]) == ds.ERR_NONFINITE_INPUT
+        assert ds.check(out["workspace"]) == ds.ERR_NONFINITE_INPUT, "path %d" % path
         out = _sample(rnd, path=path)   # the same call on clean inputs
-        assert ds.check(out["workspace"]) == 0
+        assert ds.check(out["workspace"]) == 0, "path %d" % path
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
