@@ -13,8 +13,7 @@
  *  - Every tensor pointer is a caller-owned DEVICE pointer (for example the
  *    storage of a torch tensor) in row-major layout with the shape stated. The
  *    library allocates nothing, keeps nothing between calls and never writes
- *    an input -- except that the RNN head's GEMM runs through one cuBLAS handle
- *    per device, created (and allocating) on that device's first RNN-head call.
+ *    an input.
  *  - Scratch memory is a caller-owned device buffer of at least the size the
  *    matching *_workspace_size call reports; distinct concurrent calls need
  *    distinct workspaces. The workspace's first 256 bytes hold a device status
@@ -104,7 +103,8 @@ enum {
  * (zhongzhuzhou.org notes, eq. 6):
  *   z_k = [s_{k-1}; W_1[x_{k-1}]; h[r][k]],  [y_g; y_c; y_o] = W_rnn z_k,  s_0 = 0,
  *   s_k = sigmoid(y_g) * s_{k-1} + (1 - sigmoid(y_g)) * tanh(y_c),  B_k = tanh(y_o) W_2.
- *   The h part of W_rnn z_k is one GEMM over all positions (cuBLAS, fp32 accumulation), the
+ *   The h part of W_rnn z_k is one GEMM over all positions (this library's tcgen05 GEMM for bf16
+ *   shapes the copy engine takes, else a CUDA-core GEMM; fp32 accumulation), the
  *   rest a per-step kernel. On the tensor-core path (bf16, r a multiple of 64 up to 256,
  *   (2r + d) a multiple of 8, 16-byte aligned W_rnn and a_rows) that kernel is a tcgen05 GEMM
  *   whose fp32 state enters as two bf16 operands (its rounding and the rounding of the
@@ -172,8 +172,8 @@ dspark_status dspark_sample_block(const dspark_sample_args* args, void* workspac
  * process exits. It calls no cudaMalloc, cudaFree or allocating library routine.
  *  - Arguments and results are those of dspark_sample_block.
  *  - Shapes whose dspark_sample_workspace_size exceeds DSPARK_STATIC_WORKSPACE_BYTES return
- *    DSPARK_ERR_UNSUPPORTED_SHAPE before any launch, and so does head = DSPARK_HEAD_RNN (its
- *    GEMM runs through a cuBLAS handle, which allocates).
+ *    DSPARK_ERR_UNSUPPORTED_SHAPE before any launch (the RNN head's scratch grows with
+ *    R * gamma_max * 3r, so it fits only for small shapes).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *    that device current; make that first call before any stream capture.
  *  - Every call on a device shares the one array, which keeps the previous call's contents (the
@@ -347,7 +347,8 @@ enum {
     DSPARK_KERNEL_RESIDUAL_STATS = 6,
     DSPARK_KERNEL_RESIDUAL_PICK = 7,
     DSPARK_KERNEL_ASSEMBLE = 8,
-    DSPARK_KERNEL_RNN_STEP = 9       /* RNN head: the per-step state update (the cuBLAS hidden GEMM is not timed) */
+    DSPARK_KERNEL_RNN_STEP = 9,      /* RNN head: the per-step state update */
+    DSPARK_KERNEL_RNN_HIDDEN = 10    /* RNN head: the h part of the projection, every position, once per call */
 };
 
 typedef struct {

@@ -90,7 +90,8 @@ EXPORTS = ("dspark_sample_workspace_size", "dspark_sample_block", "dspark_schedu
            "dspark_assemble_workspace_size", "dspark_assemble")
 
 KERNELS = {"draft_setup": 0, "draft_stats": 1, "draft_commit": 2, "schedule": 3, "verify_rows": 4,
-           "verify_decide": 5, "residual_stats": 6, "residual_pick": 7, "assemble": 8, "rnn_step": 9}
+           "verify_decide": 5, "residual_stats": 6, "residual_pick": 7, "assemble": 8, "rnn_step": 9,
+           "rnn_hidden": 10}
 
 
 class EventPair(C.Structure):
@@ -325,7 +326,8 @@ def sample_block_static(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd,
                         W_rnn=None):
     """dspark_sample_block_static: the sampler with its scratch in the library's static device
     array (for callers that cannot allocate device memory). Only the output tensors are
-    allocated here, by torch, when `out` is not given. The RNN head is refused here."""
+    allocated here, by torch, when `out` is not given. Shapes whose scratch exceeds the array
+    are refused."""
     a, out = sample_args(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, gamma=gamma,
                          conf_token=conf_token, bias_first=bias_first, path=path, out=out, sts_temp=sts_temp,
                          head=head, W_rnn=W_rnn)

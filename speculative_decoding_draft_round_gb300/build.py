@@ -66,7 +66,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB + ".%d.tmp" % os.getpid()
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-lcublas"]
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))

@@ -33,8 +33,8 @@ const char* kernel_name(int kernel)
 {
     static const char* names[] = {"draft_setup", "draft_stats", "draft_commit", "schedule",
                                   "verify_rows", "verify_decide", "residual_stats", "residual_pick",
-                                  "assemble", "rnn_step"};
-    return kernel >= 0 && kernel <= DSPARK_KERNEL_RNN_STEP ? names[kernel] : "?";
+                                  "assemble", "rnn_step", "rnn_hidden"};
+    return kernel >= 0 && kernel <= DSPARK_KERNEL_RNN_HIDDEN ? names[kernel] : "?";
 }
 
 thread_local char g_last_error[256] = "no error";
@@ -298,8 +298,8 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.zbuf = rnn && tc ? at<unsigned char>(ws, L.zbuf) : nullptr;
     cudaError_t e = launch(DSPARK_KERNEL_DRAFT_SETUP, s, [&] { return launch_draft_setup(p, s); });
     if (rnn && e == cudaSuccess) {
-        // the h part of the RNN projection: a cuBLAS GEMM, not one of this library's kernels
-        e = launch_rnn_hidden(p, s);
+        // the h part of the RNN projection, every position: one GEMM before the serial loop
+        e = launch(DSPARK_KERNEL_RNN_HIDDEN, s, [&] { return launch_rnn_hidden(p, s); });
         if (e != cudaSuccess)
             snprintf(g_last_error, sizeof g_last_error, "rnn hidden GEMM: %s (%s)", cudaGetErrorName(e),
                      cudaGetErrorString(e));
@@ -480,7 +480,7 @@ dspark_status dspark_time_kernel(int32_t kernel, dspark_event_pair* events, int3
         g_timer = KernelTimer();
         return DSPARK_OK;
     }
-    if (kernel > DSPARK_KERNEL_RNN_STEP || !events || capacity < 0 || !count) return DSPARK_ERR_INVALID_ARGUMENT;
+    if (kernel > DSPARK_KERNEL_RNN_HIDDEN || !events || capacity < 0 || !count) return DSPARK_ERR_INVALID_ARGUMENT;
     g_timer.kernel = kernel;
     g_timer.events = events;
     g_timer.capacity = capacity;

@@ -146,7 +146,7 @@ cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t s);
 cudaError_t launch_assemble(const AssembleParams& p, cudaStream_t s);
 
 // rnn.cu (RNN head)
-cudaError_t launch_rnn_hidden(const DraftStep& p, cudaStream_t s);   // yh = W_rnn[:, 2r:] h for all positions
+cudaError_t launch_rnn_hidden(const DraftStep& p, cudaStream_t s);   // rnn_hidden.cu: yh = W_rnn[:, 2r:] h, every position
 cudaError_t launch_rnn_step(const DraftStep& p, cudaStream_t s);     // step k: state, bias operand
 // rnn_tc.cu (RNN head on the tensor cores)
 bool rnn_tc_supported(const DraftStep& p);

@@ -4,15 +4,11 @@
 //   s_k = sigmoid(y_g) * s_{k-1} + (1 - sigmoid(y_g)) * tanh(y_c),  s_0 = 0,
 //   B_k = tanh(y_o) W_2  -- the bias contraction of the Markov head with A = tanh(y_o).
 // The h part of W_rnn z_k does not depend on the draws: one GEMM over every (request, position)
-// before the serial loop (cuBLAS, bf16 or fp32 inputs, fp32 accumulation). Each step then adds
+// before the serial loop (rnn_hidden.cu, fp32 accumulation). Each step then adds
 // the [s_{k-1}; W_1[x_{k-1}]] part in fp32 (rnn_step_kernel), updates the state and writes the
 // bias operand: fp32 rows for the CUDA-core path and the commit, and for the tensor-core path
 // its bf16 rounding (the A tile copies) plus the bf16 rounding of the remainder (a second A
 // operand in TMEM), so the contraction keeps about 16 significant bits of the operand.
-#include <cublas_v2.h>
-
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,18 +22,6 @@ constexpr int kRnnThreads = 32 * kRnnWarps;
 constexpr int kRnnSpan = 256;     // K elements a warp covers per pass: lane l takes 4l.. and 128+4l..
 constexpr int kRnnPre = 2;        // passes of W_rnn fetched before the dependency wait (2r <= 512)
 constexpr int kRnnVals = 3 * kRnnReq;   // per-lane partial sums: gates g, c, o of each request
-
-std::mutex g_blas_mutex;
-cublasHandle_t g_blas[64] = {};
-
-// one cuBLAS handle per device, created on the first RNN-head call on that device
-cublasHandle_t blas_handle()
-{
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!g_blas[dev] && cublasCreate(&g_blas[dev]) != CUBLAS_STATUS_SUCCESS) g_blas[dev] = nullptr;
-    return g_blas[dev];
-}
 
 // Four consecutive elements of a row, kept in the row's own type until used: one 16-byte (fp32)
 // or 8-byte (bf16) load when the row is aligned for it, else element by element (zero at and
@@ -279,28 +263,6 @@ __global__ void __launch_bounds__(kRnnThreads, 2) rnn_step_kernel(DraftStep p)
 }
 
 }  // namespace
-
-cudaError_t launch_rnn_hidden(const DraftStep& p, cudaStream_t s)
-{
-    // s_0 = 0
-    cudaError_t e = cudaMemsetAsync(p.state, 0, sizeof(float) * (size_t)p.R * p.r, s);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(g_blas_mutex);
-    cublasHandle_t h = blas_handle();
-    if (!h) return cudaErrorNotSupported;
-    if (cublasSetStream(h, s) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
-    // yh [R*G][3r] = h [R*G][d] x W_rnn[:, 2r:2r+d]^T, in column-major terms
-    // C (3r x RG, ld 3r) = A^T (A: the d x 3r column-major view of W_rnn from column 2r, ld 2r+d) x B (d x RG)
-    const float one = 1.f, zero = 0.f;
-    const int Z = 2 * p.r + p.d;
-    const cudaDataType_t dt = p.dtype == DSPARK_BF16 ? CUDA_R_16BF : CUDA_R_32F;
-    const size_t es = p.dtype == DSPARK_BF16 ? 2 : 4;
-    const void* A = static_cast<const char*>(p.W_rnn) + 2 * (size_t)p.r * es;
-    const cublasStatus_t st =
-        cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, 3 * p.r, p.R * p.G, p.d, &one, A, dt, Z, p.h, dt, p.d, &zero, p.yh,
-                     CUDA_R_32F, 3 * p.r, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    return st == CUBLAS_STATUS_SUCCESS ? cudaGetLastError() : cudaErrorUnknown;
-}
 
 cudaError_t launch_rnn_step(const DraftStep& p, cudaStream_t s)
 {

@@ -48,8 +48,6 @@ extern "C" dspark_status dspark_sample_block_static(const dspark_sample_args* ar
     size_t need = 0;
     const dspark_status st = dspark_sample_workspace_size(args, &need);
     if (st != DSPARK_OK) return st;
-    // the RNN head's hidden-state GEMM goes through a cuBLAS handle, which allocates when created
-    if (args->head == DSPARK_HEAD_RNN) return DSPARK_ERR_UNSUPPORTED_SHAPE;
     if (need > (size_t)DSPARK_STATIC_WORKSPACE_BYTES) return DSPARK_ERR_UNSUPPORTED_SHAPE;
     void* ws = nullptr;
     const dspark_status sw = static_workspace(&ws);

@@ -159,3 +159,11 @@ def test_verify_validation(L):
     assert L.dspark_verify_workspace_size(C.byref(a), C.byref(n)) == 0
     a.keep = None
     assert L.dspark_verify_workspace_size(C.byref(a), C.byref(n)) == 1
+
+
+def test_library_links_no_vendor_math_library(L):
+    """Every contraction on the path runs in this library's own kernels: the shared object
+    links the CUDA runtime only, no cuBLAS / cuDNN."""
+    out = subprocess.run(["ldd", ds.LIB_PATH], capture_output=True, text=True).stdout
+    for lib in ("cublas", "cudnn", "cusparse"):
+        assert lib not in out, out

@@ -258,12 +258,19 @@ def test_markov_head_reports_its_operand_rows():
     check_sample(rnd, out, np.arange(rnd.R))   # compares a_rows with W_1[x_{k-1}]
 
 
-def test_static_entry_refuses_the_rnn_head():
-    rnd, W_rnn = _rnn_round(RNN_SPECS[0], 43)
-    with pytest.raises(ds.DsparkError) as err:
-        ds.sample_block_static(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
-                               rnd.seed, rnd.round, gamma=rnd.gamma, head=ds.HEAD_RNN, W_rnn=W_rnn)
-    assert err.value.code == 2
+def test_static_entry_runs_the_rnn_head():
+    # no library handle or allocation on the RNN head's path: the static entry takes it when its
+    # scratch fits the array, and matches the workspace entry
+    rnd, W_rnn = _rnn_round(RNN_SPECS[2], 43)
+    ref = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                          rnd.seed, rnd.round, gamma=rnd.gamma, head=ds.HEAD_RNN, W_rnn=W_rnn)
+    assert ds.check(ref["workspace"]) == 0
+    got = ds.sample_block_static(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                                 rnd.seed, rnd.round, gamma=rnd.gamma, head=ds.HEAD_RNN, W_rnn=W_rnn)
+    assert ds.check_static() == 0
+    assert torch.equal(got["tokens"], ref["tokens"])
+    for k in ("conf", "surv", "draft_lse", "draft_logit"):
+        assert torch.allclose(got[k], ref[k], rtol=0, atol=1e-5 * max(1.0, float(ref[k].abs().max()))), k
 
 
 def test_step_ready_events_keep_the_results():
