@@ -80,9 +80,16 @@ enum {
 };
 
 enum {
-    DSPARK_PATH_AUTO = 0,            /* tensor cores when the shape allows, else CUDA cores */
+    DSPARK_PATH_AUTO = 0,            /* tensor cores per step when the shape allows, else CUDA cores */
     DSPARK_PATH_CUDA_CORE = 1,       /* fp32 FMA bias contraction */
-    DSPARK_PATH_TENSOR_CORE = 2      /* tcgen05 bias contraction (bf16, r % 64 == 0, V % 8 == 0) */
+    DSPARK_PATH_TENSOR_CORE = 2,     /* tcgen05 bias contraction, one launch per step (bf16, r % 64 == 0,
+                                        V % 8 == 0) */
+    DSPARK_PATH_RESIDENT = 3         /* sampler only, on request: every step in one persistent launch, one
+                                        CTA per SM, each keeping its slice of W in tensor and shared memory
+                                        between steps (bf16, Markov head, R <= 128, r = 256, V % 8 == 0,
+                                        V >= 1024); with step_ready events it waits for all of them first.
+                                        Same results as the other paths; slower than the per-step tensor-core
+                                        kernels at the measured shapes */
 };
 
 /*
@@ -155,8 +162,8 @@ typedef struct {
 } dspark_sample_args;
 
 dspark_status dspark_sample_workspace_size(const dspark_sample_args* args, size_t* bytes);
-/* The bias-contraction path these arguments select (DSPARK_PATH_CUDA_CORE or
- * DSPARK_PATH_TENSOR_CORE), or -status for invalid arguments. */
+/* The bias-contraction path these arguments select (DSPARK_PATH_CUDA_CORE,
+ * DSPARK_PATH_TENSOR_CORE or DSPARK_PATH_RESIDENT), or -status for invalid arguments. */
 int32_t dspark_sample_path(const dspark_sample_args* args);
 dspark_status dspark_sample_block(const dspark_sample_args* args, void* workspace, size_t workspace_bytes,
                                   void* stream);
@@ -348,7 +355,8 @@ enum {
     DSPARK_KERNEL_RESIDUAL_PICK = 7,
     DSPARK_KERNEL_ASSEMBLE = 8,
     DSPARK_KERNEL_RNN_STEP = 9,      /* RNN head: the per-step state update */
-    DSPARK_KERNEL_RNN_HIDDEN = 10    /* RNN head: the h part of the projection, every position, once per call */
+    DSPARK_KERNEL_RNN_HIDDEN = 10,   /* RNN head: the h part of the projection, every position, once per call */
+    DSPARK_KERNEL_DRAFT_LOOP = 11    /* the resident path's one launch: every draft step and its commit */
 };
 
 typedef struct {

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_PKG, "libdspark.so")
 
 F32, BF16 = 0, 1
 SCHED_SYNC, SCHED_ASYNC_CAPACITY, SCHED_FULL_SCAN, SCHED_THRESHOLD = 0, 1, 2, 3
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_RESIDENT = 0, 1, 2, 3
 HEAD_MARKOV, HEAD_RNN = 0, 1
 NOISE_BLOCK = 128
 MAX_GAMMA = 32
@@ -91,7 +91,7 @@ EXPORTS = ("dspark_sample_workspace_size", "dspark_sample_block", "dspark_schedu
 
 KERNELS = {"draft_setup": 0, "draft_stats": 1, "draft_commit": 2, "schedule": 3, "verify_rows": 4,
            "verify_decide": 5, "residual_stats": 6, "residual_pick": 7, "assemble": 8, "rnn_step": 9,
-           "rnn_hidden": 10}
+           "rnn_hidden": 10, "draft_loop": 11}
 
 
 class EventPair(C.Structure):

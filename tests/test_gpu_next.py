@@ -293,3 +293,27 @@ def test_step_ready_events_keep_the_results():
     got = runner.results()
     for k in ("tokens", "conf", "surv", "keep", "accepted", "next_token"):
         assert torch.equal(got[k], ref[k]), k
+
+
+# ------------------------------------------------------------------ the resident loop's variants
+
+def test_resident_loop_variants_match_oracle():
+    """Greedy requests mixed with sampled ones, per-position confidence temperatures, no bias at the
+    first step, the conditioning-token choice of eq. 7, reported operand rows and ragged draft
+    lengths, on the persistent W-resident path (one CTA per vocabulary block here)."""
+    temp = lambda R_, g, dev: torch.where(torch.arange(R_, device=dev) % 3 == 0, torch.zeros(R_, device=dev),
+                                          0.5 + torch.rand((R_,), generator=g, device=dev))
+    for conf_token, bias_first in ((0, 0), (1, 1)):
+        rnd = wl.make_round("loop_var", 96, 5, 12800, 256, 64, "bf16", seed=51, device=DEV, temperature=temp,
+                            sps=wl.sps_hyperbolic(96 * 6), conf_token=conf_token, bias_first=bias_first,
+                            gamma=[5, 3, 0, 4, 5, 1] * 16)
+        rnd.round = 7
+        t = torch.tensor([0.7, 1.3, 2.0, 0.9, 1.1], dtype=torch.float32, device=DEV)
+        out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                              rnd.seed, rnd.round, gamma=rnd.gamma, conf_token=conf_token, bias_first=bias_first,
+                              path=ds.PATH_RESIDENT, sts_temp=t, a_rows=True)
+        torch.cuda.synchronize()
+        assert ds.check(out["workspace"]) == 0
+        check_sample(rnd, out, np.arange(rnd.R), sts_temp=t)
+        g = to_np(rnd.temperature) == 0
+        np.testing.assert_array_equal(to_np(out["draft_lse"])[g], to_np(out["draft_logit"])[g])

@@ -25,12 +25,17 @@ def _lib():
 
 
 def _paths(rnd):
-    """The contraction paths these inputs support: CUDA cores always, tensor cores when the shape allows."""
+    """The contraction paths these inputs support: CUDA cores always; the per-step tensor-core
+    kernels and the resident loop when the shape allows."""
     paths = [ds.PATH_CUDA_CORE]
-    a, _ = ds.sample_args(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
-                          rnd.seed, rnd.round, gamma=rnd.gamma)
-    if ds.sample_path(a) == ds.PATH_TENSOR_CORE:
-        paths.append(ds.PATH_TENSOR_CORE)
+    for path in (ds.PATH_TENSOR_CORE, ds.PATH_RESIDENT):
+        a, _ = ds.sample_args(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                              rnd.seed, rnd.round, gamma=rnd.gamma, path=path)
+        try:
+            if ds.sample_path(a) == path:
+                paths.append(path)
+        except ds.DsparkError:
+            pass
     return paths
 
 
@@ -42,6 +47,10 @@ SMALL = [
          temperature=lambda R, g, dev: 0.4 + torch.rand((R,), generator=g, device=dev)),
     dict(name="wide_bf16", R=37, G=4, V=2056, r=256, d=64, dtype="bf16", ew_std=0.05,
          gamma=[4, 2] * 18 + [3]),
+    # the resident loop with W tiles in tensor memory, in shared memory and streamed (6 blocks per
+    # CTA on 152 SMs), two request halves with a ragged second one
+    dict(name="resident_bf16", R=100, G=3, V=100000, r=256, d=64, dtype="bf16", ew_std=0.05,
+         temperature=lambda R, g, dev: 0.5 + torch.rand((R,), generator=g, device=dev)),
 ]
 
 
@@ -227,9 +236,10 @@ def test_verify_matches_oracle(spec):
             else:
                 keep = (torch.rand(rnd.R, generator=gen) * (g + 1)).floor().to(torch.int32)
             keep = keep.to(torch.int32).to(DEV)
+            vpath = ds.PATH_TENSOR_CORE if path == ds.PATH_RESIDENT else path   # the verifier's residual path
             vout = ds.verify(rnd.target, rnd.U, rnd.E, rnd.W, rnd.anchor, sout["tokens"], sout["draft_lse"],
                              sout["draft_logit"], keep, rnd.temperature, rnd.seed, rnd.round, gamma=rnd.gamma,
-                             path=path)
+                             path=vpath)
             assert ds.check(vout["workspace"]) == 0
             add_counts(total, check_verify(rnd, sout, keep, vout, ids))
         report("verify %s path=%d" % (spec["name"], path), total)

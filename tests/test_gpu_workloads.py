@@ -89,3 +89,21 @@ def test_full_size_round(workload):
     assert total["draw"] + total["residual_fp32"] <= max(2, total["checked_tokens"] // 1000)
     assert total["accept"] <= max(2, total["checked_requests"] // 100)
     assert total["theta"] <= 1
+
+
+@pytest.mark.parametrize("workload", [2, 3])
+def test_full_size_round_resident_loop(workload):
+    """The resident loop (one persistent launch for every draft step, W held on chip between
+    steps) at the full sizes it takes, every request compared with the oracle."""
+    torch.cuda.empty_cache()
+    rnd = wl.WORKLOADS[workload](device=DEV)
+    rnd.round = 4
+    out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                          rnd.seed, rnd.round, gamma=rnd.gamma, path=ds.PATH_RESIDENT)
+    assert ds.check(out["workspace"]) == 0
+    total = new_counts()
+    for s0 in range(0, rnd.R, 64):
+        add_counts(total, check_sample(rnd, out, np.arange(s0, min(rnd.R, s0 + 64))))
+    report("resident loop, workload %d" % workload, total)
+    assert total["checked_requests"] == rnd.R
+    assert total["draw"] <= max(2, total["checked_tokens"] // 1000)
