@@ -280,6 +280,136 @@ def cpu_threads():
     return max(1, min(16, os.cpu_count() or 1))
 
 
+def library_draft_logp(ds, rnd, rnd_index):
+    """Input preparation for the controlled-distance workload: its target rows are scored on the
+    drafted prefix, so they are built from the realised draft distribution. The library drafts
+    round `rnd_index` once (outside any timing); log p_d of every drafted position is then
+    formed with plain torch ops from those tokens (softmax((U_k + W_1[x_{k-1}] W_2) / T))."""
+    out = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                          rnd.seed, rnd_index, gamma=rnd.gamma)
+    tokens = out["tokens"].clamp(min=0).long()
+    W = rnd.W.float()
+
+    def fn(ids):
+        q = torch.as_tensor(ids, device=rnd.U.device)
+        prev = torch.cat([rnd.anchor[q].long().unsqueeze(1), tokens[q, :-1]], dim=1)
+        bias = rnd.E[prev].float() @ W
+        if not rnd.bias_first:
+            bias[:, 0] = 0.0
+        logits = (rnd.U[q].float() + bias) / rnd.temperature[q].view(-1, 1, 1)
+        return torch.log_softmax(logits, dim=2)
+    return fn
+
+
+def oracle_draft_logp(rnd, rnd_index, threads):
+    """The same input preparation from the oracle's own draft (the reference arm runs no library
+    code)."""
+    import oracle
+
+    def to_np(t):
+        t = t.detach().contiguous().cpu()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    def fn(ids):
+        idx = torch.as_tensor(ids, dtype=torch.long, device=rnd.U.device)
+        g = None if rnd.gamma is None else to_np(rnd.gamma)[ids]
+        o = oracle.sample_block(to_np(rnd.U.index_select(0, idx)), to_np(rnd.E), to_np(rnd.W),
+                                to_np(rnd.h.index_select(0, idx)), to_np(rnd.w_h), to_np(rnd.w_e), rnd.b,
+                                to_np(rnd.temperature)[ids], to_np(rnd.anchor)[ids], rnd.seed, rnd_index, gamma=g,
+                                req_ids=np.asarray(ids), logp=True, threads=threads)
+        return torch.from_numpy(o["logp"])
+    return fn
+
+
+def make_workload(wl, n, dev, ds=None, threads=None):
+    """Workload n on device dev; the controlled-distance one gets its target from the round-0
+    draft (the library's, or the oracle's when ds is None)."""
+    rnd = wl.WORKLOADS[n](device=dev)
+    if "tv_delta" in rnd.extra:
+        fn = library_draft_logp(ds, rnd, 0) if ds is not None else oracle_draft_logp(rnd, 0, threads or 1)
+        wl.fill_controlled_tv_target(rnd, fn)
+    return rnd
+
+
+def sfu_floor(rnd, keep_sum, n_rej, sm_mhz, sms):
+    """Special-function-unit operations of one round and the time they take at the documented
+    rate of 16 per SM per clock (exp2 / log2 on the MUFU pipe), at the SM clock measured under
+    load. Counted: one exp2 per draft vocabulary element (block statistics), one per target
+    element read (verify rows), two per element of each rejected row (the residual), and the
+    block- and element-level Gumbel logs (two each)."""
+    g = rnd.gamma.cpu().numpy() if rnd.gamma is not None else np.full(rnd.R, rnd.gamma_max)
+    drafted = int(g.sum())
+    nblk = (rnd.V + 127) // 128
+    ops = {"draft_exp2": drafted * rnd.V,
+           "draft_gumbel_logs": 2 * drafted * (nblk + 128),
+           "verify_exp2": (keep_sum + rnd.R) * rnd.V,
+           "residual_exp2": 2 * n_rej * rnd.V}
+    ops["total"] = sum(ops.values())
+    rate = 16.0 * sms * sm_mhz * 1e6
+    return {"ops_per_round": ops, "rate_ops_per_s": rate, "floor_us": ops["total"] / rate * 1e6,
+            "basis": "16 MUFU results per SM per clock x %d SMs x %.0f MHz (median under load)" % (sms, sm_mhz)}
+
+
+def time_rounds(ds, rnd, runner, flush, n, stream, first_round):
+    """n whole rounds between CUDA events on the launch stream, L2 flushed before each outside the
+    events; returns the per-round milliseconds."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    torch.cuda.synchronize()
+    for s in range(n):
+        flush.zero_()
+        runner.set_round(first_round + s)
+        starts[s].record(stream)
+        runner.run()
+        stops[s].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, stops)]
+
+
+def percentiles(ms):
+    a = np.asarray(ms)
+    return {"median_ms": float(np.median(a)), "p10_ms": float(np.percentile(a, 10)),
+            "p90_ms": float(np.percentile(a, 90)), "mean_ms": float(a.mean())}
+
+
+def other_workloads(ds, wl, dev, flush, stream, n=10, sm_mhz=None):
+    """The other full-size workloads, timed like the headline in the same run: resident inputs,
+    n rounds between events on the launch stream, L2 flushed between rounds."""
+    peaks = measured_peaks()
+    rows = {}
+    for w in (2, 4, 5):
+        rnd = make_workload(wl, w, dev, ds=ds)
+        cap = None
+        if rnd.mode == wl.SCHED_ASYNC_CAPACITY:
+            cap = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
+                                  rnd.seed, 0, gamma=rnd.gamma)["surv"].clone()
+        runner = ds.RoundRunner(rnd, surv_capacity=cap)
+        for i in range(3):
+            runner.set_round(2 + i)
+            runner.run()
+        ms = time_rounds(ds, rnd, runner, flush, n, stream, 3000)
+        status = runner.check()
+        if status:
+            raise RuntimeError("device status %d in workload %d" % (status, w))
+        res = runner.results()
+        keep_sum = int(res["keep"].sum())
+        n_rej = int(res["resampled"].to(torch.int32).sum())
+        rb = round_bytes(rnd, keep_sum, n_rej)
+        mean_s = float(np.mean(ms)) / 1e3
+        rows[rnd.name] = {"draft_tokens_per_s": rnd.draft_tokens() / mean_s, "rounds_per_s": 1.0 / mean_s,
+                          **percentiles(ms), "admitted_per_round": keep_sum,
+                          "committed_per_round": int(res["accepted"].sum()) + rnd.R,
+                          "round_roofline_frac": rb["total"] / mean_s / 1e9 / peaks["hbm_gbs"],
+                          "round_floor_us": rb["total"] / (peaks["hbm_gbs"] * 1e9) * 1e6,
+                          "sched_mode": {0: "sync", 1: "async_capacity", 2: "full_scan"}[rnd.mode]}
+        del runner, rnd, res
+        torch.cuda.empty_cache()
+    rows["note"] = ("same event protocol as the headline, %d rounds each; the controlled-distance workload's "
+                    "target rows are built from the library's round-0 draft (its timed rounds draw other "
+                    "tokens, so their distance is near, not at, the set value)" % n)
+    return rows
+
+
 # ------------------------------------------------------------------ arms
 
 def bench_reference(args):
@@ -288,8 +418,8 @@ def bench_reference(args):
         return
     from speculative_decoding_draft_round_gb300 import workloads as wl
     dev = "cuda:%d" % local if torch.cuda.is_available() else "cpu"
-    rnd = wl.WORKLOADS[args.workload](device=dev)
     threads = cpu_threads()
+    rnd = make_workload(wl, args.workload, dev, ds=None, threads=threads)
     n_req = threads
     ids = list(range(0, rnd.R, max(1, rnd.R // n_req)))[:n_req]
     for i in range(args.warmup):
@@ -392,10 +522,13 @@ def bench_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     dsbuild.build()
-    path = {"auto": ds.PATH_AUTO, "cuda_core": ds.PATH_CUDA_CORE, "tensor_core": ds.PATH_TENSOR_CORE}[args.path]
+    path = {"auto": ds.PATH_AUTO, "cuda_core": ds.PATH_CUDA_CORE, "tensor_core": ds.PATH_TENSOR_CORE,
+            "resident": ds.PATH_RESIDENT}[args.path]
     rnd = wl.WORKLOADS[args.workload](device=dev)
     if world > 1:   # independent replica per rank
         rnd.seed = replica_seed(rnd.seed, rank)
+    if "tv_delta" in rnd.extra:
+        wl.fill_controlled_tv_target(rnd, library_draft_logp(ds, rnd, 0))
     cap = None
     if rnd.mode == wl.SCHED_ASYNC_CAPACITY:
         old = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
@@ -404,7 +537,8 @@ def bench_ours(args):
     runner = ds.RoundRunner(rnd, surv_capacity=cap, path=path)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    uses_tc = ds.sample_path(runner.sa) == ds.PATH_TENSOR_CORE
+    spath = ds.sample_path(runner.sa)
+    uses_tc = spath in (ds.PATH_TENSOR_CORE, ds.PATH_RESIDENT)
 
     clocks = ClockSampler(gpu_id_for(local))
     clocks.start()
@@ -444,13 +578,22 @@ def bench_ours(args):
     total_ms = sum(step_ms)
     # the same K rounds again with events around every launch of the dominant kernel, for its
     # average launch duration
-    timer = ds.KernelTimer("draft_stats", n_timed * rnd.gamma_max)
+    dom = "draft_loop" if spath == ds.PATH_RESIDENT else "draft_stats"
+    timer = ds.KernelTimer(dom, n_timed * rnd.gamma_max)
+    keep_tot = torch.zeros((), dtype=torch.int64, device=dev)
+    commit_tot = torch.zeros((), dtype=torch.int64, device=dev)
     with timer:
         for s in range(n_timed):
             flush.zero_()
             runner.set_round(1000 + s)
             runner.run()
+            # the same rounds as the timed ones: admitted and committed tokens (device sums, untimed)
+            keep_tot += runner.cout["keep"].sum()
+            commit_tot += runner.vout["accepted"].sum() + rnd.R
     stats_ms = timer.durations_ms()
+    if spath == ds.PATH_RESIDENT:   # one launch per round covers every step: per-step average
+        stats_ms = [m / rnd.gamma_max for m in stats_ms]
+    admitted_total, committed_total = int(keep_tot.item()), int(commit_tot.item())
     status = runner.check()
     if status:
         raise RuntimeError("device status %d after timing" % status)
@@ -515,6 +658,7 @@ def bench_ours(args):
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_starts, e_stops))
     h2d = h2d_fixed + target_rows * row_bytes // n_e2e
     next_rows = time_next_rows(ds, rnd, res, flush)
+    others = other_workloads(ds, wl, dev, flush, stream) if (world == 1 and not args.no_other_workloads) else None
     clock = clocks.stop()
 
     drafted = rnd.draft_tokens()
@@ -528,9 +672,10 @@ def bench_ours(args):
     reread_bytes = draft_stats_launch_bytes(rnd, w_every_step=True)
     stats_mean_s = (sum(stats_ms) / len(stats_ms)) / 1e3 if stats_ms else float("nan")
     achieved = launch_bytes / stats_mean_s / 1e9
+    resident = spath == ds.PATH_RESIDENT
     src = ["speculative_decoding_draft_round_gb300/csrc/%s" % f for f in
-           (("sample_tc.cu",) if uses_tc else ("sample.cu",)) + ("common.cuh",)]
-    kname = "draft_stats_tc" if uses_tc else "draft_stats_simt"
+           (("draft_loop.cu",) if resident else ("sample_tc.cu",) if uses_tc else ("sample.cu",)) + ("common.cuh",)]
+    kname = "draft_loop" if resident else "draft_stats_tc" if uses_tc else "draft_stats_simt"
     traffic = profiled_traffic(kname, rnd.name, kernel_hash(src))
     rb = round_bytes(rnd, keep_sum, n_rej)
     round_s = total_s / n_timed
@@ -540,11 +685,15 @@ def bench_ours(args):
         "dtype": "bf16" if uses_tc else "f32", "data": "synthetic",
         "config": {"workload": rnd.name, "R": rnd.R, "gamma": rnd.gamma_max, "V": rnd.V, "r": rnd.r, "d": rnd.d,
                    "sched_mode": {0: "sync", 1: "async_capacity", 2: "full_scan"}[rnd.mode],
-                   "path": "tensor_core" if uses_tc else "cuda_core", "parallelism": "replica x%d" % world,
+                   "path": "resident" if resident else "tensor_core" if uses_tc else "cuda_core",
+                   "parallelism": "replica x%d" % world,
                    "l2": "flushed between steps (256 MiB write, outside the timed events)",
                    "inputs": "resident in HBM"},
         "rounds_per_s": world * n_timed / total_s,
         "admitted_per_round": keep_sum,
+        "admitted_tokens_per_s": world * admitted_total / total_s,
+        "committed_tokens_per_s": world * committed_total / total_s,
+        "round_ms": percentiles(step_ms),
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "bytes_per_launch": launch_bytes, "launch_us": stats_mean_s * 1e6,
@@ -566,6 +715,11 @@ def bench_ours(args):
         "next_rows": next_rows,
         "clocks": clock,
     }
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_mhz = (clock or {}).get("sm_mhz") or 2070.0
+    line["sfu_floor"] = sfu_floor(rnd, keep_sum, n_rej, sm_mhz, sms)
+    if others is not None:
+        line["other_workloads"] = others
     if rank == 0 and not args.no_cpu_baseline:
         # the oracle on this host's cores over a bounded sample of the same round: chunks of
         # `threads` requests (one per thread), each a whole round for those requests, until about
@@ -584,6 +738,10 @@ def bench_ours(args):
                                 "sample": "%d request-rounds of the %d-request workload in %d chunks of %d, "
                                           "each a whole round (sample+schedule+verify), %.1f s"
                                           % (n_req, rnd.R, n_chunks, min(threads, rnd.R), t_tot)}
+        # and on one core: two requests, one whole round each
+        d1, t1 = run_oracle_round(rnd, [0, 1], 1, 3)
+        line["cpu_baseline"]["single_thread"] = {"value": d1 / t1, "unit": UNIT, "cores": 1,
+                                                 "sample": "2 request-rounds, %.1f s" % t1}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -597,8 +755,9 @@ def bench_profile(args):
     from speculative_decoding_draft_round_gb300 import build as dsbuild
     from speculative_decoding_draft_round_gb300 import workloads as wl
     dsbuild.build()
-    path = {"auto": ds.PATH_AUTO, "cuda_core": ds.PATH_CUDA_CORE, "tensor_core": ds.PATH_TENSOR_CORE}[args.path]
-    rnd = wl.WORKLOADS[args.workload](device="cuda")
+    path = {"auto": ds.PATH_AUTO, "cuda_core": ds.PATH_CUDA_CORE, "tensor_core": ds.PATH_TENSOR_CORE,
+            "resident": ds.PATH_RESIDENT}[args.path]
+    rnd = make_workload(wl, args.workload, "cuda", ds=ds)
     cap = None
     if rnd.mode == wl.SCHED_ASYNC_CAPACITY:
         cap = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature, rnd.anchor,
@@ -634,8 +793,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--path", choices=["auto", "cuda_core", "tensor_core"], default="auto")
+    ap.add_argument("--path", choices=["auto", "cuda_core", "tensor_core", "resident"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true", help="skip timing workloads 2, 4 and 5")
     ap.add_argument("--profile", action="store_true", help="plain rounds for ncu (no timing, no baselines)")
     ap.add_argument("--head", choices=["markov", "rnn"], default="markov",
                     help="with --profile: rnn runs only the sampler, with the RNN sequential head")

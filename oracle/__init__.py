@@ -61,6 +61,7 @@ class _SampleArgs(C.Structure):
         ("tokens", C.c_void_p), ("conf", C.c_void_p), ("surv", C.c_void_p), ("lse", C.c_void_p),
         ("logit", C.c_void_p), ("gap1", C.c_void_p), ("gap2", C.c_void_p),
         ("sts_temp", C.c_void_p), ("head", C.c_int), ("W_rnn", C.c_void_p), ("a_rows", C.c_void_p),
+        ("logp", C.c_void_p),
     ]
 
 
@@ -174,11 +175,12 @@ def _run(fn, parts, threads):
 
 def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gamma=None,
                  req_ids=None, conf_token=0, bias_first=1, noise_block=128, forced_tokens=None,
-                 sts_temp=None, head=HEAD_MARKOV, W_rnn=None, threads=1):
+                 sts_temp=None, head=HEAD_MARKOV, W_rnn=None, threads=1, logp=False):
     """Markov-head serial sampling, confidence head and survival products for R requests.
 
     U [R][G][V], E [V][r], W [r][V], h [R][G][d] share one element type
-    (float32, float64 or uint16 bf16 bits). Returns a dict of numpy arrays."""
+    (float32, float64 or uint16 bf16 bits). Returns a dict of numpy arrays; with logp=True
+    also "logp" [R][G][V] float32, the draft distribution log p_d of every active position."""
     U, E, W, h = _c(U), _c(E), _c(W), _c(h)
     dt = _dtype_code(U)
     if not (_dtype_code(E) == dt and _dtype_code(W) == dt and _dtype_code(h) == dt):
@@ -201,6 +203,8 @@ def sample_block(U, E, W, h, w_h, w_e, b, temperature, anchor, seed, rnd, *, gam
         "lse": np.zeros((R, G)), "logit": np.zeros((R, G)), "gap1": np.zeros((R, G)),
         "gap2": np.zeros((R, G)), "a_rows": np.zeros((R, G, r)),
     }
+    if logp:
+        out["logp"] = np.zeros((R, G, V), np.float32)
 
     def part(se):
         s, e = se

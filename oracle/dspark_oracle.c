@@ -250,6 +250,8 @@ int dso_sample_block(const dso_sample_args* a)
                 a->gap1[idx] = a->gap2[idx] = INFINITY;
                 if (a->a_rows)
                     for (int i = 0; i < r; ++i) a->a_rows[idx * r + i] = 0.0;
+                if (a->logp)
+                    for (int v = 0; v < V; ++v) a->logp[idx * V + v] = 0.0f;
                 continue;
             }
             const int use_bias = (k > 0) || a->bias_first;
@@ -285,6 +287,11 @@ int dso_sample_block(const dso_sample_args* a)
             /* temperature 0: the draft is a point mass, reported as lse = logit (log p_d = 0) */
             a->lse[idx] = T == 0.0 ? l[commit] : logsumexp(l, V);
             a->logit[idx] = l[commit];
+            if (a->logp) {
+                float* lp = a->logp + idx * V;
+                for (int v = 0; v < V; ++v)
+                    lp[v] = T == 0.0 ? (v == commit ? 0.0f : -INFINITY) : (float)(l[v] - a->lse[idx]);
+            }
             /* eq. (7): c_k = sigmoid(w^T [h_k; W_1[x]]) + b */
             const int xc = a->conf_token ? commit : prev;
             double dot = (double)a->b;

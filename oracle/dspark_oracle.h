@@ -84,6 +84,9 @@ typedef struct {
     const void* W_rnn;                  /* [3r][2r+d] (dtype): rows W_g, then W_c, then W_o (RNN head) */
     double* a_rows;                     /* [R][gamma_max][r] or NULL: out, the bias operand of each step
                                            (W_1[x_{k-1}] for the Markov head, tanh(W_o z_k) for the RNN head) */
+    float* logp;                        /* [R][gamma_max][V] or NULL: out, the draft distribution of each
+                                           active position, log p_d(v) = l_k(v) - lse (a point mass at the
+                                           committed token for temperature 0); 0 past gamma_r */
 } dso_sample_args;
 
 int dso_sample_block(const dso_sample_args* a);

@@ -103,10 +103,8 @@ def make_round(name: str, R: int, gamma_max: int, V: int, r: int, d: int, dtype:
       (before the bias) and to the same token in target row k; the bonus row gets its
       own top-1 boosted with probability p.
     entropy_split=(n_low, scale): requests r < n_low have U and target scaled by `scale`.
-    tv_range=(lo, hi): target row k = T log p_t with p_t = (1-lam) p_base + lam e_v0,
-      p_base = softmax(U_k / T), v0 = argmin p_base, lam = delta / (1 - p_base(v0)),
-      delta ~ U[lo, hi] per position, so TV(p_t, p_base) = delta (p_base omits the
-      small Markov bias).
+    tv_range=(lo, hi): delta ~ U[lo, hi] per position, kept in extra["tv_delta"]; the target
+      rows are then built by fill_controlled_tv_target from the realised draft distribution.
     """
     dev = torch.device(device)
     g = _gen(seed, dev)
@@ -140,17 +138,10 @@ def make_round(name: str, R: int, gamma_max: int, V: int, r: int, d: int, dtype:
         top_b = target[:, G].argmax(dim=1)
         target[:, G].scatter_add_(1, top_b.unsqueeze(1), hit_b.unsqueeze(1))
     if tv_range is not None:
+        # the target rows of the drafted positions are built from the realised draft distribution
+        # once it is known (fill_controlled_tv_target); until then they keep their N(0, t_std) draw
         lo, hi = tv_range
-        delta = lo + (hi - lo) * torch.rand((R, G), generator=g, device=dev)
-        for q in range(R):  # row by row keeps peak memory at one [G][V] slab
-            p_base = torch.softmax(U[q] / temp[q], dim=1)            # [G][V]
-            v0 = p_base.argmin(dim=1)
-            pv0 = p_base.gather(1, v0.unsqueeze(1)).squeeze(1)
-            lam = (delta[q] / (1.0 - pv0)).clamp(max=1.0)
-            p_t = (1.0 - lam).unsqueeze(1) * p_base
-            p_t.scatter_add_(1, v0.unsqueeze(1), lam.unsqueeze(1))
-            target[q, :G] = (temp[q] * torch.log(p_t)).clamp(min=-30.0 * float(temp[q]))
-        delta_out = delta
+        delta_out = lo + (hi - lo) * torch.rand((R, G), generator=g, device=dev)
     else:
         delta_out = None
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
@@ -164,6 +155,42 @@ def make_round(name: str, R: int, gamma_max: int, V: int, r: int, d: int, dtype:
     if delta_out is not None:
         rnd.extra["tv_delta"] = delta_out
     return rnd
+
+
+def tv_target_rows(logp_d: torch.Tensor, temperature: torch.Tensor, delta: torch.Tensor,
+                   floor: float = -30.0) -> torch.Tensor:
+    """Target logit rows at a controlled total-variation distance from a given distribution.
+
+    logp_d [n][G][V]: log p_d of the positions' draft distributions; temperature [n] (> 0);
+    delta [n][G] in [0, 1). With v0 = argmin p_d and lam = delta / (1 - p_d(v0)),
+    p_t = (1 - lam) p_d + lam e_v0, so that TV(p_t, p_d) = lam (1 - p_d(v0)) = delta; returns
+    T log p_t [n][G][V] (fp32), clamped below at floor * T. Input shaping only: the draft
+    distribution comes from whoever drafted."""
+    p_d = torch.exp(logp_d.float())
+    v0 = p_d.argmin(dim=2, keepdim=True)
+    pv0 = p_d.gather(2, v0)
+    lam = (delta.unsqueeze(2) / (1.0 - pv0)).clamp(max=1.0)
+    p_t = (1.0 - lam) * p_d
+    p_t.scatter_add_(2, v0, lam)
+    T = temperature.view(-1, 1, 1)
+    return torch.maximum(T * torch.log(p_t), floor * T)
+
+
+def fill_controlled_tv_target(rnd: Round, draft_logp, chunk: int = 32) -> None:
+    """Replace target rows 0..gamma_r - 1 of every request with rows at the controlled distance
+    rnd.extra["tv_delta"] from the realised draft distribution: draft_logp(ids) returns log p_d
+    [len(ids)][G][V] of those requests' drafted positions. Rows past gamma_r and the bonus row
+    keep their draw. The rows are rounded to the round's element type like every input."""
+    delta = rnd.extra["tv_delta"]
+    G = rnd.gamma_max
+    g = None if rnd.gamma is None else rnd.gamma.cpu().tolist()
+    for s0 in range(0, rnd.R, chunk):
+        ids = list(range(s0, min(rnd.R, s0 + chunk)))
+        lp = draft_logp(ids).to(rnd.target.device)
+        rows = tv_target_rows(lp, rnd.temperature[ids], delta[ids].to(lp.device))
+        for j, q in enumerate(ids):
+            n = G if g is None else int(g[q])
+            rnd.target[q, :n] = rows[j, :n].to(rnd.target.dtype)
 
 
 def tiny(device="cpu") -> Round:
@@ -208,8 +235,9 @@ def _temp_controlled_tv(R, g, dev):
 
 def controlled_tv(device="cpu") -> Round:
     """R=512, gamma 8 (r < 256) or 16, V=129280, r=256, d=7168, bf16; target differs from
-    the draft by TV ~U[0.05, 0.6] per position; T ~U[0.3, 1.2]; staircase SPS, 8704
-    entries; full-scan scheduling over 8192 slots."""
+    the draft by TV ~U[0.05, 0.6] per position once fill_controlled_tv_target has built its
+    rows from the realised draft; T ~U[0.3, 1.2]; staircase SPS, 8704 entries; full-scan
+    scheduling over 8192 slots."""
     R = 512
     gamma = [8] * (R // 2) + [16] * (R // 2)
     return make_round("R512_g8-16_V129280_bf16", R, 16, 129280, 256, 7168, "bf16", seed=4,

@@ -10,7 +10,7 @@ import torch
 import oracle
 import speculative_decoding_draft_round_gb300 as ds
 from speculative_decoding_draft_round_gb300 import workloads as wl
-from parity import add_counts, check_sample, check_schedule, check_verify, new_counts, report, to_np
+from parity import _threads, add_counts, check_sample, check_schedule, check_verify, new_counts, report, rows, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -30,6 +30,38 @@ def _capacity_survivals(rnd, rnd_idx):
     return old["surv"].clone()
 
 
+def _check_acceptance_is_one_minus_tv(rnd, tv, o_tok):
+    """[P3] eq. 8a-8c: a draft token drawn from p_d is accepted with probability
+    sum_v min(p_t, p_d) = 1 - TV(p_t, p_d). The round's draft is verified with every drafted
+    position admitted; over every position the verifier tests (up to and including the first
+    rejection) on requests whose draft equals the oracle's, the number accepted must match the
+    sum of 1 - TV within 5 standard deviations."""
+    keep = rnd.gamma.clone() if rnd.gamma is not None else torch.full((rnd.R,), rnd.gamma_max, dtype=torch.int32,
+                                                                       device=DEV)
+    v = ds.verify(rnd.target, rnd.U, rnd.E, rnd.W, rnd.anchor, _last["tokens"].clamp(min=0), _last["draft_lse"],
+                  _last["draft_logit"], keep, rnd.temperature, rnd.seed, rnd.round, gamma=rnd.gamma)
+    assert ds.check(v["workspace"]) == 0
+    tok, kp, acc = to_np(_last["tokens"]), to_np(keep), to_np(v["accepted"])
+    acc_sum, exp_sum, var, n_tested = 0.0, 0.0, 0.0, 0
+    for q in range(rnd.R):
+        kq, aq = int(kp[q]), int(acc[q])
+        if kq == 0 or not np.array_equal(tok[q, :kq], o_tok[q, :kq]):
+            continue
+        for j in range(min(aq + 1, kq)):
+            acc_sum += 1.0 if j < aq else 0.0
+            exp_sum += 1.0 - tv[q, j]
+            var += tv[q, j] * (1.0 - tv[q, j])
+            n_tested += 1
+    z = (acc_sum - exp_sum) / max(np.sqrt(var), 1e-9)
+    print("acceptance vs 1 - TV: %d tested positions, %.0f accepted, %.1f expected, z = %.2f" % (
+        n_tested, acc_sum, exp_sum, z))
+    assert n_tested >= 500
+    assert abs(z) < 5
+
+
+_last = {}
+
+
 def _check_round(rnd, workload, t):
     cap = _capacity_survivals(rnd, t - 2) if rnd.mode == wl.SCHED_ASYNC_CAPACITY else None
     runner = ds.RoundRunner(rnd, surv_capacity=cap)
@@ -38,6 +70,8 @@ def _check_round(rnd, workload, t):
     runner.run()
     assert runner.check() == 0
     res = runner.results()
+    _last.clear()
+    _last.update(res)
     R, G = rnd.R, rnd.gamma_max
     counts = new_counts()
     # every request, in chunks that keep the oracle's copies of U and the target small
@@ -76,13 +110,45 @@ def _check_round(rnd, workload, t):
     return counts
 
 
+def _fill_tv_target(rnd, t):
+    """Target rows of the controlled-distance workload from the oracle's own draft at round t
+    (its draft distribution of every drafted position); returns TV(p_t, p_d) [R][G] recomputed
+    after the rows were rounded to bf16, and the oracle's tokens."""
+    G, R = rnd.gamma_max, rnd.R
+    tv = np.zeros((R, G))
+    tokens = np.zeros((R, G), np.int32)
+    g = to_np(rnd.gamma)
+    for s0 in range(0, R, 32):
+        ids = np.arange(s0, min(R, s0 + 32))
+        o = oracle.sample_block(rows(rnd.U, ids), to_np(rnd.E), to_np(rnd.W), rows(rnd.h, ids), to_np(rnd.w_h),
+                                to_np(rnd.w_e), rnd.b, to_np(rnd.temperature)[ids], to_np(rnd.anchor)[ids], rnd.seed,
+                                t, gamma=g[ids], req_ids=ids, logp=True, threads=_threads())
+        tokens[ids] = o["tokens"]
+        lp = torch.from_numpy(o["logp"]).to(DEV)
+        idx = torch.as_tensor(ids, device=DEV)
+        new = wl.tv_target_rows(lp, rnd.temperature[idx], rnd.extra["tv_delta"][idx])
+        for j, q in enumerate(ids):
+            n = int(g[q])
+            rnd.target[q, :n] = new[j, :n].to(rnd.target.dtype)
+        # the distance the verifier sees: p_t from the rounded rows at temperature T
+        zt = rnd.target[idx, :G].double() / rnd.temperature[idx].double().view(-1, 1, 1)
+        p_t = torch.softmax(zt, dim=2)
+        tv[ids] = (0.5 * (p_t - torch.exp(lp.double())).abs().sum(dim=2)).cpu().numpy()
+    return tv, tokens
+
+
 @pytest.mark.parametrize("workload", [2, 3, 4, 5])
 def test_full_size_round(workload):
     torch.cuda.empty_cache()
     rnd = wl.WORKLOADS[workload](device=DEV)
     total = new_counts()
+    if workload == 5:
+        # the target is scored on the drafted prefix: build it from round 2's draft
+        tv, o_tok = _fill_tv_target(rnd, 2)
     for t in (2, 3):
         add_counts(total, _check_round(rnd, workload, t))
+        if workload == 5 and t == 2:
+            _check_acceptance_is_one_minus_tv(rnd, tv, o_tok)
     report("workload %d, two rounds" % workload, total)
     # every request of both rounds was compared; excusals stay rare
     assert total["checked_requests"] == 2 * rnd.R

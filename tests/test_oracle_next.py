@@ -127,3 +127,23 @@ def test_sts_scales_the_logit_and_keeps_the_order():
     # and the survival is the running product of the scaled confidences; the draws do not move
     np.testing.assert_allclose(sts["surv"], np.cumprod(sts["conf"], axis=1), rtol=1e-12)
     np.testing.assert_array_equal(sts["tokens"], base["tokens"])
+
+
+def test_controlled_tv_rows_have_the_asked_distance():
+    """Input shaping of the controlled-distance workload: rows built from a draft distribution
+    p_d sit at exactly the asked total-variation distance from it (before rounding), the mass
+    moves to the least likely token, and T log p_t recovers p_t."""
+    import torch
+    from speculative_decoding_draft_round_gb300 import workloads as wl
+    g = torch.Generator().manual_seed(3)
+    n, G, V = 5, 4, 300
+    logits = torch.randn((n, G, V), generator=g, dtype=torch.float64) * 2.0
+    lp = torch.log_softmax(logits, dim=2)
+    T = torch.tensor([0.3, 0.7, 1.0, 1.2, 0.5], dtype=torch.float64)
+    delta = 0.05 + 0.55 * torch.rand((n, G), generator=g, dtype=torch.float64)
+    rows = wl.tv_target_rows(lp, T, delta, floor=-1e9).double()
+    p_t = torch.softmax(rows / T.view(-1, 1, 1), dim=2)
+    p_d = torch.exp(lp)
+    tv = 0.5 * (p_t - p_d).abs().sum(dim=2)
+    assert torch.allclose(tv, delta, atol=1e-5)
+    assert torch.equal((p_t - p_d).argmax(dim=2), p_d.argmin(dim=2))
