@@ -139,48 +139,63 @@ __device__ __forceinline__ float2 row_block_argmax(const T* row, int V, int b, i
     return make_float2(best.v, (float)best.i);   // indices below 2^24 are exact in fp32
 }
 
-// grid (vocabulary chunks, R): the CTA walks target rows 0..keep[r] of its request
+// grid (vocabulary chunks, R): the CTA walks target rows 0..keep[r] of its request. Row 0 is
+// verified whatever keep is (rows 0..keep), and its statistics read only inputs: they are formed
+// before the dependency wait, while the scheduler runs, and stored after it (the workspace may
+// still be read by the kernel before this one); rows 1..keep follow once keep exists.
+//
+// This warp's statistics of row i for blocks b0 .. b0 + 7, held by lanes 0-7 (lane bb: block b0 + bb)
+template <typename T>
+__device__ __forceinline__ float2 row_stats_of(const VerifyParams& p, int q, int i, int b0, bool greedy, float scale,
+                                               bool vec, int lane, bool& nonfinite)
+{
+    const T* row = static_cast<const T*>(p.target) + ((size_t)q * (p.G + 1) + i) * p.V;
+    float2 mine = make_float2(-INFINITY, 0.f);
+    if (greedy) {
+        for (int bb = 0; bb < kRowBlocksPerWarp && b0 + bb < p.nblk; ++bb) {
+            const float2 st = row_block_argmax<T>(row, p.V, b0 + bb, lane, nonfinite);
+            if (lane == bb) mine = st;
+        }
+        return mine;
+    }
+    float2 st[kRowBlocksPerWarp];
+    row_block_stats8<T>(row, p.V, b0, scale, lane, vec, st);
+    mine = st[0];
+#pragma unroll
+    for (int bb = 1; bb < kRowBlocksPerWarp; ++bb)
+        if (lane == bb) mine = st[bb];
+    // a NaN or +inf logit leaves a NaN sum or an infinite maximum (-inf is a zero weight)
+    if (lane < kRowBlocksPerWarp && b0 + lane < p.nblk && (!(mine.y >= 0.f) || mine.x == INFINITY || mine.x != mine.x))
+        nonfinite = true;
+    return mine;
+}
+
+__device__ __forceinline__ void store_row_stats(const VerifyParams& p, int q, int i, int b0, int lane, float2 v)
+{
+    if (lane < kRowBlocksPerWarp && b0 + lane < p.nblk) p.row_stats[((size_t)q * (p.G + 1) + i) * p.nblk + b0 + lane] = v;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParams p)
 {
-    pdl_enter();   // keep comes from the scheduler; the workspace is read by the previous call
     const int q = blockIdx.y;
-    const int ell = request_keep(p, q);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool greedy = p.temperature[q] == 0.f;
     const float scale = greedy ? 1.f : kLog2e / p.temperature[q];
     const bool vec = (p.V % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.target) & 15u) == 0);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.n_rej = 0;   // verify_decide counts from zero
     const int b0 = (blockIdx.x * kRowWarps + warp) * kRowBlocksPerWarp;
-    if (b0 >= p.nblk) return;
-    if (greedy) {
-        for (int i = 0; i <= ell; ++i) {
-            const T* row = static_cast<const T*>(p.target) + ((size_t)q * (p.G + 1) + i) * p.V;
-            float2* out = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
-            bool nonfinite = false;
-            for (int bb = 0; bb < kRowBlocksPerWarp && b0 + bb < p.nblk; ++bb) {
-                const float2 st = row_block_argmax<T>(row, p.V, b0 + bb, lane, nonfinite);
-                if (lane == 0) out[b0 + bb] = st;
-            }
-            if (nonfinite) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
-        }
-        return;
+    bool nonfinite = false;
+    float2 row0 = make_float2(-INFINITY, 0.f);
+    if (b0 < p.nblk) row0 = row_stats_of<T>(p, q, 0, b0, greedy, scale, vec, lane, nonfinite);
+    pdl_enter();   // keep comes from the scheduler
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.n_rej = 0;   // verify_decide counts from zero
+    const int ell = request_keep(p, q);
+    if (b0 < p.nblk) {
+        store_row_stats(p, q, 0, b0, lane, row0);
+        for (int i = 1; i <= ell; ++i)
+            store_row_stats(p, q, i, b0, lane, row_stats_of<T>(p, q, i, b0, greedy, scale, vec, lane, nonfinite));
     }
-    for (int i = 0; i <= ell; ++i) {
-        const T* row = static_cast<const T*>(p.target) + ((size_t)q * (p.G + 1) + i) * p.V;
-        float2* out = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
-        float2 st[kRowBlocksPerWarp];
-        row_block_stats8<T>(row, p.V, b0, scale, lane, vec, st);
-        if (lane < kRowBlocksPerWarp && b0 + lane < p.nblk) {
-            float2 v = st[0];
-#pragma unroll
-            for (int bb = 1; bb < kRowBlocksPerWarp; ++bb)
-                if (lane == bb) v = st[bb];
-            out[b0 + lane] = v;
-            // a NaN or +inf logit leaves a NaN sum or an infinite maximum (-inf is a zero weight)
-            if (!(v.y >= 0.f) || v.x == INFINITY || v.x != v.x) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
-        }
-    }
+    if (nonfinite) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
 }
 
 // ----------------------------------------------------------------- accept tests and bonus
@@ -190,15 +205,27 @@ constexpr int kDecideThreads = 128;
 template <typename T>
 __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyParams p)
 {
-    pdl_enter();   // the row statistics and the zeroed rejection counter come from verify_rows
     __shared__ float red[8];
     __shared__ float sv[8];
     __shared__ int si[8];
     __shared__ float lse_s[DSPARK_MAX_GAMMA + 1];
     const int q = blockIdx.x, t = threadIdx.x;
+    // keep, the draft outputs and the inputs were complete before the previous kernel started (it
+    // waited for the scheduler): the acceptance tests' operands are gathered before the wait, so
+    // that only the row log-normalisers are read after it
     const int ell = request_keep(p, q);
     const T* target = static_cast<const T*>(p.target);
-    if (p.temperature[q] == 0.f) {
+    const bool greedy_q = p.temperature[q] == 0.f;
+    float a_zt = 0.f, a_lpd = 0.f, a_lu = 0.f;   // thread t < ell: position t's z_t(x) / T, log p_d(x), log u
+    if (!greedy_q && t < ell) {
+        const size_t o = (size_t)q * p.G + t;
+        const int x = checked_index(p.tokens[o], p.V, p.status);
+        a_zt = ld(target, ((size_t)q * (p.G + 1) + t) * p.V + x) * (1.f / p.temperature[q]);
+        a_lpd = p.draft_logit[o] - p.draft_lse[o];
+        a_lu = logf(uniform_at(make_key(p.seed), p.round, kAccept, (uint32_t)q, (uint32_t)t, 0u));
+    }
+    pdl_enter();   // the row statistics and the zeroed rejection counter come from verify_rows
+    if (greedy_q) {
         // greedy decoding: accept while the draft token equals the target's arg-max; the first
         // mismatch is replaced by that arg-max, else the arg-max of row ell is the bonus token
         __shared__ int s_next;
@@ -245,14 +272,10 @@ __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyPar
     // accept x_j with probability min(1, p_t / p_d): log u < log p_t(x) - log p_d(x)
     const PhiloxKey key = make_key(p.seed);
     int first_reject = ell;
-    for (int j = t; j < ell; j += kDecideThreads) {
-        const size_t o = (size_t)q * p.G + j;
-        const int x = checked_index(p.tokens[o], p.V, p.status);
-        const float zt = ld(target, ((size_t)q * (p.G + 1) + j) * p.V + x) * invT;
-        const float log_pt = zt - lse_s[j];
-        const float log_pd = p.draft_logit[o] - p.draft_lse[o];
-        const float u = uniform_at(key, p.round, kAccept, (uint32_t)q, (uint32_t)j, 0u);
-        if (!(logf(u) < log_pt - log_pd)) first_reject = min(first_reject, j);
+    static_assert(DSPARK_MAX_GAMMA <= kDecideThreads, "one position per thread");
+    if (t < ell) {
+        const float log_pt = a_zt - lse_s[t];
+        if (!(a_lu < log_pt - a_lpd)) first_reject = t;
     }
     const int n = block_min_int<kDecideThreads>(first_reject, si);
     if (t == 0) {
