@@ -120,8 +120,14 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 #pragma unroll
         for (int u = 0; u < 3; ++u) yh[u] = *reinterpret_cast<const float4*>(yrow + u * r + el);
     }
-    pdl_wait();      // the operand rows and the state come from the previous step's kernels
-    pdl_trigger();   // the statistics kernel may start its prologue
+    // The operand rows z[parity] = [hi(s_{k-1}); lo(s_{k-1}); W_1[x_{k-1}]]: the state halves were written by
+    // the previous step's kernel, which completed before the kernel this one follows (the commit) started; only
+    // W_1[x_{k-1}] comes from that commit. So the state chunks and every W_rnn chunk are copied before the
+    // dependency wait, and only the last r columns after it. Step 0 waits first: its seed kernel (zero state,
+    // the anchor's row) is the one it follows.
+    if (k == 0 || !(warp == 0 && lane == 0)) {
+        if (k == 0) pdl_wait();
+    }
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer: chunk c of A = z[parity] columns [64c, 64c + 64) of the tile's
@@ -129,9 +135,16 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         const uint64_t pol = l2_policy_evict_last();
         const int par = k & 1;
         int issued = 0;
+        bool waited = k == 0;
         for (int c = 0; c < n_chunks && !*s_abort; ++c) {
             const int st = c % kRtStages;
             if (c >= kRtStages && !rt_wait(empty(st), ((c / kRtStages) - 1) & 1u, s_abort, p.status)) break;
+            if (!waited && c >= 2 * kc_r) {
+                pdl_wait();      // W_1[x_{k-1}] comes from the commit this kernel follows
+                waited = true;
+            }
+            if (c == 2 * kc_r || (k == 0 && c == 0))
+                pdl_trigger();   // the statistics kernel may start its prologue
             const uint32_t dst = sbase + st * kRtStageBytes;
             mbar_expect_tx(full(st), kRtStageBytes);
             tma_load_3d(dst, &zmap, c * kRtK, mt * kRtM, par, full(st), pol);
