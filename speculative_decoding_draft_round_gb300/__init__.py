@@ -466,7 +466,8 @@ def verify(target, U, E, W, anchor, tokens, draft_lse, draft_logit, keep, temper
 class RoundRunner:
     """Runs sample_block -> schedule -> verify for one workload with persistent
     argument structs, outputs and workspaces (the launch sequence a serving
-    loop would replay every round)."""
+    loop would replay every round). path selects the sampler's contraction path; the verifier
+    has no resident loop and takes the per-step tensor-core kernels for PATH_RESIDENT."""
 
     def __init__(self, rnd, *, path=PATH_AUTO, surv_capacity=None, device=None):
         self.rnd = rnd
@@ -483,7 +484,8 @@ class RoundRunner:
         self.va, self.vout = verify_args(rnd.target, rnd.U, rnd.E, rnd.W, rnd.anchor, self.sout["tokens"],
                                          self.sout["draft_lse"], self.sout["draft_logit"], self.cout["keep"],
                                          rnd.temperature, rnd.seed, rnd.round, gamma=rnd.gamma,
-                                         bias_first=rnd.bias_first, path=path)
+                                         bias_first=rnd.bias_first,
+                                         path=PATH_TENSOR_CORE if path == PATH_RESIDENT else path)
         self.vws = torch.zeros(workspace_bytes("verify", self.va), dtype=torch.uint8, device=dev)
 
     def set_round(self, rnd_index: int):

@@ -12,19 +12,29 @@
 // up to 3 tiles) and one more in shared memory; the rest are streamed each step.
 //
 // One step, on every CTA (roles by warp):
-//   warp 0      TMA producer: U tiles [64 requests x 128 columns] of the step, streamed W chunks
+//   warp 0      TMA producer: U tiles [64 requests x 128 columns] of the step, streamed W chunks;
+//               it runs ahead into the next step as far as its rings allow (neither depends on
+//               the draws)
 //   warp 1      TMEM owner and MMA issuer: D[v][q] = sum_i W[i][v] E[x_{k-1}(q)][i] per block and
 //               request half (M = 128 vocabulary rows, N = 64 requests, K = 16 per instruction)
-//   warp 2      grid barriers and the copy of the next step's conditioning rows (E tile)
-//   warps 4-11  epilogue: lane quarter (warp % 4) = 32 vocabulary rows, column group = 32 requests.
-//               y = (U + D) log2(e) / T; per (request, block) the block maximum and sum of
-//               2^(y - max) by reduce-scatter over the lanes and a combine across the quarters;
-//               the block key of the two-level draw; the CTA's running (max, sum) of each row;
-//               the logits of each row's leading block are saved to a per-CTA slot.
-//   then, after a grid barrier, the commit: per request (one warp), the winning block and CTA
-//   from the packed 64-bit key, the log-normaliser from the CTAs' partials, the element-level
-//   Gumbel-max over the saved logits, the confidence head and survival product, and the next
-//   step's conditioning row W_1[x_k] in 8 copies; a second grid barrier, then the E tile.
+//   warp 2      the grid barrier; then waits for the step's tokens and gathers their W_1 rows
+//               (4 rows per TMA instruction) into the next step's E tile
+//   warp 3      the outputs of this CTA's requests (q = cta mod P): log-normaliser, confidence
+//               head and survival product; off the serial path
+//   warps 4-19  epilogue, two sets of eight warps, one set per request half. A warp holds lane
+//               quarter (warp % 4) = 32 vocabulary rows and a column group of 32 requests. With the
+//               16x256b TMEM load each thread holds 4 vocabulary rows x 8 requests, so the
+//               per-request block maximum and sum of 2^(y - max) cost 3 in-thread steps per 4 rows
+//               and a reduce-scatter over 8 threads (3 shuffle levels); the four quarters' partials
+//               meet in shared memory behind one named barrier, and every thread then merges the
+//               partials of one request (the four warps hold identical copies of each request's
+//               running state, so each decides alone whether the block leads, and writes its own
+//               rows of the leading block's logits to the CTA's slot).
+//   After its last block every CTA posts, per request, its leading block's key in a packed
+//   64-bit atomicMax (key, block, CTA). One grid barrier; then the CTA that holds the winning
+//   block draws the element from its slot (Gumbel-max over 128 logits, one Philox call per lane)
+//   and publishes the token with a release store, tagged with the step. Every CTA waits for the
+//   tags and gathers the next E tile; the draw costs one request per winner, not one per CTA.
 // Every wait is bounded by the global timer. A wait that runs out records DSPARK_ERR_TIMEOUT and
 // sets an abort flag every CTA polls; each role then stops issuing, lets its own copies and MMAs
 // land, and the CTA frees its tensor memory and returns.
@@ -40,30 +50,38 @@
 namespace dspark {
 namespace {
 
-constexpr int LP_THREADS = 384;                 // 12 warps
-constexpr int LP_EPI_WARP0 = 4;                 // warps 4-11: epilogue and commit
-constexpr int LP_EPI_WARPS = 8;
+constexpr int LP_THREADS = 640;                 // 20 warps
+constexpr int LP_EPI_WARP0 = 4;                 // warps 4-19: epilogue
+constexpr int LP_EPI_WARPS = 16;
+constexpr int SET_WARPS = 8;                    // epilogue warps per request half
 constexpr int NHALF = 64;                       // requests per MMA (N)
 constexpr int RMAX = 128;                       // requests handled by this path
 constexpr int KR = 256;                         // Markov rank r
 constexpr int KCH = 64;                         // K per chunk (128 bytes of bf16)
 constexpr int NKC = KR / KCH;                   // 4 chunks
 constexpr int TM_TILES = 3;                     // W tiles held in tensor memory
+constexpr int NT_MAX = 8;                       // vocabulary blocks per CTA
 constexpr uint32_t TILE_COLS = KR / 2;          // TMEM columns of one W^T tile (bf16 pairs)
 constexpr uint32_t ACC_COL = TM_TILES * TILE_COLS;   // 384: two accumulators of 64 columns
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t CHUNK_BYTES = KCH * 128 * 2;      // 16 KB: [64 K rows x 128 vocabulary] as 2 boxes
 constexpr uint32_t BOX_BYTES = 8192;                 // [64 rows x 64 elements] bf16
+constexpr uint32_t U_BYTES = NHALF * 128 * 2;        // one U stage [64 requests x 128 columns]
 constexpr int WR_ST = 2;                        // streamed W chunk stages
-constexpr int U_ST = 3;                         // U half-tile stages [64 requests x 128 columns]
+constexpr int U_ST = 3;                         // U stages
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_E = 0;                                   // E tile: 4 chunks [128 rows x 64 K]
 constexpr uint32_t OFF_S = OFF_E + NKC * RMAX * 128;           // 64 KB: the W tile kept in shared memory
 constexpr uint32_t OFF_WR = OFF_S + NKC * CHUNK_BYTES;         // streamed W chunks
 constexpr uint32_t OFF_U = OFF_WR + WR_ST * CHUNK_BYTES;       // U stages
-constexpr uint32_t OFF_RED = OFF_U + U_ST * (NHALF * 128 * 2); // [2 cg][2 kinds][4 quarters][32] floats
-constexpr uint32_t OFF_SCALE = OFF_RED + 2 * 2 * 4 * 32 * 4;   // [128] floats: log2(e) / T per request
-constexpr uint32_t OFF_MISC = OFF_SCALE + RMAX * 4;            // lead masks, flags, TMEM base
+constexpr uint32_t OFF_RED = OFF_U + U_ST * U_BYTES;           // [2 parity][2 set][2 cg][4 quarter][32] float2
+constexpr uint32_t RED_BYTES = 2 * 2 * 2 * 4 * 32 * 8;
+constexpr uint32_t OFF_GUM = OFF_RED + RED_BYTES;              // [NT_MAX][RMAX] block Gumbels of the step
+constexpr uint32_t OFF_SCALE = OFF_GUM + NT_MAX * RMAX * 4;    // [RMAX] log2(e) / T per request
+constexpr uint32_t OFF_TOK = OFF_SCALE + RMAX * 4;             // [RMAX] the step's tokens (warp 2 -> warp 3)
+constexpr uint32_t OFF_PREV = OFF_TOK + RMAX * 4;              // [RMAX] x_{k-1} of the CTA's own requests
+constexpr uint32_t OFF_SURV = OFF_PREV + RMAX * 4;             // [RMAX] survival of the CTA's own requests
+constexpr uint32_t OFF_MISC = OFF_SURV + RMAX * 4;             // flags, TMEM base
 constexpr uint32_t OFF_BAR = OFF_MISC + 64;
 constexpr int N_BARS = 2 * WR_ST + 2 * U_ST + 4 + 5;
 constexpr uint32_t SMEM_USED = OFF_BAR + N_BARS * 8;
@@ -73,7 +91,15 @@ static_assert(OFF_S % 1024 == 0 && OFF_WR % 1024 == 0 && OFF_U % 1024 == 0, "swi
 // the initial batch of TMEM-resident chunks is staged over E, S, W-ring and U regions
 static_assert(TM_TILES * NKC * CHUNK_BYTES <= OFF_RED, "initial staging fits");
 
+// named barriers: 1-4 the quarters of one (set, column group); the step barrier (warps 2-19);
+// the epilogue warps; warps 2 and 3
+constexpr int BAR_STEP = 5, BAR_STEP_N = 32 * (LP_THREADS / 32 - 2);
+constexpr int BAR_EPI = 6, BAR_EPI_N = 32 * LP_EPI_WARPS;
+constexpr int BAR_TOK = 7, BAR_TOK_N = 64;
+
 constexpr unsigned long long DRAIN_NS = 4000000000ull;
+constexpr uint32_t TAG_SHIFT = 18;                   // token tag: (step + 1) << 18 | token
+constexpr uint32_t TOK_MASK = (1u << TAG_SHIFT) - 1u;
 
 // instruction descriptors, kind::f16, D fp32, A = B = bf16, B K-major (request rows), N = 64,
 // M = 128: A from tensor memory, or A from shared memory MN-major (vocabulary contiguous)
@@ -83,7 +109,6 @@ constexpr uint32_t IDESC_SA = IDESC_TA | (1u << 15);
 struct LoopParams {
     DraftStep d;
     float* slots;            // [P][128][128] fp32: per CTA and request, the leading block's logits y
-    float* hdot;             // [R][G] w_h . h_k
     unsigned int* gbar;      // grid barrier counter (zero at launch)
     int* gabort;             // grid-wide abort flag (zero at launch)
     int P;                   // CTAs
@@ -122,19 +147,20 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+// 16 lanes x 8 columns, four times along the columns (+8 each): thread t receives, in register
+// 4j + {0, 1, 2, 3}, (lane t/4, column 2(t%4) + 8j), (t/4, 2(t%4) + 1 + 8j), (t/4 + 8, 2(t%4) + 8j),
+// (t/4 + 8, 2(t%4) + 1 + 8j) relative to the address. Completion: tmem_wait_ld.
+__device__ __forceinline__ void tmem_ld16x256(uint32_t taddr, uint32_t* v)
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
 {
@@ -176,20 +202,36 @@ __device__ __forceinline__ int ld_relaxed_s32(const int* p)
     return v;
 }
 
+__device__ __forceinline__ void st_release_u32(unsigned int* p, unsigned int v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
-// Reduce 32 values over the 32 lanes of the warp: value i of every lane belongs to column i; on
-// return lane l holds op over all lanes of column l. Fixed pairing order: deterministic.
+// four rows (r0..r3) of a 2-D map, columns [col, col + box width), into consecutive rows at dst
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0, int r1, int r2,
+                                            int r3, uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Reduce 8 values over the 8 lanes that share lane % 4 (lane bits 2-4): value c of every lane
+// belongs to column c; on return lane l holds op over those lanes of column l / 4. Fixed pairing
+// order: deterministic, and the same in every warp.
 template <bool MAX>
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
+__device__ __forceinline__ float reduce_scatter8(float (&v)[8], int lane)
 {
 #pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        const bool up = (lane & s) != 0;
+    for (int s = 4; s >= 1; s >>= 1) {
+        const bool up = ((lane >> 2) & s) != 0;
 #pragma unroll
         for (int j = 0; j < s; ++j) {
             const float send = up ? v[j] : v[j + s];
             const float keep = up ? v[j + s] : v[j];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, s);
+            const float recv = __shfl_xor_sync(0xffffffffu, send, s << 2);
             v[j] = MAX ? fmaxf(keep, recv) : keep + recv;
         }
     }
@@ -214,6 +256,13 @@ struct LoopCtl {
     unsigned long long limit;
 };
 
+__device__ __forceinline__ void give_up(LoopCtl c)
+{
+    *c.abort = 1;
+    atomicExch(c.gabort, 1);
+    raise_status(c.status, DSPARK_ERR_TIMEOUT);
+}
+
 // Bounded wait on a shared-memory barrier phase; false when the CTA aborted or the wait ran out.
 __device__ __noinline__ bool lp_wait(uint32_t bar, uint32_t parity, LoopCtl c)
 {
@@ -223,9 +272,7 @@ __device__ __noinline__ bool lp_wait(uint32_t bar, uint32_t parity, LoopCtl c)
         if (mbar_try_wait(bar, parity)) return true;
         if (*c.abort) return false;
         if (globaltimer() - t0 > c.limit) {
-            *c.abort = 1;
-            atomicExch(c.gabort, 1);
-            raise_status(c.status, DSPARK_ERR_TIMEOUT);
+            give_up(c);
             return false;
         }
     }
@@ -253,9 +300,7 @@ __device__ __noinline__ bool grid_sync(unsigned int* gbar, unsigned int target, 
             return false;
         }
         if (globaltimer() - t0 > c.limit) {
-            *c.abort = 1;
-            atomicExch(c.gabort, 1);
-            raise_status(c.status, DSPARK_ERR_TIMEOUT);
+            give_up(c);
             return false;
         }
     }
@@ -263,11 +308,33 @@ __device__ __noinline__ bool grid_sync(unsigned int* gbar, unsigned int target, 
     return true;
 }
 
+// Bounded wait for the token of one request at step k, published by the CTA that drew it with
+// a release store of ((k + 1) << 18) | token; -1 when the wait ran out or another CTA gave up.
+__device__ __noinline__ int wait_token(const unsigned int* tag, int k, LoopCtl c)
+{
+    const unsigned int want = (unsigned int)(k + 1);
+    unsigned int v = ld_acquire_u32(tag);
+    if ((v >> TAG_SHIFT) == want) return (int)(v & TOK_MASK);
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        v = ld_acquire_u32(tag);
+        if ((v >> TAG_SHIFT) == want) return (int)(v & TOK_MASK);
+        if (*c.abort || ld_relaxed_s32(c.gabort)) {
+            *c.abort = 1;
+            return -1;
+        }
+        if (globaltimer() - t0 > c.limit) {
+            give_up(c);
+            return -1;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ kernel
 
 __global__ void __launch_bounds__(LP_THREADS, 1)
     draft_loop_kernel(const LoopParams L, const __grid_constant__ CUtensorMap tmW,
-                      const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmE)
+                      const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmG)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -284,9 +351,11 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
     const int n_tm = nt < TM_TILES ? nt : TM_TILES;
     const int n_sm = nt > n_tm ? 1 : 0;
 
-    float* s_red = reinterpret_cast<float*>(smem + OFF_RED);
     float* s_scale = reinterpret_cast<float*>(smem + OFF_SCALE);
-    uint32_t* s_lead = reinterpret_cast<uint32_t*>(smem + OFF_MISC);        // [2] lead masks per column group
+    float* s_gum = reinterpret_cast<float*>(smem + OFF_GUM);
+    int* s_tok = reinterpret_cast<int*>(smem + OFF_TOK);
+    int* s_prev = reinterpret_cast<int*>(smem + OFF_PREV);
+    float* s_surv = reinterpret_cast<float*>(smem + OFF_SURV);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + OFF_MISC + 16);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC + 20);
     // written only by warp 2 lane 0 between two named barriers: a decision all its warps share
@@ -304,6 +373,8 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
     const uint32_t init_full = e_full + 24u;
     const uint32_t mma_done = e_full + 32u;
     const LoopCtl ctl{s_abort, L.gabort, p.status, p.wait_ns};
+    const PhiloxKey key = make_key(p.seed);
+    unsigned int* tags = reinterpret_cast<unsigned int*>(p.x_cur);
 
     if (tid == 0) {
         for (int i = 0; i < WR_ST; ++i) {
@@ -312,11 +383,11 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
         }
         for (int i = 0; i < U_ST; ++i) {
             mbar_init(u_full(i), 1);
-            mbar_init(u_empty(i), LP_EPI_WARPS);
+            mbar_init(u_empty(i), SET_WARPS);
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(acc_full(h), 1);
-            mbar_init(acc_empty(h), LP_EPI_WARPS);
+            mbar_init(acc_empty(h), SET_WARPS);
         }
         mbar_init(e_full, 1);
         mbar_init(e_empty, 1);
@@ -353,30 +424,6 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
                 tma_load_2d(dst + BOX_BYTES, &tmW, (b0 + t) * 128 + 64, kc * KCH, init_full, pol);
             }
     }
-    // w_h . h_k of every position (inputs only), spread over all warps of the grid
-    {
-        const int gw = cta * (LP_THREADS / 32) + warp, nw = P * (LP_THREADS / 32);
-        const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(p.h);
-        const bool vec = p.d % 8 == 0 && (reinterpret_cast<uintptr_t>(p.h) & 15u) == 0 &&
-                         (reinterpret_cast<uintptr_t>(p.w_h) & 15u) == 0;
-        for (int pi = gw; pi < R * G; pi += nw) {
-            const __nv_bfloat16* hr = H + (size_t)pi * p.d;
-            float acc = 0.f;
-            if (vec) {
-                for (int c = lane * 8; c < p.d; c += 256) {
-                    float x[8], w[8];
-                    load8<__nv_bfloat16>(hr + c, x);
-                    load8<float>(p.w_h + c, w);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc = fmaf(w[e], x[e], acc);
-                }
-            } else {
-                for (int c = lane; c < p.d; c += 32) acc = fmaf(p.w_h[c], __bfloat162float(hr[c]), acc);
-            }
-            acc = warp_sum(acc);
-            if (lane == 0) L.hdot[pi] = acc;
-        }
-    }
     // the tiles' columns into TMEM: warp 4 + j holds vocabulary rows 32j .. 32j + 31 (its lane
     // quarter); K pair (2c, 2c + 1) in column c of the tile
     if (warp >= LP_EPI_WARP0 && warp < LP_EPI_WARP0 + 4 && n_tm > 0) {
@@ -399,8 +446,6 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
                 }
         }
         tc5::fence_before();
-    } else if (tid == 0 && n_tm > 0) {
-        // thread 0 is not among the converting warps: nothing to do until the staging is consumed
     }
     __syncthreads();
     tc5::fence_after();
@@ -414,43 +459,6 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
             tma_load_2d(dst, &tmW, (b0 + n_tm) * 128, kc * KCH, s_full, pol);
             tma_load_2d(dst + BOX_BYTES, &tmW, (b0 + n_tm) * 128 + 64, kc * KCH, s_full, pol);
         }
-    }
-
-    // ---------------- set-up 2 (the commit warps): conditioning rows of step 0 and cleared pick slots
-    const __nv_bfloat16* E = static_cast<const __nv_bfloat16*>(p.E);
-    __nv_bfloat16* an = static_cast<__nv_bfloat16*>(p.a_next);
-    const size_t rep_stride = (size_t)R * KR;
-    if (warp >= LP_EPI_WARP0) {
-        const int ew = warp - LP_EPI_WARP0;
-        for (int q = cta + P * ew; q < R; q += P * LP_EPI_WARPS) {
-            for (int k = lane; k < G; k += 32) p.pick[(size_t)k * R + q] = 0ull;
-            const int x0 = checked_index(p.anchor[q], V, p.status);
-            uint4 row = make_uint4(0, 0, 0, 0);
-            if (p.bias_first) row = *reinterpret_cast<const uint4*>(E + (size_t)x0 * KR + lane * 8);
-            for (int rp = 0; rp < kAReplicas; ++rp)
-                *reinterpret_cast<uint4*>(an + rp * rep_stride + (size_t)q * KR + lane * 8) = row;
-        }
-    }
-    unsigned int n_grid = 0;   // grid barriers entered (warp 2 lane 0)
-    int e_loads = 0;           // E tile copies issued (warp 2 lane 0)
-    // warp 2 (all lanes take part in the named barriers; lane 0 does the grid work)
-    const int BAR_STEP = 3, BAR_STEP_N = 32 * (1 + LP_EPI_WARPS);
-    if (warp == 2 || warp >= LP_EPI_WARP0) {
-        bar_sync(BAR_STEP, BAR_STEP_N);
-        if (warp == 2 && lane == 0) {
-            ++n_grid;
-            if (grid_sync(L.gbar, n_grid * (unsigned)P, ctl)) {
-                // E tile of step 0
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                mbar_expect_tx(e_full, NKC * RMAX * 128);
-                for (int kc = 0; kc < NKC; ++kc)
-                    tma_load_3d(sbase + OFF_E + (uint32_t)kc * (RMAX * 128), &tmE, kc * KCH, 0, cta % kAReplicas, e_full,
-                                l2_policy_evict_last());
-                ++e_loads;
-            }
-            *s_stop = *s_abort;
-        }
-        bar_sync(BAR_STEP, BAR_STEP_N);
     }
 
     // ======================================================================= the serial steps
@@ -486,8 +494,8 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
                         stop = true;
                         break;
                     }
-                    const uint32_t dst = sbase + OFF_U + (uint32_t)us * (NHALF * 128 * 2);
-                    mbar_expect_tx(u_full(us), NHALF * 128 * 2);
+                    const uint32_t dst = sbase + OFF_U + (uint32_t)us * U_BYTES;
+                    mbar_expect_tx(u_full(us), U_BYTES);
                     tma_load_3d(dst, &tmU, b * 128, k, h * NHALF, u_full(us), pol_u);
                     tma_load_3d(dst + BOX_BYTES, &tmU, b * 128 + 64, k, h * NHALF, u_full(us), pol_u);
                     ++u_fills;
@@ -559,199 +567,370 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
         // every MMA issued above completes before TMEM is freed (after an abort too)
         tc5::commit(mma_done);
         lp_drain(mma_done, 0u);
-    } else if (warp == 2 || warp >= LP_EPI_WARP0) {
-        // ---------------- epilogue (warps 4-11) and the grid work (warp 2)
-        const bool epi = warp >= LP_EPI_WARP0;
-        const int qw = warp & 3, cg = (warp - LP_EPI_WARP0) >> 2, ew = warp - LP_EPI_WARP0;
-        const int vl = 32 * qw + lane;
-        const uint32_t ubox = (uint32_t)(vl >> 6) * BOX_BYTES, uvv = (uint32_t)(vl & 63);
-        const PhiloxKey key = make_key(p.seed);
-        int us = 0;
-        uint32_t uph = 0, n_tile = 0;
-        // owner threads (quarter 0) of request 64 h + 32 cg + lane: draft length, greedy flag
-        int o_gamma[2] = {0, 0};
-        bool o_greedy[2] = {false, false};
-        if (epi && qw == 0)
-            for (int h = 0; h < 2; ++h) {
-                const int q = h * NHALF + 32 * cg + lane;
-                if (q < R) {
-                    int g = p.gamma ? p.gamma[q] : G;
-                    if (g < 0 || g > G) {
-                        raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
-                        g = g < 0 ? 0 : G;
-                    }
-                    o_gamma[h] = g;
-                    o_greedy[h] = p.temperature[q] == 0.f;
-                }
+    } else if (warp == 2) {
+        // ---------------- grid barrier, the step's tokens, the next E tile
+        int gam[4];
+        int rows[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int q = 4 * lane + r;
+            int g = 0;
+            rows[r] = 0;
+            if (q < R) {
+                g = p.gamma ? p.gamma[q] : G;
+                g = g < 0 ? 0 : (g > G ? G : g);   // out-of-range lengths are flagged by the epilogue
+                rows[r] = checked_index(p.anchor[q], V, p.status);
             }
-        // commit warps keep, per assigned request, the previous token and survival
-        int c_prev[2] = {0, 0};
-        float c_surv[2] = {1.f, 1.f};
-        bool dead = false;
-        for (int k = 0; k < G && !dead; ++k) {
-            if (epi) {
-                Lse2 run[2] = {{-INFINITY, 0.f}, {-INFINITY, 0.f}};
-                float best_z[2] = {-INFINITY, -INFINITY};
-                int best_b[2] = {-1, -1};
-                for (int t = 0; t < nt; ++t) {
-                    const int b = b0 + t;
-                    const bool vin = b * 128 + vl < V;
-                    for (int h = 0; h < NH; ++h) {
-                        uint32_t acc[32];
-                        const bool a_ok = __all_sync(0xffffffffu, lp_wait(acc_full(h), n_tile & 1u, ctl));
-                        if (a_ok) {
-                            tc5::fence_after();
-                            tmem_ld32(tmem + ((uint32_t)(qw * 32) << 16) + ACC_COL + (uint32_t)(h * NHALF + 32 * cg), acc);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) acc[i] = 0u;
-                        }
-                        tc5::fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty(h));
-                        const bool u_ok = __all_sync(0xffffffffu, lp_wait(u_full(us), uph, ctl));
-                        float y[32];
-                        const uint32_t ust = sbase + OFF_U + (uint32_t)us * (NHALF * 128 * 2) + ubox;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const uint32_t rr = (uint32_t)(32 * cg + i);
-                            float u = 0.f;
-                            if (u_ok)
-                                u = __uint_as_float((uint32_t)lds_u16(ust + rr * 128 + ((((uvv >> 3) ^ (rr & 7)) << 4) |
-                                                                                         ((uvv & 7) << 1)))
-                                                    << 16);
-                            const float x = u + __uint_as_float(acc[i]);
-                            y[i] = vin ? x * s_scale[h * NHALF + 32 * cg + i] : -INFINITY;
-                        }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(u_empty(us));
-                        if (++us == U_ST) {
-                            us = 0;
-                            uph ^= 1u;
-                        }
-                        // block maximum per request: lanes, then the four quarters
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = y[i];
-                        const float mq = reduce_scatter32<true>(v, lane);
-                        float* red_m = s_red + (cg * 2 + 0) * 128;
-                        float* red_s = s_red + (cg * 2 + 1) * 128;
-                        red_m[qw * 32 + lane] = mq;
-                        bar_sync(1 + cg, 128);
-                        const float M = fmaxf(fmaxf(red_m[lane], red_m[32 + lane]), fmaxf(red_m[64 + lane], red_m[96 + lane]));
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float Mi = __shfl_sync(0xffffffffu, M, i);
-                            v[i] = Mi == -INFINITY ? 0.f : ex2(y[i] - Mi);
-                        }
-                        const float sq = reduce_scatter32<false>(v, lane);
-                        red_s[qw * 32 + lane] = sq;
-                        bar_sync(1 + cg, 128);
-                        const float S = (red_s[lane] + red_s[32 + lane]) + (red_s[64 + lane] + red_s[96 + lane]);
-                        if (qw == 0) {
-                            // owner of request q: block key, running log-normaliser, leading block
-                            const int q = h * NHALF + 32 * cg + lane;
-                            bool lead = false;
-                            if (q < R && k < o_gamma[h] && a_ok && u_ok) {
-                                if (!(S >= 0.f) || M == INFINITY || M != M) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
-                                if (S > 0.f) {
-                                    run[h] = lse2_merge(run[h], Lse2{M, S});
-                                    const float z = o_greedy[h]
-                                                        ? M
-                                                        : (M + log2f(S)) * kLn2 -
-                                                              logf(-logf(uniform_at(key, p.round, kDraftBlock, (uint32_t)q,
-                                                                                    (uint32_t)k, (uint32_t)b)));
-                                    if (z > best_z[h]) {
-                                        best_z[h] = z;
-                                        best_b[h] = b;
-                                        lead = true;
-                                    }
-                                }
-                            }
-                            const uint32_t mask = __ballot_sync(0xffffffffu, lead);
-                            if (lane == 0) s_lead[cg] = mask;
-                        }
-                        bar_sync(1 + cg, 128);
-                        // the leading block's logits of these requests, for the commit's element draw
-                        const uint32_t mask = s_lead[cg];
-                        if (mask) {
-                            float* slot = L.slots + ((size_t)cta * RMAX + h * NHALF + 32 * cg) * 128 + vl;
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if ((mask >> i) & 1u) slot[(size_t)i * 128] = y[i];
-                        }
-                    }
-                    ++n_tile;
-                }
-                if (qw == 0)
-                    for (int h = 0; h < NH; ++h) {
-                        const int q = h * NHALF + 32 * cg + lane;
-                        if (q < R && k < o_gamma[h]) {
-                            p.stats[(size_t)q * P + cta] = make_float2(run[h].m, run[h].s);
-                            if (best_b[h] >= 0)
-                                atomicMax(p.pick + (size_t)k * R + q,
-                                          pack_pick(best_z[h], (int)(((uint32_t)best_b[h] << 15) | (uint32_t)cta)));
-                        }
-                    }
+            gam[r] = g;
+        }
+        unsigned int n_grid = 0;
+        int e_loads = 0;
+        // E tile of step 0: W_1 rows of the anchors, or zeros when the first step has no bias
+        if (!*s_abort) {
+            if (p.bias_first) {
+                if (lane == 0) mbar_expect_tx(e_full, NKC * RMAX * 128);
+                __syncwarp();
+                const uint64_t pol = l2_policy_evict_last();
+                for (int kc = 0; kc < NKC; ++kc)
+                    tma_gather4(sbase + OFF_E + (uint32_t)kc * (RMAX * 128) + (uint32_t)lane * 512, &tmG, kc * KCH,
+                                rows[0], rows[1], rows[2], rows[3], e_full, pol);
+            } else {
+                uint4* e4 = reinterpret_cast<uint4*>(smem + OFF_E);
+                for (int i = lane; i < NKC * RMAX * 128 / 16; i += 32) e4[i] = make_uint4(0, 0, 0, 0);
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(e_full);
             }
-            // ---- grid barrier 1: every CTA's partials, block keys and slots are written
+            e_loads = 1;
+        }
+        for (int k = 0; k < G; ++k) {
             bar_sync(BAR_STEP, BAR_STEP_N);
-            if (warp == 2 && lane == 0) {
+            if (lane == 0) {
                 ++n_grid;
                 (void)grid_sync(L.gbar, n_grid * (unsigned)P, ctl);
                 *s_stop = *s_abort;
             }
             bar_sync(BAR_STEP, BAR_STEP_N);
-            if (*s_stop) {
-                dead = true;
-                break;
+            if (*s_stop) break;
+            // the tokens of step k, as their winners publish them
+            bool got = true;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int q = 4 * lane + r;
+                int tok = -1;
+                if (q < R && k < gam[r]) {
+                    tok = wait_token(tags + q, k, ctl);
+                    got = got && tok >= 0;
+                }
+                s_tok[q] = tok;
+                rows[r] = (q < R && k + 1 < gam[r] && tok >= 0) ? tok : 0;
             }
-            // ---- commit: one warp per request
-            if (epi) {
-                int j = 0;
-                for (int q = cta + P * ew; q < R; q += P * LP_EPI_WARPS, ++j) {
-                    const int jj = j < 2 ? j : 1;   // at most two requests per warp keep state (R <= 128)
-                    const size_t o = (size_t)q * G + k;
-                    int g = p.gamma ? p.gamma[q] : G;
-                    g = g < 0 ? 0 : (g > G ? G : g);
-                    if (k == 0) {
-                        c_prev[jj] = checked_index(p.anchor[q], V, p.status);
-                        c_surv[jj] = 1.f;
+            bar_sync(BAR_TOK, BAR_TOK_N);
+            got = __all_sync(0xffffffffu, got);
+            if (k + 1 < G && got) {
+                bool free_ok = true;
+                if (lane == 0) free_ok = lp_wait(e_empty, (uint32_t)k & 1u, ctl);
+                free_ok = __shfl_sync(0xffffffffu, free_ok, 0);
+                if (free_ok) {
+                    if (lane == 0) mbar_expect_tx(e_full, NKC * RMAX * 128);
+                    __syncwarp();
+                    const uint64_t pol = l2_policy_evict_last();
+                    for (int kc = 0; kc < NKC; ++kc)
+                        tma_gather4(sbase + OFF_E + (uint32_t)kc * (RMAX * 128) + (uint32_t)lane * 512, &tmG, kc * KCH,
+                                    rows[0], rows[1], rows[2], rows[3], e_full, pol);
+                    ++e_loads;
+                }
+            }
+        }
+        // the last E tile copy lands before exit (it may be unconsumed after an abort)
+        if (lane == 0 && e_loads > 0) lp_drain(e_full, (uint32_t)(e_loads - 1) & 1u);
+    } else if (warp == 3) {
+        // ---------------- outputs of this CTA's requests (q = cta + P j), one step behind the draw
+        const __nv_bfloat16* E = static_cast<const __nv_bfloat16*>(p.E);
+        const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(p.h);
+        const bool hvec = p.d % 8 == 0 && (reinterpret_cast<uintptr_t>(p.h) & 15u) == 0 &&
+                          (reinterpret_cast<uintptr_t>(p.w_h) & 15u) == 0;
+        if (lane == 0)
+            for (int q = cta; q < R; q += P) {
+                s_prev[q] = checked_index(p.anchor[q], V, p.status);
+                s_surv[q] = 1.f;
+            }
+        __syncwarp();
+        for (int k = 0; k < G; ++k) {
+            bar_sync(BAR_STEP, BAR_STEP_N);
+            bar_sync(BAR_STEP, BAR_STEP_N);
+            if (*s_stop) break;
+            bar_sync(BAR_TOK, BAR_TOK_N);
+            for (int q = cta; q < R; q += P) {
+                const size_t o = (size_t)q * G + k;
+                int g = p.gamma ? p.gamma[q] : G;
+                g = g < 0 ? 0 : (g > G ? G : g);
+                if (k >= g) {
+                    if (lane == 0) {
+                        p.tokens[o] = -1;
+                        p.conf[o] = p.surv[o] = p.draft_lse[o] = p.draft_logit[o] = 0.f;
                     }
-                    if (k >= g) {
-                        if (lane == 0) {
-                            p.tokens[o] = -1;
-                            p.conf[o] = p.surv[o] = p.draft_lse[o] = p.draft_logit[o] = 0.f;
-                        }
-                        if (p.a_rows)
-                            for (int i = lane; i < KR; i += 32) p.a_rows[o * KR + i] = 0.f;
-                        continue;
-                    }
-                    const bool greedy = p.temperature[q] == 0.f;
-                    const unsigned long long pk = *reinterpret_cast<volatile unsigned long long*>(p.pick + (size_t)k * R + q);
-                    const uint32_t idx = ~(uint32_t)pk;
-                    int bstar = (int)(idx >> 15), cstar = (int)(idx & 0x7FFFu);
-                    if (pk == 0ull || bstar >= nblk || cstar >= P) {
-                        raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
-                        bstar = 0;
-                        cstar = 0;
-                    }
-                    // log-normaliser from the CTAs' partials
+                    if (p.a_rows)
+                        for (int i = lane; i < KR; i += 32) p.a_rows[o * KR + i] = 0.f;
+                    continue;
+                }
+                const int tok = s_tok[q];
+                if (tok < 0) continue;   // the wait for it ran out: the call has failed
+                const bool greedy = p.temperature[q] == 0.f;
+                if (!greedy) {
+                    // log-normaliser from the CTAs' partials of this step (written before the grid barrier)
                     Lse2 tot{-INFINITY, 0.f};
+                    const float2* st = p.stats + ((size_t)(k & 1) * R + q) * P;
                     for (int c2 = lane; c2 < P; c2 += 32) {
-                        // written by other CTAs before the grid barrier: load past L1 (not coherent)
-                        const float2 st = __ldcg(p.stats + (size_t)q * P + c2);
-                        tot = lse2_merge(tot, Lse2{st.x, st.y});
+                        const float2 v = __ldcg(st + c2);
+                        tot = lse2_merge(tot, Lse2{v.x, v.y});
                     }
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) {
-                        const Lse2 o2{__shfl_xor_sync(0xffffffffu, tot.m, off), __shfl_xor_sync(0xffffffffu, tot.s, off)};
+                        const Lse2 o2{__shfl_xor_sync(0xffffffffu, tot.m, off),
+                                      __shfl_xor_sync(0xffffffffu, tot.s, off)};
                         tot = lse2_merge(tot, o2);
                     }
-                    // element-level draw over the winning block's saved logits (4 per lane)
-                    const float4 y4 = __ldcg(reinterpret_cast<const float4*>(
-                        L.slots + ((size_t)cstar * RMAX + q) * 128 + lane * 4));
-                    const float yv[4] = {y4.x, y4.y, y4.z, y4.w};
+                    if (lane == 0) p.draft_lse[o] = (tot.m + log2f(tot.s)) * kLn2;
+                }
+                // confidence head (eq. 7) on W_1[x_{k-1}] (or W_1[x_k]) and the hidden state h_k
+                const int prev = s_prev[q];
+                float ep[8], en[8], we[8];
+                load8<__nv_bfloat16>(E + (size_t)prev * KR + lane * 8, ep);
+                load8<__nv_bfloat16>(E + (size_t)tok * KR + lane * 8, en);
+                load8<float>(p.w_e + lane * 8, we);
+                float dot = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dot = fmaf(we[i], p.conf_token ? en[i] : ep[i], dot);
+                float hd = 0.f;
+                const __nv_bfloat16* hr = H + o * p.d;
+                if (hvec) {
+                    for (int c = lane * 8; c < p.d; c += 256) {
+                        float x[8], w[8];
+                        load8<__nv_bfloat16>(hr + c, x);
+                        load8<float>(p.w_h + c, w);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) hd = fmaf(w[e], x[e], hd);
+                    }
+                } else {
+                    for (int c = lane; c < p.d; c += 32) hd = fmaf(p.w_h[c], __bfloat162float(hr[c]), hd);
+                }
+                dot = warp_sum(dot) + warp_sum(hd);
+                const float lc = (dot + p.b) / (p.sts_temp ? p.sts_temp[k] : 1.f);
+                const float c = 1.f / (1.f + expf(-lc));
+                const float s = s_surv[q] * c;
+                if (p.a_rows)   // the Markov operand row W_1[x_{k-1}] (reported even when no bias is added)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) p.a_rows[o * KR + lane * 8 + i] = ep[i];
+                __syncwarp();
+                if (lane == 0) {
+                    if (!isfinite(lc)) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
+                    p.conf[o] = c;
+                    p.surv[o] = s;
+                    s_prev[q] = tok;
+                    s_surv[q] = s;
+                }
+                __syncwarp();
+            }
+        }
+    } else if (warp >= LP_EPI_WARP0) {
+        // ---------------- epilogue
+        const int ew = warp - LP_EPI_WARP0, set = ew >> 3, cg = (ew >> 2) & 1, qw = warp & 3;
+        const int t4 = lane & 3, tq = lane >> 2;
+        const bool live = set < NH;
+        // this thread's 8 requests: local column c = 2j + e is request colbase + e + 8j
+        const int colbase = NHALF * set + 32 * cg + 2 * t4;
+        float sc[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) sc[c] = s_scale[colbase + (c & 1) + 8 * (c >> 1)];
+        // the request whose block statistics this thread holds after the reductions (column tq)
+        const int q_own = colbase + (tq & 1) + 8 * (tq >> 1);
+        const int loc_own = q_own - NHALF * set - 32 * cg;
+        const float sc_own = s_scale[q_own];
+        int g_own = 0;
+        bool greedy_own = false;
+        if (q_own < R) {
+            int g = p.gamma ? p.gamma[q_own] : G;
+            if (g < 0 || g > G) {
+                if (live && qw == 0) raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+                g = g < 0 ? 0 : G;
+            }
+            g_own = g;
+            greedy_own = p.temperature[q_own] == 0.f;
+        }
+        // U element (row e + 8j of this thread's column group, vocabulary row 32 qw + tq + 8i of
+        // the block) in a stage: two boxes of [64 rows x 64 columns], 128-byte swizzle
+        uint32_t uoff[4][2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                uoff[i][e] = (uint32_t)(qw >> 1) * BOX_BYTES + (uint32_t)(32 * cg + 2 * t4 + e) * 128u +
+                             ((((uint32_t)(4 * (qw & 1) + i)) ^ (uint32_t)(2 * t4 + e)) << 4) + (uint32_t)tq * 2u;
+        const uint32_t t_acc = tmem + ((uint32_t)(32 * qw) << 16) + ACC_COL + (uint32_t)(set * NHALF + 32 * cg);
+        float2* s_red = reinterpret_cast<float2*>(smem + OFF_RED);
+        uint32_t n_tile = 0;
+        // the block Gumbels of step k: one Philox call per request and group of 4 blocks
+        auto block_gumbels = [&](int k) {
+            const int e = ew * 32 + lane, q = e >> 2, grp = (b0 >> 2) + (e & 3);
+            if (q < R && 4 * grp < b0 + nt) {
+                const uint4 w = philox4x32_10(
+                    make_uint4((uint32_t)grp, (uint32_t)k, (uint32_t)q, counter_word3(p.round, kDraftBlock)), key);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const int b = 4 * grp + s;
+                    if (b >= b0 && b < b0 + nt) s_gum[(b - b0) * RMAX + q] = -logf(-logf(bits_to_uniform(ww[s])));
+                }
+            }
+        };
+        block_gumbels(0);
+        bar_sync(BAR_EPI, BAR_EPI_N);
+        for (int k = 0; k < G; ++k) {
+            const bool act = q_own < R && k < g_own;
+            Lse2 run{-INFINITY, 0.f};
+            float best_z = -INFINITY;
+            int best_b = -1;
+            if (live)
+                for (int t = 0; t < nt; ++t) {
+                    const int b = b0 + t;
+                    const uint32_t par = n_tile & 1u;
+                    uint32_t a[32];
+                    const bool a_ok = __all_sync(0xffffffffu, lp_wait(acc_full(set), par, ctl));
+                    if (a_ok) {
+                        tc5::fence_after();
+                        tmem_ld16x256(t_acc, a);
+                        tmem_ld16x256(t_acc + (16u << 16), a + 16);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) a[i] = 0u;
+                    }
+                    tc5::fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty(set));
+                    const uint32_t pos = n_tile * (uint32_t)NH + (uint32_t)set;
+                    const int us = (int)(pos % U_ST);
+                    const bool u_ok = __all_sync(0xffffffffu, lp_wait(u_full(us), (pos / U_ST) & 1u, ctl));
+                    const uint32_t ust = sbase + OFF_U + (uint32_t)us * U_BYTES;
+                    // y = U + D (unscaled) for vocabulary rows i, local columns c: y[4c + i]
+                    float y[32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const bool vin = b * 128 + 32 * qw + tq + 8 * i < V;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                float u = 0.f;
+                                if (u_ok) u = __uint_as_float((uint32_t)lds_u16(ust + uoff[i][e] + j * 1024) << 16);
+                                const float x = u + __uint_as_float(a[16 * (i >> 1) + 4 * j + 2 * (i & 1) + e]);
+                                y[4 * (2 * j + e) + i] = vin ? x : -INFINITY;
+                            }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(u_empty(us));
+                    // per-request maximum over the quarter's 32 rows: 4 in-thread, then 8 threads
+                    float v[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = fmaxf(fmaxf(y[4 * c], y[4 * c + 1]), fmaxf(y[4 * c + 2], y[4 * c + 3]));
+                    const float m_q = reduce_scatter8<true>(v, lane);
+                    float off[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float mc = __shfl_sync(0xffffffffu, m_q, (c << 2) | t4);
+                        off[c] = mc == -INFINITY ? 0.f : mc * sc[c];
+                    }
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = (ex2(fmaf(y[4 * c], sc[c], -off[c])) + ex2(fmaf(y[4 * c + 1], sc[c], -off[c]))) +
+                               (ex2(fmaf(y[4 * c + 2], sc[c], -off[c])) + ex2(fmaf(y[4 * c + 3], sc[c], -off[c])));
+                    const float s_q = reduce_scatter8<false>(v, lane);
+                    if (act && a_ok && u_ok && (!(s_q >= 0.f) || m_q == INFINITY || m_q != m_q))
+                        raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
+                    // the four quarters' partials of each request; every thread merges its request's
+                    float2* red = s_red + (size_t)((par * 2 + set) * 2 + cg) * 4 * 32;
+                    red[qw * 32 + loc_own] = make_float2(m_q == -INFINITY ? -INFINITY : m_q * sc_own, s_q);
+                    bar_sync(1 + 2 * set + cg, 128);
+                    float2 pq[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) pq[j] = red[j * 32 + loc_own];
+                    const float mb = fmaxf(fmaxf(pq[0].x, pq[1].x), fmaxf(pq[2].x, pq[3].x));
+                    float sb = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (pq[j].y > 0.f) sb += pq[j].y * ex2(pq[j].x - mb);
+                    bool lead = false;
+                    if (act && a_ok && u_ok && sb > 0.f) {
+                        run = lse2_merge(run, Lse2{mb, sb});
+                        const float z = greedy_own ? mb : (mb + log2f(sb)) * kLn2 + s_gum[t * RMAX + q_own];
+                        if (z > best_z) {
+                            best_z = z;
+                            best_b = b;
+                            lead = true;
+                        }
+                    }
+                    // the leading block's logits of these requests, for the element draw
+                    const uint32_t mask = __ballot_sync(0xffffffffu, lead);
+                    if (mask) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            if ((mask >> ((c << 2) | t4)) & 1u) {
+                                float* slot = L.slots + ((size_t)cta * RMAX + colbase + (c & 1) + 8 * (c >> 1)) * 128 +
+                                              32 * qw + tq;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) slot[8 * i] = y[4 * c + i] * sc[c];
+                            }
+                    }
+                    ++n_tile;
+                }
+            // the CTA's partial log-normaliser and leading block key of each request
+            if (live && qw == 0 && act) {
+                p.stats[((size_t)(k & 1) * R + q_own) * P + cta] = make_float2(run.m, run.s);
+                if (best_b >= 0)
+                    atomicMax(p.pick + (size_t)k * R + q_own,
+                              pack_pick(best_z, (int)(((uint32_t)best_b << 15) | (uint32_t)cta)));
+            }
+            bar_sync(BAR_EPI, BAR_EPI_N);   // every slot of the step is written
+            // this warp's requests for the draw (q = ew + 16 jj): the CTA's own slots, in case it won
+            float4 pre[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int q = ew + 16 * jj;
+                pre[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (q < R)
+                    pre[jj] = __ldcg(reinterpret_cast<const float4*>(L.slots + ((size_t)cta * RMAX + q) * 128 + lane * 4));
+            }
+            bar_sync(BAR_STEP, BAR_STEP_N);
+            bar_sync(BAR_STEP, BAR_STEP_N);   // warp 2 has passed the grid barrier
+            if (*s_stop) break;
+            // the draw of every request whose winning block this CTA holds
+            unsigned long long pk_l = 0ull;
+            int g_l = 0;
+            if (lane < 8 && ew + 16 * lane < R) {
+                const int q = ew + 16 * lane;
+                pk_l = *reinterpret_cast<volatile unsigned long long*>(p.pick + (size_t)k * R + q);
+                int g = p.gamma ? p.gamma[q] : G;
+                g_l = g < 0 ? 0 : (g > G ? G : g);
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int q = ew + 16 * jj;
+                if (q >= R) break;
+                const unsigned long long pk = __shfl_sync(0xffffffffu, pk_l, jj);
+                const int g = __shfl_sync(0xffffffffu, g_l, jj);
+                if (k >= g) continue;
+                const uint32_t idx = ~(uint32_t)pk;
+                const int bstar = (int)(idx >> 15), cstar = (int)(idx & 0x7FFFu);
+                const bool valid = pk != 0ull && bstar < nblk && cstar < P;
+                if (valid ? cstar != cta : q % P != cta) continue;
+                const bool greedy = p.temperature[q] == 0.f;
+                int tok = 0;
+                float logit = 0.f;
+                if (valid) {
+                    // element-level Gumbel-max over the winning block's saved logits (4 per lane)
+                    const float yv[4] = {pre[jj].x, pre[jj].y, pre[jj].z, pre[jj].w};
                     const int vb = bstar * 128 + lane * 4;
                     uint4 w4 = make_uint4(0, 0, 0, 0);
                     if (!greedy)
@@ -763,76 +942,40 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
                     float lv_best = 0.f;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const int v = vb + i;
-                        if (v < V) {
+                        const int vv = vb + i;
+                        if (vv < V) {
                             const float lv = yv[i] * kLn2;
-                            const float c = greedy ? lv : lv - logf(-logf(bits_to_uniform(wv[i])));
-                            if (best.i < 0 || c > best.v) {
-                                best = ArgMax{c, v};
+                            const float cand = greedy ? lv : lv - logf(-logf(bits_to_uniform(wv[i])));
+                            if (best.i < 0 || cand > best.v) {
+                                best = ArgMax{cand, vv};
                                 lv_best = lv;
                             }
                         }
                     }
                     const ArgMax win = warp_argmax(best);
-                    int tok = win.i;
+                    tok = win.i;
                     const int src = tok >= 0 ? ((tok - bstar * 128) >> 2) : 0;
-                    const float logit = __shfl_sync(0xffffffffu, lv_best, src & 31);
+                    logit = __shfl_sync(0xffffffffu, lv_best, src & 31);
                     if (tok < 0) {
                         raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
                         tok = min(bstar * 128, V - 1);
                     }
-                    // confidence head (eq. 7) on W_1[x_{k-1}] (or W_1[x_k]), survival product
-                    const int prev = c_prev[jj];
-                    float ep[8], en[8], we[8];
-                    load8<__nv_bfloat16>(E + (size_t)prev * KR + lane * 8, ep);
-                    load8<__nv_bfloat16>(E + (size_t)tok * KR + lane * 8, en);
-                    load8<float>(p.w_e + lane * 8, we);
-                    float dot = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) dot = fmaf(we[i], p.conf_token ? en[i] : ep[i], dot);
-                    dot = warp_sum(dot) + __ldcg(L.hdot + o);
-                    const float lc = (dot + p.b) / (p.sts_temp ? p.sts_temp[k] : 1.f);
-                    const float c = 1.f / (1.f + expf(-lc));
-                    const float s = c_surv[jj] * c;
-                    if (lane == 0) {
-                        if (!isfinite(lc)) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
-                        p.tokens[o] = tok;
-                        p.conf[o] = c;
-                        p.surv[o] = s;
-                        p.draft_lse[o] = greedy ? logit : (tot.m + log2f(tot.s)) * kLn2;
-                        p.draft_logit[o] = logit;
-                    }
-                    if (p.a_rows)   // the Markov operand row W_1[x_{k-1}] (reported even when no bias is added)
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) p.a_rows[o * KR + lane * 8 + i] = ep[i];
-                    // the next step's conditioning row, in every copy
-                    const uint4 row = *reinterpret_cast<const uint4*>(E + (size_t)tok * KR + lane * 8);
-                    for (int rp = 0; rp < kAReplicas; ++rp)
-                        *reinterpret_cast<uint4*>(an + rp * rep_stride + (size_t)q * KR + lane * 8) = row;
-                    c_prev[jj] = tok;
-                    c_surv[jj] = s;
+                } else {
+                    raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
+                }
+                if (lane == 0) {
+                    const size_t o = (size_t)q * G + k;
+                    p.tokens[o] = tok;
+                    p.draft_logit[o] = logit;
+                    if (greedy) p.draft_lse[o] = logit;
+                    st_release_u32(tags + q, ((uint32_t)(k + 1) << TAG_SHIFT) | (uint32_t)tok);
                 }
             }
-            if (k + 1 == G) break;
-            // ---- grid barrier 2: every conditioning row of step k + 1 is written; then the E tile
-            bar_sync(BAR_STEP, BAR_STEP_N);
-            if (warp == 2 && lane == 0) {
-                ++n_grid;
-                if (grid_sync(L.gbar, n_grid * (unsigned)P, ctl) && lp_wait(e_empty, (uint32_t)k & 1u, ctl)) {
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    mbar_expect_tx(e_full, NKC * RMAX * 128);
-                    for (int kc = 0; kc < NKC; ++kc)
-                        tma_load_3d(sbase + OFF_E + (uint32_t)kc * (RMAX * 128), &tmE, kc * KCH, 0, cta % kAReplicas,
-                                    e_full, l2_policy_evict_last());
-                    ++e_loads;
-                }
-                *s_stop = *s_abort;
+            if (k + 1 < G) {
+                block_gumbels(k + 1);
+                bar_sync(BAR_EPI, BAR_EPI_N);
             }
-            bar_sync(BAR_STEP, BAR_STEP_N);
-            if (*s_stop) dead = true;
         }
-        // the last E tile copy lands before exit (it may be unconsumed after an abort)
-        if (warp == 2 && lane == 0 && e_loads > 0) lp_drain(e_full, (uint32_t)(e_loads - 1) & 1u);
     }
     __syncwarp();
     tc5::fence_before();
@@ -911,20 +1054,21 @@ bool loop_supported(int dtype, int head, int R, int V, int r, const void* U, con
                     const void* h, const void* w_h, const void* w_e)
 {
     if (dtype != DSPARK_BF16 || head != DSPARK_HEAD_MARKOV || R < 1 || R > RMAX || r != KR || V % 8 != 0) return false;
-    // at least 8 CTAs, so that each commit warp keeps at most two requests
-    if ((V + 127) / 128 < 8 || loop_ctas(R, V) < 8) return false;
+    // tokens fit the step tag; at least 8 CTAs, each with at most NT_MAX vocabulary blocks
+    if (V > (int)TOK_MASK + 1) return false;
+    const int nblk = (V + 127) / 128, P = loop_ctas(R, V);
+    if (nblk < 8 || P < 8 || (nblk + P - 1) / P > NT_MAX) return false;
     if (!a16(U) || !a16(E) || !a16(W) || !a16(h) || !a16(w_h) || !a16(w_e)) return false;
     return lp_encode_fn() != nullptr;
 }
 
 size_t loop_slot_bytes(int R, int V) { return (size_t)loop_ctas(R, V) * RMAX * 128 * sizeof(float); }
 
-cudaError_t launch_draft_loop(const DraftStep& p, float* slots, float* hdot, unsigned int* gbar, int* gabort,
-                              cudaStream_t s)
+cudaError_t launch_draft_loop(const DraftStep& p, float* slots, unsigned int* gbar, int* gabort, cudaStream_t s)
 {
     const int P = loop_ctas(p.R, p.V);
     if (P < 8) return cudaErrorNotSupported;
-    CUtensorMap tmW, tmU, tmE;
+    CUtensorMap tmW, tmU, tmG;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)p.V, (cuuint64_t)p.r};
         const cuuint64_t strides[1] = {(cuuint64_t)p.V * 2};
@@ -940,10 +1084,11 @@ cudaError_t launch_draft_loop(const DraftStep& p, float* slots, float* hdot, uns
         if (e != cudaSuccess) return e;
     }
     {
-        const cuuint64_t dims[3] = {(cuuint64_t)p.r, (cuuint64_t)p.R, (cuuint64_t)kAReplicas};
-        const cuuint64_t strides[2] = {(cuuint64_t)p.r * 2, (cuuint64_t)p.R * p.r * 2};
-        const cuuint32_t box[3] = {KCH, RMAX, 1};
-        const cudaError_t e = enc(&tmE, p.a_next, 3, dims, strides, box);
+        // W_1 [V][r] for the row gathers: boxes of one row x 64 columns (tile::gather4 takes 4 rows)
+        const cuuint64_t dims[2] = {(cuuint64_t)p.r, (cuuint64_t)p.V};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.r * 2};
+        const cuuint32_t box[2] = {KCH, 1};
+        const cudaError_t e = enc(&tmG, p.E, 2, dims, strides, box);
         if (e != cudaSuccess) return e;
     }
     LoopParams L;
@@ -951,12 +1096,18 @@ cudaError_t launch_draft_loop(const DraftStep& p, float* slots, float* hdot, uns
     L.d = p;
     L.d.n_stats = P;
     L.slots = slots;
-    L.hdot = hdot;
     L.gbar = gbar;
     L.gabort = gabort;
     L.P = P;
+    // cleared per call: the grid barrier, the abort flag, and the step tags (x_cur) through the
+    // pick slots (the partial statistics between them are rewritten before they are read)
     cudaError_t e = cudaMemsetAsync(gbar, 0, sizeof(unsigned int), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(gabort, 0, sizeof(int), s);
+    if (e == cudaSuccess) {
+        const char* lo = reinterpret_cast<const char*>(p.x_cur);
+        const char* hi = reinterpret_cast<const char*>(p.pick + (size_t)p.G * p.R);
+        e = cudaMemsetAsync(p.x_cur, 0, (size_t)(hi - lo), s);
+    }
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(P);
@@ -968,7 +1119,7 @@ cudaError_t launch_draft_loop(const DraftStep& p, float* slots, float* hdot, uns
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, draft_loop_kernel, L, tmW, tmU, tmE);
+    e = cudaLaunchKernelEx(&cfg, draft_loop_kernel, L, tmW, tmU, tmG);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
