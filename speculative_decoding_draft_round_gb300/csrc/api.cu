@@ -71,7 +71,7 @@ dspark_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSPARK_OK :
 // ------------------------------------------------------------ sample_block
 
 struct SampleLayout {
-    size_t x_cur, stats, pick, a_next, yh, state, a_rows, a_lo, zbuf, slots, total;
+    size_t x_cur, stats, pick, a_next, yh, state, a_rows, a_lo, zbuf, slots, hdot, total;
 };
 
 // the status word sits at offset 0 of every workspace; the resident loop's grid barrier counter
@@ -145,6 +145,8 @@ SampleLayout sample_layout(const dspark_sample_args* a)
     o = align_up(o + (rnn && sample_uses_tc(a) ? 2 * 2 * (size_t)a->R * 3 * a->r : 0), kAlign);
     L.slots = o;   // the loop: per CTA and request, the leading block's logits
     o = align_up(o + (loop ? loop_slot_bytes(a->R, a->V) : 0), kAlign);
+    L.hdot = o;    // the loop: w_h . h_k of every position
+    o = align_up(o + (loop ? sizeof(float) * (size_t)a->R * a->gamma_max : 0), kAlign);
     L.total = o;
     return L;
 }
@@ -329,8 +331,8 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
                 e = cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(const_cast<void*>(a->step_ready[k])), 0);
         if (e == cudaSuccess)
             e = launch(DSPARK_KERNEL_DRAFT_LOOP, s, [&] {
-                return launch_draft_loop(p, at<float>(ws, L.slots), at<unsigned int>(ws, kGridBarOffset),
-                                         at<int>(ws, kGridAbortOffset), s);
+                return launch_draft_loop(p, at<float>(ws, L.slots), at<float>(ws, L.hdot),
+                                         at<unsigned int>(ws, kGridBarOffset), at<int>(ws, kGridAbortOffset), s);
             });
         return cuda_status(e);
     }

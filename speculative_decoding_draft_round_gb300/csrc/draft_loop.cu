@@ -17,8 +17,8 @@
 //               the draws)
 //   warp 1      TMEM owner and MMA issuer: D[v][q] = sum_i W[i][v] E[x_{k-1}(q)][i] per block and
 //               request half (M = 128 vocabulary rows, N = 64 requests, K = 16 per instruction)
-//   warp 2      the grid barrier; then waits for the step's tokens and gathers their W_1 rows
-//               (4 rows per TMA instruction) into the next step's E tile
+//   warp 2      the grid barrier; then waits for the step's tokens and loads the next step's E
+//               tile (their W_1 rows) from one of 8 replicas with 4 TMA copies
 //   warp 3      the outputs of this CTA's requests (q = cta mod P): log-normaliser, confidence
 //               head and survival product; off the serial path
 //   warps 4-19  epilogue, two sets of eight warps, one set per request half. A warp holds lane
@@ -33,8 +33,9 @@
 //   After its last block every CTA posts, per request, its leading block's key in a packed
 //   64-bit atomicMax (key, block, CTA). One grid barrier; then the CTA that holds the winning
 //   block draws the element from its slot (Gumbel-max over 128 logits, one Philox call per lane)
-//   and publishes the token with a release store, tagged with the step. Every CTA waits for the
-//   tags and gathers the next E tile; the draw costs one request per winner, not one per CTA.
+//   and writes the token's W_1 row into the 8 replicas, then publishes the token with a release
+//   store tagged with the step. Every CTA waits for the tags and loads the next E tile; the draw
+//   costs one request per winner, not one per CTA.
 // Every wait is bounded by the global timer. A wait that runs out records DSPARK_ERR_TIMEOUT and
 // sets an abort flag every CTA polls; each role then stops issuing, lets its own copies and MMAs
 // land, and the CTA frees its tensor memory and returns.
@@ -61,6 +62,7 @@ constexpr int KCH = 64;                         // K per chunk (128 bytes of bf1
 constexpr int NKC = KR / KCH;                   // 4 chunks
 constexpr int TM_TILES = 3;                     // W tiles held in tensor memory
 constexpr int NT_MAX = 8;                       // vocabulary blocks per CTA
+constexpr int MAX_P = 256;                      // CTAs (one per SM)
 constexpr uint32_t TILE_COLS = KR / 2;          // TMEM columns of one W^T tile (bf16 pairs)
 constexpr uint32_t ACC_COL = TM_TILES * TILE_COLS;   // 384: two accumulators of 64 columns
 constexpr uint32_t TMEM_COLS = 512;
@@ -69,6 +71,7 @@ constexpr uint32_t BOX_BYTES = 8192;                 // [64 rows x 64 elements] 
 constexpr uint32_t U_BYTES = NHALF * 128 * 2;        // one U stage [64 requests x 128 columns]
 constexpr int WR_ST = 2;                        // streamed W chunk stages
 constexpr int U_ST = 3;                         // U stages
+constexpr int PF_TILES = 2;                     // tiles requested into L2 ahead of the rings
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_E = 0;                                   // E tile: 4 chunks [128 rows x 64 K]
 constexpr uint32_t OFF_S = OFF_E + NKC * RMAX * 128;           // 64 KB: the W tile kept in shared memory
@@ -98,6 +101,7 @@ constexpr int BAR_EPI = 6, BAR_EPI_N = 32 * LP_EPI_WARPS;
 constexpr int BAR_TOK = 7, BAR_TOK_N = 64;
 
 constexpr unsigned long long DRAIN_NS = 4000000000ull;
+constexpr uint32_t WAIT_HINT_NS = 100000;            // suspend hint of one mbarrier try_wait
 constexpr uint32_t TAG_SHIFT = 18;                   // token tag: (step + 1) << 18 | token
 constexpr uint32_t TOK_MASK = (1u << TAG_SHIFT) - 1u;
 
@@ -109,6 +113,7 @@ constexpr uint32_t IDESC_SA = IDESC_TA | (1u << 15);
 struct LoopParams {
     DraftStep d;
     float* slots;            // [P][128][128] fp32: per CTA and request, the leading block's logits y
+    float* hdot;             // [R][G] w_h . h_k
     unsigned int* gbar;      // grid barrier counter (zero at launch)
     int* gabort;             // grid-wide abort flag (zero at launch)
     int P;                   // CTAs
@@ -127,12 +132,15 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo, uint
     return d;
 }
 
+// The MMA warp runs its loop converged, with warp-uniform operands; one lane, elected inside the
+// instruction sequence, issues each MMA and commit.
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t acc)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(IDESC_TA), "r"(acc)
         : "memory");
 }
@@ -140,11 +148,36 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t acc)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(IDESC_SA), "r"(acc)
         : "memory");
+}
+
+__device__ __forceinline__ void commit_elect(uint32_t bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+// try_wait that lets the hardware suspend the thread (up to the hint) until the phase completes,
+// so that waiting warps leave the issue slots to the working ones
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(WAIT_HINT_NS)
+        : "memory");
+    return ok != 0;
 }
 
 // 16 lanes x 8 columns, four times along the columns (+8 each): thread t receives, in register
@@ -188,10 +221,10 @@ __device__ __forceinline__ void bar_sync(int id, int count)
     asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p)
+__device__ __forceinline__ unsigned int ld_relaxed_u32(const unsigned int* p)
 {
     unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
@@ -216,6 +249,23 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// L2 prefetch of one box of a 2-D / 3-D map (no shared memory, no completion)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
 }
 
 // Reduce 8 values over the 8 lanes that share lane % 4 (lane bits 2-4): value c of every lane
@@ -264,12 +314,15 @@ __device__ __forceinline__ void give_up(LoopCtl c)
 }
 
 // Bounded wait on a shared-memory barrier phase; false when the CTA aborted or the wait ran out.
-__device__ __noinline__ bool lp_wait(uint32_t bar, uint32_t parity, LoopCtl c)
+// Inline: a call in the MMA and epilogue loops makes the compiler keep values live across it in
+// the stack, and with the shared memory this kernel takes, L1 holds little of that stack (the MMA
+// issue measured 3-4x slower with the call).
+__device__ __forceinline__ bool lp_wait(uint32_t bar, uint32_t parity, LoopCtl c)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*c.abort) return false;
         if (globaltimer() - t0 > c.limit) {
             give_up(c);
@@ -294,7 +347,7 @@ __device__ __noinline__ bool grid_sync(unsigned int* gbar, unsigned int target, 
     __threadfence();
     atomicAdd(gbar, 1u);
     const unsigned long long t0 = globaltimer();
-    while (ld_acquire_u32(gbar) < target) {
+    while (ld_relaxed_u32(gbar) < target) {
         if (ld_relaxed_s32(c.gabort)) {
             *c.abort = 1;
             return false;
@@ -308,24 +361,38 @@ __device__ __noinline__ bool grid_sync(unsigned int* gbar, unsigned int target, 
     return true;
 }
 
-// Bounded wait for the token of one request at step k, published by the CTA that drew it with
-// a release store of ((k + 1) << 18) | token; -1 when the wait ran out or another CTA gave up.
-__device__ __noinline__ int wait_token(const unsigned int* tag, int k, LoopCtl c)
+// Bounded wait for the tokens of four requests (q0 .. q0 + 3, those with need[r]) at step k,
+// each published by the CTA that drew it with a release store of ((k + 1) << 18) | token. The
+// four tags are polled together with relaxed loads (an acquire load per tag serialises the
+// polls); one acquire fence after the last one orders what the publishers wrote before their
+// tags. false when the wait ran out or another CTA gave up.
+__device__ __noinline__ bool wait_tokens(const unsigned int* tags, int q0, const bool (&need)[4], int k, int (&tok)[4],
+                                         LoopCtl c)
 {
     const unsigned int want = (unsigned int)(k + 1);
-    unsigned int v = ld_acquire_u32(tag);
-    if ((v >> TAG_SHIFT) == want) return (int)(v & TOK_MASK);
     const unsigned long long t0 = globaltimer();
     while (true) {
-        v = ld_acquire_u32(tag);
-        if ((v >> TAG_SHIFT) == want) return (int)(v & TOK_MASK);
-        if (*c.abort || ld_relaxed_s32(c.gabort)) {
-            *c.abort = 1;
-            return -1;
-        }
         if (globaltimer() - t0 > c.limit) {
             give_up(c);
-            return -1;
+            return false;
+        }
+        bool all = true;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            if (need[r] && tok[r] < 0) {
+                const unsigned int v = ld_relaxed_u32(tags + q0 + r);
+                if ((v >> TAG_SHIFT) == want)
+                    tok[r] = (int)(v & TOK_MASK);
+                else
+                    all = false;
+            }
+        if (all) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            return true;
+        }
+        if (*c.abort || ld_relaxed_s32(c.gabort)) {
+            *c.abort = 1;
+            return false;
         }
     }
 }
@@ -334,7 +401,8 @@ __device__ __noinline__ int wait_token(const unsigned int* tag, int k, LoopCtl c
 
 __global__ void __launch_bounds__(LP_THREADS, 1)
     draft_loop_kernel(const LoopParams L, const __grid_constant__ CUtensorMap tmW,
-                      const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmG)
+                      const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmG,
+                      const __grid_constant__ CUtensorMap tmE)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -461,6 +529,33 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
         }
     }
 
+    // w_h . h_k of every position (inputs only), spread over warps 2-19 of the grid: they enter the
+    // step barrier before the first grid barrier, which publishes these writes
+    if (warp >= 2) {
+        const int gw = cta * (LP_THREADS / 32 - 2) + (warp - 2), nw = P * (LP_THREADS / 32 - 2);
+        const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(p.h);
+        const bool vec = p.d % 8 == 0 && (reinterpret_cast<uintptr_t>(p.h) & 15u) == 0 &&
+                         (reinterpret_cast<uintptr_t>(p.w_h) & 15u) == 0;
+        for (int pi = gw; pi < R * G; pi += nw) {
+            const __nv_bfloat16* hr = H + (size_t)pi * p.d;
+            float acc = 0.f;
+            if (vec) {
+#pragma unroll 4
+                for (int c = lane * 8; c < p.d; c += 256) {
+                    float x[8], w[8];
+                    load8<__nv_bfloat16>(hr + c, x);
+                    load8<float>(p.w_h + c, w);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc = fmaf(w[e], x[e], acc);
+                }
+            } else {
+                for (int c = lane; c < p.d; c += 32) acc = fmaf(p.w_h[c], __bfloat162float(hr[c]), acc);
+            }
+            acc = warp_sum(acc);
+            if (lane == 0) L.hdot[pi] = acc;
+        }
+    }
+
     // ======================================================================= the serial steps
     if (warp == 0 && lane == 0) {
         // ---------------- producer: per step, per tile, the streamed W chunks then the U halves
@@ -469,9 +564,28 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
         uint32_t uph = 0, wph = 0;
         int u_fills = 0, w_fills = 0;
         bool stop = false;
+        // tiles are taken in order n = k nt + t; the W chunks and U halves of tile n + PF_TILES are
+        // requested into L2 when tile n is loaded, so that more bytes are in flight than the rings hold
+        const int n_all = G * nt;
+        int n_pf = 0;
+        auto prefetch_upto = [&](int n_end) {
+            for (; n_pf < n_end && n_pf < n_all; ++n_pf) {
+                const int pk = n_pf / nt, pt = n_pf - pk * nt, pb = b0 + pt;
+                if (pt >= n_tm + n_sm)
+                    for (int kc = 0; kc < NKC; ++kc) {
+                        tma_prefetch_2d(&tmW, pb * 128, kc * KCH);
+                        tma_prefetch_2d(&tmW, pb * 128 + 64, kc * KCH);
+                    }
+                for (int h = 0; h < NH; ++h) {
+                    tma_prefetch_3d(&tmU, pb * 128, pk, h * NHALF);
+                    tma_prefetch_3d(&tmU, pb * 128 + 64, pk, h * NHALF);
+                }
+            }
+        };
         for (int k = 0; k < G && !stop; ++k)
             for (int t = 0; t < nt && !stop; ++t) {
                 const int b = b0 + t;
+                prefetch_upto(k * nt + t + 1 + PF_TILES);
                 if (t >= n_tm + n_sm) {
                     for (int kc = 0; kc < NKC && !stop; ++kc) {
                         if (!lp_wait(w_empty(ws), wph ^ 1u, ctl)) {
@@ -510,48 +624,59 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
             lp_drain(u_full(n % U_ST), (uint32_t)(n / U_ST) & 1u);
         for (int n = (w_fills > WR_ST ? w_fills - WR_ST : 0); n < w_fills; ++n)
             lp_drain(w_full(n % WR_ST), (uint32_t)(n / WR_ST) & 1u);
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer
+    } else if (warp == 1) {
+        // ---------------- MMA issuer: the warp runs converged (uniform operands, descriptors as a
+        // base plus constant offsets); lane 0 waits, one elected lane issues
         int ws = 0;
         uint32_t wph = 0;
         uint32_t n_tile = 0;   // tiles issued over the whole call (accumulator phases)
+        auto wait_w = [&](uint32_t bar, uint32_t parity) {
+            bool r = true;
+            if (lane == 0) r = lp_wait(bar, parity, ctl);
+            return __shfl_sync(0xffffffffu, (int)r, 0) != 0;
+        };
+        // descriptor address fields are 16-byte units: + (bytes >> 4) moves a descriptor
+        const uint64_t dE = sw128_desc(sbase + OFF_E, 16, 1024);
+        const uint64_t dS = sw128_desc(sbase + OFF_S, BOX_BYTES, 1024);
+        const uint64_t dR = sw128_desc(sbase + OFF_WR, BOX_BYTES, 1024);
         bool ok = true;
-        if (n_sm) ok = lp_wait(s_full, 0u, ctl);
+        if (n_sm) ok = wait_w(s_full, 0u);
         for (int k = 0; k < G && ok; ++k) {
-            if (!lp_wait(e_full, (uint32_t)k & 1u, ctl)) break;
+            if (!wait_w(e_full, (uint32_t)k & 1u)) break;
             tc5::fence_after();
             for (int t = 0; t < nt && ok; ++t) {
-                for (int h = 0; h < NH && ok; ++h) ok = lp_wait(acc_empty(h), (n_tile & 1u) ^ 1u, ctl);
+                for (int h = 0; h < NH && ok; ++h) ok = wait_w(acc_empty(h), (n_tile & 1u) ^ 1u);
                 if (!ok) break;
                 tc5::fence_after();
                 const bool in_tmem = t < n_tm, in_smem = !in_tmem && t < n_tm + n_sm;
+                const uint32_t a_tm = tmem + (uint32_t)(t * TILE_COLS);
                 for (int kc = 0; kc < NKC; ++kc) {
-                    uint32_t a_base = 0;
+                    uint64_t dA = dS + (uint64_t)((kc * CHUNK_BYTES) >> 4);
                     if (!in_tmem && !in_smem) {
-                        if (!lp_wait(w_full(ws), wph, ctl)) {
+                        if (!wait_w(w_full(ws), wph)) {
                             ok = false;
                             break;
                         }
                         tc5::fence_after();
-                        a_base = sbase + OFF_WR + (uint32_t)ws * CHUNK_BYTES;
-                    } else if (in_smem) {
-                        a_base = sbase + OFF_S + (uint32_t)kc * CHUNK_BYTES;
+                        dA = dR + (uint64_t)((ws * CHUNK_BYTES) >> 4);
                     }
-                    for (int h = 0; h < NH; ++h) {
-                        const uint32_t d = tmem + ACC_COL + (uint32_t)(h * NHALF);
+                    const uint64_t dB = dE + (uint64_t)((kc * (RMAX * 128)) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < KCH / 16; ++kk) {
-                            const uint64_t bd =
-                                sw128_desc(sbase + OFF_E + (uint32_t)kc * (RMAX * 128) + (uint32_t)h * (NHALF * 128) + kk * 32, 16, 1024);
-                            const uint32_t acc = (kc | kk) != 0;
-                            if (in_tmem)
-                                mma_ts(d, tmem + (uint32_t)(t * TILE_COLS + kc * 32 + kk * 8), bd, acc);
-                            else
-                                mma_ss(d, sw128_desc(a_base + kk * (16 * 128), BOX_BYTES, 1024), bd, acc);
+                    for (int h = 0; h < 2; ++h)
+                        if (h < NH) {
+                            const uint32_t d = tmem + ACC_COL + (uint32_t)(h * NHALF);
+#pragma unroll
+                            for (int kk = 0; kk < KCH / 16; ++kk) {
+                                const uint64_t bd = dB + (uint64_t)((h * (NHALF * 128) + kk * 32) >> 4);
+                                const uint32_t acc = (kc | kk) != 0;
+                                if (in_tmem)
+                                    mma_ts(d, a_tm + (uint32_t)(kc * 32 + kk * 8), bd, acc);
+                                else
+                                    mma_ss(d, dA + (uint64_t)((kk * 16 * 128) >> 4), bd, acc);
+                            }
                         }
-                    }
                     if (!in_tmem && !in_smem) {
-                        tc5::commit(w_empty(ws));
+                        commit_elect(w_empty(ws));
                         if (++ws == WR_ST) {
                             ws = 0;
                             wph ^= 1u;
@@ -559,14 +684,14 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                for (int h = 0; h < NH; ++h) tc5::commit(acc_full(h));
+                for (int h = 0; h < NH; ++h) commit_elect(acc_full(h));
                 ++n_tile;
             }
-            if (ok) tc5::commit(e_empty);
+            if (ok) commit_elect(e_empty);
         }
         // every MMA issued above completes before TMEM is freed (after an abort too)
-        tc5::commit(mma_done);
-        lp_drain(mma_done, 0u);
+        commit_elect(mma_done);
+        if (lane == 0) lp_drain(mma_done, 0u);
     } else if (warp == 2) {
         // ---------------- grid barrier, the step's tokens, the next E tile
         int gam[4];
@@ -612,44 +737,35 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
             }
             bar_sync(BAR_STEP, BAR_STEP_N);
             if (*s_stop) break;
-            // the tokens of step k, as their winners publish them
-            bool got = true;
+            // the tokens of step k, as their winners publish them (with the W_1 rows in the replicas)
+            bool need[4];
+            int tok[4];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                const int q = 4 * lane + r;
-                int tok = -1;
-                if (q < R && k < gam[r]) {
-                    tok = wait_token(tags + q, k, ctl);
-                    got = got && tok >= 0;
-                }
-                s_tok[q] = tok;
-                rows[r] = (q < R && k + 1 < gam[r] && tok >= 0) ? tok : 0;
+                need[r] = 4 * lane + r < R && k < gam[r];
+                tok[r] = -1;
             }
+            const bool got = __all_sync(0xffffffffu, wait_tokens(tags, 4 * lane, need, k, tok, ctl));
+#pragma unroll
+            for (int r = 0; r < 4; ++r) s_tok[4 * lane + r] = tok[r];
             bar_sync(BAR_TOK, BAR_TOK_N);
-            got = __all_sync(0xffffffffu, got);
-            if (k + 1 < G && got) {
-                bool free_ok = true;
-                if (lane == 0) free_ok = lp_wait(e_empty, (uint32_t)k & 1u, ctl);
-                free_ok = __shfl_sync(0xffffffffu, free_ok, 0);
-                if (free_ok) {
-                    if (lane == 0) mbar_expect_tx(e_full, NKC * RMAX * 128);
-                    __syncwarp();
-                    const uint64_t pol = l2_policy_evict_last();
-                    for (int kc = 0; kc < NKC; ++kc)
-                        tma_gather4(sbase + OFF_E + (uint32_t)kc * (RMAX * 128) + (uint32_t)lane * 512, &tmG, kc * KCH,
-                                    rows[0], rows[1], rows[2], rows[3], e_full, pol);
-                    ++e_loads;
-                }
+            if (k + 1 < G && got && lane == 0 && lp_wait(e_empty, (uint32_t)k & 1u, ctl)) {
+                // the replicas were written with generic stores before each tag's release
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                mbar_expect_tx(e_full, NKC * RMAX * 128);
+                const uint64_t pol = l2_policy_evict_last();
+                for (int kc = 0; kc < NKC; ++kc)
+                    tma_load_3d(sbase + OFF_E + (uint32_t)kc * (RMAX * 128), &tmE, kc * KCH, 0, cta % kAReplicas, e_full,
+                                pol);
+                ++e_loads;
             }
+            e_loads = __shfl_sync(0xffffffffu, e_loads, 0);
         }
         // the last E tile copy lands before exit (it may be unconsumed after an abort)
         if (lane == 0 && e_loads > 0) lp_drain(e_full, (uint32_t)(e_loads - 1) & 1u);
     } else if (warp == 3) {
         // ---------------- outputs of this CTA's requests (q = cta + P j), one step behind the draw
         const __nv_bfloat16* E = static_cast<const __nv_bfloat16*>(p.E);
-        const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(p.h);
-        const bool hvec = p.d % 8 == 0 && (reinterpret_cast<uintptr_t>(p.h) & 15u) == 0 &&
-                          (reinterpret_cast<uintptr_t>(p.w_h) & 15u) == 0;
         if (lane == 0)
             for (int q = cta; q < R; q += P) {
                 s_prev[q] = checked_index(p.anchor[q], V, p.status);
@@ -679,12 +795,14 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
                 const bool greedy = p.temperature[q] == 0.f;
                 if (!greedy) {
                     // log-normaliser from the CTAs' partials of this step (written before the grid barrier)
-                    Lse2 tot{-INFINITY, 0.f};
                     const float2* st = p.stats + ((size_t)(k & 1) * R + q) * P;
-                    for (int c2 = lane; c2 < P; c2 += 32) {
-                        const float2 v = __ldcg(st + c2);
-                        tot = lse2_merge(tot, Lse2{v.x, v.y});
-                    }
+                    float2 v[MAX_P / 32];
+#pragma unroll
+                    for (int i = 0; i < MAX_P / 32; ++i)
+                        v[i] = lane + 32 * i < P ? __ldcg(st + lane + 32 * i) : make_float2(-INFINITY, 0.f);
+                    Lse2 tot{-INFINITY, 0.f};
+#pragma unroll
+                    for (int i = 0; i < MAX_P / 32; ++i) tot = lse2_merge(tot, Lse2{v[i].x, v[i].y});
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) {
                         const Lse2 o2{__shfl_xor_sync(0xffffffffu, tot.m, off),
@@ -702,20 +820,7 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
                 float dot = 0.f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) dot = fmaf(we[i], p.conf_token ? en[i] : ep[i], dot);
-                float hd = 0.f;
-                const __nv_bfloat16* hr = H + o * p.d;
-                if (hvec) {
-                    for (int c = lane * 8; c < p.d; c += 256) {
-                        float x[8], w[8];
-                        load8<__nv_bfloat16>(hr + c, x);
-                        load8<float>(p.w_h + c, w);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) hd = fmaf(w[e], x[e], hd);
-                    }
-                } else {
-                    for (int c = lane; c < p.d; c += 32) hd = fmaf(p.w_h[c], __bfloat162float(hr[c]), hd);
-                }
-                dot = warp_sum(dot) + warp_sum(hd);
+                dot = warp_sum(dot) + __ldcg(L.hdot + o);
                 const float lc = (dot + p.b) / (p.sts_temp ? p.sts_temp[k] : 1.f);
                 const float c = 1.f / (1.f + expf(-lc));
                 const float s = s_surv[q] * c;
@@ -784,6 +889,16 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
                 }
             }
         };
+        // the draw's requests of this warp (q = ew + 16 jj, held by lane jj): length, greedy flag
+        const __nv_bfloat16* E = static_cast<const __nv_bfloat16*>(p.E);
+        __nv_bfloat16* an = static_cast<__nv_bfloat16*>(p.a_next);
+        int d_gam = 0, d_greedy = 0;
+        if (lane < 8 && ew + 16 * lane < R) {
+            const int q = ew + 16 * lane;
+            const int g = p.gamma ? p.gamma[q] : G;
+            d_gam = g < 0 ? 0 : (g > G ? G : g);
+            d_greedy = p.temperature[q] == 0.f;
+        }
         block_gumbels(0);
         bar_sync(BAR_EPI, BAR_EPI_N);
         for (int k = 0; k < G; ++k) {
@@ -907,25 +1022,20 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
             if (*s_stop) break;
             // the draw of every request whose winning block this CTA holds
             unsigned long long pk_l = 0ull;
-            int g_l = 0;
-            if (lane < 8 && ew + 16 * lane < R) {
-                const int q = ew + 16 * lane;
-                pk_l = *reinterpret_cast<volatile unsigned long long*>(p.pick + (size_t)k * R + q);
-                int g = p.gamma ? p.gamma[q] : G;
-                g_l = g < 0 ? 0 : (g > G ? G : g);
-            }
+            if (lane < 8 && ew + 16 * lane < R)
+                pk_l = *reinterpret_cast<volatile unsigned long long*>(p.pick + (size_t)k * R + ew + 16 * lane);
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
                 const int q = ew + 16 * jj;
                 if (q >= R) break;
                 const unsigned long long pk = __shfl_sync(0xffffffffu, pk_l, jj);
-                const int g = __shfl_sync(0xffffffffu, g_l, jj);
+                const int g = __shfl_sync(0xffffffffu, d_gam, jj);
                 if (k >= g) continue;
                 const uint32_t idx = ~(uint32_t)pk;
                 const int bstar = (int)(idx >> 15), cstar = (int)(idx & 0x7FFFu);
                 const bool valid = pk != 0ull && bstar < nblk && cstar < P;
                 if (valid ? cstar != cta : q % P != cta) continue;
-                const bool greedy = p.temperature[q] == 0.f;
+                const bool greedy = __shfl_sync(0xffffffffu, d_greedy, jj) != 0;
                 int tok = 0;
                 float logit = 0.f;
                 if (valid) {
@@ -963,6 +1073,15 @@ __global__ void __launch_bounds__(LP_THREADS, 1)
                 } else {
                     raise_status(p.status, DSPARK_ERR_DEVICE_INPUT);
                 }
+                // the next step's conditioning row W_1[x_k], in every replica, before the tag
+                if (k + 1 < g) {
+                    const uint4 row = *reinterpret_cast<const uint4*>(E + (size_t)tok * KR + lane * 8);
+#pragma unroll
+                    for (int rp = 0; rp < kAReplicas; ++rp)
+                        *reinterpret_cast<uint4*>(an + ((size_t)rp * R + q) * KR + lane * 8) = row;
+                }
+                // the lanes' stores are ordered before lane 0's release by the warp barrier
+                __syncwarp();
                 if (lane == 0) {
                     const size_t o = (size_t)q * G + k;
                     p.tokens[o] = tok;
@@ -1057,18 +1176,19 @@ bool loop_supported(int dtype, int head, int R, int V, int r, const void* U, con
     // tokens fit the step tag; at least 8 CTAs, each with at most NT_MAX vocabulary blocks
     if (V > (int)TOK_MASK + 1) return false;
     const int nblk = (V + 127) / 128, P = loop_ctas(R, V);
-    if (nblk < 8 || P < 8 || (nblk + P - 1) / P > NT_MAX) return false;
+    if (nblk < 8 || P < 8 || P > MAX_P || (nblk + P - 1) / P > NT_MAX) return false;
     if (!a16(U) || !a16(E) || !a16(W) || !a16(h) || !a16(w_h) || !a16(w_e)) return false;
     return lp_encode_fn() != nullptr;
 }
 
 size_t loop_slot_bytes(int R, int V) { return (size_t)loop_ctas(R, V) * RMAX * 128 * sizeof(float); }
 
-cudaError_t launch_draft_loop(const DraftStep& p, float* slots, unsigned int* gbar, int* gabort, cudaStream_t s)
+cudaError_t launch_draft_loop(const DraftStep& p, float* slots, float* hdot, unsigned int* gbar, int* gabort,
+                              cudaStream_t s)
 {
     const int P = loop_ctas(p.R, p.V);
     if (P < 8) return cudaErrorNotSupported;
-    CUtensorMap tmW, tmU, tmG;
+    CUtensorMap tmW, tmU, tmG, tmE;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)p.V, (cuuint64_t)p.r};
         const cuuint64_t strides[1] = {(cuuint64_t)p.V * 2};
@@ -1091,11 +1211,20 @@ cudaError_t launch_draft_loop(const DraftStep& p, float* slots, unsigned int* gb
         const cudaError_t e = enc(&tmG, p.E, 2, dims, strides, box);
         if (e != cudaSuccess) return e;
     }
+    {
+        // the replicas [kAReplicas][R][r] of the next step's W_1 rows: boxes of 64 columns x 128 rows
+        const cuuint64_t dims[3] = {(cuuint64_t)p.r, (cuuint64_t)p.R, (cuuint64_t)kAReplicas};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.r * 2, (cuuint64_t)p.R * p.r * 2};
+        const cuuint32_t box[3] = {KCH, RMAX, 1};
+        const cudaError_t e = enc(&tmE, p.a_next, 3, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
     LoopParams L;
     memset(&L, 0, sizeof L);
     L.d = p;
     L.d.n_stats = P;
     L.slots = slots;
+    L.hdot = hdot;
     L.gbar = gbar;
     L.gabort = gabort;
     L.P = P;
@@ -1119,7 +1248,7 @@ cudaError_t launch_draft_loop(const DraftStep& p, float* slots, unsigned int* gb
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, draft_loop_kernel, L, tmW, tmU, tmG);
+    e = cudaLaunchKernelEx(&cfg, draft_loop_kernel, L, tmW, tmU, tmG, tmE);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

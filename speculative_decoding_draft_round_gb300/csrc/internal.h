@@ -137,7 +137,8 @@ bool loop_supported(int dtype, int head, int R, int V, int r, const void* U, con
                     const void* h, const void* w_h, const void* w_e);
 int loop_ctas(int R, int V);                 // its grid, and the per-CTA partials of each row
 size_t loop_slot_bytes(int R, int V);        // its leading-block logit slots
-cudaError_t launch_draft_loop(const DraftStep& p, float* slots, unsigned int* gbar, int* gabort, cudaStream_t s);
+cudaError_t launch_draft_loop(const DraftStep& p, float* slots, float* hdot, unsigned int* gbar, int* gabort,
+                              cudaStream_t s);
 
 // verify.cu
 cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s);

@@ -39,7 +39,7 @@ constexpr uint32_t kHIdesc =
     (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kHN >> 3) << 17) | ((uint32_t)(kHM >> 4) << 24);
 static_assert(kHStageBytes % 1024 == 0 && kHABytes % 1024 == 0, "stages and operands on 1024-byte boundaries");
 
-__device__ __noinline__ bool h_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+__device__ __forceinline__ bool h_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
                                     unsigned long long limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;

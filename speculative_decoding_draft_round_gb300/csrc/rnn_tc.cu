@@ -41,7 +41,7 @@ constexpr uint32_t kRtIdesc =
 
 // bounded wait for a barrier phase; false (status raised, abort flag set) when it runs out or the
 // CTA already gave up
-__device__ __noinline__ bool rt_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status)
+__device__ __forceinline__ bool rt_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();

@@ -192,7 +192,7 @@ constexpr unsigned long long kCommitDrainNs = 4000000000ull;   // 4 s: a copy in
 
 // Bounded wait for phase `parity` of a shared-memory barrier; false (and DSPARK_ERR_TIMEOUT
 // recorded) when it runs out.
-__device__ __noinline__ bool commit_wait(uint32_t bar, uint32_t parity, int* status, unsigned long long limit_ns)
+__device__ __forceinline__ bool commit_wait(uint32_t bar, uint32_t parity, int* status, unsigned long long limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();

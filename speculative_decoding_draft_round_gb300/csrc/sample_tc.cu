@@ -123,7 +123,7 @@ struct Ctl {
 };
 
 // Wait for the phase of `bar` with the given parity; false if the CTA aborted or the wait ran out.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Ctl c)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Ctl c)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
