@@ -154,7 +154,7 @@ SampleLayout sample_layout(const dspark_sample_args* a)
 // ------------------------------------------------------------ verify
 
 struct VerifyLayout {
-    size_t row_stats, lse_t, rej, n_rej, rej_list, res_stats, total;
+    size_t row_stats, row_part, lse_t, rej, n_rej, rej_list, res_stats, total;
 };
 
 dspark_status check_verify(const dspark_verify_args* a)
@@ -189,6 +189,8 @@ VerifyLayout verify_layout(const dspark_verify_args* a)
     size_t o = kStatusBytes;
     L.row_stats = o;
     o = align_up(o + sizeof(float2) * (size_t)a->R * (a->gamma_max + 1) * nblk, kAlign);
+    L.row_part = o;
+    o = align_up(o + sizeof(float2) * (size_t)a->R * (a->gamma_max + 1) * verify_row_partials(nblk), kAlign);
     L.lse_t = o;
     o = align_up(o + sizeof(float) * (size_t)a->R * (a->gamma_max + 1), kAlign);
     L.rej = o;
@@ -490,6 +492,8 @@ dspark_status dspark_verify(const dspark_verify_args* a, void* ws, size_t ws_byt
     p.wait_ns = wait_limit_ns();
     p.status = at<int>(ws, 0);
     p.row_stats = at<float2>(ws, L.row_stats);
+    p.row_part = at<float2>(ws, L.row_part);
+    p.npart = verify_row_partials(p.nblk);
     p.lse_t = at<float>(ws, L.lse_t);
     p.rej = at<int32_t>(ws, L.rej);
     p.n_rej = at<int>(ws, L.n_rej);

@@ -81,6 +81,8 @@ struct VerifyParams {
     // workspace
     int* status;
     float2* row_stats;   // [R][G+1][nblk] block (max, sum) of the target rows, log2 units
+    float2* row_part;    // [R][G+1][npart] per-warp merges of 8 blocks of row_stats
+    int npart;           // ceil(nblk / 8)
     float* lse_t;        // [R][G+1]
     int32_t* rej;        // [R] rejected position, -1 if every admitted token was accepted
     int* n_rej;          // number of rejected requests (zeroed by verify_rows, counted by verify_decide)
@@ -129,6 +131,12 @@ bool tc_supported(int dtype, int R, int V, int r, const void* U, const void* E, 
 bool tc_residual_supported(int dtype, int R, int V, int r, const void* U, const void* E, const void* W);
 size_t tc_stats_rows(int R);  // rows of the block-statistics workspace the tensor-core path writes
 int tc_grid(int R, int nblk); // CTAs of the tensor-core statistics kernel
+int num_sms();                 // streaming multiprocessors of the current device
+// The scheduler's grid: one CTA that schedules and three that warm its code. Each holds every
+// register of its SM (1024 threads x 64), so the verify row pass, launched while they run, leaves
+// those SMs out of its persistent grid.
+constexpr int kScheduleCtas = 4;
+int verify_row_partials(int nblk);   // per-warp partials of one verified target row
 cudaError_t launch_draft_stats_tc(const DraftStep& p, cudaStream_t s);
 cudaError_t launch_residual_stats_tc(const VerifyParams& p, cudaStream_t s);
 

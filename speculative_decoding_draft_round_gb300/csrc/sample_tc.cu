@@ -860,6 +860,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
 int num_sms()
 {
     static int n = 0;
@@ -870,10 +875,6 @@ int num_sms()
     }
     return n;
 }
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-}  // namespace
 
 bool tc_supported(int dtype, int R, int V, int r, const void* U, const void* E, const void* W)
 {

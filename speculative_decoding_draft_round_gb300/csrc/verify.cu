@@ -14,6 +14,8 @@
 //                       position, block sums of max(0, p_t - p_d).
 //   residual_pick    -- per rejecting request: two-level Gumbel-max over the
 //                       residual (p_t of the same row if the residual is zero).
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -46,74 +48,86 @@ constexpr int kRowWarps = 8;
 constexpr int kRowBlocksPerWarp = 8;   // 1024 columns per warp: four 16-byte loads per lane
 
 // Block (max, sum exp2) of z/T (log2 units) for the 8 consecutive 128-wide blocks starting at
-// block b0, one warp: in the vector path lane l owns columns 256j + 8l .. +7 (j = 0..3), so
-// half-warp h of load j covers block b0 + 2j + h; all four loads are issued before any use.
+// block b0, one warp; lane bb < 8 receives block b0 + bb. In the bf16 vector path lane l owns
+// columns 256j + 8l .. +7 (j = 0..3), so half-warp h of load j covers block b0 + 2j + h; the four
+// 16-byte loads (row_load8) are issued before any use, and row_reduce8 forms the statistics.
 template <typename T>
-__device__ __forceinline__ void row_block_stats8(const T* row, int V, int b0, float scale, int lane, bool vec,
-                                                 float2 (&out)[kRowBlocksPerWarp])
+__device__ __forceinline__ void row_load8(const T* row, int V, int b0, int lane, uint4 (&raw)[4])
 {
-    const int half = lane >> 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int v = b0 * kNoiseBlock + j * 256 + lane * 8;
+        raw[j] = v < V ? __ldg(reinterpret_cast<const uint4*>(row + v)) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+__device__ __forceinline__ float2 row_reduce8(const uint4 (&raw)[4], int V, int b0, float scale, int lane)
+{
+    float2 mine = make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int v = b0 * kNoiseBlock + j * 256 + lane * 8;
+        const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+        float x[8];   // raw logits: the maximum is taken before scaling (scale > 0)
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            x[2 * h] = __uint_as_float(w4[h] << 16);
+            x[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
+        }
+        const bool in = v < V;   // V % 8 == 0: 8 columns all in or all out
+        float mr = -INFINITY;
+        if (in) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mr = fmaxf(mr, x[e]);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+        const float m = mr * scale;   // the block maximum of z/T in log2 units
+        float sacc = 0.f;
+        if (in && m > -INFINITY) {
+            // one fused multiply-add and one SFU exponential per element: 2^(x*scale - m)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sacc += ex2(fmaf(x[e], scale, -m));
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
+        const float m0 = __shfl_sync(0xffffffffu, m, 0), s0 = __shfl_sync(0xffffffffu, sacc, 0);
+        const float m1 = __shfl_sync(0xffffffffu, m, 16), s1 = __shfl_sync(0xffffffffu, sacc, 16);
+        if (lane == 2 * j) mine = make_float2(m0, s0);
+        if (lane == 2 * j + 1) mine = make_float2(m1, s1);
+    }
+    return mine;
+}
+
+template <typename T>
+__device__ __forceinline__ float2 row_block_stats8(const T* row, int V, int b0, float scale, int lane, bool vec)
+{
     if (vec && sizeof(T) == 2) {
         uint4 raw[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int v = b0 * kNoiseBlock + j * 256 + lane * 8;
-            raw[j] = v < V ? __ldg(reinterpret_cast<const uint4*>(row + v)) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int v = b0 * kNoiseBlock + j * 256 + lane * 8;
-            const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-            float x[8];   // raw logits: the maximum is taken before scaling (scale > 0)
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                x[2 * h] = __uint_as_float(w4[h] << 16);
-                x[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
-            }
-            const bool in = v < V;   // V % 8 == 0: 8 columns all in or all out
-            float mr = -INFINITY;
-            if (in) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mr = fmaxf(mr, x[e]);
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
-            const float m = mr * scale;   // the block maximum of z/T in log2 units
-            float sacc = 0.f;
-            if (in && m > -INFINITY) {
-                // one fused multiply-add and one SFU exponential per element: 2^(x*scale - m)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) sacc += ex2(fmaf(x[e], scale, -m));
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
-            const float m0 = __shfl_sync(0xffffffffu, m, 0), s0 = __shfl_sync(0xffffffffu, sacc, 0);
-            const float m1 = __shfl_sync(0xffffffffu, m, 16), s1 = __shfl_sync(0xffffffffu, sacc, 16);
-            out[2 * j] = make_float2(m0, s0);
-            out[2 * j + 1] = make_float2(m1, s1);
-            (void)half;
-        }
-    } else {
-#pragma unroll 1
-        for (int bb = 0; bb < kRowBlocksPerWarp; ++bb) {
-            const int b = b0 + bb;
-            float x[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int v = b * kNoiseBlock + e * 32 + lane;
-                x[e] = v < V ? ld(row, v) * scale : -INFINITY;
-            }
-            float m = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-            m = warp_max(m);
-            float sacc = 0.f;
-            if (m > -INFINITY) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sacc += exp2f(x[e] - m);
-            }
-            sacc = warp_sum(sacc);
-            out[bb] = make_float2(m, sacc);
-        }
+        row_load8(row, V, b0, lane, raw);
+        return row_reduce8(raw, V, b0, scale, lane);
     }
+    float2 mine = make_float2(-INFINITY, 0.f);
+#pragma unroll 1
+    for (int bb = 0; bb < kRowBlocksPerWarp; ++bb) {
+        const int b = b0 + bb;
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int v = b * kNoiseBlock + e * 32 + lane;
+            x[e] = v < V ? ld(row, v) * scale : -INFINITY;
+        }
+        float m = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        m = warp_max(m);
+        float sacc = 0.f;
+        if (m > -INFINITY) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc += exp2f(x[e] - m);
+        }
+        sacc = warp_sum(sacc);
+        if (lane == bb) mine = make_float2(m, sacc);
+    }
+    return mine;
 }
 
 // Greedy requests (temperature 0): per 128-wide block the maximum of the raw target logits and
@@ -144,6 +158,13 @@ __device__ __forceinline__ float2 row_block_argmax(const T* row, int V, int b, i
 // before the dependency wait, while the scheduler runs, and stored after it (the workspace may
 // still be read by the kernel before this one); rows 1..keep follow once keep exists.
 //
+// a NaN or +inf logit leaves a NaN sum or an infinite maximum (-inf is a zero weight)
+__device__ __forceinline__ void check_row_stats(const VerifyParams& p, int b0, int lane, float2 st, bool& nonfinite)
+{
+    if (lane < kRowBlocksPerWarp && b0 + lane < p.nblk && (!(st.y >= 0.f) || st.x == INFINITY || st.x != st.x))
+        nonfinite = true;
+}
+
 // This warp's statistics of row i for blocks b0 .. b0 + 7, held by lanes 0-7 (lane bb: block b0 + bb)
 template <typename T>
 __device__ __forceinline__ float2 row_stats_of(const VerifyParams& p, int q, int i, int b0, bool greedy, float scale,
@@ -158,49 +179,195 @@ __device__ __forceinline__ float2 row_stats_of(const VerifyParams& p, int q, int
         }
         return mine;
     }
-    float2 st[kRowBlocksPerWarp];
-    row_block_stats8<T>(row, p.V, b0, scale, lane, vec, st);
-    mine = st[0];
-#pragma unroll
-    for (int bb = 1; bb < kRowBlocksPerWarp; ++bb)
-        if (lane == bb) mine = st[bb];
-    // a NaN or +inf logit leaves a NaN sum or an infinite maximum (-inf is a zero weight)
-    if (lane < kRowBlocksPerWarp && b0 + lane < p.nblk && (!(mine.y >= 0.f) || mine.x == INFINITY || mine.x != mine.x))
-        nonfinite = true;
+    mine = row_block_stats8<T>(row, p.V, b0, scale, lane, vec);
+    check_row_stats(p, b0, lane, mine, nonfinite);
     return mine;
 }
 
-__device__ __forceinline__ void store_row_stats(const VerifyParams& p, int q, int i, int b0, int lane, float2 v)
+// This warp's statistics of row i, blocks b0 .. b0 + 7 (lane bb holds block b0 + bb), and the
+// merge of the eight (the warp's partial of the row: (max, sum) in log2 units, or the (max, lowest
+// index) of a greedy row) at partial slot b0 / 8.
+__device__ __forceinline__ void store_row_stats(const VerifyParams& p, int q, int i, int b0, int lane, float2 v,
+                                                bool greedy)
 {
-    if (lane < kRowBlocksPerWarp && b0 + lane < p.nblk) p.row_stats[((size_t)q * (p.G + 1) + i) * p.nblk + b0 + lane] = v;
+    const size_t row = (size_t)q * (p.G + 1) + i;
+    const bool in = lane < kRowBlocksPerWarp && b0 + lane < p.nblk;
+    if (in) p.row_stats[row * p.nblk + b0 + lane] = v;
+    float m = in ? v.x : -INFINITY, x = in ? v.y : (greedy ? -1.f : 0.f);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {   // lanes 0-7: the eight blocks (xor within the group of 8)
+        const float mo = __shfl_xor_sync(0xffffffffu, m, o), xo = __shfl_xor_sync(0xffffffffu, x, o);
+        if (greedy) {
+            const ArgMax r = argmax_better(ArgMax{m, (int)x}, ArgMax{mo, (int)xo});
+            m = r.v;
+            x = (float)r.i;
+        } else if (mo > -INFINITY) {
+            const float M = fmaxf(m, mo);
+            x = x * ex2(m - M) + xo * ex2(mo - M);
+            m = M;
+        }
+    }
+    if (lane == 0) p.row_part[row * p.npart + b0 / kRowBlocksPerWarp] = make_float2(m, x);
+}
+
+// A persistent grid walks items (request q, target row i, chunk c of 64 blocks), every warp taking
+// 8 blocks of the chunk. Row 0 is verified whatever keep is and reads only inputs: each CTA forms
+// up to kRowPre row-0 items before the dependency wait, while the scheduler runs, and stores them
+// after it (the workspace may still be read by the kernel before this one). Then the items of
+// rows 1..keep[q], numbered through the prefix sum of keep over the requests, are dealt to the
+// CTAs in turn, so that a request with many admitted tokens spreads over the whole GPU instead of
+// walking its rows one after the other. In the bf16 vector path each warp issues the next item's
+// loads before it reduces the current one.
+constexpr int kRowPre = 16;
+constexpr int kRowCtasPerSm = 4;   // resident beside a 1024-thread scheduler CTA: (2048 - 1024) / 256
+__device__ __forceinline__ int cdiv_dev(int a, int b) { return (a + b - 1) / b; }
+constexpr int kRowChunk = kRowWarps * kRowBlocksPerWarp;   // blocks per item
+
+struct RowItem {
+    int q, i, b0;   // q < 0: none
+};
+
+// Issue the loads of item `it` (bf16 vector path, temperature > 0); false: row_finish reads it
+// itself. s_scale[q]: log2(e) / T of request q, 0 for a greedy request.
+template <typename T>
+__device__ __forceinline__ bool row_start(const VerifyParams& p, const float* s_scale, const RowItem& it, bool vec,
+                                          int lane, uint4 (&raw)[4])
+{
+    if (sizeof(T) != 2 || !vec || it.q < 0 || it.b0 >= p.nblk || s_scale[it.q] == 0.f) return false;
+    row_load8(static_cast<const T*>(p.target) + ((size_t)it.q * (p.G + 1) + it.i) * p.V, p.V, it.b0, lane, raw);
+    return true;
+}
+
+// The warp's 8 block statistics of item `it` (lanes 0-7); greedy for a temperature-0 request
+template <typename T>
+__device__ __forceinline__ float2 row_finish(const VerifyParams& p, const float* s_scale, const RowItem& it,
+                                             bool started, const uint4 (&raw)[4], bool vec, int lane,
+                                             bool& nonfinite, bool& greedy)
+{
+    greedy = s_scale[it.q] == 0.f;
+    const float scale = greedy ? 1.f : s_scale[it.q];
+    if (!started) return row_stats_of<T>(p, it.q, it.i, it.b0, greedy, scale, vec, lane, nonfinite);
+    const float2 st = row_reduce8(raw, p.V, it.b0, scale, lane);
+    check_row_stats(p, it.b0, lane, st, nonfinite);
+    return st;
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParams p)
 {
-    const int q = blockIdx.y;
+    extern __shared__ int s_pref[];   // [R + 1]: rows 1..keep of requests 0 .. q-1, then s_scale [R]
+    float* s_scale = reinterpret_cast<float*>(s_pref + p.R + 1);
+    __shared__ int s_wsum[kRowWarps];
+    // row-0 statistics formed before the wait, held until it: lane l < 8 of each warp per item
+    __shared__ float2 s_pre[kRowPre][kRowWarps][kRowBlocksPerWarp];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool greedy = p.temperature[q] == 0.f;
-    const float scale = greedy ? 1.f : kLog2e / p.temperature[q];
     const bool vec = (p.V % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.target) & 15u) == 0);
-    const int b0 = (blockIdx.x * kRowWarps + warp) * kRowBlocksPerWarp;
+    const int nch = cdiv_dev(p.nblk, kRowChunk);
+    const int n0 = p.R * nch;   // row-0 items
+    const int wb = warp * kRowBlocksPerWarp;
     bool nonfinite = false;
-    float2 row0 = make_float2(-INFINITY, 0.f);
-    if (b0 < p.nblk) row0 = row_stats_of<T>(p, q, 0, b0, greedy, scale, vec, lane, nonfinite);
+    uint4 rc[4], rn[4];
+    for (int q = threadIdx.x; q < p.R; q += kRowWarps * 32) {   // an input: read before the wait
+        const float temp = p.temperature[q];
+        s_scale[q] = temp == 0.f ? 0.f : kLog2e / temp;
+    }
+    __syncthreads();
+
+    // before the wait: row 0 of items blockIdx.x + k * gridDim.x, k < kRowPre (a warp whose 8
+    // blocks lie past the vocabulary skips its part)
+    const auto pre_item = [&](int k) {
+        const int it = blockIdx.x + k * gridDim.x;
+        if (k >= kRowPre || it >= n0) return RowItem{-1, 0, 0};
+        return RowItem{it / nch, 0, (it % nch) * kRowChunk + wb};
+    };
+    {
+        RowItem c = pre_item(0);
+        bool fc = row_start<T>(p, s_scale, c, vec, lane, rc);
+        for (int k = 0; c.q >= 0; ++k) {
+            const RowItem n = pre_item(k + 1);
+            const bool fn = row_start<T>(p, s_scale, n, vec, lane, rn);
+            if (c.b0 < p.nblk) {
+                bool greedy;
+                const float2 st = row_finish<T>(p, s_scale, c, fc, rc, vec, lane, nonfinite, greedy);
+                if (lane < kRowBlocksPerWarp) s_pre[k][warp][lane] = st;
+            }
+            c = n;
+            fc = fn;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) rc[j] = rn[j];
+        }
+    }
     pdl_enter();   // keep comes from the scheduler
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.n_rej = 0;   // verify_decide counts from zero
-    const int ell = request_keep(p, q);
-    if (b0 < p.nblk) {
-        store_row_stats(p, q, 0, b0, lane, row0);
-        for (int i = 1; i <= ell; ++i)
-            store_row_stats(p, q, i, b0, lane, row_stats_of<T>(p, q, i, b0, greedy, scale, vec, lane, nonfinite));
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.n_rej = 0;   // verify_decide counts from zero
+    for (int k = 0; k < kRowPre; ++k) {
+        const RowItem it = pre_item(k);
+        if (it.q >= 0 && it.b0 < p.nblk) {
+            const float2 st = lane < kRowBlocksPerWarp ? s_pre[k][warp][lane] : make_float2(-INFINITY, 0.f);
+            store_row_stats(p, it.q, 0, it.b0, lane, st, s_scale[it.q] == 0.f);
+        }
+    }
+    // exclusive prefix over the requests of their rows 1..keep (each thread a run of requests)
+    const int per = cdiv_dev(p.R, kRowWarps * 32), q_lo = threadIdx.x * per, q_hi = min(p.R, q_lo + per);
+    int run = 0;
+    for (int q = q_lo; q < q_hi; ++q) run += request_keep(p, q);
+    int inc = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) s_wsum[warp] = inc;
+    __syncthreads();
+    int base = inc - run;
+    for (int w = 0; w < warp; ++w) base += s_wsum[w];
+    for (int q = q_lo; q < q_hi; ++q) {
+        s_pref[q] = base;
+        base += request_keep(p, q);
+    }
+    if (threadIdx.x == kRowWarps * 32 - 1) s_pref[p.R] = base;
+    __syncthreads();
+    const int n_left0 = max(0, n0 - kRowPre * (int)gridDim.x);   // row-0 items not formed before the wait
+    const int n_items = n_left0 + s_pref[p.R] * nch;
+    const auto post_item = [&](int it) {
+        if (it >= n_items) return RowItem{-1, 0, 0};
+        if (it < n_left0) {
+            const int j = kRowPre * gridDim.x + it;
+            return RowItem{j / nch, 0, (j % nch) * kRowChunk + wb};
+        }
+        const int rr = (it - n_left0) / nch;
+        int lo = 0, hi = p.R - 1;   // the last q with s_pref[q] <= rr: its row rr - s_pref[q] + 1
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_pref[mid] <= rr)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        return RowItem{lo, rr - s_pref[lo] + 1, ((it - n_left0) % nch) * kRowChunk + wb};
+    };
+    int it = blockIdx.x;
+    RowItem c = post_item(it);
+    bool fc = row_start<T>(p, s_scale, c, vec, lane, rc);
+    while (c.q >= 0) {
+        it += gridDim.x;
+        const RowItem n = post_item(it);
+        const bool fn = row_start<T>(p, s_scale, n, vec, lane, rn);
+        if (c.b0 < p.nblk) {
+            bool greedy;
+            const float2 st = row_finish<T>(p, s_scale, c, fc, rc, vec, lane, nonfinite, greedy);
+            store_row_stats(p, c.q, c.i, c.b0, lane, st, greedy);
+        }
+        c = n;
+        fc = fn;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) rc[j] = rn[j];
     }
     if (nonfinite) raise_status(p.status, DSPARK_ERR_NONFINITE_INPUT);
 }
 
 // ----------------------------------------------------------------- accept tests and bonus
 
-constexpr int kDecideThreads = 128;
+constexpr int kDecideThreads = 256;
 
 template <typename T>
 __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyParams p)
@@ -231,9 +398,9 @@ __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyPar
         __shared__ int s_next;
         int n = ell;
         for (int j = 0; j <= ell; ++j) {
-            const float2* st = p.row_stats + ((size_t)q * (p.G + 1) + j) * p.nblk;
+            const float2* pp = p.row_part + ((size_t)q * (p.G + 1) + j) * p.npart;
             ArgMax best{-INFINITY, -1};
-            for (int b = t; b < p.nblk; b += kDecideThreads) best = argmax_better(best, ArgMax{st[b].x, (int)st[b].y});
+            for (int b = t; b < p.npart; b += kDecideThreads) best = argmax_better(best, ArgMax{pp[b].x, (int)pp[b].y});
             best = block_argmax<kDecideThreads>(best, sv, si);
             const int tgt = best.i < 0 ? 0 : best.i;
             if (j == ell || checked_index(p.tokens[(size_t)q * p.G + j], p.V, p.status) != tgt) {
@@ -253,16 +420,19 @@ __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyPar
     }
     const float invT = 1.f / p.temperature[q];
 
-    // log-normalisers of target rows 0..ell (natural log)
-    for (int i = 0; i <= ell; ++i) {
-        const float2* st = p.row_stats + ((size_t)q * (p.G + 1) + i) * p.nblk;
+    // log-normalisers of target rows 0..ell (natural log), one warp per row, from the rows' per-warp
+    // partials (max, sum of 2^(z/T log2 e - max)) over 8 blocks each
+    const int warp = t >> 5, lane = t & 31;
+    for (int i = warp; i <= ell; i += kDecideThreads / 32) {
+        const float2* pp = p.row_part + ((size_t)q * (p.G + 1) + i) * p.npart;
         float lm = -INFINITY;
-        for (int b = t; b < p.nblk; b += kDecideThreads) lm = fmaxf(lm, st[b].x + log2f(st[b].y));
-        lm = block_max<kDecideThreads>(lm, red);
+        for (int b = lane; b < p.npart; b += 32) lm = fmaxf(lm, pp[b].x);
+        lm = warp_max(lm);
         float acc = 0.f;
-        for (int b = t; b < p.nblk; b += kDecideThreads) acc += exp2f(st[b].x - lm) * st[b].y;
-        acc = block_sum<kDecideThreads>(acc, red);
-        if (t == 0) {
+        if (lm > -INFINITY)
+            for (int b = lane; b < p.npart; b += 32) acc += exp2f(pp[b].x - lm) * pp[b].y;
+        acc = warp_sum(acc);
+        if (lane == 0) {
             lse_s[i] = (lm + log2f(acc)) * kLn2;
             p.lse_t[(size_t)q * (p.G + 1) + i] = lse_s[i];
         }
@@ -304,7 +474,7 @@ __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyPar
     const int bstar = best.i < 0 ? 0 : best.i;
     const int v = bstar * kNoiseBlock + t;
     ArgMax cand{-INFINITY, -1};
-    if (v < p.V) {
+    if (t < kNoiseBlock && v < p.V) {   // one thread per column of the block
         const float zt = ld(target, ((size_t)q * (p.G + 1) + ell) * p.V + v) * invT;
         cand = ArgMax{zt + gumbel_at(key, p.round, kFinalElem, (uint32_t)q, 0u, (uint32_t)v), v};
     }
@@ -484,15 +654,44 @@ __global__ void __launch_bounds__(kPickThreads) residual_pick_kernel(VerifyParam
 
 // ----------------------------------------------------------------- launchers
 
+template <typename T>
+int row_grid(const VerifyParams& p, size_t smem)
+{
+    // as many CTAs as are resident at once while the scheduler still runs, at most one per item: a
+    // CTA that started late would form its row-0 items after the wait
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_rows_kernel<T>, kRowWarps * 32, smem) !=
+            cudaSuccess ||
+        per_sm <= 0) {
+        (void)cudaGetLastError();
+        per_sm = 1;
+    }
+    const long long items = (long long)p.R * (p.G + 1) * cdiv(p.nblk, kRowChunk);
+    const int sms = std::max(1, num_sms() - kScheduleCtas);   // the scheduler's SMs are full until it ends
+    return (int)std::min<long long>(items, (long long)std::min(per_sm, kRowCtasPerSm) * sms);
+}
+
 cudaError_t launch_verify_rows(const VerifyParams& p, cudaStream_t s)
 {
-    const int per_cta = kRowWarps * kRowBlocksPerWarp;
-    const dim3 grid(cdiv(p.nblk, per_cta), p.R);
-    const cudaError_t e = p.dtype == DSPARK_BF16
-                              ? launch_pdl(verify_rows_kernel<__nv_bfloat16>, grid, kRowWarps * 32, 0, s, p)
-                              : launch_pdl(verify_rows_kernel<float>, grid, kRowWarps * 32, 0, s, p);
+    const size_t smem = sizeof(int) * ((size_t)p.R + 1) + sizeof(float) * (size_t)p.R;   // R <= DSPARK_MAX_SLOTS
+    static bool smem_set = false;
+    if (!smem_set) {   // above the default 48 KB at the largest R
+        const int most = (int)(sizeof(int) * (DSPARK_MAX_SLOTS + 1) + sizeof(float) * DSPARK_MAX_SLOTS);
+        if (cudaFuncSetAttribute(verify_rows_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(verify_rows_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
+                cudaSuccess)
+            return cudaGetLastError();
+        smem_set = true;
+    }
+    const cudaError_t e =
+        p.dtype == DSPARK_BF16
+            ? launch_pdl(verify_rows_kernel<__nv_bfloat16>, row_grid<__nv_bfloat16>(p, smem), kRowWarps * 32, smem, s, p)
+            : launch_pdl(verify_rows_kernel<float>, row_grid<float>(p, smem), kRowWarps * 32, smem, s, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
+
+int verify_row_partials(int nblk) { return cdiv(nblk, kRowBlocksPerWarp); }
 
 cudaError_t launch_verify_decide(const VerifyParams& p, cudaStream_t s)
 {
