@@ -315,7 +315,7 @@ dspark_status dspark_sample_block(const dspark_sample_args* a, void* ws, size_t 
     p.pick = at<unsigned long long>(ws, L.pick);
     p.a_next = at<unsigned char>(ws, L.a_next);
     const bool tc = sample_uses_tc(a);
-    p.a_replicas = tc ? kAReplicas : 1;
+    p.a_replicas = tc && a->head != DSPARK_HEAD_RNN ? kAReplicas : 1;
     p.head = a->head;
     p.W_rnn = a->W_rnn;
     const bool rnn = a->head == DSPARK_HEAD_RNN;

@@ -35,6 +35,9 @@ constexpr int kRtElT = kRtEl / kRtEpiGroups;                // state elements pe
 constexpr int kRtThreads = 64 + 128 * kRtEpiGroups;         // warp 0 TMA, warp 1 MMA, 16 epilogue warps
 constexpr uint32_t kRtSmem = kRtStages * kRtStageBytes + 1024 + 256;
 constexpr unsigned long long kRtWaitNs = 4000000000ull;     // 4 s
+constexpr int kRtStF = 20;                                  // staged fp32 row stride (16 + 4 of padding)
+constexpr int kRtStB = 24;                                  // staged bf16 row stride (16 + 8 of padding)
+static_assert(2 * kRtM * kRtStF * 4 + 4 * kRtM * kRtStB * 2 <= kRtStages * kRtStageBytes, "staging fits the stages");
 // instruction descriptor, kind::f16: D fp32, A = B = bf16, both K-major, N = 48, M = 128
 constexpr uint32_t kRtIdesc =
     (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kRtN >> 3) << 17) | ((uint32_t)(kRtM >> 4) << 24);
@@ -177,7 +180,6 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     } else if (epi) {
         // ---------------- epilogue: row q, elements el .. el + 3
         const float* s_prev = p.state + (size_t)(k & 1) * R * r;
-        float* s_next = p.state + (size_t)((k + 1) & 1) * R * r;
         float4 sp4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (q < R) sp4 = *reinterpret_cast<const float4*>(s_prev + (size_t)q * r + el);
         const bool ok = rt_wait(done, 0u, s_abort, p.status);
@@ -190,8 +192,15 @@ __global__ void __launch_bounds__(kRtThreads, 1)
             tc5::ld4(lane_base + kRtEl, acc[1]);
             tc5::ld4(lane_base + 2 * kRtEl, acc[2]);
         }
+        // The results go out through shared memory (the stage buffers, free once the MMAs have
+        // completed): written row by row here, then stored with 2-4 lanes per row segment, so that
+        // every 32-byte sector is written whole (a lane per row would write each sector in pieces,
+        // and the 8 operand copies made that the longest part of the step).
+        float* st_sn = reinterpret_cast<float*>(smem);            // [128][kRtStF] state
+        float* st_op = st_sn + kRtM * kRtStF;                     // [128][kRtStF] bias operand
+        __nv_bfloat16* st_b = reinterpret_cast<__nv_bfloat16*>(st_op + kRtM * kRtStF);   // [4][128][kRtStB]
+        const int cl = kRtElT * ge;   // this thread's first element within the CTA's 16
         if (all_ok && q < R) {
-            const size_t o = (size_t)q * G + k;
             const float sp[kRtElT] = {sp4.x, sp4.y, sp4.z, sp4.w};
             const float yg0[kRtElT] = {yh[0].x, yh[0].y, yh[0].z, yh[0].w};
             const float yc0[kRtElT] = {yh[1].x, yh[1].y, yh[1].z, yh[1].w};
@@ -211,7 +220,6 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                 }
             }
             // the state in fp32 and, for the next step's operand, its bf16 rounding and remainder
-            __nv_bfloat16* zn = static_cast<__nv_bfloat16*>(p.zbuf) + ((size_t)((k + 1) & 1) * R + q) * 3 * r;
             uint32_t hi2[kRtElT / 2], lo2[kRtElT / 2], ohi2[kRtElT / 2], olo2[kRtElT / 2];
 #pragma unroll
             for (int j = 0; j < kRtElT; j += 2) {
@@ -224,14 +232,49 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                 ohi2[j / 2] = pack_bf16x2(g0, g1);
                 olo2[j / 2] = pack_bf16x2(op[j] - g0, op[j + 1] - g1);
             }
-            *reinterpret_cast<float4*>(s_next + (size_t)q * r + el) = make_float4(sn[0], sn[1], sn[2], sn[3]);
-            *reinterpret_cast<float4*>(p.a_rows + o * r + el) = make_float4(op[0], op[1], op[2], op[3]);
-            *reinterpret_cast<uint2*>(zn + el) = make_uint2(hi2[0], hi2[1]);
-            *reinterpret_cast<uint2*>(zn + r + el) = make_uint2(lo2[0], lo2[1]);
-            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.a_lo) + (size_t)q * r + el) = make_uint2(olo2[0], olo2[1]);
-            for (int rp = 0; rp < p.a_replicas; ++rp)
-                *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.a_next) + ((size_t)rp * R + q) * r + el) =
-                    make_uint2(ohi2[0], ohi2[1]);
+            fence_proxy_async();   // the stage buffers were last read by the MMAs (async proxy)
+            *reinterpret_cast<float4*>(st_sn + row * kRtStF + cl) = make_float4(sn[0], sn[1], sn[2], sn[3]);
+            *reinterpret_cast<float4*>(st_op + row * kRtStF + cl) = make_float4(op[0], op[1], op[2], op[3]);
+            *reinterpret_cast<uint2*>(st_b + (0 * kRtM + row) * kRtStB + cl) = make_uint2(hi2[0], hi2[1]);
+            *reinterpret_cast<uint2*>(st_b + (1 * kRtM + row) * kRtStB + cl) = make_uint2(lo2[0], lo2[1]);
+            *reinterpret_cast<uint2*>(st_b + (2 * kRtM + row) * kRtStB + cl) = make_uint2(olo2[0], olo2[1]);
+            *reinterpret_cast<uint2*>(st_b + (3 * kRtM + row) * kRtStB + cl) = make_uint2(ohi2[0], ohi2[1]);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(128 * kRtEpiGroups) : "memory");   // the epilogue warps
+        if (all_ok) {
+            const int e = threadIdx.x - 64;   // 0 .. 511
+            // fp32 rows: 16 elements = 4 lanes x 16 bytes per row, 128 rows
+            {
+                const int rr = e >> 2, part = e & 3, qq = mt * kRtM + rr;
+                if (qq < R) {
+                    const size_t o = (size_t)qq * G + k;
+                    float* s_next = p.state + (size_t)((k + 1) & 1) * R * r;
+                    *reinterpret_cast<float4*>(s_next + (size_t)qq * r + e0 + 4 * part) =
+                        *reinterpret_cast<const float4*>(st_sn + rr * kRtStF + 4 * part);
+                    *reinterpret_cast<float4*>(p.a_rows + o * r + e0 + 4 * part) =
+                        *reinterpret_cast<const float4*>(st_op + rr * kRtStF + 4 * part);
+                }
+            }
+            // bf16 rows: 16 elements = 2 lanes x 16 bytes; state hi and lo (z, next parity),
+            // operand remainder (a_lo) and the a_replicas copies of the operand's rounding (a_next)
+            const int n_dst = 3 + p.a_replicas;
+            __nv_bfloat16* zn = static_cast<__nv_bfloat16*>(p.zbuf) + (size_t)((k + 1) & 1) * R * 3 * r;
+            for (int u = e; u < n_dst * 2 * kRtM; u += 128 * kRtEpiGroups) {
+                const int dst = u / (2 * kRtM), rr = (u >> 1) % kRtM, half = u & 1, qq = mt * kRtM + rr;
+                if (qq >= R) continue;
+                const int src = dst < 3 ? dst : 3;
+                const uint4 v = *reinterpret_cast<const uint4*>(st_b + (src * kRtM + rr) * kRtStB + 8 * half);
+                __nv_bfloat16* out;
+                if (dst == 0)
+                    out = zn + (size_t)qq * 3 * r;                       // hi(s_k)
+                else if (dst == 1)
+                    out = zn + (size_t)qq * 3 * r + r;                   // lo(s_k)
+                else if (dst == 2)
+                    out = static_cast<__nv_bfloat16*>(p.a_lo) + (size_t)qq * r;
+                else
+                    out = static_cast<__nv_bfloat16*>(p.a_next) + ((size_t)(dst - 3) * R + qq) * r;
+                *reinterpret_cast<uint4*>(out + e0 + 8 * half) = v;
+            }
         }
     }
     tc5::fence_before();

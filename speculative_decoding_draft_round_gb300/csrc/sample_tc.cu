@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const uint64_t pol = l2_policy_evict_last();
                         for (int cb = 0; cb < P.r / BK; ++cb)
                             tma_load_3d(sbase + L::OFF_A + cb * (BM * 128), &tmA, cb * BK, mt * BM,
-                                        (int)(blockIdx.x % A_REPLICAS), a_full, pol);
+                                        (int)(blockIdx.x % P.d.a_replicas), a_full, pol);
                     }
                     // RNN head: the bf16 remainder of the operand rows goes to TMEM (the second A
                     // operand) while that copy flies, warpgroup g covering K elements [64g, 64g + 64)
