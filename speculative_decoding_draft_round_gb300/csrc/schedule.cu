@@ -133,7 +133,7 @@ __device__ __noinline__ int load_pool(SchedSmem& sm, const int32_t* gamma, int G
 }
 
 // Exclusive prefix over the kHist counts in [digit][warp] order, in place (1024 threads, 8 each).
-__device__ __noinline__ void scan_hist(SchedSmem& sm)
+__device__ __forceinline__ void scan_hist(SchedSmem& sm)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int per = kHist / kSchedThreads;   // 8
@@ -171,33 +171,34 @@ __device__ __noinline__ void scan_hist(SchedSmem& sm)
     reinterpret_cast<uint4*>(sm.hist)[2 * tid + 1] = make_uint4(base + c[4], base + c[5], base + c[6], base + c[7]);
 }
 
-// One stable counting pass on 8 bits of the key, buffer `in` -> 1 - in.
+// One stable counting pass on 8 bits of the key, buffer `in` -> 1 - in. A thread's keys and, per
+// key, its slot (low 16 bits) with its rank among the equal digits of its warp (high 16 bits, below
+// 256) stay in registers across the histogram scan; the digit is formed again for the scatter.
 __device__ __noinline__ void radix_pass(SchedSmem& sm, int in, int shift, int ni)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     reinterpret_cast<uint4*>(sm.hist)[2 * tid] = make_uint4(0u, 0u, 0u, 0u);
     reinterpret_cast<uint4*>(sm.hist)[2 * tid + 1] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
-    uint32_t key[kMaxItems], dig[kMaxItems], rank[kMaxItems];
-    uint16_t val[kMaxItems];
+    uint32_t key[kMaxItems], vr[kMaxItems];
 #pragma unroll
     for (int it = 0; it < kMaxItems; ++it) {
         if (it >= ni) break;
         const int idx = striped(warp, it, lane, ni);
         key[it] = sm.key[in][sk(idx)];
-        val[it] = sm.val[in][sk(idx)];
+        vr[it] = sm.val[in][sk(idx)];
     }
 #pragma unroll
     for (int it = 0; it < kMaxItems; ++it) {
         if (it >= ni) break;
-        dig[it] = (key[it] >> shift) & (kDigits - 1);
-        uint32_t* h = sm.hist + dig[it] * kSchedWarps + warp;
-        const uint32_t peers = __match_any_sync(0xffffffffu, dig[it]);
+        const uint32_t dig = (key[it] >> shift) & (kDigits - 1);
+        uint32_t* h = sm.hist + dig * kSchedWarps + warp;
+        const uint32_t peers = __match_any_sync(0xffffffffu, dig);
         const uint32_t base = *h;
         __syncwarp();
         if (lane == __ffs(peers) - 1) *h = base + __popc(peers);
         __syncwarp();
-        rank[it] = base + __popc(peers & lanemask_lt());
+        vr[it] |= (base + __popc(peers & lanemask_lt())) << 16;
     }
     __syncthreads();
     scan_hist(sm);
@@ -206,9 +207,10 @@ __device__ __noinline__ void radix_pass(SchedSmem& sm, int in, int shift, int ni
 #pragma unroll
     for (int it = 0; it < kMaxItems; ++it) {
         if (it >= ni) break;
-        const uint32_t pos = sm.hist[dig[it] * kSchedWarps + warp] + rank[it];
+        const uint32_t dig = (key[it] >> shift) & (kDigits - 1);
+        const uint32_t pos = sm.hist[dig * kSchedWarps + warp] + (vr[it] >> 16);
         sm.key[out][sk(pos)] = key[it];
-        sm.val[out][sk(pos)] = val[it];
+        sm.val[out][sk(pos)] = (uint16_t)(vr[it] & 0xFFFFu);
     }
     __syncthreads();
 }
