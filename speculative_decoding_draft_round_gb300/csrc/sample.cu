@@ -338,6 +338,9 @@ __global__ void __launch_bounds__(kCommitThreads)
     // U at this thread's column of the block, kept in its own type until it is used
     T u_raw = T(0.f);
     if (t < kNoiseBlock && v < p.V) u_raw = U[o * p.V + v];
+    // the element Gumbel of this column: it needs only the picked block, so it is formed under the W copy
+    const float gum = (t < kNoiseBlock && v < p.V && !greedy)
+                          ? gumbel_at(key, p.round, kDraftElem, (uint32_t)q, (uint32_t)p.k, (uint32_t)v) : 0.f;
 #pragma unroll
     for (int j = 0; j < kErowPer; ++j) {
         const int i = t + j * kCommitThreads;
@@ -407,7 +410,7 @@ __global__ void __launch_bounds__(kCommitThreads)
     float lv = 0.f;
     if (t < kNoiseBlock && v < p.V) {
         lv = (to_f32<T>(u_raw) + bias) * invT;
-        cand = ArgMax{greedy ? lv : lv + gumbel_at(key, p.round, kDraftElem, (uint32_t)q, (uint32_t)p.k, (uint32_t)v), v};
+        cand = ArgMax{greedy ? lv : lv + gum, v};
     }
     const ArgMax win = block_argmax<kCommitThreads>(cand, sv, si);
     int tok = win.i;
