@@ -368,6 +368,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParam
 // ----------------------------------------------------------------- accept tests and bonus
 
 constexpr int kDecideThreads = 256;
+constexpr int kDecidePre = 2;   // block Gumbels formed before the wait: nblk <= 4 * 2 * 256
 
 template <typename T>
 __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyParams p)
@@ -390,6 +391,20 @@ __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyPar
         a_zt = ld(target, ((size_t)q * (p.G + 1) + t) * p.V + x) * (1.f / p.temperature[q]);
         a_lpd = p.draft_logit[o] - p.draft_lse[o];
         a_lu = logf(uniform_at(make_key(p.seed), p.round, kAccept, (uint32_t)q, (uint32_t)t, 0u));
+    }
+    // the bonus draw's block Gumbels -log(-log u) need only the seed, the round and the request: formed
+    // before the wait for blocks 4g4 .. 4g4 + 3, g4 = t + u * kDecideThreads (u < kDecidePre)
+    const PhiloxKey key = make_key(p.seed);
+    float gb[kDecidePre][4];
+#pragma unroll
+    for (int u = 0; u < kDecidePre; ++u) {
+        const int g4 = t + u * kDecideThreads;
+        if (!greedy_q && g4 * 4 < p.nblk) {
+            const uint4 w = philox4x32_10(make_uint4((uint32_t)g4, 0u, (uint32_t)q, counter_word3(p.round, kFinalBlock)), key);
+            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) gb[u][j] = -logf(-logf(bits_to_uniform(words[j])));
+        }
     }
     pdl_enter();   // the row statistics and the zeroed rejection counter come from verify_rows
     if (greedy_q) {
@@ -440,7 +455,6 @@ __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyPar
     __syncthreads();
 
     // accept x_j with probability min(1, p_t / p_d): log u < log p_t(x) - log p_d(x)
-    const PhiloxKey key = make_key(p.seed);
     int first_reject = ell;
     static_assert(DSPARK_MAX_GAMMA <= kDecideThreads, "one position per thread");
     if (t < ell) {
@@ -458,7 +472,16 @@ __global__ void __launch_bounds__(kDecideThreads) verify_decide_kernel(VerifyPar
     // bonus token from target row ell: two-level Gumbel-max over z_t / T
     const float2* st = p.row_stats + ((size_t)q * (p.G + 1) + ell) * p.nblk;
     ArgMax best{-INFINITY, -1};
-    for (int g4 = t; g4 * 4 < p.nblk; g4 += kDecideThreads) {
+#pragma unroll
+    for (int u = 0; u < kDecidePre; ++u) {
+        const int g4 = t + u * kDecideThreads;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = g4 * 4 + j;
+            if (b < p.nblk) best = argmax_better(best, ArgMax{(st[b].x + log2f(st[b].y)) * kLn2 + gb[u][j], b});
+        }
+    }
+    for (int g4 = t + kDecidePre * kDecideThreads; g4 * 4 < p.nblk; g4 += kDecideThreads) {   // V > 2^18
         const uint4 w = philox4x32_10(make_uint4((uint32_t)g4, 0u, (uint32_t)q, counter_word3(p.round, kFinalBlock)), key);
         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -573,11 +596,11 @@ __global__ void __launch_bounds__(kNoiseBlock) residual_stats_simt_kernel(Verify
 // ----------------------------------------------------------------- residual draw
 
 constexpr int kPickThreads = kBlockGemvThreads;
+constexpr int kPickPre = 2;   // block Gumbels formed before the wait: nblk <= 4 * 2 * kPickThreads
 
 template <typename T>
 __global__ void __launch_bounds__(kPickThreads) residual_pick_kernel(VerifyParams p)
 {
-    pdl_enter();   // the residual block sums come from the residual statistics kernel
     extern __shared__ float sm_dyn[];   // [r] W_1[prev], then [16][128] K-slice partials
     float* erow = sm_dyn;
     float* part = sm_dyn + ((p.r + 3) & ~3);
@@ -585,6 +608,10 @@ __global__ void __launch_bounds__(kPickThreads) residual_pick_kernel(VerifyParam
     __shared__ int si[kPickThreads / 32];
     __shared__ float red[kPickThreads / 32];
     const int q = blockIdx.x, t = threadIdx.x;
+    // The rejected position, the row log-normalisers and the bias operand row come from verify_decide
+    // and the sampler, both complete before the kernel this one follows started (it waited for
+    // verify_decide): they, and the block Gumbels of the draw, are formed before the dependency wait;
+    // only the residual block sums come from that kernel.
     const ResRequest rq = residual_request(p, q);
     if (!rq.active) return;
     const PhiloxKey key = make_key(p.seed);
@@ -595,29 +622,48 @@ __global__ void __launch_bounds__(kPickThreads) residual_pick_kernel(VerifyParam
     for (int i = t; i < p.r; i += kPickThreads)
         erow[i] = rq.use_bias ? (p.a_rows ? p.a_rows[((size_t)q * p.G + rq.n) * p.r + i] : ld(E, (size_t)rq.prev * p.r + i))
                               : 0.f;
+    float gb[kPickPre][4];   // -log(-log u) of blocks 4g4 .. 4g4 + 3, g4 = t + u * kPickThreads
+#pragma unroll
+    for (int u = 0; u < kPickPre; ++u) {
+        const int g4 = t + u * kPickThreads;
+        if (g4 * 4 < p.nblk) {
+            const uint4 w = philox4x32_10(make_uint4((uint32_t)g4, 0u, (uint32_t)q, counter_word3(p.round, kFinalBlock)), key);
+            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) gb[u][j] = -logf(-logf(bits_to_uniform(words[j])));
+        }
+    }
+    pdl_enter();   // the residual block sums come from the residual statistics kernel
     // residual mass anywhere?
     float tot = 0.f;
     for (int b = t; b < p.nblk; b += kPickThreads) tot += rs[b];
     tot = block_sum<kPickThreads>(tot, red);
     const bool fallback = !(tot > 0.f);   // zero only through rounding: draw from p_t of the row
-    // block level, one Philox call per 4 consecutive blocks
+    // block level, one Philox call per 4 consecutive blocks (formed above for the first kPickPre)
     ArgMax best{-INFINITY, -1};
-    for (int g4 = t; g4 * 4 < p.nblk; g4 += kPickThreads) {
+    const auto block_key = [&](int b, float g) {
+        float L;
+        if (fallback) {
+            L = (st[b].x + log2f(st[b].y)) * kLn2;
+        } else {
+            if (!(rs[b] > 0.f)) return;
+            L = logf(rs[b]);
+        }
+        best = argmax_better(best, ArgMax{L + g, b});
+    };
+#pragma unroll
+    for (int u = 0; u < kPickPre; ++u) {
+        const int g4 = t + u * kPickThreads;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (g4 * 4 + j < p.nblk) block_key(g4 * 4 + j, gb[u][j]);
+    }
+    for (int g4 = t + kPickPre * kPickThreads; g4 * 4 < p.nblk; g4 += kPickThreads) {   // V > 2^18
         const uint4 w = philox4x32_10(make_uint4((uint32_t)g4, 0u, (uint32_t)q, counter_word3(p.round, kFinalBlock)), key);
         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int b = g4 * 4 + j;
-            if (b >= p.nblk) break;
-            float L;
-            if (fallback) {
-                L = (st[b].x + log2f(st[b].y)) * kLn2;
-            } else {
-                if (!(rs[b] > 0.f)) continue;
-                L = logf(rs[b]);
-            }
-            best = argmax_better(best, ArgMax{L - logf(-logf(bits_to_uniform(words[j]))), b});
-        }
+        for (int j = 0; j < 4; ++j)
+            if (g4 * 4 + j < p.nblk) block_key(g4 * 4 + j, -logf(-logf(bits_to_uniform(words[j]))));
     }
     best = block_argmax<kPickThreads>(best, sv, si);
     const int bstar = best.i < 0 ? 0 : best.i;
