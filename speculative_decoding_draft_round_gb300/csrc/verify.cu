@@ -48,55 +48,63 @@ constexpr int kRowWarps = 8;
 constexpr int kRowBlocksPerWarp = 8;   // 1024 columns per warp: four 16-byte loads per lane
 
 // Block (max, sum exp2) of z/T (log2 units) for the 8 consecutive 128-wide blocks starting at
-// block b0, one warp; lane bb < 8 receives block b0 + bb. In the bf16 vector path lane l owns
-// columns 256j + 8l .. +7 (j = 0..3), so half-warp h of load j covers block b0 + 2j + h; the four
-// 16-byte loads (row_load8) are issued before any use, and row_reduce8 forms the statistics.
+// block b0, one warp; lane bb < 8 receives block b0 + bb. In the bf16 vector path four lanes share
+// a block: lane 4bb + qq reads columns 32j + 8qq .. +7 (j = 0..3) of block b0 + bb, so each of the
+// four 16-byte loads (row_load8, all issued before any use) covers 64 contiguous bytes of every
+// block; row_reduce8 takes the maximum on packed bf16 pairs and the sum with one fused
+// multiply-add and one SFU exponential an element, then two shuffle steps within the four lanes.
 template <typename T>
 __device__ __forceinline__ void row_load8(const T* row, int V, int b0, int lane, uint4 (&raw)[4])
 {
+    const int bb = lane >> 2, qq = lane & 3;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int v = b0 * kNoiseBlock + j * 256 + lane * 8;
+        const int v = (b0 + bb) * kNoiseBlock + j * 32 + qq * 8;
         raw[j] = v < V ? __ldg(reinterpret_cast<const uint4*>(row + v)) : make_uint4(0, 0, 0, 0);
     }
 }
 
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 __device__ __forceinline__ float2 row_reduce8(const uint4 (&raw)[4], int V, int b0, float scale, int lane)
 {
-    float2 mine = make_float2(-INFINITY, 0.f);
+    const int bb = lane >> 2, qq = lane & 3;
+    // columns past V: the whole 8-column group is out (V % 8 == 0)
+    bool in[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int v = b0 * kNoiseBlock + j * 256 + lane * 8;
-        const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-        float x[8];   // raw logits: the maximum is taken before scaling (scale > 0)
+    for (int j = 0; j < 4; ++j) in[j] = (b0 + bb) * kNoiseBlock + j * 32 + qq * 8 < V;
+    uint32_t mx2 = 0xFF80FF80u;   // (-inf, -inf)
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            x[2 * h] = __uint_as_float(w4[h] << 16);
-            x[2 * h + 1] = __uint_as_float(w4[h] & 0xFFFF0000u);
+    for (int j = 0; j < 4; ++j)
+        if (in[j]) mx2 = bf16x2_max(bf16x2_max(mx2, bf16x2_max(raw[j].x, raw[j].y)), bf16x2_max(raw[j].z, raw[j].w));
+    float mr = fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xFFFF0000u));
+    mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, 1));
+    mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, 2));
+    const float m = mr * scale;   // the block maximum of z/T in log2 units (scale > 0)
+    float s0 = 0.f, s1 = 0.f;
+    if (m > -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (!in[j]) continue;
+            const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                s0 += ex2(fmaf(__uint_as_float(w4[h] << 16), scale, -m));
+                s1 += ex2(fmaf(__uint_as_float(w4[h] & 0xFFFF0000u), scale, -m));
+            }
         }
-        const bool in = v < V;   // V % 8 == 0: 8 columns all in or all out
-        float mr = -INFINITY;
-        if (in) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mr = fmaxf(mr, x[e]);
-        }
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
-        const float m = mr * scale;   // the block maximum of z/T in log2 units
-        float sacc = 0.f;
-        if (in && m > -INFINITY) {
-            // one fused multiply-add and one SFU exponential per element: 2^(x*scale - m)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sacc += ex2(fmaf(x[e], scale, -m));
-        }
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
-        const float m0 = __shfl_sync(0xffffffffu, m, 0), s0 = __shfl_sync(0xffffffffu, sacc, 0);
-        const float m1 = __shfl_sync(0xffffffffu, m, 16), s1 = __shfl_sync(0xffffffffu, sacc, 16);
-        if (lane == 2 * j) mine = make_float2(m0, s0);
-        if (lane == 2 * j + 1) mine = make_float2(m1, s1);
     }
-    return mine;
+    float sacc = s0 + s1;
+    sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
+    sacc += __shfl_xor_sync(0xffffffffu, sacc, 2);
+    // lane bb < 8 takes block bb's statistics from lane 4bb
+    const int src = (lane & 7) * 4;
+    return make_float2(__shfl_sync(0xffffffffu, m, src), __shfl_sync(0xffffffffu, sacc, src));
 }
 
 template <typename T>
@@ -184,15 +192,11 @@ __device__ __forceinline__ float2 row_stats_of(const VerifyParams& p, int q, int
     return mine;
 }
 
-// This warp's statistics of row i, blocks b0 .. b0 + 7 (lane bb holds block b0 + bb), and the
-// merge of the eight (the warp's partial of the row: (max, sum) in log2 units, or the (max, lowest
-// index) of a greedy row) at partial slot b0 / 8.
-__device__ __forceinline__ void store_row_stats(const VerifyParams& p, int q, int i, int b0, int lane, float2 v,
-                                                bool greedy)
+// The merge of this warp's 8 block statistics (lanes 0-7; lane 0 receives it): (max, sum) in log2
+// units, or the (max, lowest index) of a greedy row.
+__device__ __forceinline__ float2 merge_row_part(const VerifyParams& p, int b0, int lane, float2 v, bool greedy)
 {
-    const size_t row = (size_t)q * (p.G + 1) + i;
     const bool in = lane < kRowBlocksPerWarp && b0 + lane < p.nblk;
-    if (in) p.row_stats[row * p.nblk + b0 + lane] = v;
     float m = in ? v.x : -INFINITY, x = in ? v.y : (greedy ? -1.f : 0.f);
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) {   // lanes 0-7: the eight blocks (xor within the group of 8)
@@ -207,7 +211,18 @@ __device__ __forceinline__ void store_row_stats(const VerifyParams& p, int q, in
             m = M;
         }
     }
-    if (lane == 0) p.row_part[row * p.npart + b0 / kRowBlocksPerWarp] = make_float2(m, x);
+    return make_float2(m, x);
+}
+
+// This warp's statistics of row i, blocks b0 .. b0 + 7 (lane bb holds block b0 + bb), and their
+// merge at partial slot b0 / 8.
+__device__ __forceinline__ void store_row_stats(const VerifyParams& p, int q, int i, int b0, int lane, float2 v,
+                                                bool greedy)
+{
+    const size_t row = (size_t)q * (p.G + 1) + i;
+    if (lane < kRowBlocksPerWarp && b0 + lane < p.nblk) p.row_stats[row * p.nblk + b0 + lane] = v;
+    const float2 part = merge_row_part(p, b0, lane, v, greedy);
+    if (lane == 0) p.row_part[row * p.npart + b0 / kRowBlocksPerWarp] = part;
 }
 
 // A persistent grid walks items (request q, target row i, chunk c of 64 blocks), every warp taking
@@ -258,8 +273,11 @@ __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParam
     extern __shared__ int s_pref[];   // [R + 1]: rows 1..keep of requests 0 .. q-1, then s_scale [R]
     float* s_scale = reinterpret_cast<float*>(s_pref + p.R + 1);
     __shared__ int s_wsum[kRowWarps];
-    // row-0 statistics formed before the wait, held until it: lane l < 8 of each warp per item
+    // row-0 statistics formed before the wait, held until it: lane l < 8 of each warp per item, the
+    // warp's merge of them, and the item's request (-1: none)
     __shared__ float2 s_pre[kRowPre][kRowWarps][kRowBlocksPerWarp];
+    __shared__ float2 s_pre_part[kRowPre][kRowWarps];
+    __shared__ int s_pre_q[kRowPre];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool vec = (p.V % 8 == 0) && ((reinterpret_cast<uintptr_t>(p.target) & 15u) == 0);
     const int nch = cdiv_dev(p.nblk, kRowChunk);
@@ -289,21 +307,29 @@ __global__ void __launch_bounds__(kRowWarps * 32) verify_rows_kernel(VerifyParam
             if (c.b0 < p.nblk) {
                 bool greedy;
                 const float2 st = row_finish<T>(p, s_scale, c, fc, rc, vec, lane, nonfinite, greedy);
+                const float2 part = merge_row_part(p, c.b0, lane, st, greedy);
                 if (lane < kRowBlocksPerWarp) s_pre[k][warp][lane] = st;
+                if (lane == 0) s_pre_part[k][warp] = part;
             }
+            if (threadIdx.x == 0) s_pre_q[k] = c.q;
             c = n;
             fc = fn;
 #pragma unroll
             for (int j = 0; j < 4; ++j) rc[j] = rn[j];
         }
     }
+    if (threadIdx.x == 0)
+        for (int k = 0; k < kRowPre; ++k)
+            if (blockIdx.x + k * gridDim.x >= n0) s_pre_q[k] = -1;
+    __syncthreads();
     pdl_enter();   // keep comes from the scheduler
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.n_rej = 0;   // verify_decide counts from zero
-    for (int k = 0; k < kRowPre; ++k) {
-        const RowItem it = pre_item(k);
-        if (it.q >= 0 && it.b0 < p.nblk) {
-            const float2 st = lane < kRowBlocksPerWarp ? s_pre[k][warp][lane] : make_float2(-INFINITY, 0.f);
-            store_row_stats(p, it.q, 0, it.b0, lane, st, s_scale[it.q] == 0.f);
+    for (int k = 0; k < kRowPre && s_pre_q[k] >= 0; ++k) {
+        const int b0 = ((blockIdx.x + k * gridDim.x) % nch) * kRowChunk + wb;
+        if (b0 < p.nblk) {
+            const size_t row = (size_t)s_pre_q[k] * (p.G + 1);   // row 0 of the request
+            if (lane < kRowBlocksPerWarp && b0 + lane < p.nblk) p.row_stats[row * p.nblk + b0 + lane] = s_pre[k][warp][lane];
+            if (lane == 0) p.row_part[row * p.npart + b0 / kRowBlocksPerWarp] = s_pre_part[k][warp];
         }
     }
     // exclusive prefix over the requests of their rows 1..keep (each thread a run of requests)
