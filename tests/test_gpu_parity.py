@@ -246,6 +246,34 @@ def test_verify_matches_oracle(spec):
         assert total["draw"] + total["accept"] + total["residual_fp32"] <= max(2, 3 * rnd.R // 100)
 
 
+def test_verify_rows_past_the_prewait_items():
+    """verify_rows forms at most 16 row-0 items per CTA before its dependency wait (a CTA per SM
+    slot, about 600 on this part); R = 2048 requests of V = 65536 hold 2048 x 8 row-0 items, so
+    the rest, and every later row, come after the wait. Sampled requests (both ends of the range
+    and random ones) are compared with the oracle; every request's outputs are checked for range."""
+    rnd = wl.make_round("R2048_g2_V65536_bf16", 2048, 2, 65536, 64, 32, "bf16", seed=99, device=DEV,
+                        sps=wl.sps_hyperbolic(2048 * 3))
+    rnd.round = 5
+    sout = ds.sample_block(rnd.U, rnd.E, rnd.W, rnd.h, rnd.w_h, rnd.w_e, rnd.b, rnd.temperature,
+                           rnd.anchor, rnd.seed, rnd.round, gamma=rnd.gamma)
+    assert ds.check(sout["workspace"]) == 0
+    gen = torch.Generator().manual_seed(6)
+    keep = (torch.rand(rnd.R, generator=gen) * 3).floor().to(torch.int32).to(DEV)
+    vout = ds.verify(rnd.target, rnd.U, rnd.E, rnd.W, rnd.anchor, sout["tokens"], sout["draft_lse"],
+                     sout["draft_logit"], keep, rnd.temperature, rnd.seed, rnd.round)
+    assert ds.check(vout["workspace"]) == 0
+    kp = to_np(keep)
+    acc = to_np(vout["accepted"])
+    nxt = to_np(vout["next_token"])
+    assert np.all((acc >= 0) & (acc <= kp)) and np.all((nxt >= 0) & (nxt < rnd.V))
+    ids = np.unique(np.concatenate([np.arange(32), np.arange(rnd.R - 32, rnd.R),
+                                    np.random.default_rng(7).choice(rnd.R, 96, replace=False)]))
+    total = check_verify(rnd, sout, keep, vout, ids)
+    report("verify R=2048 V=65536", total)
+    assert total["checked_requests"] == len(ids)
+    assert total["draw"] + total["accept"] + total["residual_fp32"] <= 2
+
+
 def test_tiny_round_end_to_end():
     """The tiny round exactly: the oracle runs alone from the inputs (its own draws feed its
     scheduler and verifier) and every output must equal the GPU's. A round in which one of the
