@@ -234,7 +234,7 @@ __device__ __forceinline__ void store_row_stats(const VerifyParams& p, int q, in
 // walking its rows one after the other. In the bf16 vector path each warp issues the next item's
 // loads before it reduces the current one.
 constexpr int kRowPre = 16;
-constexpr int kRowCtasPerSm = 4;   // resident beside a 1024-thread scheduler CTA: (2048 - 1024) / 256
+constexpr int kRowCtasPerSm = 4;   // 256 threads at 64 registers: four CTAs fill an SM's registers
 __device__ __forceinline__ int cdiv_dev(int a, int b) { return (a + b - 1) / b; }
 constexpr int kRowChunk = kRowWarps * kRowBlocksPerWarp;   // blocks per item
 
