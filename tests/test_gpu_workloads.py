@@ -173,3 +173,32 @@ def test_full_size_round_resident_loop(workload):
     report("resident loop, workload %d" % workload, total)
     assert total["checked_requests"] == rnd.R
     assert total["draw"] <= max(2, total["checked_tokens"] // 1000)
+
+
+def test_round_replays_from_a_cuda_graph():
+    """A whole round (sampler, scheduler, verifier) captured into a CUDA graph on a side stream and
+    replayed gives the eager round's outputs bit for bit: the calls allocate nothing and never wait
+    on the host, and their programmatic-launch edges survive capture."""
+    torch.cuda.empty_cache()
+    rnd = wl.WORKLOADS[2](device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        runner = ds.RoundRunner(rnd)
+        runner.set_round(9)
+        runner.run(stream=s)
+        s.synchronize()
+        assert runner.check(s) == 0
+        eager = {k: v.clone() for k, v in runner.results().items()
+                 if torch.is_tensor(v) and k != "workspace" and v.device.type == "cuda"}
+        for k, v in runner.results().items():   # poison every output before the replay
+            if k in eager:
+                v.fill_(float("nan") if v.is_floating_point() else -7)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            runner.run(stream=s)
+        g.replay()
+        s.synchronize()
+        assert runner.check(s) == 0
+        out = runner.results()
+    for k, v in eager.items():
+        assert torch.equal(out[k], v), "%s differs after graph replay" % k
