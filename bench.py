@@ -605,8 +605,9 @@ def bench_ours(args):
     # results read back, every step. U is copied one position at a time on a second stream and
     # the sampler's step k waits for its slice (step_ready events), so the draft steps run under
     # the copy. The target logits are copied after the scheduler, and only the rows verification
-    # reads (rows 0..keep[r] of each request: what the target model would have scored), one copy
-    # per request; the host reads keep back to know them.
+    # reads (rows 0..keep[r] of each request: what the target model would have scored): row 0 of
+    # every request in one strided copy, then one copy per request that admitted tokens; the host
+    # reads keep back to know them.
     host_in = {k: getattr(rnd, k).cpu().pin_memory() for k in ("h", "temperature", "anchor", "sps")}
     U_h = rnd.U.cpu().pin_memory()
     copy_stream = torch.cuda.Stream()
@@ -645,11 +646,17 @@ def bench_ours(args):
         runner.run_draft(step_ready=slice_ready)
         keep_h.copy_(res["keep"], non_blocking=True)
         stream.synchronize()
+        # row 0 of every request (always verified) in one strided copy, then rows 1..keep[r] of the
+        # requests that admitted tokens, one copy each
+        memcpy_2d(rnd.target.data_ptr(), req_bytes, target_h.data_ptr(), req_bytes, row_bytes, rnd.R,
+                  stream.cuda_stream)
+        target_rows += rnd.R
         for q, kq in enumerate(keep_h.tolist()):
-            n = (min(max(kq, 0), rnd.gamma_max) + 1)
-            memcpy_async(rnd.target.data_ptr() + q * req_bytes, target_h.data_ptr() + q * req_bytes, n * row_bytes,
-                         stream.cuda_stream)
-            target_rows += n
+            n = min(max(kq, 0), rnd.gamma_max)
+            if n:
+                memcpy_async(rnd.target.data_ptr() + q * req_bytes + row_bytes,
+                             target_h.data_ptr() + q * req_bytes + row_bytes, n * row_bytes, stream.cuda_stream)
+                target_rows += n
         runner.run_verify()
         for o, h in zip(outs, host_out):
             h.copy_(o, non_blocking=True)
